@@ -1,0 +1,255 @@
+/*
+ * tq.h -- C ABI of libtq: TurboQuant quantized KV cache on NVIDIA GB300 (sm_103a).
+ *
+ * This header is the written specification both the CUDA library and the
+ * independent CPU oracle are built from.  Sources are cited by page title and
+ * section:
+ *   [P1] issoh.co.jp "TurboQuantとは？vLLM・Ollama・LM Studioの対応状況と使い方"
+ *   [P2] ai-navigate-news.com, the turboquant-vllm article
+ *   [P3] lilting.ch "HypuraのNVMeストリーミングとTurboQuantのKVキャッシュ量子化"
+ *   [P4] qiita.com, AMD's mixed BF16/4-bit KV cache in LMCache
+ *
+ * ------------------------------------------------------------------------
+ * Method (what the library computes)
+ *
+ *  Stage 1 ([P1] §第1段, §第2段 "_nc"): every key/value vector x in R^d is
+ *  rotated by a per-layer random rotation Pi, divided by its norm, and each
+ *  coordinate is replaced by the index of its Lloyd-Max cell; the fp32 norm
+ *  correction gamma is stored beside the codes ([P2] "Bugs Nobody Else Has
+ *  Found": fp32, not fp16):
+ *      n = ||x||,  y = Pi x / n,  idx_j = #{ i : y_j >= beta_i },
+ *      gamma = n / ||c[idx]||   (TQ_NORM_CORRECTED)   or  n  (TQ_NORM_RAW),
+ *      x_hat = gamma Pi^T c[idx];   zero vector: gamma = 0, idx_j = 2^(b-1).
+ *  Ties (y_j == beta_i) go to the upper cell.
+ *
+ *  Stage 2, optional for keys ([P3] "QJL: Johnson-Lindenstrauss変換で残差を
+ *  1ビット補正する"): r = Pi x - gamma c[idx] (rotated domain), store the
+ *  m = d sign bits sigma_i = [(S r)_i >= 0] and rho = ||r|| (fp32); S is an
+ *  m x d matrix of iid N(0,1) shared by all layers and heads.  Score estimate:
+ *      <q, x> ~= gamma <Pi q, c[idx]> + sqrt(pi/2)/m rho sum_i (2 sigma_i - 1)(S Pi q)_i.
+ *
+ *  Decode attention on the packed cache (no dequantized K/V written to HBM):
+ *      q' = Pi q once per query head; s_t = sm_scale * gamma_t <q', c_K[idx_t]>
+ *      (+ the QJL term); online softmax over the context; the value sum is
+ *      accumulated in the rotated domain, sum_t p_t gamma'_t c_V[idx'_t];
+ *      one inverse rotation Pi^T per query head at the end.
+ *  Query head h reads KV head h / (H_q / H_kv) (grouped-query attention).
+ *  bf16 layers ([P1] §起動コマンド: the first and last two layers of dense
+ *  models stay at full precision; [P4] layout table, 512 B per token and head)
+ *  hold raw bf16 K/V and are attended without rotation.
+ *
+ * ------------------------------------------------------------------------
+ * Readings of the pages (they leave these open; the library and the oracle
+ * both follow them)
+ *
+ *  Random streams: SplitMix64 (Vigna).  state0 = seed ^ ((kind<<32) + layer)
+ *    * 0x9E3779B97F4A7C15 (mod 2^64); next: state += 0x9E3779B97F4A7C15,
+ *    z = state, z = (z^(z>>30))*0xBF58476D1CE4E5B9, z = (z^(z>>27))*
+ *    0x94D049BB133111EB, out = z^(z>>31).  Sign i = -1 iff bit 63 of draw i.
+ *    Uniform = (draw>>11) * 2^-53.  Gaussians: Box-Muller on consecutive
+ *    uniform pairs (u1, u2): r = sqrt(-2 ln(1-u1)), g0 = r cos(2 pi u2),
+ *    g1 = r sin(2 pi u2), filling matrices row-major.
+ *  Hadamard rotation (kind 1): Pi = H_d diag(s) / sqrt(d), H_d Sylvester.
+ *  Dense rotation (kind 2): G = d x d Gaussians; Pi = Q diag(sign(diag R))
+ *    for G = Q R (the unique Haar Q).
+ *  QJL projection (kind 3, layer 0): S = d x d Gaussians (m = d).
+ *  Codebook: Lloyd-Max for the density of one coordinate of a uniform unit
+ *    vector in R^d, f(t) ~ (1 - t^2)^((d-3)/2); Lloyd iteration in fp64 to
+ *    max |delta c| < 1e-15; centroids emitted in fp32 with the upper half
+ *    mirrored (c[2^b-1-i] = -c[i] exactly); boundaries
+ *    beta_i = fp32(fp32(c_i + c_{i+1}) * 0.5).
+ *  Packing: LSB-first bitstream; code j in bits [b j, b j + b) of the record,
+ *    bit k of a record = bit (k mod 8) of byte (k div 8).  For b = 4 this is
+ *    the 'codes[i] | codes[i+1] << 4' of [P4]'s worked example.
+ *
+ * ------------------------------------------------------------------------
+ * Memory layout (device, owned by the caller)
+ *
+ *  Block size 16 tokens.  slot = block * 16 + offset (vLLM-style slot mapping;
+ *  slot < 0 means "skip this token").
+ *  Packed pool:  [num_blocks][num_kv_heads][page_bytes]; one page per
+ *  (block, kv head):
+ *      [16 records of d*b/8 code bytes][16 x fp32 gamma]
+ *      keys with QJL add: [16 x d/8 sign bytes][16 x fp32 rho]
+ *    d = 128: 1088 B (4-bit), 832 B (3-bit), 576 B (2-bit), 896 B (2-bit+QJL).
+ *  bf16 pool: [num_blocks][num_kv_heads][16][d] bf16 (4096 B per page).
+ *  Pools must be 16-byte aligned.
+ *
+ * ------------------------------------------------------------------------
+ * Conventions for every call
+ *
+ *  - Device pointers are raw CUDA device addresses; host pointers are marked.
+ *  - Calls that take a stream enqueue asynchronously on it (a cudaStream_t
+ *    passed as void*; NULL = legacy default stream) and never synchronize,
+ *    except tq_get_device_status.
+ *  - The library never allocates device memory (scratch is the caller's
+ *    workspace) and keeps no pointer past the call.
+ *  - Arguments are validated on the host before any launch; a rejected call
+ *    launches nothing and returns a status != TQ_OK; tq_last_error() then
+ *    returns a message (thread-local, valid until the next call).
+ *  - Values that live on the device (slot mappings, block tables, context
+ *    lengths) are range-checked inside the kernels: an out-of-range entry is
+ *    skipped and recorded in a sticky per-device status word read by
+ *    tq_get_device_status.  Kernels never trap.
+ *  - Only head_dim = 128 and block_size = 16 are implemented.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TQ_FORMAT_VERSION 1u
+#define TQ_BLOCK_SIZE 16
+#define TQ_HEAD_DIM 128
+#define TQ_MAX_GROUP 8 /* query heads per KV head handled by one decode CTA */
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1,  /* bad argument; nothing launched */
+  TQ_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim != 128) */
+  TQ_ERR_WORKSPACE = 3,    /* workspace missing or too small */
+  TQ_ERR_CUDA = 4,         /* a CUDA runtime call failed */
+  TQ_ERR_DEVICE = 5,       /* the device status word reported a problem */
+  TQ_ERR_VERSION = 6       /* descriptor format_version mismatch */
+} tq_status;
+
+/* element types of q / k / v / out */
+enum { TQ_F32 = 0, TQ_BF16 = 1 };
+
+/* rotation / random stream kinds */
+enum { TQ_ROT_HADAMARD = 1, TQ_ROT_DENSE = 2, TQ_RNG_QJL = 3 };
+
+/* layer storage */
+enum { TQ_KV_PACKED = 0, TQ_KV_BF16 = 1 };
+
+/* norm handling */
+enum { TQ_NORM_CORRECTED = 0, TQ_NORM_RAW = 1 };
+
+/* device status codes (bit flags, sticky until read) */
+enum {
+  TQ_DEV_BAD_SLOT = 1,        /* slot >= num_blocks * 16 in an append/dequantize */
+  TQ_DEV_BAD_BLOCK = 2,       /* block table entry outside [0, num_blocks) */
+  TQ_DEV_BAD_CONTEXT = 4,     /* context length < 0 or > max_blocks_per_seq * 16 */
+  TQ_DEV_WAIT_TIMEOUT = 8     /* a bounded wait on a copy gave up */
+};
+
+typedef struct {
+  int32_t kv_format; /* TQ_KV_PACKED or TQ_KV_BF16 */
+  int32_t bits_k;    /* packed: 2, 3 or 4 */
+  int32_t bits_v;    /* packed: 2, 3 or 4 */
+  int32_t qjl_k;     /* packed: 1 = keys carry the 1-bit QJL residual (m = head_dim) */
+  int32_t rot_kind;  /* packed: TQ_ROT_HADAMARD or TQ_ROT_DENSE */
+  int32_t norm_mode; /* TQ_NORM_CORRECTED or TQ_NORM_RAW */
+} tq_layer_format;
+
+/* One descriptor per layer.  Codebooks travel by value; the tables must be
+ * strictly increasing and antisymmetric (c[2^b-1-i] = -c[i], beta middle = 0),
+ * as tq_make_codebook emits them.  Entries past 2^b (2^b - 1) are ignored. */
+typedef struct {
+  uint32_t format_version; /* TQ_FORMAT_VERSION */
+  int32_t head_dim;        /* 128 */
+  int32_t num_kv_heads;    /* >= 1 */
+  int32_t block_size;      /* 16 */
+  int64_t num_blocks;      /* pages per pool */
+  tq_layer_format fmt;
+  void* k_cache;           /* device pool of keys (layout above) */
+  void* v_cache;           /* device pool of values */
+  const float* rotation;   /* device: Hadamard -> signs[d] (+1.0f / -1.0f);
+                              dense -> Pi[d][d] row-major (y = Pi x); unused for bf16 */
+  const float* qjl_proj;   /* device: S[d][d] row-major; required iff fmt.qjl_k */
+  float centroids_k[16];
+  float boundaries_k[15];
+  float centroids_v[16];
+  float boundaries_v[15];
+} tq_cache_desc;
+
+/* ---- set-up (host only, no GPU needed) ---------------------------------- */
+
+/* Lloyd-Max codebook for one coordinate of a rotated unit vector in R^head_dim
+ * ([P1] §第1段; density and emission rule above).  Host outputs:
+ * centroids[2^bits], boundaries[2^bits - 1].  bits in 1..4. */
+tq_status tq_make_codebook(int head_dim, int bits, float* centroids, float* boundaries);
+
+/* Seeded matrices ([P1] §第1段, §llama.cpp本家; [P3] QJL section).  Host output:
+ *   TQ_ROT_HADAMARD: out[head_dim] = signs s (+-1.0f); Pi = H diag(s)/sqrt(d)
+ *   TQ_ROT_DENSE:    out[head_dim*head_dim] = Pi row-major (Haar, see above)
+ *   TQ_RNG_QJL:      out[head_dim*head_dim] = S row-major (layer ignored: 0)
+ * head_dim must be a power of two (Hadamard) or 1..1024 (dense, QJL). */
+tq_status tq_make_rotation(int kind, int head_dim, uint64_t seed, int layer, float* out);
+
+/* Bytes of one page (one block of one KV head) of the K (which = 0) or V
+ * (which = 1) pool; 0 if the descriptor is invalid. */
+size_t tq_page_bytes(const tq_cache_desc* desc, int which);
+
+/* ---- hot path ----------------------------------------------------------- */
+
+/* Quantize-on-append ([P1] §第1段/§第2段; [P3] online per-token quantization):
+ * k, v: device [n_tokens][num_kv_heads][head_dim] of in_dtype (TQ_F32 or
+ * TQ_BF16); either may be NULL to append only the other.  slot_mapping:
+ * device int64[n_tokens]; token t goes to slot_mapping[t] (skipped if < 0).
+ * Packed layers store codes + gamma (+ QJL for keys); bf16 layers store the
+ * values rounded to bf16.  Writes only the records of the given slots. */
+tq_status tq_quantize_append(const tq_cache_desc* desc, const void* k, const void* v, int in_dtype,
+                             const int64_t* slot_mapping, int64_t n_tokens, void* stream);
+
+/* The quantizer alone, fed rotated unit coordinates: y: device fp32
+ * [n_tokens][num_kv_heads][head_dim] (y = Pi x / ||x||), norms: device fp32
+ * [n_tokens][num_kv_heads] (||x||).  Writes codes and gamma of the K
+ * (which = 0) or V (which = 1) pool exactly as tq_quantize_append would from
+ * the same y (no QJL residual).  Packed layers only. */
+tq_status tq_quantize_rotated(const tq_cache_desc* desc, int which, const float* y, const float* norms,
+                              const int64_t* slot_mapping, int64_t n_tokens, void* stream);
+
+/* Number of context splits decode uses when num_splits == 0 (depends on the
+ * current device's SM count); 0 on error. */
+int tq_auto_splits(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks_per_seq);
+
+/* Workspace bytes tq_decode_attention needs for these sizes (num_splits = 0:
+ * the automatic choice above).  0 on error. */
+size_t tq_workspace_bytes(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks_per_seq,
+                          int num_splits);
+
+/* Decode attention over the cache (see "Method"):
+ * q: device [batch][num_q_heads][head_dim] (q_dtype TQ_F32 / TQ_BF16);
+ * block_table: device int32 [batch][max_blocks_per_seq]; context_lens: device
+ * int32 [batch] (0 gives a zero output row); out: device
+ * [batch][num_q_heads][head_dim] (out_dtype); workspace: device scratch of at
+ * least tq_workspace_bytes(...) bytes, 256-byte aligned, contents need not be
+ * initialised.  num_q_heads must be a multiple of num_kv_heads with at most
+ * TQ_MAX_GROUP query heads per KV head.  num_splits: 0 = automatic, else the
+ * number of contiguous context ranges each (sequence, KV head) is split into;
+ * results agree for every split count up to fp32 rounding. */
+tq_status tq_decode_attention(const tq_cache_desc* desc, const void* q, int q_dtype, int batch,
+                              int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                              const int32_t* context_lens, float sm_scale, void* out, int out_dtype,
+                              void* workspace, size_t workspace_bytes, int num_splits, void* stream);
+
+/* Dequantize records ([P2] "Incremental dequantization"): slots: device int64[n];
+ * out: device [n][num_kv_heads][head_dim] (out_dtype) with
+ * x_hat = gamma Pi^T c[idx] of the K (which = 0) or V (which = 1) pool
+ * (bf16 layers: the stored values).  Negative slots give zero rows. */
+tq_status tq_dequantize(const tq_cache_desc* desc, int which, const int64_t* slots, int64_t n, void* out,
+                        int out_dtype, void* stream);
+
+/* ---- status ------------------------------------------------------------- */
+
+/* Synchronizes the stream, returns the sticky device status bits of the
+ * current device in *code (host pointer) and clears them. */
+tq_status tq_get_device_status(void* stream, int32_t* code);
+
+/* Message describing the last failed call on this thread ("" if none). */
+const char* tq_last_error(void);
+
+/* TQ_FORMAT_VERSION of this build. */
+uint32_t tq_format_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

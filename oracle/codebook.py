@@ -17,7 +17,7 @@ iteration in fp64:
     c_i    = E[t | beta_{i-1} <= t < beta_i]           (centroid condition)
 
 with beta_{-1} = -1, beta_{2^b - 1} = +1, started from the quantiles
-F^{-1}((i + 1/2) / 2^b) and stopped when max |delta c| < 1e-13.  The cell mass
+F^{-1}((i + 1/2) / 2^b) and stopped when max |delta c| < 1e-15.  The cell mass
 uses the regularised incomplete beta function; the cell first moment has the
 closed form  int_a^b t f(t) dt = K/(d-1) [(1-a^2)^((d-1)/2) - (1-b^2)^((d-1)/2)].
 
@@ -94,7 +94,7 @@ def quantile(p, d):
     return -quantile(1.0 - p, d)
 
 
-def lloyd_max(d, bits, tol=1e-13, max_iter=200000):
+def lloyd_max(d, bits, tol=1e-15, max_iter=200000):
     """fp64 Lloyd iteration.  Returns (centroids[2^b], boundaries[2^b - 1], iters)."""
     k = 1 << bits
     c = np.array([quantile((i + 0.5) / k, d) for i in range(k)], dtype=np.float64)
