@@ -69,7 +69,8 @@ def test_one_bit_closed_form(d):
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
 def test_large_d_limit_is_gaussian_lloyd_max(bits):
     d = 1 << 16
-    c, beta, _ = cb.lloyd_max(d, bits)
+    # at this d the fp64 cell moments carry ~1e-14 noise, so stop earlier
+    c, beta, _ = cb.lloyd_max(d, bits, tol=1e-12)
     levels = math.sqrt(d) * c[len(c) // 2:]
     assert np.max(np.abs(levels - np.array(MAX1960_LEVELS[bits]))) < 1.5e-3
     mse = d * cb.distortion(c, beta, d)
