@@ -1,0 +1,34 @@
+// Internal declarations shared by the host and CUDA translation units of libtq.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include "tq.h"
+
+namespace tq {
+
+// Records a formatted error message for tq_last_error() and returns `st`.
+tq_status fail(tq_status st, const char* fmt, ...);
+void clear_error();
+
+// Host-side validation of a descriptor.  Returns TQ_OK or an error (message set).
+tq_status check_desc(const tq_cache_desc* desc);
+
+// Bytes of a K (which = 0) or V (which = 1) page of a valid descriptor.
+size_t page_bytes_of(const tq_cache_desc& d, int which);
+
+// Splits chosen when the caller passes 0.
+int auto_splits(int num_sms, int batch, int num_kv_heads, int max_blocks_per_seq);
+
+// Workspace layout of decode (all offsets 256-byte aligned).
+struct DecodeWorkspace {
+  size_t qrot_off;   // fp32 [batch][Hq][d]  rotated, scaled queries (+ QJL projections)
+  size_t part_off;   // fp32 [batch][Hq][splits][d] partial accumulators
+  size_t ml_off;     // fp32 [batch][Hq][splits][2] (running max, denominator)
+  size_t total;
+};
+DecodeWorkspace decode_workspace(int batch, int num_q_heads, int splits, int head_dim, bool qjl);
+
+}  // namespace tq

@@ -1,0 +1,482 @@
+// Quantize-on-append, the quantizer on given rotated coordinates, bf16-layer
+// append and dequantization (libtq, sm_103a).
+//
+// Method (issoh.co.jp TurboQuant overview, §第1段 and §第2段; lilting.ch
+// TurboQuant article, QJL section): per vector x, n = ||x||, y = Pi x / n,
+// idx_j = #{i : y_j >= beta_i}, gamma = n / ||c[idx]|| (norm correction),
+// LSB-first bit packing into the paged record, optional 1-bit QJL residual
+// sigma = [S (Pi x - gamma c[idx]) >= 0] with rho = ||Pi x - gamma c[idx]||.
+//
+// Thread layout: 4 consecutive lanes (a quad) own one vector, lane q of the
+// quad holding coordinates [32q, 32q + 32) in registers.  The Hadamard
+// rotation is a fast Walsh-Hadamard transform: 5 butterfly stages inside the
+// registers and 2 through quad shuffles.  A CTA of 256 threads handles tiles
+// of 64 vectors in a grid-stride loop.  Dense rotations and the QJL projection
+// are 128x128 mat-vecs against a padded copy of the matrix in shared memory.
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+enum { MODE_HADAMARD = 0, MODE_DENSE = 1, MODE_GIVEN_Y = 2 };
+
+struct QuantArgs {
+  const void* x;         // [n_tok][H][d] input vectors (MODE_HADAMARD / MODE_DENSE)
+  const float* y;        // [n_tok][H][d] rotated unit coordinates (MODE_GIVEN_Y)
+  const float* norms;    // [n_tok][H] norms (MODE_GIVEN_Y)
+  const int64_t* slots;  // [n_tok]
+  int64_t n_vec;         // n_tok * H
+  int H;
+  int64_t max_slot;      // num_blocks * 16
+  uint8_t* pool;
+  int page_bytes;
+  const float* rot;      // signs[d] or Pi[d][d]
+  const float* qjl;      // S[d][d]
+  Codebook cb;
+  int norm_mode;
+  unsigned* status;
+};
+
+constexpr int kTile = 64;            // vectors per CTA iteration
+constexpr int kThreads = 256;
+constexpr int kTileStride = kD + 4;  // padded row of the vector tile (floats)
+constexpr int kPadQ = 36;            // padded quarter-row of a staged matrix (floats)
+constexpr size_t kTableBytes = 4096;
+constexpr size_t kTileBytes = (size_t)kTile * kTileStride * 4;
+constexpr size_t kMatBytes = (size_t)kD * 4 * kPadQ * 4;
+
+// dst[r][q][k] = transpose ? src[32q + k][r] : src[r][32q + k]   (src row-major d x d)
+__device__ void stage_matrix(const float* __restrict__ src, float* dst, bool transpose) {
+  for (int e = threadIdx.x; e < kD * kD; e += blockDim.x) {
+    const int i = e / kD, j = e % kD;  // src[i][j], coalesced read
+    const float v = __ldg(src + e);
+    const int r = transpose ? j : i;
+    const int c = transpose ? i : j;
+    dst[(r * 4 + (c >> 5)) * kPadQ + (c & 31)] = v;
+  }
+}
+
+// out[k] = sum_r Mp[r][q][k] * vin[r]  for the 32 outputs of quarter q.
+__device__ __forceinline__ void matvec_padded(const float* Mp, const float* vin, int q, float (&out)[32]) {
+#pragma unroll
+  for (int k = 0; k < 32; ++k) out[k] = 0.0f;
+#pragma unroll 2
+  for (int r = 0; r < kD; ++r) {
+    const float v = vin[r];
+    const float4* row = reinterpret_cast<const float4*>(Mp + (r * 4 + q) * kPadQ);
+#pragma unroll
+    for (int k4 = 0; k4 < 8; ++k4) {
+      const float4 m = row[k4];
+      out[4 * k4] = fmaf(m.x, v, out[4 * k4]);
+      out[4 * k4 + 1] = fmaf(m.y, v, out[4 * k4 + 1]);
+      out[4 * k4 + 2] = fmaf(m.z, v, out[4 * k4 + 2]);
+      out[4 * k4 + 3] = fmaf(m.w, v, out[4 * k4 + 3]);
+    }
+  }
+}
+
+__device__ __forceinline__ float flip_sign(float v, uint32_t word, int bit) {
+  return __uint_as_float(__float_as_uint(v) ^ ((word << (31 - bit)) & 0x80000000u));
+}
+
+template <int BITS, typename TIn, int MODE, bool QJL>
+__global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  constexpr int H = 1 << (BITS - 1);
+  constexpr int R = 16 * BITS;  // record bytes
+  float* mag2 = reinterpret_cast<float*>(smem_raw);              // [H][32]
+  float* ctab = mag2 + 8 * 32;                                   // [2H][32]
+  uint32_t* signw = reinterpret_cast<uint32_t*>(ctab + 16 * 32);  // [4]
+  float* tile = reinterpret_cast<float*>(smem_raw + kTableBytes);
+  float* matP = reinterpret_cast<float*>(smem_raw + kTableBytes + kTileBytes);
+  float* matS = reinterpret_cast<float*>(smem_raw + kTableBytes + kTileBytes + (MODE == MODE_DENSE ? kMatBytes : 0));
+
+  const int tid = threadIdx.x, lane = tid & 31, q = tid & 3, vl = tid >> 2;
+  for (int i = tid; i < H * 32; i += kThreads) {
+    const float c = a.cb.c[H + i / 32];
+    mag2[i] = c * c;
+  }
+  if (QJL)
+    for (int i = tid; i < 2 * H * 32; i += kThreads) ctab[i] = a.cb.c[i / 32];
+  if (MODE == MODE_HADAMARD && tid < 32) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t m = __ballot_sync(0xffffffffu, __ldg(a.rot + 32 * k + lane) < 0.0f);
+      if (lane == 0) signw[k] = m;
+    }
+  }
+  if (MODE == MODE_DENSE) stage_matrix(a.rot, matP, /*transpose=*/true);  // out = Pi x
+  if (QJL) stage_matrix(a.qjl, matS, /*transpose=*/true);                 // out = S r
+  __syncthreads();
+  const uint32_t sw = (MODE == MODE_HADAMARD) ? signw[q] : 0u;
+  const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
+
+  const int64_t n_tiles = (a.n_vec + kTile - 1) / kTile;
+  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const int64_t vec_raw = t * kTile + vl;
+    const bool valid = vec_raw < a.n_vec;
+    const int64_t vec = valid ? vec_raw : (a.n_vec - 1);
+
+    float x[32];  // becomes Pi x (full scale) for the quad's 32 coordinates
+    float n;
+    if constexpr (MODE == MODE_GIVEN_Y) {
+      load32<float>(a.y + vec * kD + 32 * q, x);
+      n = __ldg(a.norms + vec);
+    } else {
+      load32<TIn>(reinterpret_cast<const TIn*>(a.x) + vec * kD + 32 * q, x);
+      float ss = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ss = fmaf(x[i], x[i], ss);
+      n = sqrtf(quad_sum(ss));
+      if constexpr (MODE == MODE_HADAMARD) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = flip_sign(x[i], sw, i);
+        fwht128_quad(x, q);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] *= inv_sqrt_d;
+      } else {
+        __syncthreads();  // previous iteration is done with the tile
+#pragma unroll
+        for (int i = 0; i < 32; ++i) tile[vl * kTileStride + 32 * q + i] = x[i];
+        __syncthreads();
+        matvec_padded(matP, tile + vl * kTileStride, q, x);
+      }
+    }
+    // y = (Pi x) / n; MODE_GIVEN_Y already holds y and uses it as is.
+    const float inv_n = (MODE == MODE_GIVEN_Y) ? 1.0f : (n > 0.0f ? 1.0f / n : 0.0f);
+
+    uint32_t code[32];
+    float c2 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float y = (MODE == MODE_GIVEN_Y) ? x[i] : x[i] * inv_n;
+      int mag;
+      code[i] = quantize_coord<BITS>(y, a.cb, &mag);
+      c2 += mag2[mag * 32 + lane];
+    }
+    c2 = quad_sum(c2);
+    float gamma;
+    if (a.norm_mode == TQ_NORM_RAW) gamma = n;
+    else gamma = (n > 0.0f && c2 > 0.0f) ? n / sqrtf(c2) : 0.0f;
+
+    uint32_t sbits = 0u;
+    float rho = 0.0f;
+    if constexpr (QJL) {
+      float rr = 0.0f;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float r = x[i] - gamma * ctab[code[i] * 32 + lane];
+        rr = fmaf(r, r, rr);
+        tile[vl * kTileStride + 32 * q + i] = r;
+      }
+      rho = sqrtf(quad_sum(rr));
+      __syncthreads();
+      float z[32];
+      matvec_padded(matS, tile + vl * kTileStride, q, z);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sbits |= (z[i] >= 0.0f ? 1u : 0u) << i;
+    }
+
+    const int64_t tok = vec / a.H;
+    const int head = (int)(vec - tok * a.H);
+    const int64_t slot = __ldg(a.slots + tok);
+    if (valid && slot >= a.max_slot) {
+      if (q == 0) flag_status(a.status, TQ_DEV_BAD_SLOT);
+    } else if (valid && slot >= 0) {
+      const int64_t blk = slot >> 4;
+      const int off = (int)(slot & 15);
+      uint8_t* page = a.pool + (blk * a.H + head) * (int64_t)a.page_bytes;
+      uint32_t w[BITS];
+      pack32<BITS>(code, w);
+      uint8_t* rec = page + off * R;
+      if constexpr (BITS == 4) {
+        *reinterpret_cast<uint4*>(rec + 16 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else if constexpr (BITS == 2) {
+        *reinterpret_cast<uint2*>(rec + 8 * q) = make_uint2(w[0], w[1]);
+      } else {
+        uint32_t* r32 = reinterpret_cast<uint32_t*>(rec + 12 * q);
+        r32[0] = w[0]; r32[1] = w[1]; r32[2] = w[2];
+      }
+      if (q == 0) *reinterpret_cast<float*>(page + 16 * R + 4 * off) = gamma;
+      if constexpr (QJL) {
+        *reinterpret_cast<uint32_t*>(page + 16 * R + 64 + 16 * off + 4 * q) = sbits;
+        if (q == 0) *reinterpret_cast<float*>(page + 16 * R + 64 + 256 + 4 * off) = rho;
+      }
+    }
+  }
+}
+
+// bf16 layers: the append is a paged copy with rounding to bf16.
+template <typename TIn>
+__global__ void __launch_bounds__(256) k_append_bf16(const TIn* __restrict__ x, const int64_t* __restrict__ slots,
+                                                     int64_t n_vec, int H, int64_t max_slot, uint8_t* pool,
+                                                     unsigned* status) {
+  const int64_t n_chunks = n_vec * 16;  // 8 elements per chunk
+  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n_chunks; c += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t vec = c >> 4;
+    const int part = (int)(c & 15);
+    const int64_t tok = vec / H;
+    const int head = (int)(vec - tok * H);
+    const int64_t slot = __ldg(slots + tok);
+    if (slot < 0) continue;
+    if (slot >= max_slot) {
+      if (part == 0) flag_status(status, TQ_DEV_BAD_SLOT);
+      continue;
+    }
+    const TIn* src = x + vec * kD + part * 8;
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __nv_bfloat16 lo = __float2bfloat16_rn(load_elem<TIn>(src + 2 * k));
+      const __nv_bfloat16 hi = __float2bfloat16_rn(load_elem<TIn>(src + 2 * k + 1));
+      w[k] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+    }
+    uint8_t* page = pool + ((slot >> 4) * H + head) * (int64_t)(kBlock * kD * 2);
+    *reinterpret_cast<uint4*>(page + (slot & 15) * (kD * 2) + part * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Dequantize: x_hat = gamma Pi^T c[idx] (rotated-domain values, then the inverse rotation).
+template <int BITS, typename TOut, bool DENSE>
+__global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t* __restrict__ pool, int page_bytes, int H,
+                                                    int64_t max_slot, const int64_t* __restrict__ slots, int64_t n_vec,
+                                                    const float* __restrict__ rot, Codebook cb, TOut* out,
+                                                    unsigned* status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  constexpr int R = 16 * BITS;
+  uint32_t* signw = reinterpret_cast<uint32_t*>(smem_raw);
+  float* ctab = reinterpret_cast<float*>(smem_raw + 16);  // [16][32]
+  float* tile = reinterpret_cast<float*>(smem_raw + kTableBytes);
+  float* matP = reinterpret_cast<float*>(smem_raw + kTableBytes + kTileBytes);
+  const int tid = threadIdx.x, lane = tid & 31, q = tid & 3, vl = tid >> 2;
+  for (int i = tid; i < 16 * 32; i += kThreads) ctab[i] = cb.c[(i / 32) & ((1 << BITS) - 1)];
+  if (!DENSE && tid < 32) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t m = __ballot_sync(0xffffffffu, __ldg(rot + 32 * k + lane) < 0.0f);
+      if (lane == 0) signw[k] = m;
+    }
+  }
+  if (DENSE) stage_matrix(rot, matP, /*transpose=*/false);  // out = Pi^T v
+  __syncthreads();
+  const uint32_t sw = DENSE ? 0u : signw[q];
+  const int64_t n_tiles = (n_vec + kTile - 1) / kTile;
+  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const int64_t vec_raw = t * kTile + vl;
+    const bool valid = vec_raw < n_vec;
+    const int64_t vec = valid ? vec_raw : (n_vec - 1);
+    const int64_t tok = vec / H;
+    const int head = (int)(vec - tok * H);
+    const int64_t slot = __ldg(slots + tok);
+    const bool ok = slot >= 0 && slot < max_slot;
+    if (valid && slot >= max_slot && q == 0) flag_status(status, TQ_DEV_BAD_SLOT);
+    float v[32];
+    if (ok) {
+      const uint8_t* page = pool + ((slot >> 4) * H + head) * (int64_t)page_bytes;
+      const uint32_t* rec = reinterpret_cast<const uint32_t*>(page + (slot & 15) * R + 4 * BITS * q);
+      uint32_t w[BITS + 1];
+#pragma unroll
+      for (int i = 0; i < BITS; ++i) w[i] = rec[i];
+      w[BITS] = 0u;
+      const float gamma = *reinterpret_cast<const float*>(page + 16 * R + 4 * (slot & 15));
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int bit = BITS * k;
+        uint32_t c = w[bit >> 5] >> (bit & 31);
+        if ((bit & 31) + BITS > 32) c |= w[(bit >> 5) + 1] << (32 - (bit & 31));
+        c &= (1u << BITS) - 1u;
+        v[k] = gamma * ctab[c * 32 + lane];
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = 0.0f;
+    }
+    if constexpr (DENSE) {
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) tile[vl * kTileStride + 32 * q + i] = v[i];
+      __syncthreads();
+      matvec_padded(matP, tile + vl * kTileStride, q, v);
+    } else {
+      fwht128_quad(v, q);  // Pi^T v = D H v / sqrt(d)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = flip_sign(v[i] * 0.08838834764831845f, sw, i);
+    }
+    if (valid) {
+      TOut* o = out + vec * kD + 32 * q;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) store_elem<TOut>(o + i, v[i]);
+    }
+  }
+}
+
+template <typename TOut>
+__global__ void __launch_bounds__(256) k_dequant_bf16(const uint8_t* __restrict__ pool, int H, int64_t max_slot,
+                                                      const int64_t* __restrict__ slots, int64_t n_vec, TOut* out,
+                                                      unsigned* status) {
+  const int64_t n = n_vec * kD;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t vec = e / kD;
+    const int j = (int)(e - vec * kD);
+    const int64_t tok = vec / H;
+    const int head = (int)(vec - tok * H);
+    const int64_t slot = __ldg(slots + tok);
+    float v = 0.0f;
+    if (slot >= 0 && slot < max_slot) {
+      const uint16_t* page =
+          reinterpret_cast<const uint16_t*>(pool + ((slot >> 4) * H + head) * (int64_t)(kBlock * kD * 2));
+      v = bf16_bits_to_float(page[(slot & 15) * kD + j]);
+    } else if (slot >= max_slot && j == 0) {
+      flag_status(status, TQ_DEV_BAD_SLOT);
+    }
+    store_elem<TOut>(out + e, v);
+  }
+}
+
+// ----------------------------------------------------------------- launchers
+
+Codebook codebook_of(const tq_cache_desc& d, int which) {
+  Codebook cb;
+  const float* c = which == 0 ? d.centroids_k : d.centroids_v;
+  const float* b = which == 0 ? d.boundaries_k : d.boundaries_v;
+  for (int i = 0; i < 16; ++i) cb.c[i] = c[i];
+  for (int i = 0; i < 15; ++i) cb.b[i] = b[i];
+  return cb;
+}
+
+template <int BITS, typename TIn, int MODE, bool QJL>
+static cudaError_t run_quantize(const QuantArgs& a, int num_sms, cudaStream_t st) {
+  auto kern = k_quantize<BITS, TIn, MODE, QJL>;
+  size_t smem = kTableBytes;
+  if (MODE == MODE_DENSE || QJL) smem += kTileBytes;
+  if (MODE == MODE_DENSE) smem += kMatBytes;
+  if (QJL) smem += kMatBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = (a.n_vec + kTile - 1) / kTile;
+  const int per_sm = (MODE == MODE_DENSE || QJL) ? 1 : 8;
+  int64_t grid = tiles < (int64_t)num_sms * per_sm ? tiles : (int64_t)num_sms * per_sm;
+  if (grid < 1) grid = 1;
+  kern<<<(unsigned)grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int BITS, typename TIn>
+static cudaError_t dispatch_mode(const QuantArgs& a, int mode, bool qjl, int num_sms, cudaStream_t st) {
+  if (mode == MODE_GIVEN_Y) return run_quantize<BITS, float, MODE_GIVEN_Y, false>(a, num_sms, st);
+  if (mode == MODE_HADAMARD)
+    return qjl ? run_quantize<BITS, TIn, MODE_HADAMARD, true>(a, num_sms, st)
+               : run_quantize<BITS, TIn, MODE_HADAMARD, false>(a, num_sms, st);
+  return qjl ? run_quantize<BITS, TIn, MODE_DENSE, true>(a, num_sms, st)
+             : run_quantize<BITS, TIn, MODE_DENSE, false>(a, num_sms, st);
+}
+
+cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, int in_dtype, const float* y,
+                            const float* norms, const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms,
+                            cudaStream_t st) {
+  if (n_tok <= 0) return cudaSuccess;
+  const int64_t n_vec = n_tok * d.num_kv_heads;
+  const int64_t max_slot = d.num_blocks * kBlock;
+  uint8_t* pool = reinterpret_cast<uint8_t*>(which == 0 ? d.k_cache : d.v_cache);
+  if (d.fmt.kv_format == TQ_KV_BF16) {
+    int64_t chunks = n_vec * 16;
+    int64_t grid = (chunks + 255) / 256;
+    if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
+    if (in_dtype == TQ_F32)
+      k_append_bf16<float><<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const float*>(x), slots, n_vec,
+                                                           d.num_kv_heads, max_slot, pool, status);
+    else
+      k_append_bf16<__nv_bfloat16><<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), slots,
+                                                                   n_vec, d.num_kv_heads, max_slot, pool, status);
+    return cudaGetLastError();
+  }
+  QuantArgs a;
+  a.x = x;
+  a.y = y;
+  a.norms = norms;
+  a.slots = slots;
+  a.n_vec = n_vec;
+  a.H = d.num_kv_heads;
+  a.max_slot = max_slot;
+  a.pool = pool;
+  a.page_bytes = (int)page_bytes_of(d, which);
+  a.rot = d.rotation;
+  a.qjl = d.qjl_proj;
+  a.cb = codebook_of(d, which);
+  a.norm_mode = d.fmt.norm_mode;
+  a.status = status;
+  const int bits = which == 0 ? d.fmt.bits_k : d.fmt.bits_v;
+  const bool qjl = which == 0 && d.fmt.qjl_k && y == nullptr;
+  const int mode = y ? MODE_GIVEN_Y : (d.fmt.rot_kind == TQ_ROT_DENSE ? MODE_DENSE : MODE_HADAMARD);
+  const bool f32 = in_dtype == TQ_F32;
+  switch (bits) {
+    case 2:
+      return f32 ? dispatch_mode<2, float>(a, mode, qjl, num_sms, st)
+                 : dispatch_mode<2, __nv_bfloat16>(a, mode, qjl, num_sms, st);
+    case 3:
+      return f32 ? dispatch_mode<3, float>(a, mode, qjl, num_sms, st)
+                 : dispatch_mode<3, __nv_bfloat16>(a, mode, qjl, num_sms, st);
+    default:
+      return f32 ? dispatch_mode<4, float>(a, mode, qjl, num_sms, st)
+                 : dispatch_mode<4, __nv_bfloat16>(a, mode, qjl, num_sms, st);
+  }
+}
+
+template <int BITS, typename TOut, bool DENSE>
+static cudaError_t run_dequant(const tq_cache_desc& d, int which, const int64_t* slots, int64_t n_vec, void* out,
+                               unsigned* status, int num_sms, cudaStream_t st) {
+  auto kern = k_dequant<BITS, TOut, DENSE>;
+  size_t smem = kTableBytes + (DENSE ? kTileBytes + kMatBytes : 0);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = (n_vec + kTile - 1) / kTile;
+  int64_t grid = tiles < (int64_t)num_sms * 4 ? tiles : (int64_t)num_sms * 4;
+  if (grid < 1) grid = 1;
+  const uint8_t* pool = reinterpret_cast<const uint8_t*>(which == 0 ? d.k_cache : d.v_cache);
+  kern<<<(unsigned)grid, kThreads, smem, st>>>(pool, (int)page_bytes_of(d, which), d.num_kv_heads,
+                                              d.num_blocks * kBlock, slots, n_vec, d.rotation, codebook_of(d, which),
+                                              reinterpret_cast<TOut*>(out), status);
+  return cudaGetLastError();
+}
+
+template <typename TOut>
+static cudaError_t dequant_bits(const tq_cache_desc& d, int which, const int64_t* slots, int64_t n_vec, void* out,
+                                unsigned* status, int num_sms, cudaStream_t st) {
+  const int bits = which == 0 ? d.fmt.bits_k : d.fmt.bits_v;
+  const bool dense = d.fmt.rot_kind == TQ_ROT_DENSE;
+  switch (bits) {
+    case 2:
+      return dense ? run_dequant<2, TOut, true>(d, which, slots, n_vec, out, status, num_sms, st)
+                   : run_dequant<2, TOut, false>(d, which, slots, n_vec, out, status, num_sms, st);
+    case 3:
+      return dense ? run_dequant<3, TOut, true>(d, which, slots, n_vec, out, status, num_sms, st)
+                   : run_dequant<3, TOut, false>(d, which, slots, n_vec, out, status, num_sms, st);
+    default:
+      return dense ? run_dequant<4, TOut, true>(d, which, slots, n_vec, out, status, num_sms, st)
+                   : run_dequant<4, TOut, false>(d, which, slots, n_vec, out, status, num_sms, st);
+  }
+}
+
+cudaError_t launch_dequant(const tq_cache_desc& d, int which, const int64_t* slots, int64_t n, void* out,
+                           int out_dtype, unsigned* status, int num_sms, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t n_vec = n * d.num_kv_heads;
+  if (d.fmt.kv_format == TQ_KV_BF16) {
+    const uint8_t* pool = reinterpret_cast<const uint8_t*>(which == 0 ? d.k_cache : d.v_cache);
+    int64_t grid = (n_vec * kD + 255) / 256;
+    if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
+    if (out_dtype == TQ_F32)
+      k_dequant_bf16<float><<<(unsigned)grid, 256, 0, st>>>(pool, d.num_kv_heads, d.num_blocks * kBlock, slots, n_vec,
+                                                             reinterpret_cast<float*>(out), status);
+    else
+      k_dequant_bf16<__nv_bfloat16><<<(unsigned)grid, 256, 0, st>>>(pool, d.num_kv_heads, d.num_blocks * kBlock,
+                                                                     slots, n_vec,
+                                                                     reinterpret_cast<__nv_bfloat16*>(out), status);
+    return cudaGetLastError();
+  }
+  return out_dtype == TQ_F32 ? dequant_bits<float>(d, which, slots, n_vec, out, status, num_sms, st)
+                             : dequant_bits<__nv_bfloat16>(d, which, slots, n_vec, out, status, num_sms, st);
+}
+
+}  // namespace tq
