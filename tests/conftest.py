@@ -16,3 +16,22 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def root():
     return ROOT
+
+
+@pytest.fixture(scope="session")
+def tqlib():
+    """Builds (if needed) and loads libtq.so; the package itself never falls back."""
+    from turboquant_quantized_kv_gb300 import build as tqbuild
+    tqbuild.build()
+    import turboquant_quantized_kv_gb300 as tq
+    tq.lib()
+    return tq
+
+
+@pytest.fixture(scope="session")
+def cuda(tqlib):
+    import torch
+    if not torch.cuda.is_available():
+        raise RuntimeError("GPU tests need a CUDA device")
+    torch.cuda.init()
+    return torch

@@ -1,0 +1,214 @@
+// extern "C" entry points of libtq: host-side validation, the sticky device
+// status word and dispatch to the kernels.  The specification of every call
+// (arguments, layouts, ownership, errors) is in include/tq.h.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+// Sticky status bits set by kernels (one word per device that loads the library).
+static __device__ unsigned g_tq_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  unsigned* status = nullptr;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+tq_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(TQ_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(TQ_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    e = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(TQ_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&di.status), g_tq_status);
+    if (e != cudaSuccess) return fail(TQ_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+    di.ready = true;
+  }
+  *out = di;
+  return TQ_OK;
+}
+
+tq_status cuda_result(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(TQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return TQ_OK;
+}
+
+bool valid_dtype(int t) { return t == TQ_F32 || t == TQ_BF16; }
+
+}  // namespace
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" {
+
+tq_status tq_quantize_append(const tq_cache_desc* desc, const void* k, const void* v, int in_dtype,
+                             const int64_t* slot_mapping, int64_t n_tokens, void* stream) {
+  clear_error();
+  tq_status s = check_desc(desc);
+  if (s != TQ_OK) return s;
+  if (!valid_dtype(in_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: in_dtype %d", in_dtype);
+  if (n_tokens < 0) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: n_tokens < 0");
+  if (n_tokens == 0) return TQ_OK;
+  if (!slot_mapping) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: null slot_mapping");
+  if (!k && !v) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: both k and v are null");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
+    return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: k/v must be 16-byte aligned");
+  DeviceInfo di;
+  if ((s = device_info(&di)) != TQ_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (k) {
+    s = cuda_result(launch_quantize(*desc, 0, k, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
+                                    di.num_sms, st), "quantize K");
+    if (s != TQ_OK) return s;
+  }
+  if (v) {
+    s = cuda_result(launch_quantize(*desc, 1, v, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
+                                    di.num_sms, st), "quantize V");
+    if (s != TQ_OK) return s;
+  }
+  return TQ_OK;
+}
+
+tq_status tq_quantize_rotated(const tq_cache_desc* desc, int which, const float* y, const float* norms,
+                              const int64_t* slot_mapping, int64_t n_tokens, void* stream) {
+  clear_error();
+  tq_status s = check_desc(desc);
+  if (s != TQ_OK) return s;
+  if (desc->fmt.kv_format != TQ_KV_PACKED) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_rotated: packed layers only");
+  if (which != 0 && which != 1) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_rotated: which %d", which);
+  if (n_tokens < 0) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_rotated: n_tokens < 0");
+  if (n_tokens == 0) return TQ_OK;
+  if (!y || !norms || !slot_mapping) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_rotated: null pointer");
+  if (reinterpret_cast<uintptr_t>(y) & 15) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_rotated: y must be 16-byte aligned");
+  DeviceInfo di;
+  if ((s = device_info(&di)) != TQ_OK) return s;
+  return cuda_result(launch_quantize(*desc, which, nullptr, TQ_F32, y, norms, slot_mapping, n_tokens, di.status,
+                                     di.num_sms, reinterpret_cast<cudaStream_t>(stream)),
+                     "quantize (rotated input)");
+}
+
+int tq_auto_splits(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks_per_seq) {
+  clear_error();
+  if (check_desc(desc) != TQ_OK || batch < 1 || num_q_heads < 1 || max_blocks_per_seq < 1) return 0;
+  DeviceInfo di;
+  if (device_info(&di) != TQ_OK) return 0;
+  const int g = num_q_heads / desc->num_kv_heads;
+  const int groups = (g + TQ_MAX_GROUP - 1) / TQ_MAX_GROUP;
+  return auto_splits(di.num_sms, batch, desc->num_kv_heads * groups, max_blocks_per_seq);
+}
+
+static int resolve_splits(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks, int num_splits) {
+  if (num_splits > 0) return num_splits < max_blocks ? (num_splits > 256 ? 256 : num_splits) : (max_blocks > 256 ? 256 : max_blocks);
+  return tq_auto_splits(desc, batch, num_q_heads, max_blocks);
+}
+
+size_t tq_workspace_bytes(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks_per_seq,
+                          int num_splits) {
+  clear_error();
+  if (check_desc(desc) != TQ_OK || batch < 1 || num_q_heads < 1 || max_blocks_per_seq < 1 || num_splits < 0) return 0;
+  const int splits = resolve_splits(desc, batch, num_q_heads, max_blocks_per_seq, num_splits);
+  if (splits < 1) return 0;
+  const bool qjl = desc->fmt.kv_format == TQ_KV_PACKED && desc->fmt.qjl_k;
+  return decode_workspace(batch, num_q_heads, splits, desc->head_dim, qjl).total;
+}
+
+tq_status tq_decode_attention(const tq_cache_desc* desc, const void* q, int q_dtype, int batch, int num_q_heads,
+                              const int32_t* block_table, int max_blocks_per_seq, const int32_t* context_lens,
+                              float sm_scale, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                              int num_splits, void* stream) {
+  clear_error();
+  tq_status s = check_desc(desc);
+  if (s != TQ_OK) return s;
+  if (batch < 0) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: batch < 0");
+  if (batch == 0) return TQ_OK;
+  if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype))
+    return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: q_dtype %d / out_dtype %d", q_dtype, out_dtype);
+  if (num_q_heads < 1 || num_q_heads % desc->num_kv_heads != 0)
+    return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: num_q_heads %d not a multiple of num_kv_heads %d",
+                num_q_heads, desc->num_kv_heads);
+  if (!q || !block_table || !context_lens || !out)
+    return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: null q/block_table/context_lens/out");
+  if (max_blocks_per_seq < 1) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: max_blocks_per_seq < 1");
+  if (num_splits < 0) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: num_splits < 0");
+  if (!(sm_scale == sm_scale)) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: sm_scale is NaN");
+  if (reinterpret_cast<uintptr_t>(q) & 15) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: q must be 16-byte aligned");
+  DeviceInfo di;
+  if ((s = device_info(&di)) != TQ_OK) return s;
+  const int splits = resolve_splits(desc, batch, num_q_heads, max_blocks_per_seq, num_splits);
+  if (splits < 1) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: could not choose a split count");
+  const bool qjl = desc->fmt.kv_format == TQ_KV_PACKED && desc->fmt.qjl_k;
+  const size_t need = decode_workspace(batch, num_q_heads, splits, desc->head_dim, qjl).total;
+  if (!workspace || workspace_bytes < need)
+    return fail(TQ_ERR_WORKSPACE, "tq_decode_attention: workspace %zu bytes, need %zu", workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: workspace must be 256-byte aligned");
+  DecodeCall c;
+  c.desc = desc;
+  c.q = q;
+  c.q_dtype = q_dtype;
+  c.batch = batch;
+  c.num_q_heads = num_q_heads;
+  c.block_table = block_table;
+  c.max_blocks = max_blocks_per_seq;
+  c.ctx_lens = context_lens;
+  c.sm_scale = sm_scale;
+  c.out = out;
+  c.out_dtype = out_dtype;
+  c.workspace = reinterpret_cast<uint8_t*>(workspace);
+  c.splits = splits;
+  c.status = di.status;
+  return cuda_result(launch_decode(c, reinterpret_cast<cudaStream_t>(stream)), "decode attention");
+}
+
+tq_status tq_dequantize(const tq_cache_desc* desc, int which, const int64_t* slots, int64_t n, void* out,
+                        int out_dtype, void* stream) {
+  clear_error();
+  tq_status s = check_desc(desc);
+  if (s != TQ_OK) return s;
+  if (which != 0 && which != 1) return fail(TQ_ERR_INVALID_ARG, "tq_dequantize: which %d", which);
+  if (!valid_dtype(out_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_dequantize: out_dtype %d", out_dtype);
+  if (n < 0) return fail(TQ_ERR_INVALID_ARG, "tq_dequantize: n < 0");
+  if (n == 0) return TQ_OK;
+  if (!slots || !out) return fail(TQ_ERR_INVALID_ARG, "tq_dequantize: null slots/out");
+  DeviceInfo di;
+  if ((s = device_info(&di)) != TQ_OK) return s;
+  return cuda_result(launch_dequant(*desc, which, slots, n, out, out_dtype, di.status, di.num_sms,
+                                    reinterpret_cast<cudaStream_t>(stream)),
+                     "dequantize");
+}
+
+tq_status tq_get_device_status(void* stream, int32_t* code) {
+  clear_error();
+  if (!code) return fail(TQ_ERR_INVALID_ARG, "tq_get_device_status: null code");
+  DeviceInfo di;
+  tq_status s = device_info(&di);
+  if (s != TQ_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  if ((s = cuda_result(cudaMemcpyAsync(&v, di.status, sizeof(v), cudaMemcpyDeviceToHost, st), "read status")) != TQ_OK)
+    return s;
+  if ((s = cuda_result(cudaStreamSynchronize(st), "synchronize")) != TQ_OK) return s;
+  if ((s = cuda_result(cudaMemsetAsync(di.status, 0, sizeof(unsigned), st), "clear status")) != TQ_OK) return s;
+  if ((s = cuda_result(cudaStreamSynchronize(st), "synchronize")) != TQ_OK) return s;
+  *code = (int32_t)v;
+  return TQ_OK;
+}
+
+}  // extern "C"

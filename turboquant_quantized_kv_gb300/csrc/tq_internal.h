@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <string>
 
+#include <cuda_runtime_api.h>
+
 #include "tq.h"
 
 namespace tq {
@@ -30,5 +32,31 @@ struct DecodeWorkspace {
   size_t total;
 };
 DecodeWorkspace decode_workspace(int batch, int num_q_heads, int splits, int head_dim, bool qjl);
+
+// One validated decode call, as the launcher sees it.
+struct DecodeCall {
+  const tq_cache_desc* desc;
+  const void* q;
+  int q_dtype;
+  int batch, num_q_heads;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* ctx_lens;
+  float sm_scale;
+  void* out;
+  int out_dtype;
+  uint8_t* workspace;
+  int splits;
+  unsigned* status;
+};
+
+// Kernel launchers (CUDA translation units).  All enqueue on `st` and return
+// the launch error, if any.
+cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, int in_dtype, const float* y,
+                            const float* norms, const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms,
+                            cudaStream_t st);
+cudaError_t launch_dequant(const tq_cache_desc& d, int which, const int64_t* slots, int64_t n, void* out,
+                           int out_dtype, unsigned* status, int num_sms, cudaStream_t st);
+cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st);
 
 }  // namespace tq
