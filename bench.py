@@ -1,0 +1,448 @@
+"""Benchmark: decode attention on the packed TurboQuant KV cache (+ quantize-append).
+
+Workload (one step): Llama-3-8B-shaped GQA decode -- batch 16, 32 query / 8 KV
+heads, head_dim 128, 32 layers, context 8192 (+1 token per step), bf16 K/V with
+per-(head, channel) lognormal(0, 1) scales, 4-bit keys and values with fp32
+norms, Hadamard rotation per layer, paged 16-token blocks under a shuffled block
+table.  A step appends one new token per sequence to every layer (quantize-
+append) and runs decode attention over every layer.  All inputs are synthetic
+and already resident in HBM; one step reads ~4.6 GB of packed cache, more
+than L2, so no flush is needed between steps.
+
+Reported: value = packed K/V bytes read by decode per step / step time (GB/s);
+roofline for the decode call; quantize-append vectors/s from the prefill;
+e2e through the public API with host buffers; the oracle's CPU throughput.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+B, HQ, HKV, D, T0, LAYERS = 16, 32, 8, 128, 8192, 32
+BLOCK = 16
+BYTES_PER_TOKEN_HEAD = 2 * (D * 4 // 8 + 4)  # 4-bit K and V records + two fp32 norms = 136 B
+APPEND_BYTES_PER_VECTOR = 2 * D + (D * 4 // 8 + 4)  # bf16 read + record written
+METRIC = "decode-attn packed-KV GB/s"
+WORKLOAD = "llama3-8b-shaped GQA decode, B16 Hq32 Hkv8 d128 ctx8192, 32 layers, 4-bit K/V, Hadamard"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "tq_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- GPU setup
+
+def setup(torch, tq, steps_total, dev):
+    """Per-layer caches filled with 8192 prefilled tokens; returns state dict."""
+    mb = (T0 + steps_total + BLOCK - 1) // BLOCK + 1
+    nb = B * mb
+    import numpy as np
+    import workloads
+    bt_np, _ = workloads.shuffled_block_table(1234, B, mb, num_blocks=nb)
+    bt = torch.from_numpy(bt_np).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(2024)
+    sk = torch.exp(torch.randn(HKV, D, generator=gen, device=dev))
+    sv = torch.exp(torch.randn(HKV, D, generator=gen, device=dev))
+    kpre = (torch.randn(B * T0, HKV, D, generator=gen, device=dev) * sk).to(torch.bfloat16)
+    vpre = (torch.randn(B * T0, HKV, D, generator=gen, device=dev) * sv).to(torch.bfloat16)
+    slots_pre = torch.from_numpy(workloads.prefill_slots(bt_np, T0)).to(dev)
+    layers = [tq.Layer(nb, HKV, bits_k=4, bits_v=4, seed=0, layer=l, device=dev) for l in range(LAYERS)]
+    # prefill (timed: quantize-append throughput on 2 x 1,048,576 vectors per layer)
+    for l in range(2):
+        layers[l].append(kpre, vpre, slots_pre)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(LAYERS)]
+    for l in range(LAYERS):
+        ev[l][0].record()
+        layers[l].append(kpre, vpre, slots_pre)
+        ev[l][1].record()
+    torch.cuda.synchronize()
+    append_ms = [a.elapsed_time(b) for a, b in ev]
+    n_vec = 2 * B * T0 * HKV
+    del kpre, vpre
+    q = [torch.randn(B, HQ, D, generator=gen, device=dev).to(torch.bfloat16) for _ in range(LAYERS)]
+    knew = [torch.randn(B, HKV, D, generator=gen, device=dev).to(torch.bfloat16) for _ in range(LAYERS)]
+    vnew = [torch.randn(B, HKV, D, generator=gen, device=dev).to(torch.bfloat16) for _ in range(LAYERS)]
+    out = [torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev) for _ in range(LAYERS)]
+    ctx = torch.full((B,), T0, dtype=torch.int32, device=dev)
+    slot_new = torch.empty(B, dtype=torch.int64, device=dev)
+    ws_bytes = layers[0].workspace_bytes(B, HQ, mb)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    return dict(layers=layers, bt=bt, bt_np=bt_np, mb=mb, nb=nb, q=q, knew=knew, vnew=vnew, out=out, ctx=ctx,
+                slot_new=slot_new, ws=ws, append_ms=append_ms, append_vectors=n_vec)
+
+
+def step_prepare(torch, st):
+    """ctx += 1 is done after the step; the new token goes to position ctx."""
+    ctx64 = st["ctx"].to(torch.int64)
+    blk = torch.gather(st["bt"], 1, (ctx64 // BLOCK).unsqueeze(1)).squeeze(1).to(torch.int64)
+    st["slot_new"].copy_(blk * BLOCK + ctx64 % BLOCK)
+    st["ctx"].add_(1)
+
+
+def layer_append(st, l):
+    st["layers"][l].append(st["knew"][l], st["vnew"][l], st["slot_new"])
+
+
+def layer_decode(st, l):
+    st["layers"][l].decode(st["q"][l], st["bt"], st["ctx"], out=st["out"][l], workspace=st["ws"])
+
+
+def run_tq(args):
+    import numpy as np
+    import torch
+
+    import turboquant_quantized_kv_gb300 as tq
+    from turboquant_quantized_kv_gb300 import build as tqbuild
+
+    tqbuild.build()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    st = setup(torch, tq, args.warmup + 2 * args.steps + 4, dev)
+    stream = torch.cuda.current_stream()
+
+    # one graph per layer for append and for decode: replays are launch-cheap and
+    # events between them time the decode call of every layer inside the timed region
+    torch.cuda.synchronize()
+    for l in range(LAYERS):  # eager warm-up (module load, attributes) before capture
+        layer_decode(st, l)
+    torch.cuda.synchronize()
+    g_prep = torch.cuda.CUDAGraph()
+    g_app = [torch.cuda.CUDAGraph() for _ in range(LAYERS)]
+    g_dec = [torch.cuda.CUDAGraph() for _ in range(LAYERS)]
+    ctx_save = st["ctx"].clone()
+    with torch.cuda.graph(g_prep):
+        step_prepare(torch, st)
+    for l in range(LAYERS):
+        with torch.cuda.graph(g_app[l]):
+            layer_append(st, l)
+        with torch.cuda.graph(g_dec[l]):
+            layer_decode(st, l)
+    st["ctx"].copy_(ctx_save)
+    torch.cuda.synchronize()
+
+    def graph_step(dec_events=None):
+        g_prep.replay()
+        for l in range(LAYERS):
+            g_app[l].replay()
+            if dec_events is not None:
+                dec_events[l][0].record(stream)
+            g_dec[l].replay()
+            if dec_events is not None:
+                dec_events[l][1].record(stream)
+
+    for _ in range(args.warmup):
+        graph_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ctx_start = int(st["ctx"][0].item())
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(LAYERS)]
+           for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for s in range(args.steps):
+        graph_step(evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    dec_ms = [a.elapsed_time(b) for row in evs for a, b in row]
+    status = tq.get_device_status()
+    # algorithmic bytes: every decode call of the timed steps reads ctx tokens x H_kv
+    # records of 136 B (4-bit K + V + fp32 norms) per sequence, plus block table, q, out
+    bytes_steps = 0
+    bytes_per_call = []
+    for s in range(args.steps):
+        ctx_s = ctx_start + s + 1
+        per_call = B * HKV * ctx_s * BYTES_PER_TOKEN_HEAD + B * st["mb"] * 4 + 2 * B * HQ * D * 2
+        bytes_per_call.append(per_call)
+        bytes_steps += LAYERS * per_call
+    value = bytes_steps * world / (ms_total * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    dec_avg_ms = statistics.mean(dec_ms)
+    achieved = statistics.mean(bytes_per_call) / (dec_avg_ms * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            with open(tpath) as f:
+                tj = json.load(f)
+            traffic = tj.get("bytes_per_launch_full_size")
+        except Exception:
+            traffic = None
+    app_ms = statistics.median(st["append_ms"][2:])
+    app_vps = st["append_vectors"] / (app_ms * 1e-3)
+    app_gbs = app_vps * APPEND_BYTES_PER_VECTOR / 1e9
+
+    # end to end through the public API with host buffers (pinned), eager calls
+    e2e = run_e2e(torch, st, args, stream)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u4 codes + fp32 norms (bf16 q/out, fp16 MMA with fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D,
+                   "context": T0, "layers": LAYERS, "bits_k": 4, "bits_v": 4, "block_size": BLOCK,
+                   "l2": "inputs larger than L2 (~4.6 GB of packed cache per step)", "parallelism": "replicas"},
+        "roofline": {"kernel": "tq_decode_attention (rotate-q + split-K decode + combine)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind, "traffic": traffic},
+        "append": {"vectors_per_s": round(app_vps, 1), "gbs": round(app_gbs, 1), "frac": round(app_gbs / peak, 4),
+                   "vectors": st["append_vectors"], "bytes_per_vector": APPEND_BYTES_PER_VECTOR},
+        "e2e": e2e,
+        "gpu_launches": args.steps * (LAYERS * 5 + 4),
+        "clocks": clk,
+        "device_status": status,
+    }
+    if rank == 0 and args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(st, args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(torch, st, args, stream):
+    """Public API, host buffers: per step H2D of the new K/V tokens and queries of
+    every layer from pinned memory, append + decode per layer, D2H of all outputs."""
+    hk = [t.cpu().pin_memory() for t in st["knew"]]
+    hv = [t.cpu().pin_memory() for t in st["vnew"]]
+    hq = [t.cpu().pin_memory() for t in st["q"]]
+    ho = [torch.empty(B, HQ, D, dtype=torch.bfloat16).pin_memory() for _ in range(LAYERS)]
+    h2d = sum(t.numel() * t.element_size() for t in hk + hv + hq)
+    d2h = sum(t.numel() * t.element_size() for t in ho)
+
+    def step():
+        step_prepare(torch, st)
+        for l in range(LAYERS):
+            st["knew"][l].copy_(hk[l], non_blocking=True)
+            st["vnew"][l].copy_(hv[l], non_blocking=True)
+            st["q"][l].copy_(hq[l], non_blocking=True)
+            layer_append(st, l)
+            layer_decode(st, l)
+            ho[l].copy_(st["out"][l], non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    ctx_start = int(st["ctx"][0].item())
+    n = max(2, args.steps // 2)
+    t = time.perf_counter()
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t
+    nbytes = sum(LAYERS * B * HKV * (ctx_start + s + 1) * BYTES_PER_TOKEN_HEAD for s in range(n))
+    return {"value": round(nbytes / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": round(dt / n * 1e3, 4)}
+
+
+# ------------------------------------------------------------- oracle (CPU)
+
+def _oracle_unit(payload):
+    """One (sequence, KV head) unit of the oracle decode: unpack + exact attention."""
+    import numpy as np
+    from oracle import attention as oa, codebook as ocb, pack as opack, rotation as orot
+    kpages, vpages, q, layer_idx = payload
+    c4 = ocb.codebook_fp32(D, 4)[0].astype(np.float64)
+    pi = orot.hadamard_rotation_seeded(0, layer_idx, D)
+    kc, kg = opack.split_pages(kpages, D, 4)
+    vc, vg = opack.split_pages(vpages, D, 4)
+    khat = (c4[kc.reshape(-1, D)] * kg.reshape(-1)[:, None]) @ pi
+    vhat = (c4[vc.reshape(-1, D)] * vg.reshape(-1)[:, None]) @ pi
+    for h in range(q.shape[0]):
+        s = (khat @ q[h]) / math.sqrt(D)
+        oa.softmax_weights(s) @ vhat
+    return kpages.nbytes + vpages.nbytes
+
+
+def _oracle_payloads(n_units, rng_seed=0):
+    """Packed pages for n_units (sequence, KV head) units of 8192 tokens, made by the oracle."""
+    import numpy as np
+    import workloads
+    from oracle import codebook as ocb, pack as opack, quantize as oq, rotation as orot
+    c4, b4 = ocb.codebook_fp32(D, 4)
+    out = []
+    for u in range(n_units):
+        kb, vb = workloads.lognormal_channel_kv(rng_seed + u, T0, 1, D)
+        pi = orot.hadamard_rotation_seeded(0, u % LAYERS, D)
+        pages = []
+        for xb in (kb, vb):
+            idx, gamma, _ = oq.quantize(oq.bf16_bits_to_f64(xb[:, 0]), pi, c4, b4)
+            rec = opack.pack_records(idx, 4).reshape(T0 // BLOCK, BLOCK * 64)
+            g = gamma.astype("<f4").view(np.uint8).reshape(T0 // BLOCK, BLOCK * 4)
+            pages.append(np.concatenate([rec, g], axis=1))
+        q = oq.bf16_bits_to_f64(workloads.queries(rng_seed + u, 1, HQ // HKV, D))[0]
+        out.append((pages[0], pages[1], q, u % LAYERS))
+    return out
+
+
+def cpu_baseline(st, args):
+    """The oracle as it stands on the host cores, on a bounded sample (spawned pool)."""
+    import multiprocessing as mp
+    cores = min(os.cpu_count() or 1, 16)
+    n_units = cores * 2
+    payloads = _oracle_payloads(n_units)
+    ctxm = mp.get_context("spawn")
+    env_keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in env_keep:
+        os.environ[k] = "1"
+    try:
+        with ctxm.Pool(cores) as pool:
+            pool.map(_oracle_unit, payloads[:cores])  # warm the workers
+            t = time.perf_counter()
+            nbytes = sum(pool.map(_oracle_unit, payloads))
+            dt = time.perf_counter() - t
+    finally:
+        for k, v in env_keep.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d (sequence, KV head) units x 8192 tokens x 4 query heads of one layer each "
+                      "(packed by the oracle), unpack + exact fp64 attention; %d worker processes, 1 BLAS thread each"
+                      % (n_units, cores), "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import multiprocessing as mp
+    cores = min(os.cpu_count() or 1, 16)
+    per_step = cores
+    payloads = _oracle_payloads(per_step)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    ctxm = mp.get_context("spawn")
+    with ctxm.Pool(cores) as pool:
+        for _ in range(args.warmup):
+            pool.map(_oracle_unit, payloads)
+        t = time.perf_counter()
+        nbytes = 0
+        for _ in range(args.steps):
+            nbytes += sum(pool.map(_oracle_unit, payloads))
+        dt = time.perf_counter() - t
+    value = nbytes / dt / 1e9
+    sample = ("per step %d (sequence, KV head) units x 8192 tokens x 4 query heads (1/%d of one layer-step "
+              "of the workload), unpack + exact fp64 attention, %d processes" % (per_step, B * HKV // per_step
+                                                                               if per_step <= B * HKV else 1, cores))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D,
+                   "context": T0, "layers": LAYERS, "bits_k": 4, "bits_v": 4, "block_size": BLOCK},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle", "cores": cores,
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_tq(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+"""GPU parity of decode attention on the packed (and bf16) cache against the
+oracle's exact softmax attention over the GPU's own cache."""
+import math
+
+import numpy as np
+import pytest
+
+import workloads
+from oracle import attention as oa, quantize as oq
+from tests._gpu_util import D, max_rel_err, oracle_layer
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 2e-3
+TOL_BF16 = 5e-3
+
+
+def to_dev(cuda, arr, bf16=False):
+    if bf16:
+        return cuda.from_numpy(np.ascontiguousarray(arr).view(np.int16)).cuda().view(cuda.bfloat16)
+    return cuda.from_numpy(np.ascontiguousarray(arr)).cuda()
+
+
+def fill_cache(cuda, layer, kx, vx, block_table, ctx, bf16):
+    """Append token t of sequence b at its block-table slot (one batched call)."""
+    bsz = block_table.shape[0]
+    slots = []
+    ks, vs = [], []
+    for b in range(bsz):
+        pos = np.arange(ctx[b])
+        slots.append(workloads.slot_mapping(block_table[b:b + 1], pos[None, :])[0])
+        ks.append(kx[b, : ctx[b]])
+        vs.append(vx[b, : ctx[b]])
+    slots = np.concatenate(slots).astype(np.int64)
+    k = np.concatenate(ks)
+    v = np.concatenate(vs)
+    layer.append(to_dev(cuda, k, bf16), to_dev(cuda, v, bf16), cuda.from_numpy(slots).cuda())
+
+
+def run_case(cuda, tq, *, B, Hq, Hkv, ctx, bits_k=4, bits_v=4, qjl=False, rot=1, bf16=True, kv_format="packed",
+             data="gauss", seed=0, num_splits=0, q_f32=False, out_f32=True, extra_blocks=3):
+    ctx = np.asarray(ctx, np.int32)
+    mb = int(max(1, math.ceil(ctx.max() / 16)))
+    bt, nb = workloads.shuffled_block_table(seed + 1, B, mb, num_blocks=B * mb + extra_blocks)
+    tmax = mb * 16
+    if data == "lognormal":
+        kb, vb = workloads.lognormal_channel_kv(seed, B * tmax, Hkv, D)
+    elif data == "heavy":
+        kb, vb = workloads.heavy_tail_kv(seed, B * tmax, Hkv, D)
+    else:
+        kb, vb = workloads.scaled_gaussian_kv(seed, B * tmax, Hkv, D)
+    kb = kb.reshape(B, tmax, Hkv, D)
+    vb = vb.reshape(B, tmax, Hkv, D)
+    layer = tq.Layer(nb, Hkv, kv_format=kv_format, bits_k=bits_k, bits_v=bits_v, qjl=qjl, rot_kind=rot,
+                     seed=seed + 7, layer=seed % 5, qjl_seed=seed + 11)
+    if bf16:
+        fill_cache(cuda, layer, kb, vb, bt, ctx, True)
+    else:
+        fill_cache(cuda, layer, workloads.bf16_to_f32(kb), workloads.bf16_to_f32(vb), bt, ctx, False)
+    qf = workloads.queries(seed + 3, B, Hq, D, dtype="f32" if q_f32 else "bf16")
+    qd = to_dev(cuda, qf, bf16=not q_f32)
+    sm = 1.0 / math.sqrt(D)
+    out = layer.decode(qd, cuda.from_numpy(bt).cuda(), cuda.from_numpy(ctx).cuda(), sm_scale=sm,
+                       out_dtype=cuda.float32 if out_f32 else cuda.bfloat16, num_splits=num_splits)
+    cuda.cuda.synchronize()
+    assert tq.get_device_status() == 0
+    qx = qf.astype(np.float64) if q_f32 else oq.bf16_bits_to_f64(qf)
+    kp, vp = layer.k_cache.cpu().numpy(), layer.v_cache.cpu().numpy()
+    if kv_format == "packed":
+        ref = oa.decode_packed(qx, kp, vp, oracle_layer(layer), nb, Hkv, bt, ctx, sm)
+    else:
+        ref = oa.decode_bf16(qx, kp.view(np.uint16), vp.view(np.uint16), nb, Hkv, bt, ctx, sm)
+    return out.float().cpu().numpy(), ref, layer
+
+
+def assert_close(out, ref, tol, ctx):
+    live = np.asarray(ctx) > 0
+    err = max_rel_err(out[live], ref[live])
+    print("max rel err %.3e (tol %.1e)" % (err, tol))
+    assert err <= tol
+    assert np.all(out[~live] == 0.0)
+
+
+def test_tiny_single_head_fp32(cuda, tqlib):
+    # 1 seq, 1 KV head, 256 tokens, fp32 K/V with 4 outlier channels x20, 4-bit, Hadamard seed 0
+    tq = tqlib
+    k, v, q, _ = workloads.tiny_kv(seed=0)
+    layer = tq.Layer(16, 1, seed=0, layer=0)
+    slots = np.arange(256, dtype=np.int64)
+    layer.append(to_dev(cuda, k), to_dev(cuda, v), cuda.from_numpy(slots).cuda())
+    bt = np.arange(16, dtype=np.int32)[None, :]
+    ctx = np.array([256], np.int32)
+    out = layer.decode(to_dev(cuda, q), cuda.from_numpy(bt).cuda(), cuda.from_numpy(ctx).cuda())
+    cuda.cuda.synchronize()
+    ref = oa.decode_packed(q.astype(np.float64), layer.k_cache.cpu().numpy(), layer.v_cache.cpu().numpy(),
+                           oracle_layer(layer), 16, 1, bt, ctx, 1 / math.sqrt(D))
+    assert_close(out.cpu().numpy(), ref, TOL_F32, ctx)
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+def test_gqa_lognormal_bf16(cuda, tqlib, splits):
+    out, ref, _ = run_case(cuda, tqlib, B=3, Hq=8, Hkv=2, ctx=[1, 100, 333], data="lognormal", num_splits=splits)
+    assert_close(out, ref, TOL_BF16, [1, 100, 333])
+
+
+def test_group8_heavy_tail_k3v4(cuda, tqlib):
+    out, ref, _ = run_case(cuda, tqlib, B=2, Hq=16, Hkv=2, ctx=[500, 77], bits_k=3, bits_v=4, data="heavy", seed=2)
+    assert_close(out, ref, TOL_BF16, [500, 77])
+
+
+@pytest.mark.parametrize("bk,bv", [(2, 2), (2, 3), (3, 3), (4, 2)])
+def test_other_bit_widths(cuda, tqlib, bk, bv):
+    out, ref, _ = run_case(cuda, tqlib, B=2, Hq=4, Hkv=2, ctx=[45, 160], bits_k=bk, bits_v=bv, seed=3)
+    assert_close(out, ref, TOL_BF16, [45, 160])
+
+
+def test_qjl_keys(cuda, tqlib):
+    out, ref, _ = run_case(cuda, tqlib, B=2, Hq=8, Hkv=2, ctx=[300, 129], bits_k=2, bits_v=4, qjl=True, seed=4)
+    assert_close(out, ref, TOL_BF16, [300, 129])
+
+
+def test_dense_rotation_layer(cuda, tqlib):
+    out, ref, _ = run_case(cuda, tqlib, B=1, Hq=8, Hkv=2, ctx=[300], rot=tqlib.TQ_ROT_DENSE, seed=5, q_f32=True)
+    assert_close(out, ref, TOL_BF16, [300])
+
+
+def test_bf16_layer(cuda, tqlib):
+    out, ref, _ = run_case(cuda, tqlib, B=2, Hq=8, Hkv=2, ctx=[70, 257], kv_format="bf16", seed=6)
+    assert_close(out, ref, TOL_BF16, [70, 257])
+
+
+def test_fp32_inputs_fp32_tolerance(cuda, tqlib):
+    out, ref, _ = run_case(cuda, tqlib, B=2, Hq=4, Hkv=1, ctx=[200, 31], bf16=False, q_f32=True, seed=7)
+    assert_close(out, ref, TOL_F32, [200, 31])
+
+
+def test_sixteen_heads_per_kv_head(cuda, tqlib):
+    out, ref, _ = run_case(cuda, tqlib, B=1, Hq=16, Hkv=1, ctx=[190], seed=8)
+    assert_close(out, ref, TOL_BF16, [190])
+
+
+def test_empty_and_single_token_contexts(cuda, tqlib):
+    out, ref, _ = run_case(cuda, tqlib, B=3, Hq=4, Hkv=2, ctx=[0, 1, 17], seed=9)
+    assert_close(out, ref, TOL_BF16, [0, 1, 17])
+
+
+def test_split_count_invariance(cuda, tqlib):
+    outs = []
+    for s in (1, 2, 5, 16, 64):
+        out, ref, _ = run_case(cuda, tqlib, B=2, Hq=8, Hkv=2, ctx=[1000, 411], seed=10, num_splits=s)
+        outs.append(out)
+    for o in outs[1:]:
+        assert max_rel_err(o, outs[0]) < 2e-5
+
+
+def test_bad_block_table_entry_is_flagged(cuda, tqlib):
+    tq = tqlib
+    layer = tq.Layer(4, 1)
+    q = cuda.zeros((1, 1, D), dtype=cuda.float32).cuda()
+    bt = cuda.tensor([[0, 99]], dtype=cuda.int32).cuda()
+    ctx = cuda.tensor([20], dtype=cuda.int32).cuda()
+    layer.decode(q, bt, ctx)
+    assert tq.get_device_status() & tq.TQ_DEV_BAD_BLOCK
+    ctx = cuda.tensor([1000], dtype=cuda.int32).cuda()
+    layer.decode(q, bt[:, :1].contiguous(), ctx)
+    assert tq.get_device_status() & tq.TQ_DEV_BAD_CONTEXT
+
+
+def test_llama8b_shape_full_size_sampled(cuda, tqlib):
+    """Batch 16, 32/8 heads, context 8192, lognormal channels, shuffled table;
+    the oracle checks sampled (sequence, KV head) pairs of the full-size run."""
+    tq = tqlib
+    B, Hq, Hkv, T = 16, 32, 8, 8192
+    mb = T // 16
+    bt, nb = workloads.shuffled_block_table(21, B, mb + 1)
+    layer = tq.Layer(nb, Hkv, seed=0, layer=0)
+    torch = cuda
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    scale_k = torch.exp(torch.randn(Hkv, D, generator=gen, device="cuda"))
+    scale_v = torch.exp(torch.randn(Hkv, D, generator=gen, device="cuda"))
+    k = (torch.randn(B * T, Hkv, D, generator=gen, device="cuda") * scale_k).to(torch.bfloat16)
+    v = (torch.randn(B * T, Hkv, D, generator=gen, device="cuda") * scale_v).to(torch.bfloat16)
+    slots = workloads.prefill_slots(bt, T)
+    layer.append(k, v, torch.from_numpy(slots).cuda())
+    ctx = np.full(B, T, np.int32)
+    q = torch.randn(B, Hq, D, generator=gen, device="cuda").to(torch.bfloat16)
+    out = layer.decode(q, torch.from_numpy(bt).cuda(), torch.from_numpy(ctx).cuda(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tq.get_device_status() == 0
+    kp, vp = layer.k_cache.cpu().numpy(), layer.v_cache.cpu().numpy()
+    ol = oracle_layer(layer)
+    qx = q.float().cpu().numpy().astype(np.float64)
+    o = out.cpu().numpy()
+    errs = []
+    for b, kvh in ((0, 0), (7, 3), (15, 7)):
+        f = oa.gather_packed(kp, vp, ol, nb, Hkv, D, bt[b], T, kvh)
+        for h in range(kvh * 4, kvh * 4 + 4):
+            s = (1 / math.sqrt(D)) * (f["k_hat"] @ qx[b, h])
+            ref = oa.softmax_weights(s) @ f["v_hat"]
+            errs.append(max_rel_err(o[b, h][None], ref[None]))
+    print("sampled max rel err %.3e" % max(errs))
+    assert max(errs) <= TOL_BF16

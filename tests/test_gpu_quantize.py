@@ -1,0 +1,199 @@
+"""GPU parity of quantize-on-append, the quantizer alone, bf16 append and
+dequantize against the oracle (all through the C ABI via the binding)."""
+import numpy as np
+import pytest
+
+import workloads
+from oracle import codebook as ocb, quantize as oq, qjl as oqjl, rotation as orot
+from tests._gpu_util import D, oracle_pi, page_fields, slot_fields, tie_band_ok
+
+pytestmark = pytest.mark.gpu
+
+
+def make_slots(cuda, n, num_blocks, seed, skip_every=0):
+    perm = np.random.default_rng(seed).permutation(num_blocks * 16)[:n].astype(np.int64)
+    if skip_every:
+        perm[::skip_every] = -1
+    return perm, cuda.from_numpy(perm).cuda()
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_quantizer_bit_exact_given_rotated_coordinates(cuda, tqlib, bits):
+    tq = tqlib
+    H, nb, n = 3, 40, 301  # 903 vectors: several CTA tiles and a ragged tail
+    layer = tq.Layer(nb, H, bits_k=bits, bits_v=bits, fill=0xA5)
+    c32, b32 = ocb.codebook_fp32(D, bits)
+    g = np.random.default_rng(bits)
+    x = g.standard_normal((n, H, D))
+    y = (x / np.linalg.norm(x, axis=-1, keepdims=True)).astype(np.float32)
+    # plant exact boundary values, their neighbours and signed zeros
+    flat = y.reshape(-1)
+    k = len(b32)
+    flat[: 3 * k] = np.concatenate([b32, np.nextafter(b32, np.float32(-1)), np.nextafter(b32, np.float32(1))])
+    flat[3 * k: 3 * k + 4] = np.array([0.0, -0.0, 1e-30, -1e-30], np.float32)
+    norms = (g.random((n, H)) * 10 + 0.1).astype(np.float32)
+    norms[5, 1] = 0.0
+    slots, slots_d = make_slots(cuda, n, nb, 7, skip_every=17)
+    layer.quantize_rotated(0, cuda.from_numpy(y).cuda(), cuda.from_numpy(norms).cuda(), slots_d)
+    cuda.cuda.synchronize()
+    kp = layer.k_cache.cpu().numpy()
+    fields = page_fields(layer, 0, kp)
+    expect = oq.codes_from_y(y, b32)
+    for h in range(H):
+        keep = slots >= 0
+        codes, gamma = slot_fields(fields, slots[keep], h)
+        assert np.array_equal(codes, expect[keep, h])
+        cn = np.sqrt(np.sum(c32.astype(np.float64)[expect[keep, h]] ** 2, axis=-1))
+        ref = norms[keep, h].astype(np.float64) / cn
+        assert np.all(np.abs(gamma - ref) <= 1e-6 * np.abs(ref))
+    # pages of skipped slots keep their 0xA5 fill
+    skipped = slots[slots < 0]
+    assert skipped.size > 0
+    written = np.zeros(nb * 16, bool)
+    written[slots[slots >= 0]] = True
+    rec = opack_record_view(kp, nb, H, bits)
+    assert np.all(rec[~written.reshape(nb, 16)] == 0xA5)
+
+
+def opack_record_view(pool, nb, H, bits):
+    """uint8 [nb, 16, H, record+4] view of code records and gammas (for fill checks)."""
+    from oracle import pack as opack
+    pb = opack.page_bytes(D, bits)
+    pages = pool.reshape(nb, H, pb)
+    rb = opack.record_bytes(D, bits)
+    codes = pages[:, :, : 16 * rb].reshape(nb, H, 16, rb)
+    gam = pages[:, :, 16 * rb: 16 * rb + 64].reshape(nb, H, 16, 4)
+    return np.concatenate([codes, gam], axis=-1).transpose(0, 2, 1, 3)
+
+
+@pytest.mark.parametrize("bits,dtype", [(4, "f32"), (3, "bf16"), (2, "bf16"), (4, "bf16")])
+def test_append_hadamard_matches_oracle_within_tie_band(cuda, tqlib, bits, dtype):
+    tq = tqlib
+    H, nb, n = 2, 24, 257
+    layer = tq.Layer(nb, H, bits_k=bits, bits_v=bits, seed=3, layer=1)
+    if dtype == "f32":
+        k, v, _, _ = workloads.tiny_kv(seed=1, n_tokens=n, d=D)
+        k = np.repeat(k, H, axis=1) * np.array([1.0, 0.01], np.float32)[None, :, None]
+        v = np.repeat(v, H, axis=1)
+        kx, vx = k.astype(np.float64), v.astype(np.float64)
+        kt, vt = cuda.from_numpy(k).cuda(), cuda.from_numpy(v).cuda()
+    else:
+        kb, vb = workloads.lognormal_channel_kv(2, n, H, D)
+        kx, vx = oq.bf16_bits_to_f64(kb), oq.bf16_bits_to_f64(vb)
+        kt = cuda.from_numpy(kb.view(np.int16)).cuda().view(cuda.bfloat16)
+        vt = cuda.from_numpy(vb.view(np.int16)).cuda().view(cuda.bfloat16)
+    slots, slots_d = make_slots(cuda, n, nb, 11)
+    layer.append(kt, vt, slots_d)
+    assert tq.get_device_status() == 0
+    pi = orot.hadamard_rotation_seeded(3, 1, D)
+    c32, b32 = ocb.codebook_fp32(D, bits)
+    kp, vp = layer.k_cache.cpu().numpy(), layer.v_cache.cpu().numpy()
+    total_mism = 0.0
+    for which, x, pool in ((0, kx, kp), (1, vx, vp)):
+        fields = page_fields(layer, which, pool)
+        for h in range(H):
+            idx, gamma, y = oq.quantize(x[:, h], pi, c32, b32)
+            codes, g_gpu = slot_fields(fields, slots, h)
+            ok, rate = tie_band_ok(y, codes, idx, b32, 1e-5)
+            assert ok, "code mismatch outside the tie band"
+            total_mism += rate
+            same = np.all(codes == idx, axis=-1)
+            assert np.all(np.abs(g_gpu[same] - gamma[same]) <= 1e-6 * np.abs(gamma[same]) + 1e-30)
+    print("tie-band mismatch rate (mean over K/V heads): %.2e" % (total_mism / (2 * H)))
+
+
+def test_append_zero_vector_and_bad_slot(cuda, tqlib):
+    tq = tqlib
+    layer = tq.Layer(4, 1)
+    x = np.zeros((2, 1, D), np.float32)
+    x[1, 0, 3] = 2.0
+    slots = cuda.tensor([5, 4 * 16 + 3], dtype=cuda.int64).cuda()  # second slot is out of range
+    layer.append(cuda.from_numpy(x).cuda(), None, slots)
+    assert tq.get_device_status() & tq.TQ_DEV_BAD_SLOT
+    assert tq.get_device_status() == 0  # cleared by the read
+    fields = page_fields(layer, 0, layer.k_cache.cpu().numpy())
+    codes, gamma = slot_fields(fields, [5], 0)
+    assert np.all(codes == 8) and gamma[0] == 0.0
+
+
+def test_dense_rotation_append_matches_oracle(cuda, tqlib):
+    tq = tqlib
+    H, nb, n = 2, 12, 150
+    layer = tq.Layer(nb, H, rot_kind=tq.TQ_ROT_DENSE, seed=5, layer=2)
+    kb, vb = workloads.scaled_gaussian_kv(4, n, H, D, scale=2.5)
+    kt = cuda.from_numpy(kb.view(np.int16)).cuda().view(cuda.bfloat16)
+    vt = cuda.from_numpy(vb.view(np.int16)).cuda().view(cuda.bfloat16)
+    slots, slots_d = make_slots(cuda, n, nb, 3)
+    layer.append(kt, vt, slots_d)
+    pi = orot.dense_rotation_seeded(5, 2, D)
+    c32, b32 = ocb.codebook_fp32(D, 4)
+    for which, xb, pool in ((0, kb, layer.k_cache), (1, vb, layer.v_cache)):
+        fields = page_fields(layer, which, pool.cpu().numpy())
+        for h in range(H):
+            idx, gamma, y = oq.quantize(oq.bf16_bits_to_f64(xb)[:, h], pi, c32, b32)
+            codes, g_gpu = slot_fields(fields, slots, h)
+            ok, rate = tie_band_ok(y, codes, idx, b32, 1e-5)
+            assert ok
+            same = np.all(codes == idx, axis=-1)
+            assert np.all(np.abs(g_gpu[same] - gamma[same]) <= 2e-6 * gamma[same])
+
+
+def test_qjl_residual_matches_oracle(cuda, tqlib):
+    tq = tqlib
+    H, nb, n = 2, 10, 130
+    layer = tq.Layer(nb, H, bits_k=2, bits_v=4, qjl=True, seed=1, qjl_seed=9)
+    kb, vb = workloads.scaled_gaussian_kv(6, n, H, D)
+    kt = cuda.from_numpy(kb.view(np.int16)).cuda().view(cuda.bfloat16)
+    slots, slots_d = make_slots(cuda, n, nb, 5)
+    layer.append(kt, None, slots_d)
+    pi = orot.hadamard_rotation_seeded(1, 0, D)
+    s = orot.qjl_matrix_seeded(9, D, D)
+    c32, b32 = ocb.codebook_fp32(D, 2)
+    fields = page_fields(layer, 0, layer.k_cache.cpu().numpy())
+    for h in range(H):
+        x = oq.bf16_bits_to_f64(kb)[:, h]
+        idx, gamma, signs, rho, r = oqjl.residual_encode(x, pi, c32, b32, s)
+        codes, g_gpu, s_gpu, rho_gpu = slot_fields(fields, slots, h)
+        same = np.all(codes == idx, axis=-1)
+        assert same.mean() > 0.95
+        # sign bits: mismatches only where |S r| is within rounding of 0
+        z = r[same] @ s.T
+        mism = s_gpu[same] != signs[same]
+        scale = np.linalg.norm(s, axis=1)[None, :] * rho[same][:, None]
+        assert np.all(np.abs(z[mism]) <= 1e-5 * scale[mism])
+        assert np.all(np.abs(rho_gpu[same] - rho[same]) <= 1e-5 * rho[same] + 1e-6)
+
+
+def test_bf16_layer_append_and_dequantize(cuda, tqlib):
+    tq = tqlib
+    H, nb, n = 2, 5, 37
+    layer = tq.Layer(nb, H, kv_format="bf16")
+    x = np.random.default_rng(0).standard_normal((n, H, D)).astype(np.float32)
+    slots, slots_d = make_slots(cuda, n, nb, 2)
+    layer.append(cuda.from_numpy(x).cuda(), cuda.from_numpy(x).cuda(), slots_d)
+    back = layer.dequantize(0, slots_d).cpu().numpy()
+    expect = workloads.bf16_to_f32(workloads.bf16_bits(x))
+    assert np.array_equal(back, expect)
+
+
+@pytest.mark.parametrize("rot", ["hadamard", "dense"])
+def test_dequantize_matches_oracle(cuda, tqlib, rot):
+    tq = tqlib
+    H, nb, n = 2, 8, 90
+    kind = tq.TQ_ROT_HADAMARD if rot == "hadamard" else tq.TQ_ROT_DENSE
+    layer = tq.Layer(nb, H, bits_k=3, bits_v=4, rot_kind=kind, seed=2, layer=4)
+    kb, vb = workloads.scaled_gaussian_kv(8, n, H, D)
+    kt = cuda.from_numpy(kb.view(np.int16)).cuda().view(cuda.bfloat16)
+    vt = cuda.from_numpy(vb.view(np.int16)).cuda().view(cuda.bfloat16)
+    slots, slots_d = make_slots(cuda, n, nb, 4)
+    layer.append(kt, vt, slots_d)
+    pi = oracle_pi(layer)
+    for which, bits in ((0, 3), (1, 4)):
+        out = layer.dequantize(which, slots_d).cpu().numpy().astype(np.float64)
+        c32, _ = ocb.codebook_fp32(D, bits)
+        fields = page_fields(layer, which, (layer.k_cache if which == 0 else layer.v_cache).cpu().numpy())
+        for h in range(H):
+            codes, gamma = slot_fields(fields, slots, h)[:2]
+            ref = oq.dequantize(codes, gamma, pi, c32)
+            err = np.max(np.abs(out[:, h] - ref), axis=-1) / np.max(np.abs(ref), axis=-1)
+            assert np.max(err) < 1e-5

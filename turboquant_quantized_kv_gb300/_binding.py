@@ -186,6 +186,9 @@ class Layer:
         d.fmt.rot_kind = rot_kind if self.packed else 0
         d.fmt.norm_mode = norm_mode
         self.bits_k, self.bits_v, self.qjl, self.rot_kind = bits_k, bits_v, bool(qjl and self.packed), rot_kind
+        self.seed, self.layer_index = seed, layer
+        self.qjl_seed = seed if qjl_seed is None else qjl_seed
+        self.explicit_rotation = rotation
         self.rotation_host = None
         self.qjl_host = None
         if self.packed:

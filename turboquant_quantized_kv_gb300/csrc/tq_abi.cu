@@ -138,6 +138,7 @@ tq_status tq_decode_attention(const tq_cache_desc* desc, const void* q, int q_dt
   if (s != TQ_OK) return s;
   if (batch < 0) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: batch < 0");
   if (batch == 0) return TQ_OK;
+  if (batch > 65535) return fail(TQ_ERR_UNSUPPORTED, "tq_decode_attention: batch %d > 65535", batch);
   if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype))
     return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: q_dtype %d / out_dtype %d", q_dtype, out_dtype);
   if (num_q_heads < 1 || num_q_heads % desc->num_kv_heads != 0)
