@@ -106,7 +106,7 @@ tq_status tq_quantize_rotated(const tq_cache_desc* desc, int which, const float*
 
 int tq_auto_splits(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks_per_seq) {
   clear_error();
-  if (check_desc(desc) != TQ_OK || batch < 1 || num_q_heads < 1 || max_blocks_per_seq < 1) return 0;
+  if (check_desc(desc, false) != TQ_OK || batch < 1 || num_q_heads < 1 || max_blocks_per_seq < 1) return 0;
   DeviceInfo di;
   if (device_info(&di) != TQ_OK) return 0;
   const int g = num_q_heads / desc->num_kv_heads;
@@ -122,7 +122,7 @@ static int resolve_splits(const tq_cache_desc* desc, int batch, int num_q_heads,
 size_t tq_workspace_bytes(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks_per_seq,
                           int num_splits) {
   clear_error();
-  if (check_desc(desc) != TQ_OK || batch < 1 || num_q_heads < 1 || max_blocks_per_seq < 1 || num_splits < 0) return 0;
+  if (check_desc(desc, false) != TQ_OK || batch < 1 || num_q_heads < 1 || max_blocks_per_seq < 1 || num_splits < 0) return 0;
   const int splits = resolve_splits(desc, batch, num_q_heads, max_blocks_per_seq, num_splits);
   if (splits < 1) return 0;
   const bool qjl = desc->fmt.kv_format == TQ_KV_PACKED && desc->fmt.qjl_k;

@@ -281,7 +281,7 @@ tq_status tq_make_rotation(int kind, int head_dim, uint64_t seed, int layer, flo
 }
 
 size_t tq_page_bytes(const tq_cache_desc* desc, int which) {
-  if (check_desc(desc) != TQ_OK || (which != 0 && which != 1)) return 0;
+  if (check_desc(desc, false) != TQ_OK || (which != 0 && which != 1)) return 0;
   return page_bytes_of(*desc, which);
 }
 
@@ -313,7 +313,7 @@ static bool table_ok(const float* c, const float* b, int bits) {
   return b[k / 2 - 1] == 0.0f;
 }
 
-tq_status check_desc(const tq_cache_desc* d) {
+tq_status check_desc(const tq_cache_desc* d, bool need_data) {
   if (!d) return fail(TQ_ERR_INVALID_ARG, "null descriptor");
   if (d->format_version != TQ_FORMAT_VERSION)
     return fail(TQ_ERR_VERSION, "descriptor format_version %u, library %u", d->format_version, TQ_FORMAT_VERSION);
@@ -322,7 +322,7 @@ tq_status check_desc(const tq_cache_desc* d) {
     return fail(TQ_ERR_UNSUPPORTED, "block_size %d: only 16 is implemented", d->block_size);
   if (d->num_kv_heads < 1 || d->num_kv_heads > 1024) return fail(TQ_ERR_INVALID_ARG, "num_kv_heads %d", d->num_kv_heads);
   if (d->num_blocks < 1) return fail(TQ_ERR_INVALID_ARG, "num_blocks %lld", (long long)d->num_blocks);
-  if (!d->k_cache || !d->v_cache) return fail(TQ_ERR_INVALID_ARG, "null cache pool");
+  if (need_data && (!d->k_cache || !d->v_cache)) return fail(TQ_ERR_INVALID_ARG, "null cache pool");
   if (((uintptr_t)d->k_cache | (uintptr_t)d->v_cache) & 15)
     return fail(TQ_ERR_INVALID_ARG, "cache pools must be 16-byte aligned");
   const tq_layer_format& f = d->fmt;
@@ -335,8 +335,8 @@ tq_status check_desc(const tq_cache_desc* d) {
   if (f.qjl_k != 0 && f.qjl_k != 1) return fail(TQ_ERR_INVALID_ARG, "qjl_k %d", f.qjl_k);
   if (f.rot_kind != TQ_ROT_HADAMARD && f.rot_kind != TQ_ROT_DENSE)
     return fail(TQ_ERR_INVALID_ARG, "rot_kind %d", f.rot_kind);
-  if (!d->rotation) return fail(TQ_ERR_INVALID_ARG, "null rotation");
-  if (f.qjl_k && !d->qjl_proj) return fail(TQ_ERR_INVALID_ARG, "qjl_k set but qjl_proj is null");
+  if (need_data && !d->rotation) return fail(TQ_ERR_INVALID_ARG, "null rotation");
+  if (need_data && f.qjl_k && !d->qjl_proj) return fail(TQ_ERR_INVALID_ARG, "qjl_k set but qjl_proj is null");
   if (!table_ok(d->centroids_k, d->boundaries_k, f.bits_k))
     return fail(TQ_ERR_INVALID_ARG, "key codebook is not increasing/antisymmetric with its midpoints");
   if (!table_ok(d->centroids_v, d->boundaries_v, f.bits_v))

@@ -16,7 +16,8 @@ tq_status fail(tq_status st, const char* fmt, ...);
 void clear_error();
 
 // Host-side validation of a descriptor.  Returns TQ_OK or an error (message set).
-tq_status check_desc(const tq_cache_desc* desc);
+// need_data = false skips the device-pointer checks (sizes only).
+tq_status check_desc(const tq_cache_desc* desc, bool need_data = true);
 
 // Bytes of a K (which = 0) or V (which = 1) page of a valid descriptor.
 size_t page_bytes_of(const tq_cache_desc& d, int which);
