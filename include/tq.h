@@ -236,6 +236,29 @@ tq_status tq_decode_attention(const tq_cache_desc* desc, const void* q, int q_dt
 tq_status tq_dequantize(const tq_cache_desc* desc, int which, const int64_t* slots, int64_t n, void* out,
                         int out_dtype, void* stream);
 
+/* Bytes of the scratch array tq_decode_attention_static keeps on every device
+ * that loads the library (held until the process exits). */
+#define TQ_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* Decode attention for callers that cannot allocate device memory.  The pages
+ * have no counterpart for this call: it exists for code that is handed only
+ * its inputs and outputs (a plugin or FFI caller inside a host application
+ * that owns the device-memory budget, or a serving loop that must not call
+ * cudaMalloc/cudaFree after start-up), so it cannot pass the workspace
+ * tq_decode_attention needs.
+ * Same arguments, result and errors as tq_decode_attention without the
+ * workspace pair; the scratch is a library-owned device array of
+ * TQ_STATIC_SCRATCH_BYTES.  Sizes whose scratch would exceed it are rejected
+ * with TQ_ERR_WORKSPACE before anything is launched.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, that
+ * device current): make it before any stream capture.  Allocates nothing.
+ * All calls on a device share the array; calls that overlap on the GPU (other
+ * streams, other host threads) race on it. */
+tq_status tq_decode_attention_static(const tq_cache_desc* desc, const void* q, int q_dtype, int batch,
+                                     int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                                     const int32_t* context_lens, float sm_scale, void* out, int out_dtype,
+                                     int num_splits, void* stream);
+
 /* ---- status ------------------------------------------------------------- */
 
 /* Synchronizes the stream, returns the sticky device status bits of the
