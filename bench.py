@@ -31,6 +31,7 @@ if ROOT not in sys.path:
 
 B, HQ, HKV, D, T0, LAYERS = 16, 32, 8, 128, 8192, 32
 BLOCK = 16
+SPLITS = 0  # decode context splits; 0 lets the library choose
 BYTES_PER_TOKEN_HEAD = 2 * (D * 4 // 8 + 4)  # 4-bit K and V records + two fp32 norms = 136 B
 APPEND_BYTES_PER_VECTOR = 2 * D + (D * 4 // 8 + 4)  # bf16 read + record written
 METRIC = "decode-attn packed-KV GB/s"
@@ -118,7 +119,7 @@ def setup(torch, tq, steps_total, dev):
     slots_pre = torch.from_numpy(workloads.prefill_slots(bt_np, T0)).to(dev)
     layers = [tq.Layer(nb, HKV, bits_k=4, bits_v=4, seed=0, layer=l, device=dev) for l in range(LAYERS)]
     # prefill (timed: quantize-append throughput on 2 x 1,048,576 vectors per layer)
-    for l in range(2):
+    for l in range(min(2, LAYERS)):  # untimed first appends
         layers[l].append(kpre, vpre, slots_pre)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(LAYERS)]
@@ -136,7 +137,7 @@ def setup(torch, tq, steps_total, dev):
     out = [torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev) for _ in range(LAYERS)]
     ctx = torch.full((B,), T0, dtype=torch.int32, device=dev)
     slot_new = torch.empty(B, dtype=torch.int64, device=dev)
-    ws_bytes = layers[0].workspace_bytes(B, HQ, mb)
+    ws_bytes = layers[0].workspace_bytes(B, HQ, mb, SPLITS)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     return dict(layers=layers, bt=bt, bt_np=bt_np, mb=mb, nb=nb, q=q, knew=knew, vnew=vnew, out=out, ctx=ctx,
                 slot_new=slot_new, ws=ws, append_ms=append_ms, append_vectors=n_vec)
@@ -155,7 +156,7 @@ def layer_append(st, l):
 
 
 def layer_decode(st, l):
-    st["layers"][l].decode(st["q"][l], st["bt"], st["ctx"], out=st["out"][l], workspace=st["ws"])
+    st["layers"][l].decode(st["q"][l], st["bt"], st["ctx"], out=st["out"][l], workspace=st["ws"], num_splits=SPLITS)
 
 
 def run_tq(args):
@@ -256,12 +257,12 @@ def run_tq(args):
             traffic = tj.get("bytes_per_launch_full_size")
         except Exception:
             traffic = None
-    app_ms = statistics.median(st["append_ms"][2:])
+    app_ms = statistics.median(st["append_ms"][2:] if len(st["append_ms"]) > 2 else st["append_ms"])
     app_vps = st["append_vectors"] / (app_ms * 1e-3)
     app_gbs = app_vps * APPEND_BYTES_PER_VECTOR / 1e9
 
     # end to end through the public API with host buffers (pinned), eager calls
-    e2e = run_e2e(torch, st, args, stream)
+    e2e = run_e2e(torch, st, args, stream) if args.e2e else None
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -270,6 +271,7 @@ def run_tq(args):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": B, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D,
                    "context": T0, "layers": LAYERS, "bits_k": 4, "bits_v": 4, "block_size": BLOCK,
+                   "splits": st["layers"][0].auto_splits(B, HQ, st["mb"]) if SPLITS == 0 else SPLITS,
                    "l2": "inputs larger than L2 (~4.6 GB of packed cache per step)", "parallelism": "replicas"},
         "roofline": {"kernel": "tq_decode_attention (rotate-q + split-K decode + combine)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -435,7 +437,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (profiling runs use fewer)")
+    ap.add_argument("--splits", type=int, default=0, help="decode context splits (0 = library default)")
     args = ap.parse_args()
+    globals()["LAYERS"] = args.layers
+    globals()["SPLITS"] = args.splits
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
