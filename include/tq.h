@@ -135,7 +135,8 @@ enum {
   TQ_DEV_BAD_SLOT = 1,        /* slot >= num_blocks * 16 in an append/dequantize */
   TQ_DEV_BAD_BLOCK = 2,       /* block table entry outside [0, num_blocks) */
   TQ_DEV_BAD_CONTEXT = 4,     /* context length < 0 or > max_blocks_per_seq * 16 */
-  TQ_DEV_WAIT_TIMEOUT = 8     /* a bounded wait on a copy gave up */
+  TQ_DEV_WAIT_TIMEOUT = 8,    /* a bounded wait on a copy gave up */
+  TQ_DEV_LAYOUT = 16          /* decode found less shared memory than its layout needs (no work done) */
 };
 
 typedef struct {
