@@ -32,6 +32,7 @@ if ROOT not in sys.path:
 B, HQ, HKV, D, T0, LAYERS = 16, 32, 8, 128, 8192, 32
 BLOCK = 16
 SPLITS = 0  # decode context splits; 0 lets the library choose
+LAUNCHES_PER_LAYER = 5  # libtq kernels per layer and step: append K, append V, rotate q, decode, combine
 BYTES_PER_TOKEN_HEAD = 2 * (D * 4 // 8 + 4)  # 4-bit K and V records + two fp32 norms = 136 B
 APPEND_BYTES_PER_VECTOR = 2 * D + (D * 4 // 8 + 4)  # bf16 read + record written
 METRIC = "decode-attn packed-KV GB/s"
@@ -250,11 +251,14 @@ def run_tq(args):
     achieved = statistics.mean(bytes_per_call) / (dec_avg_ms * 1e-3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    if os.path.exists(tpath):
+    if os.path.exists(tpath):  # counters from one ncu capture, valid only for the kernel source they came from
         try:
+            import hashlib
             with open(tpath) as f:
                 tj = json.load(f)
-            traffic = tj.get("bytes_per_launch_full_size")
+            with open(os.path.join(ROOT, "turboquant_quantized_kv_gb300", "csrc", "tq_decode.cu"), "rb") as f:
+                sha = hashlib.sha256(f.read()).hexdigest()
+            traffic = tj.get("bytes_per_launch") if tj.get("source_sha256") == sha else None
         except Exception:
             traffic = None
     app_ms = statistics.median(st["append_ms"][2:] if len(st["append_ms"]) > 2 else st["append_ms"])
@@ -279,7 +283,7 @@ def run_tq(args):
         "append": {"vectors_per_s": round(app_vps, 1), "gbs": round(app_gbs, 1), "frac": round(app_gbs / peak, 4),
                    "vectors": st["append_vectors"], "bytes_per_vector": APPEND_BYTES_PER_VECTOR},
         "e2e": e2e,
-        "gpu_launches": args.steps * (LAYERS * 5 + 4),
+        "gpu_launches": args.steps * LAYERS * LAUNCHES_PER_LAYER,
         "clocks": clk,
         "device_status": status,
     }
@@ -345,39 +349,40 @@ def _oracle_unit(payload):
     return kpages.nbytes + vpages.nbytes
 
 
-def _oracle_payloads(n_units, rng_seed=0):
-    """Packed pages for n_units (sequence, KV head) units of 8192 tokens, made by the oracle."""
+def _oracle_payload(u):
+    """Packed pages of one (sequence, KV head) unit of 8192 tokens, made by the oracle."""
     import numpy as np
     import workloads
     from oracle import codebook as ocb, pack as opack, quantize as oq, rotation as orot
     c4, b4 = ocb.codebook_fp32(D, 4)
-    out = []
-    for u in range(n_units):
-        kb, vb = workloads.lognormal_channel_kv(rng_seed + u, T0, 1, D)
-        pi = orot.hadamard_rotation_seeded(0, u % LAYERS, D)
-        pages = []
-        for xb in (kb, vb):
-            idx, gamma, _ = oq.quantize(oq.bf16_bits_to_f64(xb[:, 0]), pi, c4, b4)
-            rec = opack.pack_records(idx, 4).reshape(T0 // BLOCK, BLOCK * 64)
-            g = gamma.astype("<f4").view(np.uint8).reshape(T0 // BLOCK, BLOCK * 4)
-            pages.append(np.concatenate([rec, g], axis=1))
-        q = oq.bf16_bits_to_f64(workloads.queries(rng_seed + u, 1, HQ // HKV, D))[0]
-        out.append((pages[0], pages[1], q, u % LAYERS))
-    return out
+    kb, vb = workloads.lognormal_channel_kv(u, T0, 1, D)
+    pi = orot.hadamard_rotation_seeded(0, u % 32, D)
+    pages = []
+    for xb in (kb, vb):
+        idx, gamma, _ = oq.quantize(oq.bf16_bits_to_f64(xb[:, 0]), pi, c4, b4)
+        rec = opack.pack_records(idx, 4).reshape(T0 // BLOCK, BLOCK * 64)
+        g = gamma.astype("<f4").view(np.uint8).reshape(T0 // BLOCK, BLOCK * 4)
+        pages.append(np.concatenate([rec, g], axis=1))
+    q = oq.bf16_bits_to_f64(workloads.queries(u, 1, HQ // HKV, D))[0]
+    return pages[0], pages[1], q, u % 32
+
+
+def _oracle_payloads(n_units, pool=None):
+    return pool.map(_oracle_payload, range(n_units)) if pool else [_oracle_payload(u) for u in range(n_units)]
 
 
 def cpu_baseline(st, args):
     """The oracle as it stands on the host cores, on a bounded sample (spawned pool)."""
     import multiprocessing as mp
     cores = min(os.cpu_count() or 1, 16)
-    n_units = cores * 2
-    payloads = _oracle_payloads(n_units)
+    n_units = cores * 12
     ctxm = mp.get_context("spawn")
     env_keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
     for k in env_keep:
         os.environ[k] = "1"
     try:
         with ctxm.Pool(cores) as pool:
+            payloads = _oracle_payloads(n_units, pool)  # untimed: the oracle packs the sample
             pool.map(_oracle_unit, payloads[:cores])  # warm the workers
             t = time.perf_counter()
             nbytes = sum(pool.map(_oracle_unit, payloads))
@@ -401,11 +406,11 @@ def run_reference(args):
     import multiprocessing as mp
     cores = min(os.cpu_count() or 1, 16)
     per_step = cores
-    payloads = _oracle_payloads(per_step)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[k] = "1"
     ctxm = mp.get_context("spawn")
     with ctxm.Pool(cores) as pool:
+        payloads = _oracle_payloads(per_step, pool)
         for _ in range(args.warmup):
             pool.map(_oracle_unit, payloads)
         t = time.perf_counter()
@@ -433,7 +438,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
