@@ -32,7 +32,6 @@ if ROOT not in sys.path:
 B, HQ, HKV, D, T0, LAYERS = 16, 32, 8, 128, 8192, 32
 BLOCK = 16
 SPLITS = 0  # decode context splits; 0 lets the library choose
-LAUNCHES_PER_LAYER = 5  # libtq kernels per layer and step: append K, append V, rotate q, decode, combine
 BYTES_PER_TOKEN_HEAD = 2 * (D * 4 // 8 + 4)  # 4-bit K and V records + two fp32 norms = 136 B
 APPEND_BYTES_PER_VECTOR = 2 * D + (D * 4 // 8 + 4)  # bf16 read + record written
 METRIC = "decode-attn packed-KV GB/s"
@@ -189,6 +188,7 @@ def run_tq(args):
     g_app = [torch.cuda.CUDAGraph() for _ in range(LAYERS)]
     g_dec = [torch.cuda.CUDAGraph() for _ in range(LAYERS)]
     ctx_save = st["ctx"].clone()
+    n_before = tq.launch_count()
     with torch.cuda.graph(g_prep):
         step_prepare(torch, st)
     for l in range(LAYERS):
@@ -196,6 +196,7 @@ def run_tq(args):
             layer_append(st, l)
         with torch.cuda.graph(g_dec[l]):
             layer_decode(st, l)
+    launches_per_step = tq.launch_count() - n_before  # libtq kernels captured into one step's graphs
     st["ctx"].copy_(ctx_save)
     torch.cuda.synchronize()
 
@@ -283,7 +284,7 @@ def run_tq(args):
         "append": {"vectors_per_s": round(app_vps, 1), "gbs": round(app_gbs, 1), "frac": round(app_gbs / peak, 4),
                    "vectors": st["append_vectors"], "bytes_per_vector": APPEND_BYTES_PER_VECTOR},
         "e2e": e2e,
-        "gpu_launches": args.steps * LAYERS * LAUNCHES_PER_LAYER,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
         "device_status": status,
     }

@@ -272,6 +272,11 @@ const char* tq_last_error(void);
 /* TQ_FORMAT_VERSION of this build. */
 uint32_t tq_format_version(void);
 
+/* Number of kernels this library has enqueued in this process, all threads
+ * and devices together (a host-side count taken at each launch; a launch made
+ * during stream capture counts once, however often the graph is replayed). */
+uint64_t tq_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -98,6 +98,8 @@ def test_descriptor_validation(tqlib):
     tq = tqlib
     lib = tq.lib()
 
+    launches0 = tq.launch_count()
+
     def status(d):
         return lib.tq_quantize_append(ctypes.byref(d), ctypes.c_void_p(0x1000), None, tq.TQ_F32,
                                       ctypes.c_void_p(0x2000), 4, None)
@@ -131,6 +133,7 @@ def test_descriptor_validation(tqlib):
                                    None, tq.TQ_F32, None, 0, 0, None) == tq.TQ_OK  # empty batch
     assert lib.tq_dequantize(ctypes.byref(d), 2, ctypes.c_void_p(8), 1, ctypes.c_void_p(8), tq.TQ_F32,
                              None) == tq.TQ_ERR_INVALID_ARG
+    assert tq.launch_count() == launches0  # rejected and empty calls enqueue nothing
 
 
 def test_make_args_rejected(tqlib):

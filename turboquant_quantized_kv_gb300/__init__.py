@@ -7,7 +7,8 @@ in libtq's CUDA kernels; this package only marshals arguments.
 """
 
 from ._binding import (  # noqa: F401
-    CacheDesc, Layer, LayerFormat, TQError, get_device_status, last_error, lib, make_codebook, make_rotation,
+    CacheDesc, Layer, LayerFormat, TQError, get_device_status, last_error, launch_count, lib, make_codebook,
+    make_rotation,
     LIB_PATH, STATUS_NAMES,
     TQ_BF16, TQ_BLOCK_SIZE, TQ_DEV_BAD_BLOCK, TQ_DEV_BAD_CONTEXT, TQ_DEV_BAD_SLOT, TQ_DEV_WAIT_TIMEOUT,
     TQ_ERR_CUDA, TQ_ERR_DEVICE, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_VERSION, TQ_ERR_WORKSPACE,

@@ -75,6 +75,7 @@ _SIGNATURES = {
     "tq_get_device_status": (ctypes.c_int, [ctypes.c_void_p, _P(ctypes.c_int32)]),
     "tq_last_error": (ctypes.c_char_p, []),
     "tq_format_version": (ctypes.c_uint32, []),
+    "tq_launch_count": (ctypes.c_uint64, []),
 }
 
 _lib = None
@@ -285,3 +286,8 @@ def get_device_status(stream=None):
     code = ctypes.c_int32(0)
     _check(lib().tq_get_device_status(_stream(stream), ctypes.byref(code)))
     return int(code.value)
+
+
+def launch_count():
+    """Kernels libtq has enqueued in this process (a launch captured in a graph counts once)."""
+    return int(lib().tq_launch_count())

@@ -3,6 +3,7 @@
 // (arguments, layouts, ownership, errors) is in include/tq.h.
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "tq_device.cuh"
@@ -73,6 +74,13 @@ tq_status tq_quantize_append(const tq_cache_desc* desc, const void* k, const voi
   DeviceInfo di;
   if ((s = device_info(&di)) != TQ_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const tq_layer_format& f = desc->fmt;
+  const bool same_tables = std::memcmp(desc->centroids_k, desc->centroids_v, sizeof(desc->centroids_k)) == 0 &&
+                           std::memcmp(desc->boundaries_k, desc->boundaries_v, sizeof(desc->boundaries_k)) == 0;
+  if (k && v && f.kv_format == TQ_KV_PACKED && f.bits_k == f.bits_v && !f.qjl_k && same_tables)  // one launch
+    return cuda_result(launch_quantize(*desc, 0, k, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
+                                       di.num_sms, st, v),
+                       "quantize K+V");
   if (k) {
     s = cuda_result(launch_quantize(*desc, 0, k, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
                                     di.num_sms, st), "quantize K");

@@ -35,6 +35,7 @@
 namespace tq {
 
 constexpr int kMaxStages = 4;
+constexpr int kMaxFusedSplits = 128;  // the decode kernel merges its own chunks up to this split count
 constexpr float kRescaleThreshold = 20.0f;  // log2 units before the running max is refreshed
 constexpr float kLog2e = 1.4426950408889634f;
 // P' = w / R * kPScale lies in (0, 2^14]: fp16 keeps 11 significant bits for
@@ -226,6 +227,11 @@ struct DecodeArgs {
   int stages;  // ring depth per warp
   int lut_shared;
   int smem_bytes;  // dynamic shared memory of the launch
+  int fuse_combine;  // 0: k_combine finishes; 1: decode finishes (identity); 2: decode finishes (Hadamard)
+  int* counters;     // [units] chunks finished per unit (zeroed by k_rotate_q)
+  const float* rot;  // Hadamard signs (fuse_combine == 2)
+  void* out;
+  int out_bf16;
   float* part;  // [B][Hq][splits][d]
   float* ml;    // [B][Hq][splits][2]
   Codebook cbk, cbv;
@@ -728,17 +734,16 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   __syncthreads();
   if (!has) return;
   const bool leader = warp == 0 || runit[warp - 1] != unit;
-  if (!leader) {
-    if (lane < gc) {
-      const int64_t row = ((int64_t)b * a.Hq + head0 + lane) * a.splits + s;
-      a.ml[row * 2] = -INFINITY;
-      a.ml[row * 2 + 1] = 0.0f;
-    }
-    return;
-  }
+  if (!leader) return;
   int wend = warp + 1;
   while (wend < NW && runit[wend] == unit) ++wend;
+  const int covered = wend - warp;  // chunks s .. s + covered - 1 of this unit
   for (int h = 0; h < gc; ++h) {
+    if (lane > 0 && lane < covered) {  // merged into slot s: mark the group's other slots empty
+      const int64_t row2 = ((int64_t)b * a.Hq + head0 + h) * a.splits + s + lane;
+      a.ml[row2 * 2] = -INFINITY;
+      a.ml[row2 * 2 + 1] = 0.0f;
+    }
     float Mt = -INFINITY;
     for (int w = warp; w < wend; ++w) Mt = fmaxf(Mt, rm[w * 8 + h]);
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -760,6 +765,100 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
       a.ml[row * 2 + 1] = L;
     }
   }
+  if (!a.fuse_combine) return;
+
+  // ---- the warp that completes a unit merges its chunks and applies Pi^T
+  __threadfence();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(a.counters + unit, covered) + covered == a.splits;
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();
+  // (max, denominator) of every (head, slot): lane l holds slots l + 32 g, all loads in flight at once
+  constexpr int kG = kMaxFusedSplits / 32;
+  const int64_t row0 = ((int64_t)b * a.Hq + head0) * a.splits;
+  float fm[8][kG], fl[8][kG];
+#pragma unroll
+  for (int h = 0; h < 8; ++h)
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      const int s2 = lane + 32 * g;
+      const bool in = h < gc && s2 < a.splits;
+      fm[h][g] = in ? __ldcg(a.ml + (row0 + (int64_t)h * a.splits + s2) * 2) : -INFINITY;
+      fl[h][g] = in ? __ldcg(a.ml + (row0 + (int64_t)h * a.splits + s2) * 2 + 1) : 0.0f;
+    }
+  float Lh[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < kG; ++g) mx = fmaxf(mx, fm[h][g]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float L = 0.0f;
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {  // fm becomes the slot weight
+      fm[h][g] = fm[h][g] == -INFINITY ? 0.0f : exp2f(fm[h][g] - mx);
+      L = fmaf(fl[h][g], fm[h][g], L);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    Lh[h] = L;
+  }
+  // sum the few non-empty slots (emptiness is per chunk, the same for every head)
+  float yh[8][4];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) yh[h][0] = yh[h][1] = yh[h][2] = yh[h][3] = 0.0f;
+#pragma unroll
+  for (int g = 0; g < kG; ++g) {
+    uint32_t live = __ballot_sync(0xffffffffu, fm[0][g] > 0.0f);
+    while (live) {
+      const int src = __ffs(live) - 1;
+      live &= live - 1;
+      const int s2 = src + 32 * g;
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float f = __shfl_sync(0xffffffffu, fm[h][g], src);
+        if (h < gc) {
+          const float4 v =
+              __ldcg(reinterpret_cast<const float4*>(a.part + (row0 + (int64_t)h * a.splits + s2) * kD) + lane);
+          yh[h][0] = fmaf(v.x, f, yh[h][0]);
+          yh[h][1] = fmaf(v.y, f, yh[h][1]);
+          yh[h][2] = fmaf(v.z, f, yh[h][2]);
+          yh[h][3] = fmaf(v.w, f, yh[h][3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    if (h >= gc) break;
+    const float rl = Lh[h] > 0.0f ? 1.0f / Lh[h] : 0.0f;
+    float y[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] = yh[h][k] * rl;
+    if (a.fuse_combine == 2) {  // Hadamard: Pi^T y = D H y / sqrt(d); lane holds coordinates 4 lane + k
+      float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
+      y[0] = t0 + t2; y[2] = t0 - t2; y[1] = t1 + t3; y[3] = t1 - t3;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float o = __shfl_xor_sync(0xffffffffu, y[k], m);
+          y[k] = upper ? (o - y[k]) : (y[k] + o);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) y[k] *= 0.08838834764831845f * __ldg(a.rot + 4 * lane + k);
+    }
+    const int64_t orow = ((int64_t)b * a.Hq + head0 + h) * kD + 4 * lane;
+    if (a.out_bf16) {
+      uint2 pk = make_uint2(pack_bf162(y[0], y[1]), pack_bf162(y[2], y[3]));
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow) = pk;
+    } else {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + orow) = make_float4(y[0], y[1], y[2], y[3]);
+    }
+  }
 }
 
 // ------------------------------------------------------------- prologue
@@ -767,10 +866,12 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
 enum { ROTQ_IDENTITY = 0, ROTQ_HADAMARD = 1, ROTQ_DENSE = 2 };
 
 // One warp per (sequence, query head).  qrot = Pi q * scale; uq = S qrot (QJL).
+// Also zeroes the decode's per-unit chunk counters.
 template <typename TQ>
 __global__ void __launch_bounds__(128) k_rotate_q(const TQ* __restrict__ q, int64_t n_rows, int kind,
                                                   const float* __restrict__ rot, const float* __restrict__ S,
-                                                  float scale, float* qrot, float* uq) {
+                                                  float scale, float* qrot, float* uq, int* counters, int n_counters) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_counters; i += gridDim.x * blockDim.x) counters[i] = 0;
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= n_rows) return;
@@ -896,6 +997,7 @@ static cudaError_t run_decode(DecodeArgs a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((a.chunks + NW - 1) / NW);
   kern<<<grid, NW * 32, (size_t)optin, st>>>(a);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -926,12 +1028,16 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   const int64_t rows = (int64_t)c.batch * c.num_q_heads;
   const float scale = c.sm_scale * kLog2e;
   const unsigned rgrid = (unsigned)((rows + 3) / 4);
+  int* counters = reinterpret_cast<int*>(c.workspace + ws.cnt_off);
+  const int n_counters = (int)rows;  // >= batch * kv heads * head groups
   if (c.q_dtype == TQ_F32)
     k_rotate_q<float><<<rgrid, 128, 0, st>>>(reinterpret_cast<const float*>(c.q), rows, kind, d.rotation,
-                                             qjl ? d.qjl_proj : nullptr, scale, qrot, uq);
+                                             qjl ? d.qjl_proj : nullptr, scale, qrot, uq, counters, n_counters);
   else
     k_rotate_q<__nv_bfloat16><<<rgrid, 128, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(c.q), rows, kind,
-                                                     d.rotation, qjl ? d.qjl_proj : nullptr, scale, qrot, uq);
+                                                     d.rotation, qjl ? d.qjl_proj : nullptr, scale, qrot, uq,
+                                                     counters, n_counters);
+  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -959,6 +1065,12 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   a.lut_shared = (!bf16 && same_table(a.cbk, a.cbv, d.fmt.bits_k, d.fmt.bits_v)) ? 1 : 0;
   a.qjl_coef = 1.2533141373155003f / (float)kD;  // sqrt(pi/2) / m
   a.status = c.status;
+  // the decode kernel finishes the job itself unless the inverse rotation is a dense mat-vec
+  a.fuse_combine = (kind == ROTQ_DENSE || c.splits > kMaxFusedSplits) ? 0 : (kind == ROTQ_HADAMARD ? 2 : 1);
+  a.counters = counters;
+  a.rot = d.rotation;
+  a.out = c.out;
+  a.out_bf16 = c.out_dtype == TQ_BF16 ? 1 : 0;
   // ring depth: 4 stages; 3 when two code tables would not leave room for 2 CTAs per SM;
   // 2 for bf16 pages (8 KB per block, one CTA per SM)
   a.stages = bf16 ? 3 : 4;
@@ -981,12 +1093,14 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
     }
   }
   if (e != cudaSuccess) return e;
+  if (a.fuse_combine) return cudaSuccess;
   const unsigned cgrid = (unsigned)rows;
   if (c.out_dtype == TQ_F32)
     k_combine<float><<<cgrid, 128, 0, st>>>(a.part, a.ml, c.splits, kind, d.rotation, reinterpret_cast<float*>(c.out));
   else
     k_combine<__nv_bfloat16><<<cgrid, 128, 0, st>>>(a.part, a.ml, c.splits, kind, d.rotation,
                                                     reinterpret_cast<__nv_bfloat16*>(c.out));
+  count_launch();
   return cudaGetLastError();
 }
 

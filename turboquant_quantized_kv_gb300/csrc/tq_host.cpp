@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -208,6 +209,12 @@ static bool lloyd_max(int d, int bits, std::vector<double>& c) {
   return false;
 }
 
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 }  // namespace tq
 
 using namespace tq;
@@ -217,6 +224,8 @@ extern "C" {
 const char* tq_last_error(void) { return g_last_error.c_str(); }
 
 uint32_t tq_format_version(void) { return TQ_FORMAT_VERSION; }
+
+uint64_t tq_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 tq_status tq_make_codebook(int head_dim, int bits, float* centroids, float* boundaries) {
   clear_error();
@@ -367,7 +376,8 @@ DecodeWorkspace decode_workspace(int batch, int num_q_heads, int splits, int hea
   size_t qbytes = bh * head_dim * sizeof(float) * (qjl ? 2 : 1);
   w.part_off = align256(w.qrot_off + qbytes);
   w.ml_off = align256(w.part_off + bh * splits * head_dim * sizeof(float));
-  w.total = align256(w.ml_off + bh * splits * 2 * sizeof(float));
+  w.cnt_off = align256(w.ml_off + bh * splits * 2 * sizeof(float));
+  w.total = align256(w.cnt_off + bh * sizeof(int32_t));
   return w;
 }
 

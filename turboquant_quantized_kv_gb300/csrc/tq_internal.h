@@ -15,6 +15,9 @@ namespace tq {
 tq_status fail(tq_status st, const char* fmt, ...);
 void clear_error();
 
+// Adds one to the count tq_launch_count() reports; called after each kernel launch.
+void count_launch();
+
 // Host-side validation of a descriptor.  Returns TQ_OK or an error (message set).
 // need_data = false skips the device-pointer checks (sizes only).
 tq_status check_desc(const tq_cache_desc* desc, bool need_data = true);
@@ -30,6 +33,7 @@ struct DecodeWorkspace {
   size_t qrot_off;   // fp32 [batch][Hq][d]  rotated, scaled queries (+ QJL projections)
   size_t part_off;   // fp32 [batch][Hq][splits][d] partial accumulators
   size_t ml_off;     // fp32 [batch][Hq][splits][2] (running max, denominator)
+  size_t cnt_off;    // int32 [batch][Hq] finished-chunk counters (zeroed by the query prologue)
   size_t total;
 };
 DecodeWorkspace decode_workspace(int batch, int num_q_heads, int splits, int head_dim, bool qjl);
@@ -53,9 +57,11 @@ struct DecodeCall {
 
 // Kernel launchers (CUDA translation units).  All enqueue on `st` and return
 // the launch error, if any.
+// x_v != nullptr (packed layers, which = 0): the values are quantized in the same
+// launch; the caller guarantees the K and V formats agree (bits, no QJL).
 cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, int in_dtype, const float* y,
                             const float* norms, const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms,
-                            cudaStream_t st);
+                            cudaStream_t st, const void* x_v = nullptr);
 cudaError_t launch_dequant(const tq_cache_desc& d, int which, const int64_t* slots, int64_t n, void* out,
                            int out_dtype, unsigned* status, int num_sms, cudaStream_t st);
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st);

@@ -35,6 +35,10 @@ struct QuantArgs {
   Codebook cb;
   int norm_mode;
   unsigned* status;
+  // Keys and values of one append share a launch when their formats and tables
+  // agree: blocks with blockIdx.y = 1 read x_v and write pool_v instead.
+  const void* x_v;
+  uint8_t* pool_v;
 };
 
 constexpr int kTile = 64;            // vectors per CTA iteration
@@ -81,6 +85,8 @@ __device__ __forceinline__ float flip_sign(float v, uint32_t word, int bit) {
 
 template <int BITS, typename TIn, int MODE, bool QJL>
 __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
+  const void* const x_in = blockIdx.y ? a.x_v : a.x;
+  uint8_t* const pool = blockIdx.y ? a.pool_v : a.pool;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   constexpr int H = 1 << (BITS - 1);
   constexpr int R = 16 * BITS;  // record bytes
@@ -123,7 +129,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
       load32<float>(a.y + vec * kD + 32 * q, x);
       n = __ldg(a.norms + vec);
     } else {
-      load32<TIn>(reinterpret_cast<const TIn*>(a.x) + vec * kD + 32 * q, x);
+      load32<TIn>(reinterpret_cast<const TIn*>(x_in) + vec * kD + 32 * q, x);
       float ss = 0.0f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) ss = fmaf(x[i], x[i], ss);
@@ -186,7 +192,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
     } else if (valid && slot >= 0) {
       const int64_t blk = slot >> 4;
       const int off = (int)(slot & 15);
-      uint8_t* page = a.pool + (blk * a.H + head) * (int64_t)a.page_bytes;
+      uint8_t* page = pool + (blk * a.H + head) * (int64_t)a.page_bytes;
       uint32_t w[BITS];
       pack32<BITS>(code, w);
       uint8_t* rec = page + off * R;
@@ -346,7 +352,7 @@ Codebook codebook_of(const tq_cache_desc& d, int which) {
 }
 
 template <int BITS, typename TIn, int MODE, bool QJL>
-static cudaError_t run_quantize(const QuantArgs& a, int num_sms, cudaStream_t st) {
+static cudaError_t run_quantize(const QuantArgs& a, int ny, int num_sms, cudaStream_t st) {
   auto kern = k_quantize<BITS, TIn, MODE, QJL>;
   size_t smem = kTableBytes;
   if (MODE == MODE_DENSE || QJL) smem += kTileBytes;
@@ -356,25 +362,49 @@ static cudaError_t run_quantize(const QuantArgs& a, int num_sms, cudaStream_t st
   if (e != cudaSuccess) return e;
   const int64_t tiles = (a.n_vec + kTile - 1) / kTile;
   const int per_sm = (MODE == MODE_DENSE || QJL) ? 1 : 8;
-  int64_t grid = tiles < (int64_t)num_sms * per_sm ? tiles : (int64_t)num_sms * per_sm;
+  const int64_t cap = (int64_t)num_sms * per_sm / ny;
+  int64_t grid = tiles < cap ? tiles : cap;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kThreads, smem, st>>>(a);
+  kern<<<dim3((unsigned)grid, (unsigned)ny), kThreads, smem, st>>>(a);
+  count_launch();
   return cudaGetLastError();
 }
 
 template <int BITS, typename TIn>
-static cudaError_t dispatch_mode(const QuantArgs& a, int mode, bool qjl, int num_sms, cudaStream_t st) {
-  if (mode == MODE_GIVEN_Y) return run_quantize<BITS, float, MODE_GIVEN_Y, false>(a, num_sms, st);
+static cudaError_t dispatch_mode(const QuantArgs& a, int ny, int mode, bool qjl, int num_sms, cudaStream_t st) {
+  if (mode == MODE_GIVEN_Y) return run_quantize<BITS, float, MODE_GIVEN_Y, false>(a, ny, num_sms, st);
   if (mode == MODE_HADAMARD)
-    return qjl ? run_quantize<BITS, TIn, MODE_HADAMARD, true>(a, num_sms, st)
-               : run_quantize<BITS, TIn, MODE_HADAMARD, false>(a, num_sms, st);
-  return qjl ? run_quantize<BITS, TIn, MODE_DENSE, true>(a, num_sms, st)
-             : run_quantize<BITS, TIn, MODE_DENSE, false>(a, num_sms, st);
+    return qjl ? run_quantize<BITS, TIn, MODE_HADAMARD, true>(a, ny, num_sms, st)
+               : run_quantize<BITS, TIn, MODE_HADAMARD, false>(a, ny, num_sms, st);
+  return qjl ? run_quantize<BITS, TIn, MODE_DENSE, true>(a, ny, num_sms, st)
+             : run_quantize<BITS, TIn, MODE_DENSE, false>(a, ny, num_sms, st);
+}
+
+static QuantArgs quant_args(const tq_cache_desc& d, int which, const void* x, const float* y, const float* norms,
+                            const int64_t* slots, int64_t n_tok, unsigned* status) {
+  QuantArgs a;
+  a.x = x;
+  a.y = y;
+  a.norms = norms;
+  a.slots = slots;
+  a.n_vec = n_tok * d.num_kv_heads;
+  a.H = d.num_kv_heads;
+  a.max_slot = d.num_blocks * kBlock;
+  a.pool = reinterpret_cast<uint8_t*>(which == 0 ? d.k_cache : d.v_cache);
+  a.page_bytes = (int)page_bytes_of(d, which);
+  a.rot = d.rotation;
+  a.qjl = d.qjl_proj;
+  a.cb = codebook_of(d, which);
+  a.norm_mode = d.fmt.norm_mode;
+  a.status = status;
+  a.x_v = nullptr;
+  a.pool_v = nullptr;
+  return a;
 }
 
 cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, int in_dtype, const float* y,
                             const float* norms, const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms,
-                            cudaStream_t st) {
+                            cudaStream_t st, const void* x_v) {
   if (n_tok <= 0) return cudaSuccess;
   const int64_t n_vec = n_tok * d.num_kv_heads;
   const int64_t max_slot = d.num_blocks * kBlock;
@@ -389,37 +419,30 @@ cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, in
     else
       k_append_bf16<__nv_bfloat16><<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), slots,
                                                                    n_vec, d.num_kv_heads, max_slot, pool, status);
+    count_launch();
     return cudaGetLastError();
   }
-  QuantArgs a;
-  a.x = x;
-  a.y = y;
-  a.norms = norms;
-  a.slots = slots;
-  a.n_vec = n_vec;
-  a.H = d.num_kv_heads;
-  a.max_slot = max_slot;
-  a.pool = pool;
-  a.page_bytes = (int)page_bytes_of(d, which);
-  a.rot = d.rotation;
-  a.qjl = d.qjl_proj;
-  a.cb = codebook_of(d, which);
-  a.norm_mode = d.fmt.norm_mode;
-  a.status = status;
+  QuantArgs a = quant_args(d, which, x, y, norms, slots, n_tok, status);
+  int ny = 1;
+  if (x_v) {  // values in the same launch (caller checked that the formats and tables agree)
+    a.x_v = x_v;
+    a.pool_v = reinterpret_cast<uint8_t*>(d.v_cache);
+    ny = 2;
+  }
   const int bits = which == 0 ? d.fmt.bits_k : d.fmt.bits_v;
   const bool qjl = which == 0 && d.fmt.qjl_k && y == nullptr;
   const int mode = y ? MODE_GIVEN_Y : (d.fmt.rot_kind == TQ_ROT_DENSE ? MODE_DENSE : MODE_HADAMARD);
   const bool f32 = in_dtype == TQ_F32;
   switch (bits) {
     case 2:
-      return f32 ? dispatch_mode<2, float>(a, mode, qjl, num_sms, st)
-                 : dispatch_mode<2, __nv_bfloat16>(a, mode, qjl, num_sms, st);
+      return f32 ? dispatch_mode<2, float>(a, ny, mode, qjl, num_sms, st)
+                 : dispatch_mode<2, __nv_bfloat16>(a, ny, mode, qjl, num_sms, st);
     case 3:
-      return f32 ? dispatch_mode<3, float>(a, mode, qjl, num_sms, st)
-                 : dispatch_mode<3, __nv_bfloat16>(a, mode, qjl, num_sms, st);
+      return f32 ? dispatch_mode<3, float>(a, ny, mode, qjl, num_sms, st)
+                 : dispatch_mode<3, __nv_bfloat16>(a, ny, mode, qjl, num_sms, st);
     default:
-      return f32 ? dispatch_mode<4, float>(a, mode, qjl, num_sms, st)
-                 : dispatch_mode<4, __nv_bfloat16>(a, mode, qjl, num_sms, st);
+      return f32 ? dispatch_mode<4, float>(a, ny, mode, qjl, num_sms, st)
+                 : dispatch_mode<4, __nv_bfloat16>(a, ny, mode, qjl, num_sms, st);
   }
 }
 
@@ -437,6 +460,7 @@ static cudaError_t run_dequant(const tq_cache_desc& d, int which, const int64_t*
   kern<<<(unsigned)grid, kThreads, smem, st>>>(pool, (int)page_bytes_of(d, which), d.num_kv_heads,
                                               d.num_blocks * kBlock, slots, n_vec, d.rotation, codebook_of(d, which),
                                               reinterpret_cast<TOut*>(out), status);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -473,6 +497,7 @@ cudaError_t launch_dequant(const tq_cache_desc& d, int which, const int64_t* slo
       k_dequant_bf16<__nv_bfloat16><<<(unsigned)grid, 256, 0, st>>>(pool, d.num_kv_heads, d.num_blocks * kBlock,
                                                                      slots, n_vec,
                                                                      reinterpret_cast<__nv_bfloat16*>(out), status);
+    count_launch();
     return cudaGetLastError();
   }
   return out_dtype == TQ_F32 ? dequant_bits<float>(d, which, slots, n_vec, out, status, num_sms, st)
