@@ -148,8 +148,6 @@ __device__ __forceinline__ uint32_t lut(uint32_t lbase, uint32_t w, int k) {
   return lds32(__byte_perm(w, lbase, 0x7604u | ((uint32_t)k << 4)));
 }
 
-__device__ __forceinline__ uint32_t byte_of(uint32_t w, int k) { return __byte_perm(w, 0u, 0x4440u | (uint32_t)k); }
-
 // ------------------------------------------------------- codes -> nibbles
 
 // 3-bit codes of a 24-bit group -> one code per nibble.
@@ -225,7 +223,6 @@ struct DecodeArgs {
   int splits;  // chunks per unit
   int chunks;  // units * splits
   int stages;  // ring depth per warp
-  int lut_shared;
   int smem_bytes;  // dynamic shared memory of the launch
   int fuse_combine;  // 0: k_combine finishes; 1: decode finishes (identity); 2: decode finishes (Hadamard)
   int* counters;     // [units] chunks finished per unit (zeroed by k_rotate_q)
@@ -239,10 +236,31 @@ struct DecodeArgs {
   unsigned* status;
 };
 
-// Splits one fp32 query row (32 coordinates of quarter tig) into hi/lo A
-// fragments of 8 k-chunks (fp16 with a power-of-two scale, or bf16).  Returns 1/scale.
+// Lane layout of a warp (g_ = lane / 4, tig = lane % 4) for NT n-tiles of 4 heads.
+//
+// Keys: logits = K_hat (16 tokens x 16 coordinates) x Q'^T (16 x 8) per k-chunk c:
+// A rows are tokens g_, g_ + 8 of the block; the k index 2 tig + e maps to
+// coordinate 32 tig + 4 c + e and 2 tig + 8 + e to 32 tig + 4 c + 2 + e, so a
+// lane's A entries are the code bytes 16 tig + 2c, 2c + 1 of its two records.
+// Column n = 2 h + part (part 0: fp16 hi of the query, 1: the lo remainder), so
+// the lane holding D gets head 4 nt + tig for tokens g_ and g_ + 8.
+//
+// Values: acc (32 coordinates x 8 columns) += A (16 coordinate pairs x 16) x B
+// per m-tile mt and token tile kt, with k = (position p, parity e) and a block-
+// diagonal B[(p, e)][(h, e')] = P'[h][token(p)] [e = e'].  A[(row j)][(p, e)] is
+// the code pair byte of token(p), so bytes are used as stored.  Row g_ of m-tile
+// mt is the lane's byte 2 mt of coordinates [16 g_, 16 g_ + 16), row g_ + 8 byte
+// 2 mt + 1; position p = tig of tile kt is token 2 tig + 8 kt and p = tig + 4 is
+// token 2 tig + 1 + 8 kt.  The lane holding D gets head 4 nt + tig at coordinates
+// 16 g_ + 4 mt + {0, 1, 2, 3} = acc[nt][mt][0..3].
+
+// Key-side B fragments of one n-tile: lane (g_, tig) holds column g_ (head 4 nt +
+// g_ / 2, part g_ & 1) at coordinates 32 tig + [0, 32): chunk c, b0 = {4c, 4c + 1},
+// b1 = {4c + 2, 4c + 3}.  fp16 with a power-of-two scale per head (max |q| scale
+// < 2^14), or bf16.  Returns 1 / scale.
 template <bool BF16>
-__device__ __forceinline__ float make_q_frags(const float* qrow, bool valid, int tig, uint32_t (&a)[8][4]) {
+__device__ __forceinline__ float make_q_frags(const float* qrow, bool valid, int part, int tig,
+                                              uint32_t (&bq)[8][2]) {
   float v[32];
   if (valid) {
     load32<float>(qrow + 32 * tig, v);
@@ -255,105 +273,142 @@ __device__ __forceinline__ float make_q_frags(const float* qrow, bool valid, int
     float mx = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(v[i]));
-    mx = quad_max(mx);
+    mx = quad_max(mx);  // the quad (same g_) holds one head
     int e = 0;
     if (mx > 0.0f) frexpf(mx, &e);
-    scale = ldexpf(1.0f, 14 - e);  // max |q| * scale < 2^14
+    scale = ldexpf(1.0f, 14 - e);
   }
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    float hi[4], lo[4];
+    float x[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float s = v[4 * c + k] * scale;
-      hi[k] = BF16 ? __bfloat162float(__float2bfloat16_rn(s)) : __half2float(__float2half_rn(s));
-      lo[k] = s - hi[k];
+      const float sv = v[4 * c + k] * scale;
+      const float hi = BF16 ? __bfloat162float(__float2bfloat16_rn(sv)) : __half2float(__float2half_rn(sv));
+      x[k] = part ? sv - hi : hi;
     }
     if (BF16) {
-      a[c][0] = pack_bf162(hi[0], hi[1]);
-      a[c][1] = pack_bf162(lo[0], lo[1]);
-      a[c][2] = pack_bf162(hi[2], hi[3]);
-      a[c][3] = pack_bf162(lo[2], lo[3]);
+      bq[c][0] = pack_bf162(x[0], x[1]);
+      bq[c][1] = pack_bf162(x[2], x[3]);
     } else {
-      a[c][0] = pack_half2(hi[0], hi[1]);
-      a[c][1] = pack_half2(lo[0], lo[1]);
-      a[c][2] = pack_half2(hi[2], hi[3]);
-      a[c][3] = pack_half2(lo[2], lo[3]);
+      bq[c][0] = pack_half2(x[0], x[1]);
+      bq[c][1] = pack_half2(x[2], x[3]);
     }
   }
   return 1.0f / scale;
 }
 
-// Online-softmax state of one warp for head g_ (the thread's row): running max
-// M of the base-2 logits, partial denominator l = sum 2^(u - M), and a running
-// value reference R >= max_t 2^(u_t - M) gamma'_t.  The rotated-domain
-// accumulator fragments acc[i] (columns = heads 2 tig, 2 tig + 1; rows = coords
-// 16 g_ + 2i, +1) hold sum_t (2^(u_t - M) gamma'_t / R) c_V[idx'_t], so the MMA
-// operand P' = 2^(u - M) gamma' / R never exceeds 1 in fp16 and the MMA
-// accumulates straight into acc; the true sum is acc * R.
+// Online-softmax state of head 4 nt + tig, replicated on the 8 lanes of that tig:
+// running max M (integral, base 2), this lane's share of l = sum 2^(u - M), and a
+// power-of-two reference R >= every weight 2^(u - M) gamma' seen, so the fp16
+// MMA operand P' = w kPScale / R stays in (0, kPScale].  acc holds
+// sum_t P'_t c_V[idx'_t]; the true sum is acc R / kPScale.
+template <int NT>
 struct SoftmaxState {
-  float M, l, R, rR;
-  float acc[8][4];
+  float M[NT], l[NT], R[NT], rR[NT];
+  float acc[NT][4][4];
 };
 
-// Given the 4 scaled logits u (tokens 2tig, 2tig+1, 8+2tig, 9+2tig) and value
-// weights wv (gamma' or 1), updates M, l, R (rescaling acc when either moves)
-// and returns the B fragments of P' (fp16, or bf16 hi + lo).
-template <bool BF16>
-__device__ __forceinline__ void softmax_block(SoftmaxState& st, const float (&u)[4], const float (&wv)[4], int tig,
-                                              uint32_t& bp0, uint32_t& bp1, uint32_t& bl0, uint32_t& bl1) {
-  // M is kept integral and R a power of two, so every rescale is exact and the
-  // fp16 rounding of P' does not depend on which tokens came before.
-  float bmax = fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3]));
-  bmax = quad_max(bmax);
-  if (__any_sync(0xffffffffu, bmax > st.M + kRescaleThreshold)) {
-    const bool need = bmax > st.M + kRescaleThreshold;
-    const float newM = need ? ceilf(bmax) : st.M;
-    const float alpha = (st.M == -INFINITY) ? 0.0f : ldexpf(1.0f, (int)(st.M - newM));
-    st.l *= alpha;
-    st.R *= alpha;  // acc / R is unchanged by a common factor
-    st.M = newM;
-  }
-  float w[4];
-  float wmax = 0.0f;
+// Max over the 8 lanes sharing tig.
+__device__ __forceinline__ float col_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+}
+
+__device__ __forceinline__ float col_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  return v + __shfl_xor_sync(0xffffffffu, v, 16);
+}
+
+// u[nt][i]: base-2 logits of head 4 nt + tig for tokens g_ + 8 i (-inf when
+// masked); wv[i]: their value weights (gamma' or 1).  Updates the state and
+// returns P' of the two tokens packed as one pair (fp16; bf16 hi in pk, lo in pl).
+template <int NT, bool BF16>
+__device__ __forceinline__ void softmax_block(SoftmaxState<NT>& st, const float (&u)[NT][2], const float (&wv)[2],
+                                              uint32_t (&pk)[NT], uint32_t (&pl)[NT]) {
+  // M integral and R a power of two: every rescale is exact, and the rounding of
+  // P' does not depend on the tokens that came before (split invariance).
+  bool up = false;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float p = fast_exp2(u[e] - st.M);
-    st.l += p;
-    w[e] = p * wv[e];
-    wmax = fmaxf(wmax, w[e]);
-  }
-  wmax = quad_max(wmax);
-  if (__any_sync(0xffffffffu, wmax > st.R)) {
-    // smallest power of two >= max(R, wmax)
-    const float m = fmaxf(st.R, wmax);
-    const float newR = m > 0.0f ? __uint_as_float((__float_as_uint(m) + 0x007FFFFFu) & 0xFF800000u) : 0.0f;
-    const float beta = newR > 0.0f ? st.R / newR : 1.0f;
-    st.R = newR;
-    st.rR = newR > 0.0f ? kPScale / newR : 0.0f;
-    const float b0 = __shfl_sync(0xffffffffu, beta, (2 * tig) * 4);
-    const float b1 = __shfl_sync(0xffffffffu, beta, (2 * tig + 1) * 4);
+  for (int nt = 0; nt < NT; ++nt) up |= fmaxf(u[nt][0], u[nt][1]) > st.M[nt] + kRescaleThreshold;
+  if (__any_sync(0xffffffffu, up)) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      st.acc[i][0] *= b0; st.acc[i][1] *= b1; st.acc[i][2] *= b0; st.acc[i][3] *= b1;
+    for (int nt = 0; nt < NT; ++nt) {
+      const float bm = col_max(fmaxf(u[nt][0], u[nt][1]));
+      if (bm > st.M[nt] + kRescaleThreshold) {  // the same on the head's lanes
+        const float newM = ceilf(bm);
+        const float alpha = (st.M[nt] == -INFINITY) ? 0.0f : ldexpf(1.0f, (int)(st.M[nt] - newM));
+        st.l[nt] *= alpha;
+        st.R[nt] *= alpha;  // acc R is the true sum: scale R, keep acc
+        st.rR[nt] = st.R[nt] > 0.0f ? kPScale / st.R[nt] : 0.0f;
+        st.M[nt] = newM;
+      }
     }
   }
-  float pn[4];
+  float w[NT][2];
+  bool grow = false;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) pn[e] = w[e] * st.rR;
-  if (BF16) {
-    bp0 = pack_bf162(pn[0], pn[1]);
-    bp1 = pack_bf162(pn[2], pn[3]);
-    const __nv_bfloat162 h0 = *reinterpret_cast<__nv_bfloat162*>(&bp0);
-    const __nv_bfloat162 h1 = *reinterpret_cast<__nv_bfloat162*>(&bp1);
-    bl0 = pack_bf162(pn[0] - __low2float(h0), pn[1] - __high2float(h0));
-    bl1 = pack_bf162(pn[2] - __low2float(h1), pn[3] - __high2float(h1));
-  } else {
-    bp0 = pack_half2(pn[0], pn[1]);
-    bp1 = pack_half2(pn[2], pn[3]);
-    bl0 = bl1 = 0u;
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float p = fast_exp2(u[nt][i] - st.M[nt]);
+      st.l[nt] += p;
+      w[nt][i] = p * wv[i];
+      grow |= w[nt][i] > st.R[nt];
+    }
+  if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float wm = col_max(fmaxf(w[nt][0], w[nt][1]));
+      if (wm > st.R[nt]) {
+        const float newR = __uint_as_float((__float_as_uint(wm) + 0x007FFFFFu) & 0xFF800000u);  // pow2 >= wm
+        const float beta = st.R[nt] / newR;
+        st.R[nt] = newR;
+        st.rR[nt] = kPScale / newR;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) st.acc[nt][mt][e] *= beta;
+      }
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float p0 = w[nt][0] * st.rR[nt], p1 = w[nt][1] * st.rR[nt];
+    if (BF16) {
+      pk[nt] = pack_bf162(p0, p1);
+      const __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&pk[nt]);
+      pl[nt] = pack_bf162(p0 - __low2float(h), p1 - __high2float(h));
+    } else {
+      pk[nt] = pack_half2(p0, p1);
+      pl[nt] = 0u;
+    }
   }
 }
+
+// Value-side B fragments from the packed P' pairs: lane (g, t) takes head 4 nt + g/2
+// at tokens 2t, 2t + 8 (from lane 8t + g/2) and 2t + 1, 2t + 9 (lane 8t + 4 + g/2),
+// each placed in half g & 1 of its pair (the other half 0).
+struct PTranspose {
+  int srcx, srcy;
+  uint32_t sel0, sel1;  // byte selectors for token tile 0 (low halves) and 1 (high halves)
+  __device__ __forceinline__ void init(int g_, int tig) {
+    srcx = 8 * tig + (g_ >> 1);
+    srcy = srcx + 4;
+    sel0 = (g_ & 1) ? 0x1044u : 0x4410u;
+    sel1 = (g_ & 1) ? 0x3244u : 0x4432u;
+  }
+  __device__ __forceinline__ void apply(uint32_t pk, uint32_t (&bv)[2][2]) const {
+    const uint32_t x = __shfl_sync(0xffffffffu, pk, srcx);
+    const uint32_t y = __shfl_sync(0xffffffffu, pk, srcy);
+    bv[0][0] = __byte_perm(x, 0u, sel0);
+    bv[0][1] = __byte_perm(y, 0u, sel0);
+    bv[1][0] = __byte_perm(x, 0u, sel1);
+    bv[1][1] = __byte_perm(y, 0u, sel1);
+  }
+};
 
 // Block-table entries of one warp's chunk, read 32 at a time into a register
 // (lane k holds entry 32 r + k) with the next 32 already in flight, so issuing a
@@ -412,151 +467,171 @@ __device__ __forceinline__ bool issue_block(const Ring& r, int stage, const Deco
 
 // ------------------------------------------------------------ block compute
 
+// Per-warp constants of the block loop.
+template <int NT>
+struct WarpConsts {
+  uint32_t bq[NT][8][2];  // key-side query fragments
+  uint32_t bu[NT][8][2];  // QJL: fragments of S q'
+  float inv_qs[NT];       // 1 / query scale of head 4 nt + tig
+  float inv_us[NT];
+  PTranspose pt;
+  uint32_t lk, lv;        // code-table lane bases
+  int g_, tig;
+};
+
 // One 16-token block of packed K/V for one warp.
-template <int BK, int BV, bool QJL>
-__device__ __forceinline__ void packed_block(SoftmaxState& st, const uint8_t* sk, const uint8_t* sv, int t0, int ctx,
-                                             const uint32_t (&aq)[8][4], const uint32_t (&au)[8][4], float inv_qs,
-                                             float inv_us, uint32_t lk, uint32_t lv, float qjl_coef, int g_,
-                                             int tig) {
+template <int NT, int BK, int BV, bool QJL>
+__device__ __forceinline__ void packed_block(SoftmaxState<NT>& st, const WarpConsts<NT>& wc, const uint8_t* sk,
+                                             const uint8_t* sv, int t0, int ctx, float qjl_coef) {
   constexpr int RK = 16 * BK, RV = 16 * BV;
-  float s[2][4], sq[2][4];
+  const int g_ = wc.g_, tig = wc.tig;
+  // ---- keys: 8 k-chunks, two accumulation chains per n-tile
   uint32_t kn[2][4];
   load_quarter<BK>(sk + g_ * RK, tig, kn[0]);
-  load_quarter<BK>(sk + (8 + g_) * RK, tig, kn[1]);
-  {
-    // two independent accumulation chains per n-tile (even / odd k-chunks)
-    float acc2[2][2][4];
+  load_quarter<BK>(sk + (g_ + 8) * RK, tig, kn[1]);
+  float dk[NT][2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int p = 0; p < 2; ++p)
+    for (int p = 0; p < 2; ++p)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc2[nt][p][e] = 0.0f;
+      for (int e = 0; e < 4; ++e) dk[nt][p][e] = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int wi = c >> 1, bi = 2 * (c & 1);
+    const uint32_t ak[4] = {lut(wc.lk, kn[0][wi], bi), lut(wc.lk, kn[1][wi], bi), lut(wc.lk, kn[0][wi], bi + 1),
+                            lut(wc.lk, kn[1][wi], bi + 1)};
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mma_f16(dk[nt][c & 1], ak, wc.bq[nt][c][0], wc.bq[nt][c][1], dk[nt][c & 1]);
+  }
+  float sq[NT][2];
+  if constexpr (QJL) {  // sign term: rows = tokens, columns = S q' (hi, lo)
+    const uint32_t sw0 = *reinterpret_cast<const uint32_t*>(sk + 16 * RK + 64 + 16 * g_ + 4 * tig);
+    const uint32_t sw1 = *reinterpret_cast<const uint32_t*>(sk + 16 * RK + 64 + 16 * (g_ + 8) + 4 * tig);
+    float dq[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) dq[nt][0] = dq[nt][1] = dq[nt][2] = dq[nt][3] = 0.0f;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
+      // stored bit 1 = +1: f16x2 of (+-1, +-1) with the sign bits from the complement
+      const uint32_t n0 = ~sw0 >> (4 * c), n1 = ~sw1 >> (4 * c);
+      const uint32_t a[4] = {0x3C003C00u | ((n0 & 1u) << 15) | ((n0 & 2u) << 30),
+                             0x3C003C00u | ((n1 & 1u) << 15) | ((n1 & 2u) << 30),
+                             0x3C003C00u | ((n0 & 4u) << 13) | ((n0 & 8u) << 28),
+                             0x3C003C00u | ((n1 & 4u) << 13) | ((n1 & 8u) << 28)};
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const uint32_t w = kn[nt][c >> 1];
-        const int k0 = 2 * (c & 1);
-        mma_f16(acc2[nt][c & 1], aq[c], lut(lk, w, k0), lut(lk, w, k0 + 1), acc2[nt][c & 1]);
-      }
+      for (int nt = 0; nt < NT; ++nt) mma_f16(dq[nt], a, wc.bu[nt][c][0], wc.bu[nt][c][1], dq[nt]);
     }
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[nt][e] = acc2[nt][0][e] + acc2[nt][1][e];
+    for (int nt = 0; nt < NT; ++nt) {
+      sq[nt][0] = dq[nt][0] + dq[nt][1];
+      sq[nt][1] = dq[nt][2] + dq[nt][3];
+    }
   }
+  const float* gk = reinterpret_cast<const float*>(sk + 16 * RK);
+  const float* gv = reinterpret_cast<const float*>(sv + 16 * RV);
+  const float gk0 = gk[g_], gk1 = gk[g_ + 8];
+  const float wv[2] = {gv[g_], gv[g_ + 8]};
+  const bool in0 = t0 + g_ < ctx, in1 = t0 + g_ + 8 < ctx;
+  float u[NT][2];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
+  for (int nt = 0; nt < NT; ++nt) {
+    float v0 = gk0 * ((dk[nt][0][0] + dk[nt][0][1]) + (dk[nt][1][0] + dk[nt][1][1])) * wc.inv_qs[nt];
+    float v1 = gk1 * ((dk[nt][0][2] + dk[nt][0][3]) + (dk[nt][1][2] + dk[nt][1][3])) * wc.inv_qs[nt];
     if constexpr (QJL) {
-      const uint32_t sw = *reinterpret_cast<const uint32_t*>(sk + 16 * RK + 64 + 16 * (8 * nt + g_) + 4 * tig);
-      float accq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t nb = ~(sw >> (4 * c));
-        const uint32_t b0 = 0x3C003C00u | ((nb & 1u) << 15) | ((nb & 2u) << 30);
-        const uint32_t b1 = 0x3C003C00u | ((nb & 4u) << 13) | ((nb & 8u) << 28);
-        mma_f16(accq, au[c], b0, b1, accq);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sq[nt][e] = accq[e];
+      const float* rh = reinterpret_cast<const float*>(sk + 16 * RK + 64 + 256);
+      v0 += qjl_coef * rh[g_] * sq[nt][0] * wc.inv_us[nt];
+      v1 += qjl_coef * rh[g_ + 8] * sq[nt][1] * wc.inv_us[nt];
     }
+    u[nt][0] = in0 ? v0 : -INFINITY;
+    u[nt][1] = in1 ? v1 : -INFINITY;
   }
-  float u[4], wv[4];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    const float2 gk = *reinterpret_cast<const float2*>(sk + 16 * RK + 4 * (8 * nt + 2 * tig));
-    const float2 gv = *reinterpret_cast<const float2*>(sv + 16 * RV + 4 * (8 * nt + 2 * tig));
-    float v0 = gk.x * (s[nt][0] + s[nt][2]) * inv_qs;
-    float v1 = gk.y * (s[nt][1] + s[nt][3]) * inv_qs;
-    if constexpr (QJL) {
-      const float2 rh = *reinterpret_cast<const float2*>(sk + 16 * RK + 64 + 256 + 4 * (8 * nt + 2 * tig));
-      v0 += qjl_coef * rh.x * (sq[nt][0] + sq[nt][2]) * inv_us;
-      v1 += qjl_coef * rh.y * (sq[nt][1] + sq[nt][3]) * inv_us;
-    }
-    const int tt = t0 + 8 * nt + 2 * tig;
-    u[2 * nt] = tt < ctx ? v0 : -INFINITY;
-    u[2 * nt + 1] = tt + 1 < ctx ? v1 : -INFINITY;
-    wv[2 * nt] = gv.x;
-    wv[2 * nt + 1] = gv.y;
-  }
-  uint32_t bp0, bp1, bl0, bl1;
-  softmax_block<false>(st, u, wv, tig, bp0, bp1, bl0, bl1);
+  uint32_t pk[NT], pl[NT];
+  softmax_block<NT, false>(st, u, wv, pk, pl);
 
-  // values: rows = coordinates 16 g_ + 2i (+1), k = tokens 2tig, 2tig+1, 2tig+8, 2tig+9
-  uint32_t vA[2], vB[2], vC[2], vD[2];
-  load_sixteenth<BV>(sv + (2 * tig) * RV, g_, vA);
-  load_sixteenth<BV>(sv + (2 * tig + 1) * RV, g_, vB);
-  load_sixteenth<BV>(sv + (2 * tig + 8) * RV, g_, vC);
-  load_sixteenth<BV>(sv + (2 * tig + 9) * RV, g_, vD);
+  // ---- values: tokens 2 tig (+1) of tile 0 and 2 tig + 8 (+1) of tile 1
+  uint32_t vw[4][2];
+  load_sixteenth<BV>(sv + (2 * tig) * RV, g_, vw[0]);
+  load_sixteenth<BV>(sv + (2 * tig + 1) * RV, g_, vw[1]);
+  load_sixteenth<BV>(sv + (2 * tig + 8) * RV, g_, vw[2]);
+  load_sixteenth<BV>(sv + (2 * tig + 9) * RV, g_, vw[3]);
+  uint32_t bv[NT][2][2];
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
+  for (int nt = 0; nt < NT; ++nt) wc.pt.apply(pk[nt], bv[nt]);
 #pragma unroll
-    for (int q2 = 0; q2 < 2; ++q2) {
-      // byte m of a nibble word holds codes (2m, 2m+1): m-tiles 4 half + 2 q2 + {0, 1}
-      const uint32_t sel = q2 ? 0x7362u : 0x5140u;
-      const uint32_t xab = __byte_perm(vA[half], vB[half], sel);  // A(m), B(m), A(m+1), B(m+1)
-      const uint32_t xcd = __byte_perm(vC[half], vD[half], sel);
-      // pair bytes (token-A code | token-B code << 4): low nibbles -> row g_, high nibbles -> row g_+8
-      const uint32_t lab = (xab & 0x0F0F0F0Fu) | ((xab >> 4) & 0xF0F0F0F0u);
-      const uint32_t hab = ((xab >> 4) & 0x0F0F0F0Fu) | ((xab >> 8) & 0xF0F0F0F0u);
-      const uint32_t lcd = (xcd & 0x0F0F0F0Fu) | ((xcd >> 4) & 0xF0F0F0F0u);
-      const uint32_t hcd = ((xcd >> 4) & 0x0F0F0F0Fu) | ((xcd >> 8) & 0xF0F0F0F0u);
+  for (int kt = 0; kt < 2; ++kt)
 #pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const int mt = 4 * half + 2 * q2 + m;
-        const uint32_t av[4] = {lut(lv, lab, 2 * m), lut(lv, hab, 2 * m), lut(lv, lcd, 2 * m),
-                                lut(lv, hcd, 2 * m)};
-        mma_f16(st.acc[mt], av, bp0, bp1, st.acc[mt]);
-      }
+    for (int mt = 0; mt < 4; ++mt) {
+      const int wi = mt >> 1, bi = 2 * (mt & 1);
+      const uint32_t av[4] = {lut(wc.lv, vw[2 * kt][wi], bi), lut(wc.lv, vw[2 * kt][wi], bi + 1),
+                              lut(wc.lv, vw[2 * kt + 1][wi], bi), lut(wc.lv, vw[2 * kt + 1][wi], bi + 1)};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_f16(st.acc[nt][mt], av, bv[nt][kt][0], bv[nt][kt][1], st.acc[nt][mt]);
     }
-  }
 }
 
-// One 16-token block of raw bf16 K/V for one warp.
-__device__ __forceinline__ void bf16_block(SoftmaxState& st, const uint8_t* sk, const uint8_t* sv, int t0, int ctx,
-                                           const uint32_t (&aq)[8][4], int g_, int tig) {
+// One 16-token block of raw bf16 K/V for one warp (same fragment layout; bf16
+// MMAs, P' split into bf16 hi + lo).
+template <int NT>
+__device__ __forceinline__ void bf16_block(SoftmaxState<NT>& st, const WarpConsts<NT>& wc, const uint8_t* sk,
+                                           const uint8_t* sv, int t0, int ctx) {
   constexpr int RB = kD * 2;  // bytes per token row
-  const float ones[4] = {1.0f, 1.0f, 1.0f, 1.0f};
-  float u[4];
+  const int g_ = wc.g_, tig = wc.tig;
+  const uint4* kr0 = reinterpret_cast<const uint4*>(sk + g_ * RB + 64 * tig);
+  const uint4* kr1 = reinterpret_cast<const uint4*>(sk + (g_ + 8) * RB + 64 * tig);
+  float dk[NT][2][4];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    // keys of token 8 nt + g_, coordinates [32 tig, 32 tig + 32): 64 contiguous bytes
-    const uint4* kr = reinterpret_cast<const uint4*>(sk + (8 * nt + g_) * RB + 64 * tig);
-    uint32_t kw[16];
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const uint4 v = kr[x];
-      kw[4 * x] = v.x; kw[4 * x + 1] = v.y; kw[4 * x + 2] = v.z; kw[4 * x + 3] = v.w;
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dk[nt][p][e] = 0.0f;
+#pragma unroll
+  for (int c2 = 0; c2 < 4; ++c2) {
+    const uint4 k0 = kr0[c2], k1 = kr1[c2];
+    const uint32_t a0[4] = {k0.x, k1.x, k0.y, k1.y};  // chunk 2 c2
+    const uint32_t a1[4] = {k0.z, k1.z, k0.w, k1.w};  // chunk 2 c2 + 1
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mma_bf16(dk[nt][0], a0, wc.bq[nt][2 * c2][0], wc.bq[nt][2 * c2][1], dk[nt][0]);
+      mma_bf16(dk[nt][1], a1, wc.bq[nt][2 * c2 + 1][0], wc.bq[nt][2 * c2 + 1][1], dk[nt][1]);
     }
-    float accs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int c = 0; c < 8; ++c) mma_bf16(accs, aq[c], kw[2 * c], kw[2 * c + 1], accs);
-    const int tt = t0 + 8 * nt + 2 * tig;
-    u[2 * nt] = tt < ctx ? accs[0] + accs[2] : -INFINITY;
-    u[2 * nt + 1] = tt + 1 < ctx ? accs[1] + accs[3] : -INFINITY;
   }
-  uint32_t bp0, bp1, bl0, bl1;
-  softmax_block<true>(st, u, ones, tig, bp0, bp1, bl0, bl1);
-  const uint4* va = reinterpret_cast<const uint4*>(sv + (2 * tig) * RB + 32 * g_);
-  const uint4* vb = reinterpret_cast<const uint4*>(sv + (2 * tig + 1) * RB + 32 * g_);
-  const uint4* vc = reinterpret_cast<const uint4*>(sv + (2 * tig + 8) * RB + 32 * g_);
-  const uint4* vd = reinterpret_cast<const uint4*>(sv + (2 * tig + 9) * RB + 32 * g_);
-  uint32_t wa[8], wb[8], wc[8], wd[8];
+  const bool in0 = t0 + g_ < ctx, in1 = t0 + g_ + 8 < ctx;
+  float u[NT][2];
 #pragma unroll
-  for (int x = 0; x < 2; ++x) {
-    uint4 t;
-    t = va[x]; wa[4 * x] = t.x; wa[4 * x + 1] = t.y; wa[4 * x + 2] = t.z; wa[4 * x + 3] = t.w;
-    t = vb[x]; wb[4 * x] = t.x; wb[4 * x + 1] = t.y; wb[4 * x + 2] = t.z; wb[4 * x + 3] = t.w;
-    t = vc[x]; wc[4 * x] = t.x; wc[4 * x + 1] = t.y; wc[4 * x + 2] = t.z; wc[4 * x + 3] = t.w;
-    t = vd[x]; wd[4 * x] = t.x; wd[4 * x + 1] = t.y; wd[4 * x + 2] = t.z; wd[4 * x + 3] = t.w;
+  for (int nt = 0; nt < NT; ++nt) {
+    const float v0 = (dk[nt][0][0] + dk[nt][0][1]) + (dk[nt][1][0] + dk[nt][1][1]);
+    const float v1 = (dk[nt][0][2] + dk[nt][0][3]) + (dk[nt][1][2] + dk[nt][1][3]);
+    u[nt][0] = in0 ? v0 : -INFINITY;
+    u[nt][1] = in1 ? v1 : -INFINITY;
+  }
+  const float ones[2] = {1.0f, 1.0f};
+  uint32_t pk[NT], pl[NT];
+  softmax_block<NT, true>(st, u, ones, pk, pl);
+  uint32_t bh[NT][2][2], bl[NT][2][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    wc.pt.apply(pk[nt], bh[nt]);
+    wc.pt.apply(pl[nt], bl[nt]);
   }
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const uint32_t av[4] = {__byte_perm(wa[mt], wb[mt], 0x5410u), __byte_perm(wa[mt], wb[mt], 0x7632u),
-                            __byte_perm(wc[mt], wd[mt], 0x5410u), __byte_perm(wc[mt], wd[mt], 0x7632u)};
-    mma_bf16(st.acc[mt], av, bp0, bp1, st.acc[mt]);
-    mma_bf16(st.acc[mt], av, bl0, bl1, st.acc[mt]);
+  for (int kt = 0; kt < 2; ++kt) {
+    // coordinates [16 g_, 16 g_ + 16) of tokens 2 tig + 8 kt (F) and 2 tig + 1 + 8 kt (S)
+    const uint4* rf = reinterpret_cast<const uint4*>(sv + (2 * tig + 8 * kt) * RB + 32 * g_);
+    const uint4* rs = reinterpret_cast<const uint4*>(sv + (2 * tig + 1 + 8 * kt) * RB + 32 * g_);
+    const uint4 f0 = rf[0], f1 = rf[1], s0 = rs[0], s1 = rs[1];
+    const uint32_t wf[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+    const uint32_t ws[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const uint32_t av[4] = {wf[2 * mt], wf[2 * mt + 1], ws[2 * mt], ws[2 * mt + 1]};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_bf16(st.acc[nt][mt], av, bh[nt][kt][0], bh[nt][kt][1], st.acc[nt][mt]);
+        mma_bf16(st.acc[nt][mt], av, bl[nt][kt][0], bl[nt][kt][1], st.acc[nt][mt]);
+      }
+    }
   }
 }
 
@@ -569,8 +644,9 @@ __device__ __forceinline__ void bf16_block(SoftmaxState& st, const uint8_t* sk, 
 //           [0x10000, 0x20000), rings of the other warps from 0x20000;
 //   bf16:   rings from base.  mbarriers at the top.  The merge scratch of the
 //   epilogue reuses the rings above the tables (drained by then).
-template <int KIND, int BK, int BV, bool QJL, int NW>
+template <int KIND, int BK, int BV, bool QJL, int NT, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
+  constexpr int HPW = 4 * NT;  // heads per warp
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g_ = lane >> 2, tig = lane & 3;
@@ -598,8 +674,8 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   const int b = has ? unit / per_b : 0;
   const int r = has ? unit - b * per_b : 0;
   const int kvh = r / a.ngroups, hg = r - (r / a.ngroups) * a.ngroups;
-  const int head0 = kvh * a.g + hg * 8;
-  const int gc = min(8, a.g - hg * 8);
+  const int head0 = kvh * a.g + hg * HPW;
+  const int gc = min(HPW, a.g - hg * HPW);
   int ctx = has ? __ldg(a.ctx_lens + b) : 0;
   if (ctx < 0 || ctx > a.max_blocks * kBlock) {
     if (lane == 0 && s == 0 && r == 0) flag_status(a.status, TQ_DEV_BAD_CONTEXT);
@@ -629,39 +705,53 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
 
   if constexpr (KIND == 0) {
     if (layout_ok) {
-      // row e (pair byte, low nibble first) = f16x2(c[e & 15], c[e >> 4]), once per lane, K then V;
-      // lanes 0..15 hold the key centroids, lanes 16..31 the value centroids
+      // row e (pair byte, low nibble first) = f16x2(c[e & 15], c[e >> 4]) once per lane:
+      // 16-byte word j of a row holds lanes 4j..4j+3 (j < 8: keys, j >= 8: values)
       constexpr uint32_t MK = (1u << BK) - 1u, MV = (1u << BV) - 1u;
       const float cl = lane < 16 ? a.cbk.c[lane & MK] : a.cbv.c[(lane - 16) & MV];
-      uint32_t* tab = reinterpret_cast<uint32_t*>(gen(kLutAddr));
-      for (int i = threadIdx.x; i < 256 * 64; i += blockDim.x) {
-        const int e = i >> 6;              // warp-uniform
-        const int vo = (i & 32) ? 16 : 0;  // warp-uniform
+      uint4* tab = reinterpret_cast<uint4*>(gen(kLutAddr));
+      for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
+        const int e = i >> 4, vo = (i & 8) ? 16 : 0;
         const float lo = __shfl_sync(0xffffffffu, cl, vo + (e & 15));
         const float hi = __shfl_sync(0xffffffffu, cl, vo + (e >> 4));
-        tab[i] = pack_half2(lo, hi);
+        const uint32_t v = pack_half2(lo, hi);
+        tab[i] = make_uint4(v, v, v, v);
       }
     }
   }
   __syncthreads();  // tables ready
 
-  const bool hv = g_ < gc;
-  const int64_t qrow = ((int64_t)b * a.Hq + head0 + (hv ? g_ : 0)) * kD;
-  uint32_t aq[8][4];
-  uint32_t au[8][4];
-  float inv_qs = 1.0f, inv_us = 0.0f;
-  inv_qs = make_q_frags<KIND == 1>(a.qrot + qrow, hv && has, tig, aq);
-  if constexpr (QJL) inv_us = make_q_frags<false>(a.uqjl + qrow, hv && has, tig, au);
-  const uint32_t lk = kLutAddr | (4u * lane);
-  const uint32_t lv = lk + 128u;
-
-  SoftmaxState st;
-  st.M = -INFINITY;
-  st.l = 0.0f;
-  st.R = 0.0f;
-  st.rR = 0.0f;
+  // per-warp constants: query fragments of column g_ (head 4 nt + g_ / 2, part g_ & 1)
+  WarpConsts<NT> wc;
+  wc.g_ = g_;
+  wc.tig = tig;
+  wc.pt.init(g_, tig);
+  wc.lk = kLutAddr | (4u * lane);
+  wc.lv = wc.lk + 128u;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) st.acc[i][0] = st.acc[i][1] = st.acc[i][2] = st.acc[i][3] = 0.0f;
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hq = 4 * nt + (g_ >> 1);
+    const bool hv = has && hq < gc;
+    const int64_t qrow = ((int64_t)b * a.Hq + head0 + (hv ? hq : 0)) * kD;
+    const float iq = make_q_frags<KIND == 1>(a.qrot + qrow, hv, g_ & 1, tig, wc.bq[nt]);
+    wc.inv_qs[nt] = __shfl_sync(0xffffffffu, iq, 8 * tig);  // scale of head 4 nt + tig
+    wc.inv_us[nt] = 0.0f;
+    if constexpr (QJL) {
+      const float iu = make_q_frags<false>(a.uqjl + qrow, hv, g_ & 1, tig, wc.bu[nt]);
+      wc.inv_us[nt] = __shfl_sync(0xffffffffu, iu, 8 * tig);
+    }
+  }
+
+  SoftmaxState<NT> st;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    st.M[nt] = -INFINITY;
+    st.l[nt] = 0.0f;
+    st.R[nt] = 0.0f;
+    st.rR[nt] = 0.0f;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) st.acc[nt][mt][0] = st.acc[nt][mt][1] = st.acc[nt][mt][2] = st.acc[nt][mt][3] = 0.0f;
+  }
 
   int i = 0, stage = 0;
   uint32_t phase = 0u;
@@ -677,9 +767,9 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
       const uint8_t* sv = sk + a.kpage;
       const int t0 = (j0 + i) * kBlock;
       if constexpr (KIND == 0)
-        packed_block<BK, BV, QJL>(st, sk, sv, t0, ctx, aq, au, inv_qs, inv_us, lk, lv, a.qjl_coef, g_, tig);
+        packed_block<NT, BK, BV, QJL>(st, wc, sk, sv, t0, ctx, a.qjl_coef);
       else
-        bf16_block(st, sk, sv, t0, ctx, aq, g_, tig);
+        bf16_block<NT>(st, wc, sk, sv, t0, ctx);
     }
     __syncwarp();
     if (i + a.stages < n_my) {
@@ -698,19 +788,22 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
       mbar_wait(ring.bar + stg, ph);
       if (++stg == a.stages) { stg = 0; ph ^= 1u; }
     }
-    st.M = -INFINITY;
-    st.l = 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      st.M[nt] = -INFINITY;
+      st.l[nt] = 0.0f;
+    }
   }
 
   // ---- merge the warps of this CTA that share a unit; one partial per group
-  st.l = quad_sum(st.l);
-  {  // acc holds sum / R per column (head): restore the scale
-    const float r0 = __shfl_sync(0xffffffffu, st.R, (2 * tig) * 4) * (1.0f / kPScale);
-    const float r1 = __shfl_sync(0xffffffffu, st.R, (2 * tig + 1) * 4) * (1.0f / kPScale);
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      st.acc[mt][0] *= r0; st.acc[mt][1] *= r1; st.acc[mt][2] *= r0; st.acc[mt][3] *= r1;
-    }
+  for (int nt = 0; nt < NT; ++nt) {
+    st.l[nt] = col_sum(st.l[nt]);
+    const float rs = st.R[nt] * (1.0f / kPScale);  // acc holds sum / R (scaled)
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) st.acc[nt][mt][e] *= rs;
   }
   __syncthreads();  // every ring is drained: reuse the stage memory
   float* racc = reinterpret_cast<float*>(gen(hi0));  // [NW warps][8 heads][128]
@@ -718,17 +811,16 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   float* rl = rm + NW * 8;                            // [NW][8]
   int* runit = reinterpret_cast<int*>(rl + NW * 8);
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int c0 = 16 * g_ + 2 * mt;
-    float* base = racc + warp * 8 * kD;
-    base[(2 * tig) * kD + c0] = st.acc[mt][0];
-    base[(2 * tig + 1) * kD + c0] = st.acc[mt][1];
-    base[(2 * tig) * kD + c0 + 1] = st.acc[mt][2];
-    base[(2 * tig + 1) * kD + c0 + 1] = st.acc[mt][3];
-  }
-  if (tig == 0) {
-    rm[warp * 8 + g_] = st.M;
-    rl[warp * 8 + g_] = st.l;
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hl = 4 * nt + tig;
+    float4* dst = reinterpret_cast<float4*>(racc + (warp * 8 + hl) * kD + 16 * g_);
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+      dst[mt] = make_float4(st.acc[nt][mt][0], st.acc[nt][mt][1], st.acc[nt][mt][2], st.acc[nt][mt][3]);
+    if (g_ == 0) {
+      rm[warp * 8 + hl] = st.M[nt];
+      rl[warp * 8 + hl] = st.l[nt];
+    }
   }
   if (lane == 0) runit[warp] = unit;
   __syncthreads();
@@ -776,9 +868,9 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   // (max, denominator) of every (head, slot): lane l holds slots l + 32 g, all loads in flight at once
   constexpr int kG = kMaxFusedSplits / 32;
   const int64_t row0 = ((int64_t)b * a.Hq + head0) * a.splits;
-  float fm[8][kG], fl[8][kG];
+  float fm[HPW][kG], fl[HPW][kG];
 #pragma unroll
-  for (int h = 0; h < 8; ++h)
+  for (int h = 0; h < HPW; ++h)
 #pragma unroll
     for (int g = 0; g < kG; ++g) {
       const int s2 = lane + 32 * g;
@@ -786,9 +878,9 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
       fm[h][g] = in ? __ldcg(a.ml + (row0 + (int64_t)h * a.splits + s2) * 2) : -INFINITY;
       fl[h][g] = in ? __ldcg(a.ml + (row0 + (int64_t)h * a.splits + s2) * 2 + 1) : 0.0f;
     }
-  float Lh[8];
+  float Lh[HPW];
 #pragma unroll
-  for (int h = 0; h < 8; ++h) {
+  for (int h = 0; h < HPW; ++h) {
     float mx = -INFINITY;
 #pragma unroll
     for (int g = 0; g < kG; ++g) mx = fmaxf(mx, fm[h][g]);
@@ -805,9 +897,9 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     Lh[h] = L;
   }
   // sum the few non-empty slots (emptiness is per chunk, the same for every head)
-  float yh[8][4];
+  float yh[HPW][4];
 #pragma unroll
-  for (int h = 0; h < 8; ++h) yh[h][0] = yh[h][1] = yh[h][2] = yh[h][3] = 0.0f;
+  for (int h = 0; h < HPW; ++h) yh[h][0] = yh[h][1] = yh[h][2] = yh[h][3] = 0.0f;
 #pragma unroll
   for (int g = 0; g < kG; ++g) {
     uint32_t live = __ballot_sync(0xffffffffu, fm[0][g] > 0.0f);
@@ -816,7 +908,7 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
       live &= live - 1;
       const int s2 = src + 32 * g;
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
+      for (int h = 0; h < HPW; ++h) {
         const float f = __shfl_sync(0xffffffffu, fm[h][g], src);
         if (h < gc) {
           const float4 v =
@@ -830,7 +922,7 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     }
   }
 #pragma unroll
-  for (int h = 0; h < 8; ++h) {
+  for (int h = 0; h < HPW; ++h) {
     if (h >= gc) break;
     const float rl = Lh[h] > 0.0f ? 1.0f / Lh[h] : 0.0f;
     float y[4];
@@ -983,10 +1075,10 @@ Codebook codebook_of(const tq_cache_desc& d, int which);
 constexpr int kPackedWarps = 16;
 constexpr int kWideWarps = 8;
 
-template <int KIND, int BK, int BV, bool QJL>
-static cudaError_t run_decode(DecodeArgs a, cudaStream_t st) {
+template <int KIND, int BK, int BV, bool QJL, int NT>
+static cudaError_t run_decode_nt(DecodeArgs a, cudaStream_t st) {
   constexpr int NW = (KIND == 0 && !QJL) ? kPackedWarps : kWideWarps;
-  auto kern = k_decode<KIND, BK, BV, QJL, NW>;
+  auto kern = k_decode<KIND, BK, BV, QJL, NT, NW>;
   int dev = 0, optin = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1001,6 +1093,12 @@ static cudaError_t run_decode(DecodeArgs a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Heads per warp: 4 (one n-tile) for GQA groups of up to 4 query heads, else 8.
+template <int KIND, int BK, int BV, bool QJL>
+static cudaError_t run_decode(const DecodeArgs& a, cudaStream_t st) {
+  return a.g <= 4 ? run_decode_nt<KIND, BK, BV, QJL, 1>(a, st) : run_decode_nt<KIND, BK, BV, QJL, 2>(a, st);
+}
+
 template <int BK, bool QJL>
 static cudaError_t dispatch_bv(const DecodeArgs& a, int bv, cudaStream_t st) {
   switch (bv) {
@@ -1008,13 +1106,6 @@ static cudaError_t dispatch_bv(const DecodeArgs& a, int bv, cudaStream_t st) {
     case 3: return run_decode<0, BK, 3, QJL>(a, st);
     default: return run_decode<0, BK, 4, QJL>(a, st);
   }
-}
-
-static bool same_table(const Codebook& x, const Codebook& y, int bx, int by) {
-  if (bx != by) return false;
-  for (int i = 0; i < (1 << bx); ++i)
-    if (x.c[i] != y.c[i]) return false;
-  return true;
 }
 
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
@@ -1055,14 +1146,13 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   a.uqjl = uq;
   a.Hq = c.num_q_heads;
   a.g = c.num_q_heads / d.num_kv_heads;
-  a.ngroups = (a.g + 7) / 8;
+  a.ngroups = (a.g + (a.g <= 4 ? 3 : 7)) / (a.g <= 4 ? 4 : 8);  // head groups of 4 or 8 per warp
   a.splits = c.splits;
   a.chunks = c.batch * d.num_kv_heads * a.ngroups * c.splits;
   a.part = reinterpret_cast<float*>(c.workspace + ws.part_off);
   a.ml = reinterpret_cast<float*>(c.workspace + ws.ml_off);
   a.cbk = codebook_of(d, 0);
   a.cbv = codebook_of(d, 1);
-  a.lut_shared = (!bf16 && same_table(a.cbk, a.cbv, d.fmt.bits_k, d.fmt.bits_v)) ? 1 : 0;
   a.qjl_coef = 1.2533141373155003f / (float)kD;  // sqrt(pi/2) / m
   a.status = c.status;
   // the decode kernel finishes the job itself unless the inverse rotation is a dense mat-vec
