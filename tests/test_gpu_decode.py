@@ -200,3 +200,40 @@ def test_llama8b_shape_full_size_sampled(cuda, tqlib):
             errs.append(max_rel_err(o[b, h][None], ref[None]))
     print("sampled max rel err %.3e" % max(errs))
     assert max(errs) <= TOL_BF16
+
+
+def test_late_max_jump_after_large_weight(cuda, tqlib):
+    """Rescale path of the online softmax: token A (large value norm) sits just
+    under the lazy-rescale threshold and sets the value reference, then token B
+    moves the running maximum by more than the threshold while its own weight
+    stays below the rescaled reference.  One chunk per unit, fp32 throughout."""
+    tq = tqlib
+    rng = np.random.default_rng(17)
+    Hkv, Hq, T = 1, 4, 128
+    q = rng.standard_normal((1, Hq, D))
+    sm = 1.0 / math.sqrt(D)
+    qn = q[0, 0] / np.linalg.norm(q[0, 0])
+    per_unit = np.linalg.norm(q[0, 0]) * sm / math.log(2.0)  # base-2 logit per unit of k along q
+    k = rng.standard_normal((1, T, Hkv, D)) * 0.02
+    v = rng.standard_normal((1, T, Hkv, D))
+    k[0, 3, 0] = qn * (0.5 / per_unit)    # block 0: running max 1
+    k[0, 40, 0] = qn * (20.5 / per_unit)  # under max + 20: weight ~2^19.5
+    v[0, 40, 0] *= 10.0
+    k[0, 90, 0] = qn * (21.6 / per_unit)  # over max + 20: the maximum moves to 22
+    bt, nb = workloads.shuffled_block_table(3, 1, T // 16, num_blocks=T // 16 + 2)
+    layer = tq.Layer(nb, Hkv, seed=4, layer=1)
+    fill_cache(cuda, layer, k.astype(np.float32), v.astype(np.float32), bt, [T], False)
+    ctx = np.array([T], np.int32)
+    out = layer.decode(to_dev(cuda, q.astype(np.float32)), cuda.from_numpy(bt).cuda(), cuda.from_numpy(ctx).cuda(),
+                       sm_scale=sm, out_dtype=cuda.float32, num_splits=1)
+    cuda.cuda.synchronize()
+    assert tq.get_device_status() == 0
+    kp, vp = layer.k_cache.cpu().numpy(), layer.v_cache.cpu().numpy()
+    ol = oracle_layer(layer)
+    f = oa.gather_packed(kp, vp, ol, nb, Hkv, D, bt[0], T, 0)
+    u = (f["k_hat"] @ q[0, 0]) * sm / math.log(2.0)
+    # the scenario holds on the quantized cache
+    assert math.ceil(u[:16].max()) == 1 and u[40] < 21.0 < u[90] and math.ceil(u[90]) == 22
+    assert f["v_gamma"][40] > 4.0 * f["v_gamma"][90]
+    ref = oa.decode_packed(q, kp, vp, ol, nb, Hkv, bt, ctx, sm)
+    assert_close(out.cpu().numpy(), ref, TOL_F32, ctx)

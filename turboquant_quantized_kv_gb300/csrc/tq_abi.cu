@@ -118,8 +118,9 @@ int tq_auto_splits(const tq_cache_desc* desc, int batch, int num_q_heads, int ma
   DeviceInfo di;
   if (device_info(&di) != TQ_OK) return 0;
   const int g = num_q_heads / desc->num_kv_heads;
-  const int groups = (g + TQ_MAX_GROUP - 1) / TQ_MAX_GROUP;
-  return auto_splits(di.num_sms, batch, desc->num_kv_heads * groups, max_blocks_per_seq);
+  const int hpw = g <= 4 ? 4 : 8;  // heads per decode warp
+  const int groups = (g + hpw - 1) / hpw;
+  return auto_splits(di.num_sms, decode_warps(*desc, g), batch, desc->num_kv_heads * groups, max_blocks_per_seq);
 }
 
 static int resolve_splits(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks, int num_splits) {

@@ -250,24 +250,21 @@ struct DecodeArgs {
 // diagonal B[(p, e)][(h, e')] = P'[h][token(p)] [e = e'].  A[(row j)][(p, e)] is
 // the code pair byte of token(p), so bytes are used as stored.  Row g_ of m-tile
 // mt is the lane's byte 2 mt of coordinates [16 g_, 16 g_ + 16), row g_ + 8 byte
-// 2 mt + 1; position p = tig of tile kt is token 2 tig + 8 kt and p = tig + 4 is
-// token 2 tig + 1 + 8 kt.  The lane holding D gets head 4 nt + tig at coordinates
-// 16 g_ + 4 mt + {0, 1, 2, 3} = acc[nt][mt][0..3].
+// 2 mt + 1; position p = tig of tile kt is token ta(tig) + 8 kt and p = tig + 4 is
+// token tb(tig) + 8 kt, where {ta, tb} = {2 tig, 2 tig + 1} with ta odd for odd tig:
+// the four records one load instruction reads then alternate between the two
+// 64-byte halves of a 128-byte bank line (fewer shared-memory bank conflicts).
+// The lane holding D gets head 4 nt + tig at coordinates 16 g_ + 4 mt + {0, 1, 2, 3}
+// = acc[nt][mt][0..3].
+__device__ __forceinline__ int tok_a(int tig) { return 2 * tig + (tig & 1); }
+__device__ __forceinline__ int tok_b(int tig) { return 2 * tig + 1 - (tig & 1); }
 
 // Key-side B fragments of one n-tile: lane (g_, tig) holds column g_ (head 4 nt +
-// g_ / 2, part g_ & 1) at coordinates 32 tig + [0, 32): chunk c, b0 = {4c, 4c + 1},
-// b1 = {4c + 2, 4c + 3}.  fp16 with a power-of-two scale per head (max |q| scale
-// < 2^14), or bf16.  Returns 1 / scale.
+// g_ / 2, part g_ & 1) at coordinates 32 tig + [0, 32) (v = the query row there):
+// chunk c, b0 = {4c, 4c + 1}, b1 = {4c + 2, 4c + 3}.  fp16 with a power-of-two
+// scale per head (max |q| scale < 2^14), or bf16.  Returns 1 / scale.
 template <bool BF16>
-__device__ __forceinline__ float make_q_frags(const float* qrow, bool valid, int part, int tig,
-                                              uint32_t (&bq)[8][2]) {
-  float v[32];
-  if (valid) {
-    load32<float>(qrow + 32 * tig, v);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-  }
+__device__ __forceinline__ float make_q_frags(const float (&v)[32], int part, uint32_t (&bq)[8][2]) {
   float scale = 1.0f;
   if (!BF16) {
     float mx = 0.0f;
@@ -296,6 +293,15 @@ __device__ __forceinline__ float make_q_frags(const float* qrow, bool valid, int
     }
   }
   return 1.0f / scale;
+}
+
+__device__ __forceinline__ void load_q(const float* qrow, bool valid, int tig, float (&v)[32]) {
+  if (valid) {
+    load32<float>(qrow + 32 * tig, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+  }
 }
 
 // Online-softmax state of head 4 nt + tig, replicated on the 8 lanes of that tig:
@@ -389,14 +395,14 @@ __device__ __forceinline__ void softmax_block(SoftmaxState<NT>& st, const float 
 }
 
 // Value-side B fragments from the packed P' pairs: lane (g, t) takes head 4 nt + g/2
-// at tokens 2t, 2t + 8 (from lane 8t + g/2) and 2t + 1, 2t + 9 (lane 8t + 4 + g/2),
-// each placed in half g & 1 of its pair (the other half 0).
+// at tokens ta(t), ta(t) + 8 (from lane 4 ta(t) + g/2) and tb(t), tb(t) + 8 (lane
+// 4 tb(t) + g/2), each placed in half g & 1 of its pair (the other half 0).
 struct PTranspose {
   int srcx, srcy;
   uint32_t sel0, sel1;  // byte selectors for token tile 0 (low halves) and 1 (high halves)
   __device__ __forceinline__ void init(int g_, int tig) {
-    srcx = 8 * tig + (g_ >> 1);
-    srcy = srcx + 4;
+    srcx = 4 * tok_a(tig) + (g_ >> 1);
+    srcy = 4 * tok_b(tig) + (g_ >> 1);
     sel0 = (g_ & 1) ? 0x1044u : 0x4410u;
     sel1 = (g_ & 1) ? 0x3244u : 0x4432u;
   }
@@ -549,12 +555,13 @@ __device__ __forceinline__ void packed_block(SoftmaxState<NT>& st, const WarpCon
   uint32_t pk[NT], pl[NT];
   softmax_block<NT, false>(st, u, wv, pk, pl);
 
-  // ---- values: tokens 2 tig (+1) of tile 0 and 2 tig + 8 (+1) of tile 1
+  // ---- values: tokens ta, tb of tile 0 and ta + 8, tb + 8 of tile 1
+  const int ta = tok_a(tig), tb = tok_b(tig);
   uint32_t vw[4][2];
-  load_sixteenth<BV>(sv + (2 * tig) * RV, g_, vw[0]);
-  load_sixteenth<BV>(sv + (2 * tig + 1) * RV, g_, vw[1]);
-  load_sixteenth<BV>(sv + (2 * tig + 8) * RV, g_, vw[2]);
-  load_sixteenth<BV>(sv + (2 * tig + 9) * RV, g_, vw[3]);
+  load_sixteenth<BV>(sv + ta * RV, g_, vw[0]);
+  load_sixteenth<BV>(sv + tb * RV, g_, vw[1]);
+  load_sixteenth<BV>(sv + (ta + 8) * RV, g_, vw[2]);
+  load_sixteenth<BV>(sv + (tb + 8) * RV, g_, vw[3]);
   uint32_t bv[NT][2][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) wc.pt.apply(pk[nt], bv[nt]);
@@ -617,9 +624,9 @@ __device__ __forceinline__ void bf16_block(SoftmaxState<NT>& st, const WarpConst
   }
 #pragma unroll
   for (int kt = 0; kt < 2; ++kt) {
-    // coordinates [16 g_, 16 g_ + 16) of tokens 2 tig + 8 kt (F) and 2 tig + 1 + 8 kt (S)
-    const uint4* rf = reinterpret_cast<const uint4*>(sv + (2 * tig + 8 * kt) * RB + 32 * g_);
-    const uint4* rs = reinterpret_cast<const uint4*>(sv + (2 * tig + 1 + 8 * kt) * RB + 32 * g_);
+    // coordinates [16 g_, 16 g_ + 16) of tokens ta + 8 kt (F) and tb + 8 kt (S)
+    const uint4* rf = reinterpret_cast<const uint4*>(sv + (tok_a(tig) + 8 * kt) * RB + 32 * g_);
+    const uint4* rs = reinterpret_cast<const uint4*>(sv + (tok_b(tig) + 8 * kt) * RB + 32 * g_);
     const uint4 f0 = rf[0], f1 = rf[1], s0 = rs[0], s1 = rs[1];
     const uint32_t wf[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
     const uint32_t ws[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
@@ -637,8 +644,38 @@ __device__ __forceinline__ void bf16_block(SoftmaxState<NT>& st, const WarpConst
 
 // ------------------------------------------------------------ decode kernel
 
-// KIND 0: packed codes (BK, BV, QJL); KIND 1: bf16 pages.  NW warps per CTA, one
-// CTA per SM holding all of the SM's shared memory.
+// Live partial slots.  Chunk ch = unit * splits + s runs on CTA ch / NW; the
+// warps of one CTA that share a unit are merged into the slot of the first of
+// them, so slot s of a unit is live iff s == 0 or (unit * splits + s) % NW == 0.
+__device__ __forceinline__ bool slot_live(int unit, int splits, int s, int nw) {
+  return s == 0 || ((int64_t)unit * splits + s) % nw == 0;
+}
+
+// In-place inverse Hadamard rotation of head rows spread over the CTA: thread t
+// holds coordinate c = t % 128 of row t / 128 (y), xs is [rows][128] scratch.
+// Returns Pi^T y = D H y / sqrt(d) at coordinate c.  Every thread of the CTA calls it.
+__device__ __forceinline__ float inv_hadamard_cta(float y, int c, float* xs_row, const float* rot) {
+  const int lane = c & 31;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {  // bits 0..4 of the coordinate: lanes of one warp
+    const float o = __shfl_xor_sync(0xffffffffu, y, m);
+    y = (lane & m) ? (o - y) : (y + o);
+  }
+  xs_row[c] = y;
+  __syncthreads();
+  const int ch = c >> 5;  // bits 5, 6: the four warps of the row
+  float r = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float z = xs_row[lane + 32 * j];
+    r += (__popc(ch & j) & 1) ? -z : z;
+  }
+  __syncthreads();
+  return r * 0.08838834764831845f * __ldg(rot + c);
+}
+
+// KIND 0: packed codes (BK, BV, QJL); KIND 1: bf16 pages.  NT n-tiles of 4 heads
+// per warp, NW warps per CTA, one CTA per SM holding all of the SM's shared memory.
 // Shared layout (absolute shared addresses; base = start of the dynamic window):
 //   packed: rings of warps [0, n_lo) in [base, 0x10000), code tables in
 //           [0x10000, 0x20000), rings of the other warps from 0x20000;
@@ -651,14 +688,20 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g_ = lane >> 2, tig = lane & 3;
   const int stage_bytes = a.kpage + a.vpage;
-  const uint32_t ring_bytes = (uint32_t)(a.stages * stage_bytes);
   const uint32_t base = smem_u32(smem_raw);
   const uint32_t bars_addr = (base + (uint32_t)a.smem_bytes - (uint32_t)(NW * kMaxStages * 8)) & ~15u;
   const uint32_t lo0 = (base + 127u) & ~127u;
-  const uint32_t n_lo = (KIND == 0 && kLutAddr > lo0) ? (kLutAddr - lo0) / ring_bytes : 0u;
   const uint32_t hi0 = KIND == 0 ? kLutAddr + kLutBytes : lo0;
-  const uint32_t n_hi = bars_addr > hi0 ? (bars_addr - hi0) / ring_bytes : 0u;
-  const uint32_t red_bytes = (uint32_t)(NW * 8 * kD + 2 * NW * 8 + NW) * 4u;
+  // the deepest ring (<= a.stages) of which NW copies fit below and above the tables
+  int stages = a.stages;
+  uint32_t ring_bytes = 0u, n_lo = 0u, n_hi = 0u;
+  for (;; --stages) {
+    ring_bytes = (uint32_t)(stages * stage_bytes);
+    n_lo = (KIND == 0 && kLutAddr > lo0) ? (kLutAddr - lo0) / ring_bytes : 0u;
+    n_hi = bars_addr > hi0 ? (bars_addr - hi0) / ring_bytes : 0u;
+    if (n_lo + n_hi >= (uint32_t)NW || stages == 1) break;
+  }
+  const uint32_t red_bytes = (uint32_t)(NW * HPW * kD + 2 * NW * HPW + NW) * 4u;
   const bool layout_ok = (KIND == 1 || (base <= kLutAddr && kLutAddr + kLutBytes <= bars_addr)) &&
                          n_lo + n_hi >= (uint32_t)NW && hi0 + red_bytes <= bars_addr;
   auto gen = [&](uint32_t addr) { return smem_raw + (addr - base); };
@@ -676,15 +719,20 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   const int kvh = r / a.ngroups, hg = r - (r / a.ngroups) * a.ngroups;
   const int head0 = kvh * a.g + hg * HPW;
   const int gc = min(HPW, a.g - hg * HPW);
-  int ctx = has ? __ldg(a.ctx_lens + b) : 0;
-  if (ctx < 0 || ctx > a.max_blocks * kBlock) {
-    if (lane == 0 && s == 0 && r == 0) flag_status(a.status, TQ_DEV_BAD_CONTEXT);
-    ctx = ctx < 0 ? 0 : a.max_blocks * kBlock;
+
+  // ---- prologue: start the long-latency loads first (context length, query rows),
+  // build the code tables while they are in flight, then the block ids and copies
+  const int ctx_raw = has ? __ldg(a.ctx_lens + b) : 0;
+  float qv[NT][32];
+  float uv[QJL ? NT : 1][32];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hq = 4 * nt + (g_ >> 1);
+    const bool hv = has && hq < gc;
+    const int64_t qrow = ((int64_t)b * a.Hq + head0 + (hv ? hq : 0)) * kD;
+    load_q(a.qrot + qrow, hv, tig, qv[nt]);
+    if constexpr (QJL) load_q(a.uqjl + qrow, hv, tig, uv[nt]);
   }
-  const int nblk = (ctx + kBlock - 1) / kBlock;
-  const int j0 = (int)((int64_t)s * nblk / a.splits);
-  const int j1 = (int)((int64_t)(s + 1) * nblk / a.splits);
-  const int n_my = has ? j1 - j0 : 0;
 
   Ring ring;
   ring.stage_bytes = stage_bytes;
@@ -692,16 +740,9 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   ring.buf = gen(rw < n_lo ? lo0 + rw * ring_bytes : hi0 + (rw - n_lo) * ring_bytes);
   ring.bar = reinterpret_cast<uint64_t*>(gen(bars_addr)) + warp * kMaxStages;
   if (lane == 0)
-    for (int k = 0; k < a.stages; ++k) mbar_init(ring.bar + k, 1);
+    for (int k = 0; k < stages; ++k) mbar_init(ring.bar + k, 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncwarp();  // this warp's barriers are ready
-
-  // first copies go out before the tables are built, to overlap their latency
-  BlockIds ids;
-  ids.init(a.block_table + (int64_t)b * a.max_blocks + j0, n_my, lane);
-  uint32_t valid_mask = 0u;
-  for (int k = 0; k < a.stages && k < n_my; ++k)
-    if (issue_block(ring, k, a, ids.get(k, lane), kvh, lane)) valid_mask |= 1u << k;
 
   if constexpr (KIND == 0) {
     if (layout_ok) {
@@ -719,7 +760,18 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
       }
     }
   }
-  __syncthreads();  // tables ready
+
+  int ctx = ctx_raw;
+  if (ctx < 0 || ctx > a.max_blocks * kBlock) {
+    if (lane == 0 && s == 0 && r == 0) flag_status(a.status, TQ_DEV_BAD_CONTEXT);
+    ctx = ctx < 0 ? 0 : a.max_blocks * kBlock;
+  }
+  const int nblk = (ctx + kBlock - 1) / kBlock;
+  const int j0 = (int)((int64_t)s * nblk / a.splits);
+  const int j1 = (int)((int64_t)(s + 1) * nblk / a.splits);
+  const int n_my = has ? j1 - j0 : 0;
+  BlockIds ids;
+  ids.init(a.block_table + (int64_t)b * a.max_blocks + j0, n_my, lane);
 
   // per-warp constants: query fragments of column g_ (head 4 nt + g_ / 2, part g_ & 1)
   WarpConsts<NT> wc;
@@ -730,17 +782,18 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   wc.lv = wc.lk + 128u;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int hq = 4 * nt + (g_ >> 1);
-    const bool hv = has && hq < gc;
-    const int64_t qrow = ((int64_t)b * a.Hq + head0 + (hv ? hq : 0)) * kD;
-    const float iq = make_q_frags<KIND == 1>(a.qrot + qrow, hv, g_ & 1, tig, wc.bq[nt]);
+    const float iq = make_q_frags<KIND == 1>(qv[nt], g_ & 1, wc.bq[nt]);
     wc.inv_qs[nt] = __shfl_sync(0xffffffffu, iq, 8 * tig);  // scale of head 4 nt + tig
     wc.inv_us[nt] = 0.0f;
     if constexpr (QJL) {
-      const float iu = make_q_frags<false>(a.uqjl + qrow, hv, g_ & 1, tig, wc.bu[nt]);
+      const float iu = make_q_frags<false>(uv[nt], g_ & 1, wc.bu[nt]);
       wc.inv_us[nt] = __shfl_sync(0xffffffffu, iu, 8 * tig);
     }
   }
+
+  uint32_t valid_mask = 0u;
+  for (int k = 0; k < stages && k < n_my; ++k)
+    if (issue_block(ring, k, a, ids.get(k, lane), kvh, lane)) valid_mask |= 1u << k;
 
   SoftmaxState<NT> st;
 #pragma unroll
@@ -752,6 +805,7 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt) st.acc[nt][mt][0] = st.acc[nt][mt][1] = st.acc[nt][mt][2] = st.acc[nt][mt][3] = 0.0f;
   }
+  __syncthreads();  // tables ready
 
   int i = 0, stage = 0;
   uint32_t phase = 0u;
@@ -772,11 +826,11 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
         bf16_block<NT>(st, wc, sk, sv, t0, ctx);
     }
     __syncwarp();
-    if (i + a.stages < n_my) {
-      if (issue_block(ring, stage, a, ids.get(i + a.stages, lane), kvh, lane)) valid_mask |= 1u << stage;
+    if (i + stages < n_my) {
+      if (issue_block(ring, stage, a, ids.get(i + stages, lane), kvh, lane)) valid_mask |= 1u << stage;
       else valid_mask &= ~(1u << stage);
     }
-    if (++stage == a.stages) {
+    if (++stage == stages) {
       stage = 0;
       phase ^= 1u;
     }
@@ -784,9 +838,9 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   if (aborted) {  // drain copies still in flight into this warp's ring before the smem is reused
     int stg = stage;
     uint32_t ph = phase;
-    for (int k = i; k < n_my && k < i + a.stages; ++k) {
+    for (int k = i; k < n_my && k < i + stages; ++k) {
       mbar_wait(ring.bar + stg, ph);
-      if (++stg == a.stages) { stg = 0; ph ^= 1u; }
+      if (++stg == stages) { stg = 0; ph ^= 1u; }
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -795,160 +849,132 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     }
   }
 
-  // ---- merge the warps of this CTA that share a unit; one partial per group
+  // ---- epilogue 1: per-warp results to shared memory (true sums, l over the head's lanes)
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     st.l[nt] = col_sum(st.l[nt]);
-    const float rs = st.R[nt] * (1.0f / kPScale);  // acc holds sum / R (scaled)
+    const float rs = st.R[nt] * (1.0f / kPScale);
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) st.acc[nt][mt][e] *= rs;
   }
   __syncthreads();  // every ring is drained: reuse the stage memory
-  float* racc = reinterpret_cast<float*>(gen(hi0));  // [NW warps][8 heads][128]
-  float* rm = racc + NW * 8 * kD;                     // [NW][8]
-  float* rl = rm + NW * 8;                            // [NW][8]
-  int* runit = reinterpret_cast<int*>(rl + NW * 8);
+  float* racc = reinterpret_cast<float*>(gen(hi0));  // [NW warps][HPW heads][128]
+  float* rm = racc + NW * HPW * kD;                   // [NW][HPW]
+  float* rl = rm + NW * HPW;                          // [NW][HPW]
+  int* last_flag = reinterpret_cast<int*>(rl + NW * HPW);  // [NW] units this CTA completes
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int hl = 4 * nt + tig;
-    float4* dst = reinterpret_cast<float4*>(racc + (warp * 8 + hl) * kD + 16 * g_);
+    float4* dst = reinterpret_cast<float4*>(racc + (warp * HPW + hl) * kD + 16 * g_);
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
       dst[mt] = make_float4(st.acc[nt][mt][0], st.acc[nt][mt][1], st.acc[nt][mt][2], st.acc[nt][mt][3]);
     if (g_ == 0) {
-      rm[warp * 8 + hl] = st.M[nt];
-      rl[warp * 8 + hl] = st.l[nt];
+      rm[warp * HPW + hl] = st.M[nt];
+      rl[warp * HPW + hl] = st.l[nt];
     }
   }
-  if (lane == 0) runit[warp] = unit;
   __syncthreads();
-  if (!has) return;
-  const bool leader = warp == 0 || runit[warp - 1] != unit;
-  if (!leader) return;
-  int wend = warp + 1;
-  while (wend < NW && runit[wend] == unit) ++wend;
-  const int covered = wend - warp;  // chunks s .. s + covered - 1 of this unit
-  for (int h = 0; h < gc; ++h) {
-    if (lane > 0 && lane < covered) {  // merged into slot s: mark the group's other slots empty
-      const int64_t row2 = ((int64_t)b * a.Hq + head0 + h) * a.splits + s + lane;
-      a.ml[row2 * 2] = -INFINITY;
-      a.ml[row2 * 2 + 1] = 0.0f;
-    }
-    float Mt = -INFINITY;
-    for (int w = warp; w < wend; ++w) Mt = fmaxf(Mt, rm[w * 8 + h]);
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+
+  // ---- epilogue 2: one partial per (unit present in this CTA, head), all threads
+  const int c0 = blockIdx.x * NW;
+  const int c1 = min(c0 + NW, a.chunks);
+  if (!layout_ok || c0 >= c1) return;  // uniform
+  const int u0 = c0 / a.splits;
+  const int nu = (c1 - 1) / a.splits - u0 + 1;
+  for (int it = threadIdx.x; it < nu * HPW * 32; it += NW * 32) {
+    const int ui = it / (HPW * 32), h = (it >> 5) % HPW, qd = it & 31;
+    const int u = u0 + ui;
+    const int ub = u / per_b, ur = u - ub * per_b, ukvh = ur / a.ngroups, uhg = ur - ukvh * a.ngroups;
+    if (h >= min(HPW, a.g - uhg * HPW)) continue;
+    const int wb = max(u * a.splits, c0) - c0, we = min((u + 1) * a.splits, c1) - c0;
+    float M = -INFINITY;
+    for (int w = wb; w < we; ++w) M = fmaxf(M, rm[w * HPW + h]);
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     float L = 0.0f;
-    for (int w = warp; w < wend; ++w) {
-      const float mw = rm[w * 8 + h];
-      const float f = (mw == -INFINITY) ? 0.0f : exp2f(mw - Mt);
-      const float4 v = *reinterpret_cast<const float4*>(racc + (w * 8 + h) * kD + 4 * lane);
-      acc[0] = fmaf(v.x, f, acc[0]);
-      acc[1] = fmaf(v.y, f, acc[1]);
-      acc[2] = fmaf(v.z, f, acc[2]);
-      acc[3] = fmaf(v.w, f, acc[3]);
-      L = fmaf(rl[w * 8 + h], f, L);
+    for (int w = wb; w < we; ++w) {
+      const float mw = rm[w * HPW + h];
+      const float f = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
+      const float4 v = *reinterpret_cast<const float4*>(racc + (w * HPW + h) * kD + 4 * qd);
+      acc.x = fmaf(v.x, f, acc.x);
+      acc.y = fmaf(v.y, f, acc.y);
+      acc.z = fmaf(v.z, f, acc.z);
+      acc.w = fmaf(v.w, f, acc.w);
+      L = fmaf(rl[w * HPW + h], f, L);
     }
-    const int64_t row = ((int64_t)b * a.Hq + head0 + h) * a.splits + s;
-    *reinterpret_cast<float4*>(a.part + row * kD + 4 * lane) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    if (lane == 0) {
-      a.ml[row * 2] = Mt;
+    const int slot = c0 + wb - u * a.splits;
+    const int64_t row = ((int64_t)ub * a.Hq + ukvh * a.g + uhg * HPW + h) * a.splits + slot;
+    *reinterpret_cast<float4*>(a.part + row * kD + 4 * qd) = acc;
+    if (qd == 0) {
+      a.ml[row * 2] = M;
       a.ml[row * 2 + 1] = L;
     }
   }
   if (!a.fuse_combine) return;
 
-  // ---- the warp that completes a unit merges its chunks and applies Pi^T
+  // ---- epilogue 3: the CTA that completes a unit merges its slots and applies Pi^T
   __threadfence();
-  int last = 0;
-  if (lane == 0) last = atomicAdd(a.counters + unit, covered) + covered == a.splits;
-  if (!__shfl_sync(0xffffffffu, last, 0)) return;
-  __threadfence();
-  // (max, denominator) of every (head, slot): lane l holds slots l + 32 g, all loads in flight at once
-  constexpr int kG = kMaxFusedSplits / 32;
-  const int64_t row0 = ((int64_t)b * a.Hq + head0) * a.splits;
-  float fm[HPW][kG], fl[HPW][kG];
-#pragma unroll
-  for (int h = 0; h < HPW; ++h)
-#pragma unroll
-    for (int g = 0; g < kG; ++g) {
-      const int s2 = lane + 32 * g;
-      const bool in = h < gc && s2 < a.splits;
-      fm[h][g] = in ? __ldcg(a.ml + (row0 + (int64_t)h * a.splits + s2) * 2) : -INFINITY;
-      fl[h][g] = in ? __ldcg(a.ml + (row0 + (int64_t)h * a.splits + s2) * 2 + 1) : 0.0f;
-    }
-  float Lh[HPW];
-#pragma unroll
-  for (int h = 0; h < HPW; ++h) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int g = 0; g < kG; ++g) mx = fmaxf(mx, fm[h][g]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float L = 0.0f;
-#pragma unroll
-    for (int g = 0; g < kG; ++g) {  // fm becomes the slot weight
-      fm[h][g] = fm[h][g] == -INFINITY ? 0.0f : exp2f(fm[h][g] - mx);
-      L = fmaf(fl[h][g], fm[h][g], L);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    Lh[h] = L;
+  __syncthreads();
+  if (threadIdx.x < nu) {
+    const int u = u0 + threadIdx.x;
+    const int covered = min((u + 1) * a.splits, c1) - max(u * a.splits, c0);
+    const int done = atomicAdd(a.counters + u, covered) + covered;
+    const bool last = done == a.splits;
+    if (last) a.counters[u] = 0;  // every chunk of the unit has counted: ready for the next call
+    last_flag[threadIdx.x] = last ? 1 : 0;
   }
-  // sum the few non-empty slots (emptiness is per chunk, the same for every head)
-  float yh[HPW][4];
+  __syncthreads();
+  float* xs = racc;  // [HPW][128] scratch of the inverse rotation (the partials above are written)
+  for (int ui = 0; ui < nu; ++ui) {
+    if (!last_flag[ui]) continue;  // uniform
+    __threadfence();
+    const int u = u0 + ui;
+    const int ub = u / per_b, ur = u - ub * per_b, ukvh = ur / a.ngroups, uhg = ur - ukvh * a.ngroups;
+    const int ugc = min(HPW, a.g - uhg * HPW);
+    const int64_t hrow0 = (int64_t)ub * a.Hq + ukvh * a.g + uhg * HPW;
+    for (int o = threadIdx.x; o < HPW * kD; o += NW * 32) {  // uniform trip count: HPW * 128 % (NW * 32) == 0
+      const int h = o >> 7, c = o & (kD - 1);
+      float y = 0.0f;
+      if (h < ugc) {
+        // live slots: 0, then f1, f1 + NW, ... (the first chunk of the unit on each later CTA)
+        const int f1 = NW - (int)(((int64_t)u * a.splits) % NW);
+        float m4[4], l4[4], v4[4];
 #pragma unroll
-  for (int h = 0; h < HPW; ++h) yh[h][0] = yh[h][1] = yh[h][2] = yh[h][3] = 0.0f;
-#pragma unroll
-  for (int g = 0; g < kG; ++g) {
-    uint32_t live = __ballot_sync(0xffffffffu, fm[0][g] > 0.0f);
-    while (live) {
-      const int src = __ffs(live) - 1;
-      live &= live - 1;
-      const int s2 = src + 32 * g;
-#pragma unroll
-      for (int h = 0; h < HPW; ++h) {
-        const float f = __shfl_sync(0xffffffffu, fm[h][g], src);
-        if (h < gc) {
-          const float4 v =
-              __ldcg(reinterpret_cast<const float4*>(a.part + (row0 + (int64_t)h * a.splits + s2) * kD) + lane);
-          yh[h][0] = fmaf(v.x, f, yh[h][0]);
-          yh[h][1] = fmaf(v.y, f, yh[h][1]);
-          yh[h][2] = fmaf(v.z, f, yh[h][2]);
-          yh[h][3] = fmaf(v.w, f, yh[h][3]);
+        for (int k = 0; k < 4; ++k) {  // the loads of up to four slots in flight together
+          const int s2 = k == 0 ? 0 : f1 + (k - 1) * NW;
+          const int64_t row = (hrow0 + h) * a.splits + s2;
+          const bool in = s2 < a.splits;
+          m4[k] = in ? __ldcg(a.ml + row * 2) : -INFINITY;
+          l4[k] = in ? __ldcg(a.ml + row * 2 + 1) : 0.0f;
+          v4[k] = in ? __ldcg(a.part + row * kD + c) : 0.0f;
         }
-      }
-    }
-  }
+        float M = -INFINITY, L = 0.0f;
+        auto merge = [&](float m, float l, float v) {
+          if (m == -INFINITY) return;
+          const float nm = fmaxf(M, m);
+          const float fo = (M == -INFINITY) ? 0.0f : exp2f(M - nm), fn = exp2f(m - nm);
+          y = y * fo + v * fn;
+          L = L * fo + l * fn;
+          M = nm;
+        };
 #pragma unroll
-  for (int h = 0; h < HPW; ++h) {
-    if (h >= gc) break;
-    const float rl = Lh[h] > 0.0f ? 1.0f / Lh[h] : 0.0f;
-    float y[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) y[k] = yh[h][k] * rl;
-    if (a.fuse_combine == 2) {  // Hadamard: Pi^T y = D H y / sqrt(d); lane holds coordinates 4 lane + k
-      float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
-      y[0] = t0 + t2; y[2] = t0 - t2; y[1] = t1 + t3; y[3] = t1 - t3;
-#pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float o = __shfl_xor_sync(0xffffffffu, y[k], m);
-          y[k] = upper ? (o - y[k]) : (y[k] + o);
+        for (int k = 0; k < 4; ++k) merge(m4[k], l4[k], v4[k]);
+        for (int s2 = f1 + 3 * NW; s2 < a.splits; s2 += NW) {  // more than four slots
+          const int64_t row = (hrow0 + h) * a.splits + s2;
+          merge(__ldcg(a.ml + row * 2), __ldcg(a.ml + row * 2 + 1), __ldcg(a.part + row * kD + c));
         }
+        y = L > 0.0f ? y / L : 0.0f;
       }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) y[k] *= 0.08838834764831845f * __ldg(a.rot + 4 * lane + k);
-    }
-    const int64_t orow = ((int64_t)b * a.Hq + head0 + h) * kD + 4 * lane;
-    if (a.out_bf16) {
-      uint2 pk = make_uint2(pack_bf162(y[0], y[1]), pack_bf162(y[2], y[3]));
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow) = pk;
-    } else {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + orow) = make_float4(y[0], y[1], y[2], y[3]);
+      if (a.fuse_combine == 2) y = inv_hadamard_cta(y, c, xs + h * kD, a.rot);
+      if (h < ugc) {
+        const int64_t orow = (hrow0 + h) * kD + c;
+        if (a.out_bf16)
+          reinterpret_cast<__nv_bfloat16*>(a.out)[orow] = __float2bfloat16_rn(y);
+        else
+          reinterpret_cast<float*>(a.out)[orow] = y;
+      }
     }
   }
 }
@@ -1017,21 +1043,30 @@ __global__ void __launch_bounds__(128) k_rotate_q(const TQ* __restrict__ q, int6
 
 // ------------------------------------------------------------- combine
 
+// Heads of a decode unit and the CTA width of the decode launch, for the live slots.
+struct UnitMap {
+  int Hq, Hkv, g, hpw, ngroups, nw;
+};
+
 template <typename TO>
 __global__ void __launch_bounds__(128) k_combine(const float* __restrict__ part, const float* __restrict__ ml,
-                                                 int splits, int kind, const float* __restrict__ rot, TO* out) {
+                                                 int splits, UnitMap um, int kind, const float* __restrict__ rot,
+                                                 TO* out) {
   __shared__ float sm[256], sl[256], y[kD];
   __shared__ float stot[4];
   const int t = threadIdx.x;
   const int64_t bh = blockIdx.x;
+  const int bq = (int)(bh / um.Hq), head = (int)(bh - (int64_t)bq * um.Hq);
+  const int unit = (bq * um.Hkv + head / um.g) * um.ngroups + (head % um.g) / um.hpw;
   float mx = -INFINITY;
-  for (int s = t; s < splits; s += blockDim.x) mx = fmaxf(mx, ml[(bh * splits + s) * 2]);
+  for (int s = t; s < splits; s += blockDim.x)
+    if (slot_live(unit, splits, s, um.nw)) mx = fmaxf(mx, ml[(bh * splits + s) * 2]);
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if ((t & 31) == 0) stot[t >> 5] = mx;
   __syncthreads();
   const float M = fmaxf(fmaxf(stot[0], stot[1]), fmaxf(stot[2], stot[3]));
   for (int s = t; s < splits; s += blockDim.x) {
-    const float ms = ml[(bh * splits + s) * 2];
+    const float ms = slot_live(unit, splits, s, um.nw) ? ml[(bh * splits + s) * 2] : -INFINITY;
     const float f = (ms == -INFINITY) ? 0.0f : exp2f(ms - M);
     sm[s] = f;
     sl[s] = f > 0.0f ? ml[(bh * splits + s) * 2 + 1] * f : 0.0f;
@@ -1039,7 +1074,7 @@ __global__ void __launch_bounds__(128) k_combine(const float* __restrict__ part,
   __syncthreads();
   float acc = 0.0f, L = 0.0f;
   for (int s = 0; s < splits; ++s) {
-    if (sm[s] == 0.0f) continue;  // empty chunk or merged into another slot: its acc is not written
+    if (sm[s] == 0.0f) continue;  // empty chunk or merged into another slot
     acc = fmaf(part[(bh * splits + s) * kD + t], sm[s], acc);
     L += sl[s];
   }
@@ -1070,14 +1105,18 @@ __global__ void __launch_bounds__(128) k_combine(const float* __restrict__ part,
 
 Codebook codebook_of(const tq_cache_desc& d, int which);
 
-// Warps per decode CTA (one CTA per SM): packed codes without QJL run 16 warps
-// at 128 registers; the QJL variant and bf16 pages run 8 warps with more registers.
-constexpr int kPackedWarps = 16;
-constexpr int kWideWarps = 8;
+// Warps per decode CTA (one CTA per SM): packed codes without QJL run 24 warps at
+// 80 registers for groups of up to 4 heads (3-deep rings) and 16 warps at 128
+// registers for 8; the QJL variant and bf16 pages run 8 warps with more registers.
+constexpr int decode_nw(bool packed_plain, int nt) { return packed_plain ? (nt == 1 ? 16 : 16) : 8; }
+
+int decode_warps(const tq_cache_desc& d, int g) {
+  return decode_nw(d.fmt.kv_format == TQ_KV_PACKED && !d.fmt.qjl_k, g <= 4 ? 1 : 2);
+}
 
 template <int KIND, int BK, int BV, bool QJL, int NT>
 static cudaError_t run_decode_nt(DecodeArgs a, cudaStream_t st) {
-  constexpr int NW = (KIND == 0 && !QJL) ? kPackedWarps : kWideWarps;
+  constexpr int NW = decode_nw(KIND == 0 && !QJL, NT);
   auto kern = k_decode<KIND, BK, BV, QJL, NT, NW>;
   int dev = 0, optin = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1161,8 +1200,8 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   a.rot = d.rotation;
   a.out = c.out;
   a.out_bf16 = c.out_dtype == TQ_BF16 ? 1 : 0;
-  // ring depth: 4 stages; 3 when two code tables would not leave room for 2 CTAs per SM;
-  // 2 for bf16 pages (8 KB per block, one CTA per SM)
+  // ring depth: at most 4 stages (3 for bf16 pages, 8 KB per block); the kernel
+  // takes the deepest that fits its warps
   a.stages = bf16 ? 3 : 4;
   if (bf16) {
     e = run_decode<1, 4, 4, false>(a, st);
@@ -1185,10 +1224,18 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (a.fuse_combine) return cudaSuccess;
   const unsigned cgrid = (unsigned)rows;
+  UnitMap um;
+  um.Hq = a.Hq;
+  um.Hkv = a.Hkv;
+  um.g = a.g;
+  um.hpw = a.g <= 4 ? 4 : 8;
+  um.ngroups = a.ngroups;
+  um.nw = decode_warps(d, a.g);
   if (c.out_dtype == TQ_F32)
-    k_combine<float><<<cgrid, 128, 0, st>>>(a.part, a.ml, c.splits, kind, d.rotation, reinterpret_cast<float*>(c.out));
+    k_combine<float><<<cgrid, 128, 0, st>>>(a.part, a.ml, c.splits, um, kind, d.rotation,
+                                            reinterpret_cast<float*>(c.out));
   else
-    k_combine<__nv_bfloat16><<<cgrid, 128, 0, st>>>(a.part, a.ml, c.splits, kind, d.rotation,
+    k_combine<__nv_bfloat16><<<cgrid, 128, 0, st>>>(a.part, a.ml, c.splits, um, kind, d.rotation,
                                                     reinterpret_cast<__nv_bfloat16*>(c.out));
   count_launch();
   return cudaGetLastError();

@@ -25,8 +25,12 @@ tq_status check_desc(const tq_cache_desc* desc, bool need_data = true);
 // Bytes of a K (which = 0) or V (which = 1) page of a valid descriptor.
 size_t page_bytes_of(const tq_cache_desc& d, int which);
 
-// Splits chosen when the caller passes 0.
-int auto_splits(int num_sms, int batch, int num_kv_heads, int max_blocks_per_seq);
+// Splits chosen when the caller passes 0: one chunk per decode warp of the GPU
+// (warps = warps per decode CTA, one CTA per SM).
+int auto_splits(int num_sms, int warps, int batch, int num_kv_heads, int max_blocks_per_seq);
+
+// Warps per decode CTA for a layer format and GQA group size g.
+int decode_warps(const tq_cache_desc& d, int g);
 
 // Workspace layout of decode (all offsets 256-byte aligned).
 struct DecodeWorkspace {
