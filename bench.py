@@ -178,54 +178,55 @@ def run_tq(args):
     st = setup(torch, tq, args.warmup + 2 * args.steps + 4, dev)
     stream = torch.cuda.current_stream()
 
-    # one graph per layer for append and for decode: replays are launch-cheap and
-    # events between them time the decode call of every layer inside the timed region
+    # The step (slot bookkeeping, then append + decode of every layer) is one CUDA
+    # graph.  NG copies of it are replayed in turn; copy i holds one pair of timing
+    # events around the decode call of layer i % LAYERS (an event node inside a graph
+    # costs microseconds, so each step carries one pair), and after the timed region
+    # each copy's pair holds the duration of that decode call in its last replay.
     torch.cuda.synchronize()
     for l in range(LAYERS):  # eager warm-up (module load, attributes) before capture
         layer_decode(st, l)
     torch.cuda.synchronize()
-    g_prep = torch.cuda.CUDAGraph()
-    g_app = [torch.cuda.CUDAGraph() for _ in range(LAYERS)]
-    g_dec = [torch.cuda.CUDAGraph() for _ in range(LAYERS)]
+    ng = max(1, min(LAYERS, args.steps))
+    graphs, dec_ev = [], []
     ctx_save = st["ctx"].clone()
-    n_before = tq.launch_count()
-    with torch.cuda.graph(g_prep):
-        step_prepare(torch, st)
-    for l in range(LAYERS):
-        with torch.cuda.graph(g_app[l]):
-            layer_append(st, l)
-        with torch.cuda.graph(g_dec[l]):
-            layer_decode(st, l)
-    launches_per_step = tq.launch_count() - n_before  # libtq kernels captured into one step's graphs
+    launches_per_step = 0
+    for gi in range(ng):
+        ev = (torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+        lt = gi % LAYERS
+        g = torch.cuda.CUDAGraph()
+        n_before = tq.launch_count()
+        with torch.cuda.graph(g):
+            step_prepare(torch, st)
+            for l in range(LAYERS):
+                layer_append(st, l)
+                if l == lt:
+                    ev[0].record()
+                layer_decode(st, l)
+                if l == lt:
+                    ev[1].record()
+        if gi == 0:
+            launches_per_step = tq.launch_count() - n_before  # libtq kernels in one step's graph
+        graphs.append(g)
+        dec_ev.append(ev)
     st["ctx"].copy_(ctx_save)
     torch.cuda.synchronize()
 
-    def graph_step(dec_events=None):
-        g_prep.replay()
-        for l in range(LAYERS):
-            g_app[l].replay()
-            if dec_events is not None:
-                dec_events[l][0].record(stream)
-            g_dec[l].replay()
-            if dec_events is not None:
-                dec_events[l][1].record(stream)
-
-    for _ in range(args.warmup):
-        graph_step()
+    for w in range(args.warmup):
+        graphs[w % ng].replay()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     ctx_start = int(st["ctx"][0].item())
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(LAYERS)]
-           for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     torch.cuda.synchronize()
+    first = args.warmup % ng  # graph of timed step 0
     t0.record(stream)
-    for s in range(args.steps):
-        graph_step(evs[s])
+    for s_ in range(args.steps):
+        graphs[(first + s_) % ng].replay()
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -235,21 +236,20 @@ def run_tq(args):
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         ms_total = float(tt.item())
     ms_step = ms_total / args.steps
-    dec_ms = [a.elapsed_time(b) for row in evs for a, b in row]
+    # decode timings of the last min(ng, steps) timed steps, one layer each
+    sampled = list(range(max(0, args.steps - ng), args.steps))
+    dec_ms = [dec_ev[(first + s_) % ng][0].elapsed_time(dec_ev[(first + s_) % ng][1]) for s_ in sampled]
     status = tq.get_device_status()
     # algorithmic bytes: every decode call of the timed steps reads ctx tokens x H_kv
     # records of 136 B (4-bit K + V + fp32 norms) per sequence, plus block table, q, out
-    bytes_steps = 0
-    bytes_per_call = []
-    for s in range(args.steps):
-        ctx_s = ctx_start + s + 1
-        per_call = B * HKV * ctx_s * BYTES_PER_TOKEN_HEAD + B * st["mb"] * 4 + 2 * B * HQ * D * 2
-        bytes_per_call.append(per_call)
-        bytes_steps += LAYERS * per_call
+    def call_bytes(s_):
+        ctx_s = ctx_start + s_ + 1
+        return B * HKV * ctx_s * BYTES_PER_TOKEN_HEAD + B * st["mb"] * 4 + 2 * B * HQ * D * 2
+    bytes_steps = sum(LAYERS * call_bytes(s_) for s_ in range(args.steps))
     value = bytes_steps * world / (ms_total * 1e-3) / 1e9
     peak, peak_kind = peaks()
     dec_avg_ms = statistics.mean(dec_ms)
-    achieved = statistics.mean(bytes_per_call) / (dec_avg_ms * 1e-3) / 1e9
+    achieved = statistics.mean(call_bytes(s_) for s_ in sampled) / (dec_avg_ms * 1e-3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if os.path.exists(tpath):  # counters from one ncu capture, valid only for the kernel source they came from
