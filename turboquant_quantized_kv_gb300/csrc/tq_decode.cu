@@ -67,6 +67,10 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Waits for the grid this one was launched as a programmatic dependent of (no-op
+// for an ordinary launch).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -217,8 +221,12 @@ struct DecodeArgs {
   const int32_t* block_table;
   int max_blocks;
   const int32_t* ctx_lens;
-  const float* qrot;  // [B][Hq][d] scaled rotated queries
+  const float* qrot;  // [B][Hq][d] scaled rotated queries (q_in_kernel == 0)
   const float* uqjl;  // [B][Hq][d] S q' (QJL only)
+  const void* q;      // [B][Hq][d] raw queries (q_in_kernel != 0; 16-byte aligned rows)
+  int q_bf16;
+  int q_in_kernel;    // 0: read qrot; 1: rotate q here (Hadamard); 2: scale q here (no rotation)
+  float q_scale;      // sm_scale * log2 e
   int Hq, g, ngroups;
   int splits;  // chunks per unit
   int chunks;  // units * splits
@@ -302,6 +310,46 @@ __device__ __forceinline__ void load_q(const float* qrow, bool valid, int tig, f
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = 0.0f;
   }
+}
+
+// Raw query coordinates 32 tig + [0, 32) of row `row` (fp32 or bf16).
+__device__ __forceinline__ void load_q_raw(const void* q, bool bf16, int64_t row, bool valid, int tig,
+                                           float (&v)[32]) {
+  if (!valid) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+  } else if (bf16) {
+    load32<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16*>(q) + row * kD + 32 * tig, v);
+  } else {
+    load32<float>(reinterpret_cast<const float*>(q) + row * kD + 32 * tig, v);
+  }
+}
+
+// q' = scale * H (s * q) / sqrt(d) for a row spread over the 4 lanes of a quad (lane
+// tig holds coordinates 32 tig + i): the Walsh-Hadamard butterflies of bits 0..4 run
+// in registers, bits 5 and 6 across the quad.
+__device__ __forceinline__ void rotate_q_quad(float (&v)[32], const float* signs, int tig, float scale) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] *= __ldg(signs + 32 * tig + i);
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if ((i & h) == 0) {
+        const float x = v[i], y = v[i + h];
+        v[i] = x + y;
+        v[i + h] = x - y;
+      }
+#pragma unroll
+  for (int m = 1; m < 4; m <<= 1)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+      v[i] = (tig & m) ? (o - v[i]) : (v[i] + o);
+    }
+  const float f = scale * 0.08838834764831845f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] *= f;
 }
 
 // Online-softmax state of head 4 nt + tig, replicated on the 8 lanes of that tig:
@@ -729,9 +777,14 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   for (int nt = 0; nt < NT; ++nt) {
     const int hq = 4 * nt + (g_ >> 1);
     const bool hv = has && hq < gc;
-    const int64_t qrow = ((int64_t)b * a.Hq + head0 + (hv ? hq : 0)) * kD;
-    load_q(a.qrot + qrow, hv, tig, qv[nt]);
-    if constexpr (QJL) load_q(a.uqjl + qrow, hv, tig, uv[nt]);
+    const int64_t row = (int64_t)b * a.Hq + head0 + (hv ? hq : 0);
+    if (a.q_in_kernel) {
+      load_q_raw(a.q, a.q_bf16 != 0, row, hv, tig, qv[nt]);
+    } else {
+      grid_dep_wait();  // qrot comes from the preceding rotation pass
+      load_q(a.qrot + row * kD, hv, tig, qv[nt]);
+    }
+    if constexpr (QJL) load_q(a.uqjl + row * kD, hv, tig, uv[nt]);
   }
 
   Ring ring;
@@ -782,6 +835,12 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   wc.lv = wc.lk + 128u;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
+    if (a.q_in_kernel == 1) {
+      rotate_q_quad(qv[nt], a.rot, tig, a.q_scale);
+    } else if (a.q_in_kernel == 2) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) qv[nt][k] *= a.q_scale;
+    }
     const float iq = make_q_frags<KIND == 1>(qv[nt], g_ & 1, wc.bq[nt]);
     wc.inv_qs[nt] = __shfl_sync(0xffffffffu, iq, 8 * tig);  // scale of head 4 nt + tig
     wc.inv_us[nt] = 0.0f;
@@ -918,6 +977,7 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   __threadfence();
   __syncthreads();
   if (threadIdx.x < nu) {
+    grid_dep_wait();  // the counters are zeroed by the preceding pass
     const int u = u0 + threadIdx.x;
     const int covered = min((u + 1) * a.splits, c1) - max(u * a.splits, c0);
     const int done = atomicAdd(a.counters + u, covered) + covered;
@@ -934,7 +994,8 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     const int ub = u / per_b, ur = u - ub * per_b, ukvh = ur / a.ngroups, uhg = ur - ukvh * a.ngroups;
     const int ugc = min(HPW, a.g - uhg * HPW);
     const int64_t hrow0 = (int64_t)ub * a.Hq + ukvh * a.g + uhg * HPW;
-    for (int o = threadIdx.x; o < HPW * kD; o += NW * 32) {  // uniform trip count: HPW * 128 % (NW * 32) == 0
+    for (int o0 = 0; o0 < HPW * kD; o0 += NW * 32) {  // uniform trip count; rows of 128 threads
+      const int o = o0 + threadIdx.x;
       const int h = o >> 7, c = o & (kD - 1);
       float y = 0.0f;
       if (h < ugc) {
@@ -967,7 +1028,7 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
         }
         y = L > 0.0f ? y / L : 0.0f;
       }
-      if (a.fuse_combine == 2) y = inv_hadamard_cta(y, c, xs + h * kD, a.rot);
+      if (a.fuse_combine == 2) y = inv_hadamard_cta(y, c, xs + (o >> 7) * kD, a.rot);
       if (h < ugc) {
         const int64_t orow = (hrow0 + h) * kD + c;
         if (a.out_bf16)
@@ -984,11 +1045,14 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
 enum { ROTQ_IDENTITY = 0, ROTQ_HADAMARD = 1, ROTQ_DENSE = 2 };
 
 // One warp per (sequence, query head).  qrot = Pi q * scale; uq = S qrot (QJL).
-// Also zeroes the decode's per-unit chunk counters.
+// Also zeroes the decode's per-unit chunk counters.  The decode kernel that follows
+// is launched as its programmatic dependent: it may start right away and waits for
+// this grid (griddepcontrol.wait) only where it reads qrot / uq or the counters.
 template <typename TQ>
 __global__ void __launch_bounds__(128) k_rotate_q(const TQ* __restrict__ q, int64_t n_rows, int kind,
                                                   const float* __restrict__ rot, const float* __restrict__ S,
                                                   float scale, float* qrot, float* uq, int* counters, int n_counters) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_counters; i += gridDim.x * blockDim.x) counters[i] = 0;
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -1105,10 +1169,10 @@ __global__ void __launch_bounds__(128) k_combine(const float* __restrict__ part,
 
 Codebook codebook_of(const tq_cache_desc& d, int which);
 
-// Warps per decode CTA (one CTA per SM): packed codes without QJL run 24 warps at
-// 80 registers for groups of up to 4 heads (3-deep rings) and 16 warps at 128
-// registers for 8; the QJL variant and bf16 pages run 8 warps with more registers.
-constexpr int decode_nw(bool packed_plain, int nt) { return packed_plain ? (nt == 1 ? 16 : 16) : 8; }
+// Warps per decode CTA (one CTA per SM, NW a multiple of 4): packed codes without
+// QJL run 16 warps at 128 registers for groups of up to 4 heads and 12 warps for 8;
+// the QJL variant and bf16 pages run 8 warps with more registers.
+constexpr int decode_nw(bool packed_plain, int nt) { return packed_plain ? (nt == 1 ? 16 : 12) : 8; }
 
 int decode_warps(const tq_cache_desc& d, int g) {
   return decode_nw(d.fmt.kv_format == TQ_KV_PACKED && !d.fmt.qjl_k, g <= 4 ? 1 : 2);
@@ -1126,10 +1190,20 @@ static cudaError_t run_decode_nt(DecodeArgs a, cudaStream_t st) {
   a.smem_bytes = optin;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)((a.chunks + NW - 1) / NW);
-  kern<<<grid, NW * 32, (size_t)optin, st>>>(a);
+  // programmatic dependent of the rotation / counter pass launched just before
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((a.chunks + NW - 1) / NW));
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = (size_t)optin;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Heads per warp: 4 (one n-tile) for GQA groups of up to 4 query heads, else 8.
@@ -1157,17 +1231,25 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   const int kind = bf16 ? ROTQ_IDENTITY : (d.fmt.rot_kind == TQ_ROT_DENSE ? ROTQ_DENSE : ROTQ_HADAMARD);
   const int64_t rows = (int64_t)c.batch * c.num_q_heads;
   const float scale = c.sm_scale * kLog2e;
-  const unsigned rgrid = (unsigned)((rows + 3) / 4);
   int* counters = reinterpret_cast<int*>(c.workspace + ws.cnt_off);
-  const int n_counters = (int)rows;  // >= batch * kv heads * head groups
-  if (c.q_dtype == TQ_F32)
-    k_rotate_q<float><<<rgrid, 128, 0, st>>>(reinterpret_cast<const float*>(c.q), rows, kind, d.rotation,
-                                             qjl ? d.qjl_proj : nullptr, scale, qrot, uq, counters, n_counters);
-  else
-    k_rotate_q<__nv_bfloat16><<<rgrid, 128, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(c.q), rows, kind,
-                                                     d.rotation, qjl ? d.qjl_proj : nullptr, scale, qrot, uq,
-                                                     counters, n_counters);
-  count_launch();
+  // Hadamard and unrotated layers without QJL rotate q inside the decode kernel;
+  // dense rotations and S q' (QJL) take a separate mat-vec pass first
+  const bool q_aligned = (reinterpret_cast<uintptr_t>(c.q) & 15) == 0;
+  const int q_in_kernel = (!qjl && kind != ROTQ_DENSE && q_aligned) ? (kind == ROTQ_HADAMARD ? 1 : 2) : 0;
+  {
+    const int64_t rot_rows = q_in_kernel ? 0 : rows;
+    const int n_counters = (int)rows;  // >= batch * kv heads * head groups
+    unsigned rgrid = (unsigned)((rot_rows + 3) / 4);
+    if (rgrid == 0) rgrid = (unsigned)((n_counters + 127) / 128);
+    if (c.q_dtype == TQ_F32)
+      k_rotate_q<float><<<rgrid, 128, 0, st>>>(reinterpret_cast<const float*>(c.q), rot_rows, kind, d.rotation,
+                                               qjl ? d.qjl_proj : nullptr, scale, qrot, uq, counters, n_counters);
+    else
+      k_rotate_q<__nv_bfloat16><<<rgrid, 128, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(c.q), rot_rows, kind,
+                                                       d.rotation, qjl ? d.qjl_proj : nullptr, scale, qrot, uq,
+                                                       counters, n_counters);
+    count_launch();
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -1183,6 +1265,10 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   a.ctx_lens = c.ctx_lens;
   a.qrot = qrot;
   a.uqjl = uq;
+  a.q = c.q;
+  a.q_bf16 = c.q_dtype == TQ_BF16 ? 1 : 0;
+  a.q_in_kernel = q_in_kernel;
+  a.q_scale = scale;
   a.Hq = c.num_q_heads;
   a.g = c.num_q_heads / d.num_kv_heads;
   a.ngroups = (a.g + (a.g <= 4 ? 3 : 7)) / (a.g <= 4 ? 4 : 8);  // head groups of 4 or 8 per warp
