@@ -539,15 +539,16 @@ __device__ __forceinline__ void packed_block(SoftmaxState<NT>& st, const WarpCon
                                              const uint8_t* sv, int t0, int ctx, float qjl_coef) {
   constexpr int RK = 16 * BK, RV = 16 * BV;
   const int g_ = wc.g_, tig = wc.tig;
-  // ---- keys: 8 k-chunks, two accumulation chains per n-tile
+  // ---- keys: 8 k-chunks in KC independent accumulation chains per n-tile
+  constexpr int KC = NT == 1 ? 4 : 2;
   uint32_t kn[2][4];
   load_quarter<BK>(sk + g_ * RK, tig, kn[0]);
   load_quarter<BK>(sk + (g_ + 8) * RK, tig, kn[1]);
-  float dk[NT][2][4];
+  float dk[NT][KC][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int p = 0; p < 2; ++p)
+    for (int p = 0; p < KC; ++p)
 #pragma unroll
       for (int e = 0; e < 4; ++e) dk[nt][p][e] = 0.0f;
 #pragma unroll
@@ -556,8 +557,15 @@ __device__ __forceinline__ void packed_block(SoftmaxState<NT>& st, const WarpCon
     const uint32_t ak[4] = {lut(wc.lk, kn[0][wi], bi), lut(wc.lk, kn[1][wi], bi), lut(wc.lk, kn[0][wi], bi + 1),
                             lut(wc.lk, kn[1][wi], bi + 1)};
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma_f16(dk[nt][c & 1], ak, wc.bq[nt][c][0], wc.bq[nt][c][1], dk[nt][c & 1]);
+    for (int nt = 0; nt < NT; ++nt)
+      mma_f16(dk[nt][c % KC], ak, wc.bq[nt][c][0], wc.bq[nt][c][1], dk[nt][c % KC]);
   }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int p = 1; p < KC; ++p)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dk[nt][0][e] += dk[nt][p][e];
   float sq[NT][2];
   if constexpr (QJL) {  // sign term: rows = tokens, columns = S q' (hi, lo)
     const uint32_t sw0 = *reinterpret_cast<const uint32_t*>(sk + 16 * RK + 64 + 16 * g_ + 4 * tig);
@@ -590,8 +598,8 @@ __device__ __forceinline__ void packed_block(SoftmaxState<NT>& st, const WarpCon
   float u[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float v0 = gk0 * ((dk[nt][0][0] + dk[nt][0][1]) + (dk[nt][1][0] + dk[nt][1][1])) * wc.inv_qs[nt];
-    float v1 = gk1 * ((dk[nt][0][2] + dk[nt][0][3]) + (dk[nt][1][2] + dk[nt][1][3])) * wc.inv_qs[nt];
+    float v0 = gk0 * (dk[nt][0][0] + dk[nt][0][1]) * wc.inv_qs[nt];
+    float v1 = gk1 * (dk[nt][0][2] + dk[nt][0][3]) * wc.inv_qs[nt];
     if constexpr (QJL) {
       const float* rh = reinterpret_cast<const float*>(sk + 16 * RK + 64 + 256);
       v0 += qjl_coef * rh[g_] * sq[nt][0] * wc.inv_us[nt];
