@@ -376,21 +376,28 @@ __device__ __forceinline__ float col_sum(float v) {
   return v + __shfl_xor_sync(0xffffffffu, v, 16);
 }
 
-// u[nt][i]: base-2 logits of head 4 nt + tig for tokens g_ + 8 i (-inf when
-// masked); wv[i]: their value weights (gamma' or 1).  Updates the state and
-// returns P' of the two tokens packed as one pair (fp16; bf16 hi in pk, lo in pl).
-template <int NT, bool BF16>
-__device__ __forceinline__ void softmax_block(SoftmaxState<NT>& st, const float (&u)[NT][2], const float (&wv)[2],
-                                              uint32_t (&pk)[NT], uint32_t (&pl)[NT]) {
+// u[nt][i]: base-2 logits of head 4 nt + tig for the lane's T tokens (pairs
+// g_, g_ + 8 of T / 2 blocks; -inf when masked); wv[i]: their value weights
+// (gamma' or 1; 0 when masked).  Updates the state and returns P' of each pair
+// packed (fp16; bf16 hi in pk, lo in pl).
+template <int NT, bool BF16, int T>
+__device__ __forceinline__ void softmax_tokens(SoftmaxState<NT>& st, const float (&u)[NT][T], const float (&wv)[T],
+                                               uint32_t (&pk)[NT][T / 2], uint32_t (&pl)[NT][T / 2]) {
   // M integral and R a power of two: every rescale is exact, and the rounding of
   // P' does not depend on the tokens that came before (split invariance).
+  float um[NT];
   bool up = false;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) up |= fmaxf(u[nt][0], u[nt][1]) > st.M[nt] + kRescaleThreshold;
+  for (int nt = 0; nt < NT; ++nt) {
+    um[nt] = u[nt][0];
+#pragma unroll
+    for (int i = 1; i < T; ++i) um[nt] = fmaxf(um[nt], u[nt][i]);
+    up |= um[nt] > st.M[nt] + kRescaleThreshold;
+  }
   if (__any_sync(0xffffffffu, up)) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float bm = col_max(fmaxf(u[nt][0], u[nt][1]));
+      const float bm = col_max(um[nt]);
       if (bm > st.M[nt] + kRescaleThreshold) {  // the same on the head's lanes
         const float newM = ceilf(bm);
         const float alpha = (st.M[nt] == -INFINITY) ? 0.0f : ldexpf(1.0f, (int)(st.M[nt] - newM));
@@ -401,12 +408,12 @@ __device__ __forceinline__ void softmax_block(SoftmaxState<NT>& st, const float 
       }
     }
   }
-  float w[NT][2];
+  float w[NT][T];
   bool grow = false;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < T; ++i) {
       const float p = fast_exp2(u[nt][i] - st.M[nt]);
       st.l[nt] += p;
       w[nt][i] = p * wv[i];
@@ -415,7 +422,10 @@ __device__ __forceinline__ void softmax_block(SoftmaxState<NT>& st, const float 
   if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float wm = col_max(fmaxf(w[nt][0], w[nt][1]));
+      float wm = w[nt][0];
+#pragma unroll
+      for (int i = 1; i < T; ++i) wm = fmaxf(wm, w[nt][i]);
+      wm = col_max(wm);
       if (wm > st.R[nt]) {
         const float newR = __uint_as_float((__float_as_uint(wm) + 0x007FFFFFu) & 0xFF800000u);  // pow2 >= wm
         const float beta = st.R[nt] / newR;
@@ -429,17 +439,19 @@ __device__ __forceinline__ void softmax_block(SoftmaxState<NT>& st, const float 
     }
   }
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const float p0 = w[nt][0] * st.rR[nt], p1 = w[nt][1] * st.rR[nt];
-    if (BF16) {
-      pk[nt] = pack_bf162(p0, p1);
-      const __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&pk[nt]);
-      pl[nt] = pack_bf162(p0 - __low2float(h), p1 - __high2float(h));
-    } else {
-      pk[nt] = pack_half2(p0, p1);
-      pl[nt] = 0u;
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < T / 2; ++j) {
+      const float p0 = w[nt][2 * j] * st.rR[nt], p1 = w[nt][2 * j + 1] * st.rR[nt];
+      if (BF16) {
+        pk[nt][j] = pack_bf162(p0, p1);
+        const __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&pk[nt][j]);
+        pl[nt][j] = pack_bf162(p0 - __low2float(h), p1 - __high2float(h));
+      } else {
+        pk[nt][j] = pack_half2(p0, p1);
+        pl[nt][j] = 0u;
+      }
     }
-  }
 }
 
 // Value-side B fragments from the packed P' pairs: lane (g, t) takes head 4 nt + g/2
@@ -519,6 +531,36 @@ __device__ __forceinline__ bool issue_block(const Ring& r, int stage, const Deco
   return ok;
 }
 
+// Issues blocks blk_a and (if has_b) blk_b into the two slots of pair stage `ps`
+// (one mbarrier for both; lane 0).  kbase / vbase: this warp's KV head in the pools,
+// stride: bytes between blocks.  Returns bit 0 / bit 1 = block a / b valid.
+struct PagePtrs {
+  const uint8_t* kbase;
+  const uint8_t* vbase;
+  int64_t kstride, vstride;
+};
+
+__device__ __forceinline__ uint32_t issue_pair(const Ring& r, int ps, const DecodeArgs& a, const PagePtrs& pp,
+                                               int blk_a, int blk_b, bool has_b, int lane) {
+  const bool ok_a = blk_a >= 0 && (int64_t)blk_a < a.num_blocks;
+  const bool ok_b = has_b && blk_b >= 0 && (int64_t)blk_b < a.num_blocks;
+  if (lane == 0) {
+    uint64_t* bar = r.bar + ps;
+    uint8_t* dst = r.buf + ps * 2 * r.stage_bytes;
+    if (!ok_a || (has_b && !ok_b)) flag_status(a.status, TQ_DEV_BAD_BLOCK);
+    mbar_arrive_expect_tx(bar, (uint32_t)((ok_a ? r.stage_bytes : 0) + (ok_b ? r.stage_bytes : 0)));
+    if (ok_a) {
+      bulk_copy_g2s(dst, pp.kbase + (int64_t)blk_a * pp.kstride, (uint32_t)a.kpage, bar);
+      bulk_copy_g2s(dst + a.kpage, pp.vbase + (int64_t)blk_a * pp.vstride, (uint32_t)a.vpage, bar);
+    }
+    if (ok_b) {
+      bulk_copy_g2s(dst + r.stage_bytes, pp.kbase + (int64_t)blk_b * pp.kstride, (uint32_t)a.kpage, bar);
+      bulk_copy_g2s(dst + r.stage_bytes + a.kpage, pp.vbase + (int64_t)blk_b * pp.vstride, (uint32_t)a.vpage, bar);
+    }
+  }
+  return (ok_a ? 1u : 0u) | (ok_b ? 2u : 0u);
+}
+
 // ------------------------------------------------------------ block compute
 
 // Per-warp constants of the block loop.
@@ -533,10 +575,13 @@ struct WarpConsts {
   int g_, tig;
 };
 
-// One 16-token block of packed K/V for one warp.
-template <int NT, int BK, int BV, bool QJL>
-__device__ __forceinline__ void packed_block(SoftmaxState<NT>& st, const WarpConsts<NT>& wc, const uint8_t* sk,
-                                             const uint8_t* sv, int t0, int ctx, float qjl_coef) {
+// Keys of one 16-token block of packed K/V for one warp: base-2 logits u of head
+// 4 nt + tig at the lane's tokens g_, g_ + 8 (-inf past ctx or when !valid) and
+// their value weights wv (0 when masked), written to u[nt][o], u[nt][o + 1].
+template <int NT, int BK, int BV, bool QJL, int T>
+__device__ __forceinline__ void packed_keys(const WarpConsts<NT>& wc, const uint8_t* sk, const uint8_t* sv, int t0,
+                                            int ctx, bool valid, float qjl_coef, int o, float (&u)[NT][T],
+                                            float (&wv)[T]) {
   constexpr int RK = 16 * BK, RV = 16 * BV;
   const int g_ = wc.g_, tig = wc.tig;
   // ---- keys: 8 k-chunks in KC independent accumulation chains per n-tile
@@ -593,9 +638,9 @@ __device__ __forceinline__ void packed_block(SoftmaxState<NT>& st, const WarpCon
   const float* gk = reinterpret_cast<const float*>(sk + 16 * RK);
   const float* gv = reinterpret_cast<const float*>(sv + 16 * RV);
   const float gk0 = gk[g_], gk1 = gk[g_ + 8];
-  const float wv[2] = {gv[g_], gv[g_ + 8]};
-  const bool in0 = t0 + g_ < ctx, in1 = t0 + g_ + 8 < ctx;
-  float u[NT][2];
+  const bool in0 = valid && t0 + g_ < ctx, in1 = valid && t0 + g_ + 8 < ctx;
+  wv[o] = in0 ? gv[g_] : 0.0f;
+  wv[o + 1] = in1 ? gv[g_ + 8] : 0.0f;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     float v0 = gk0 * (dk[nt][0][0] + dk[nt][0][1]) * wc.inv_qs[nt];
@@ -605,13 +650,18 @@ __device__ __forceinline__ void packed_block(SoftmaxState<NT>& st, const WarpCon
       v0 += qjl_coef * rh[g_] * sq[nt][0] * wc.inv_us[nt];
       v1 += qjl_coef * rh[g_ + 8] * sq[nt][1] * wc.inv_us[nt];
     }
-    u[nt][0] = in0 ? v0 : -INFINITY;
-    u[nt][1] = in1 ? v1 : -INFINITY;
+    u[nt][o] = in0 ? v0 : -INFINITY;
+    u[nt][o + 1] = in1 ? v1 : -INFINITY;
   }
-  uint32_t pk[NT], pl[NT];
-  softmax_block<NT, false>(st, u, wv, pk, pl);
+}
 
-  // ---- values: tokens ta, tb of tile 0 and ta + 8, tb + 8 of tile 1
+// Values of one block: acc += V_hat^T P' (pk[nt] = P' of the lane's token pair),
+// value codes of tokens ta, tb (tile 0) and ta + 8, tb + 8 (tile 1) from stage sv.
+template <int NT, int BV>
+__device__ __forceinline__ void packed_values(SoftmaxState<NT>& st, const WarpConsts<NT>& wc, const uint8_t* sv,
+                                              const uint32_t (&pk)[NT]) {
+  constexpr int RV = 16 * BV;
+  const int g_ = wc.g_, tig = wc.tig;
   const int ta = tok_a(tig), tb = tok_b(tig);
   uint32_t vw[4][2];
   load_sixteenth<BV>(sv + ta * RV, g_, vw[0]);
@@ -669,14 +719,14 @@ __device__ __forceinline__ void bf16_block(SoftmaxState<NT>& st, const WarpConst
     u[nt][0] = in0 ? v0 : -INFINITY;
     u[nt][1] = in1 ? v1 : -INFINITY;
   }
-  const float ones[2] = {1.0f, 1.0f};
-  uint32_t pk[NT], pl[NT];
-  softmax_block<NT, true>(st, u, ones, pk, pl);
+  const float ones[2] = {in0 ? 1.0f : 0.0f, in1 ? 1.0f : 0.0f};
+  uint32_t pk[NT][1], pl[NT][1];
+  softmax_tokens<NT, true, 2>(st, u, ones, pk, pl);
   uint32_t bh[NT][2][2], bl[NT][2][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    wc.pt.apply(pk[nt], bh[nt]);
-    wc.pt.apply(pl[nt], bl[nt]);
+    wc.pt.apply(pk[nt][0], bh[nt]);
+    wc.pt.apply(pl[nt][0], bl[nt]);
   }
 #pragma unroll
   for (int kt = 0; kt < 2; ++kt) {
@@ -858,9 +908,26 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     }
   }
 
+  // packed pages go in pairs of blocks: stages / 2 pair stages, one mbarrier each
+  const int pstages = stages >= 2 ? stages / 2 : 1;
+  const int n_pairs = (n_my + 1) / 2;
+  PagePtrs pp;
+  pp.kbase = a.kpool + (int64_t)kvh * a.kpage;
+  pp.vbase = a.vpool + (int64_t)kvh * a.vpage;
+  pp.kstride = (int64_t)a.Hkv * a.kpage;
+  pp.vstride = (int64_t)a.Hkv * a.vpage;
   uint32_t valid_mask = 0u;
-  for (int k = 0; k < stages && k < n_my; ++k)
-    if (issue_block(ring, k, a, ids.get(k, lane), kvh, lane)) valid_mask |= 1u << k;
+  if constexpr (KIND == 0) {
+    for (int k = 0; k < pstages && k < n_pairs; ++k) {
+      const bool hb = 2 * k + 1 < n_my;
+      const int ba = ids.get(2 * k, lane);
+      const int bb = hb ? ids.get(2 * k + 1, lane) : -1;
+      valid_mask |= issue_pair(ring, k, a, pp, ba, bb, hb, lane) << (2 * k);
+    }
+  } else {
+    for (int k = 0; k < stages && k < n_my; ++k)
+      if (issue_block(ring, k, a, ids.get(k, lane), kvh, lane)) valid_mask |= 1u << k;
+  }
 
   SoftmaxState<NT> st;
 #pragma unroll
@@ -877,37 +944,77 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   int i = 0, stage = 0;
   uint32_t phase = 0u;
   bool aborted = false;
-  for (; i < n_my; ++i) {
-    if (!mbar_wait(ring.bar + stage, phase)) {
-      if (lane == 0) flag_status(a.status, TQ_DEV_WAIT_TIMEOUT);
-      aborted = true;
-      break;
+  if constexpr (KIND == 0) {
+    // two blocks (32 tokens) per step: keys of both, one softmax update, values of both
+    for (; i < n_pairs; ++i) {
+      if (!mbar_wait(ring.bar + stage, phase)) {
+        if (lane == 0) flag_status(a.status, TQ_DEV_WAIT_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      const uint32_t m = (valid_mask >> (2 * stage)) & 3u;
+      if (m) {
+        const uint8_t* sa = ring.buf + stage * 2 * stage_bytes;
+        const uint8_t* sb = sa + stage_bytes;
+        const int t0 = (j0 + 2 * i) * kBlock;
+        float u[NT][4], wv[4];
+        packed_keys<NT, BK, BV, QJL, 4>(wc, sa, sa + a.kpage, t0, ctx, (m & 1u) != 0, a.qjl_coef, 0, u, wv);
+        packed_keys<NT, BK, BV, QJL, 4>(wc, sb, sb + a.kpage, t0 + kBlock, ctx, (m & 2u) != 0, a.qjl_coef, 2, u, wv);
+        uint32_t pk[NT][2], pl[NT][2];
+        softmax_tokens<NT, false, 4>(st, u, wv, pk, pl);
+        uint32_t pka[NT], pkb[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          pka[nt] = pk[nt][0];
+          pkb[nt] = pk[nt][1];
+        }
+        packed_values<NT, BV>(st, wc, sa + a.kpage, pka);
+        packed_values<NT, BV>(st, wc, sb + a.kpage, pkb);
+      }
+      __syncwarp();
+      if (i + pstages < n_pairs) {
+        const int k = i + pstages;
+        const bool hb = 2 * k + 1 < n_my;
+        const int ba = ids.get(2 * k, lane);
+        const int bb = hb ? ids.get(2 * k + 1, lane) : -1;
+        valid_mask = (valid_mask & ~(3u << (2 * stage))) | (issue_pair(ring, stage, a, pp, ba, bb, hb, lane) << (2 * stage));
+      }
+      if (++stage == pstages) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
-    if (valid_mask & (1u << stage)) {
-      const uint8_t* sk = ring.buf + stage * stage_bytes;
-      const uint8_t* sv = sk + a.kpage;
-      const int t0 = (j0 + i) * kBlock;
-      if constexpr (KIND == 0)
-        packed_block<NT, BK, BV, QJL>(st, wc, sk, sv, t0, ctx, a.qjl_coef);
-      else
-        bf16_block<NT>(st, wc, sk, sv, t0, ctx);
-    }
-    __syncwarp();
-    if (i + stages < n_my) {
-      if (issue_block(ring, stage, a, ids.get(i + stages, lane), kvh, lane)) valid_mask |= 1u << stage;
-      else valid_mask &= ~(1u << stage);
-    }
-    if (++stage == stages) {
-      stage = 0;
-      phase ^= 1u;
+  } else {
+    for (; i < n_my; ++i) {
+      if (!mbar_wait(ring.bar + stage, phase)) {
+        if (lane == 0) flag_status(a.status, TQ_DEV_WAIT_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      if (valid_mask & (1u << stage)) {
+        const uint8_t* sk = ring.buf + stage * stage_bytes;
+        const uint8_t* sv = sk + a.kpage;
+        bf16_block<NT>(st, wc, sk, sv, (j0 + i) * kBlock, ctx);
+      }
+      __syncwarp();
+      if (i + stages < n_my) {
+        if (issue_block(ring, stage, a, ids.get(i + stages, lane), kvh, lane)) valid_mask |= 1u << stage;
+        else valid_mask &= ~(1u << stage);
+      }
+      if (++stage == stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
   }
   if (aborted) {  // drain copies still in flight into this warp's ring before the smem is reused
+    const int nst = KIND == 0 ? pstages : stages;
+    const int nun = KIND == 0 ? n_pairs : n_my;
     int stg = stage;
     uint32_t ph = phase;
-    for (int k = i; k < n_my && k < i + stages; ++k) {
+    for (int k = i; k < nun && k < i + nst; ++k) {
       mbar_wait(ring.bar + stg, ph);
-      if (++stg == stages) { stg = 0; ph ^= 1u; }
+      if (++stg == nst) { stg = 0; ph ^= 1u; }
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
