@@ -578,14 +578,15 @@ struct WarpConsts {
 // Keys of one 16-token block of packed K/V for one warp: base-2 logits u of head
 // 4 nt + tig at the lane's tokens g_, g_ + 8 (-inf past ctx or when !valid) and
 // their value weights wv (0 when masked), written to u[nt][o], u[nt][o + 1].
-template <int NT, int BK, int BV, bool QJL, int T>
+template <int NT, int BK, int BV, bool QJL, int T, bool MASKED>
 __device__ __forceinline__ void packed_keys(const WarpConsts<NT>& wc, const uint8_t* sk, const uint8_t* sv, int t0,
                                             int ctx, bool valid, float qjl_coef, int o, float (&u)[NT][T],
                                             float (&wv)[T]) {
   constexpr int RK = 16 * BK, RV = 16 * BV;
   const int g_ = wc.g_, tig = wc.tig;
-  // ---- keys: 8 k-chunks in KC independent accumulation chains per n-tile
-  constexpr int KC = NT == 1 ? 4 : 2;
+  // ---- keys: 8 k-chunks in KC independent accumulation chains per n-tile (the
+  // two blocks of a step give the scheduler a second independent set)
+  constexpr int KC = 2;
   uint32_t kn[2][4];
   load_quarter<BK>(sk + g_ * RK, tig, kn[0]);
   load_quarter<BK>(sk + (g_ + 8) * RK, tig, kn[1]);
@@ -638,7 +639,7 @@ __device__ __forceinline__ void packed_keys(const WarpConsts<NT>& wc, const uint
   const float* gk = reinterpret_cast<const float*>(sk + 16 * RK);
   const float* gv = reinterpret_cast<const float*>(sv + 16 * RV);
   const float gk0 = gk[g_], gk1 = gk[g_ + 8];
-  const bool in0 = valid && t0 + g_ < ctx, in1 = valid && t0 + g_ + 8 < ctx;
+  const bool in0 = !MASKED || (valid && t0 + g_ < ctx), in1 = !MASKED || (valid && t0 + g_ + 8 < ctx);
   wv[o] = in0 ? gv[g_] : 0.0f;
   wv[o + 1] = in1 ? gv[g_ + 8] : 0.0f;
 #pragma unroll
@@ -958,8 +959,14 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
         const uint8_t* sb = sa + stage_bytes;
         const int t0 = (j0 + 2 * i) * kBlock;
         float u[NT][4], wv[4];
-        packed_keys<NT, BK, BV, QJL, 4>(wc, sa, sa + a.kpage, t0, ctx, (m & 1u) != 0, a.qjl_coef, 0, u, wv);
-        packed_keys<NT, BK, BV, QJL, 4>(wc, sb, sb + a.kpage, t0 + kBlock, ctx, (m & 2u) != 0, a.qjl_coef, 2, u, wv);
+        if (m == 3u && t0 + 2 * kBlock <= ctx) {  // both blocks whole: no masks
+          packed_keys<NT, BK, BV, QJL, 4, false>(wc, sa, sa + a.kpage, t0, ctx, true, a.qjl_coef, 0, u, wv);
+          packed_keys<NT, BK, BV, QJL, 4, false>(wc, sb, sb + a.kpage, t0 + kBlock, ctx, true, a.qjl_coef, 2, u, wv);
+        } else {
+          packed_keys<NT, BK, BV, QJL, 4, true>(wc, sa, sa + a.kpage, t0, ctx, (m & 1u) != 0, a.qjl_coef, 0, u, wv);
+          packed_keys<NT, BK, BV, QJL, 4, true>(wc, sb, sb + a.kpage, t0 + kBlock, ctx, (m & 2u) != 0, a.qjl_coef, 2,
+                                                u, wv);
+        }
         uint32_t pk[NT][2], pl[NT][2];
         softmax_tokens<NT, false, 4>(st, u, wv, pk, pl);
         uint32_t pka[NT], pkb[NT];
