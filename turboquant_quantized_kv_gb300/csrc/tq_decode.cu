@@ -830,20 +830,95 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   // ---- prologue: start the long-latency loads first (context length, query rows),
   // build the code tables while they are in flight, then the block ids and copies
   const int ctx_raw = has ? __ldg(a.ctx_lens + b) : 0;
+
+  // CTA-shared query rotation (q_in_kernel != 0): the rows of this CTA's units are
+  // rotated once, one warp per row, into a scratch area past the rings
+  const int c0 = blockIdx.x * NW;
+  const int c1 = min(c0 + NW, a.chunks);
+  const int u0 = c0 / a.splits;
+  const int nu = c1 > c0 ? (c1 - 1) / a.splits - u0 + 1 : 0;
+  const uint32_t hi_rings = (uint32_t)NW > n_lo ? (uint32_t)NW - n_lo : 0u;
+  const uint32_t qs_addr = (hi0 + hi_rings * ring_bytes + 15u) & ~15u;
+  const bool q_shared = a.q_in_kernel != 0 && layout_ok && qs_addr + (uint32_t)(nu * HPW * kD * 4) <= bars_addr;
+  float* qs = reinterpret_cast<float*>(gen(qs_addr));  // [nu * HPW][128]
+  // raw query coordinates 4 lane .. 4 lane + 3 of rotation row `row` (zeros when absent)
+  auto load_rot_row = [&](int row, float (&y)[4]) {
+    y[0] = y[1] = y[2] = y[3] = 0.0f;
+    const int ur = u0 + row / HPW, h = row % HPW;
+    const int ub = ur / per_b, urr = ur - ub * per_b, ukvh = urr / a.ngroups, uhg = urr - ukvh * a.ngroups;
+    if (h >= min(HPW, a.g - uhg * HPW)) return;
+    const int64_t qrow = (int64_t)ub * a.Hq + ukvh * a.g + uhg * HPW + h;
+    if (a.q_bf16) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.q) + qrow * kD) +
+                            lane);
+      y[0] = __uint_as_float(w.x << 16); y[1] = __uint_as_float(w.x & 0xFFFF0000u);
+      y[2] = __uint_as_float(w.y << 16); y[3] = __uint_as_float(w.y & 0xFFFF0000u);
+    } else {
+      const float4 w = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.q) + qrow * kD) + lane);
+      y[0] = w.x; y[1] = w.y; y[2] = w.z; y[3] = w.w;
+    }
+  };
+  // q' = H (s * q) / sqrt(d) (or q scaled) of one row into the shared scratch
+  auto rotate_row = [&](int row, float (&y)[4]) {
+    if (a.q_in_kernel == 1) {  // bits 0, 1 of the coordinate in the lane, bits 2..6 across lanes
+#pragma unroll
+      for (int k = 0; k < 4; ++k) y[k] *= __ldg(a.rot + 4 * lane + k);
+      const float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
+      y[0] = t0 + t2; y[2] = t0 - t2; y[1] = t1 + t3; y[3] = t1 - t3;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float o = __shfl_xor_sync(0xffffffffu, y[k], m);
+          y[k] = upper ? (o - y[k]) : (y[k] + o);
+        }
+      }
+    }
+    const float f = a.q_in_kernel == 1 ? a.q_scale * 0.08838834764831845f : a.q_scale;
+    reinterpret_cast<float4*>(qs + row * kD)[lane] = make_float4(y[0] * f, y[1] * f, y[2] * f, y[3] * f);
+  };
+  float y0[4];
+  const bool row0 = q_shared && warp < nu * HPW;
+  if (row0) load_rot_row(warp, y0);  // in flight with the context length
+
   float qv[NT][32];
   float uv[QJL ? NT : 1][32];
+  if (!q_shared) {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int hq = 4 * nt + (g_ >> 1);
-    const bool hv = has && hq < gc;
-    const int64_t row = (int64_t)b * a.Hq + head0 + (hv ? hq : 0);
-    if (a.q_in_kernel) {
-      load_q_raw(a.q, a.q_bf16 != 0, row, hv, tig, qv[nt]);
-    } else {
-      grid_dep_wait();  // qrot comes from the preceding rotation pass
-      load_q(a.qrot + row * kD, hv, tig, qv[nt]);
+    for (int nt = 0; nt < NT; ++nt) {
+      const int hq = 4 * nt + (g_ >> 1);
+      const bool hv = has && hq < gc;
+      const int64_t row = (int64_t)b * a.Hq + head0 + (hv ? hq : 0);
+      if (a.q_in_kernel) {
+        load_q_raw(a.q, a.q_bf16 != 0, row, hv, tig, qv[nt]);
+      } else {
+        grid_dep_wait();  // qrot comes from the preceding rotation pass
+        load_q(a.qrot + row * kD, hv, tig, qv[nt]);
+      }
+      if constexpr (QJL) load_q(a.uqjl + row * kD, hv, tig, uv[nt]);
     }
-    if constexpr (QJL) load_q(a.uqjl + row * kD, hv, tig, uv[nt]);
+  }
+
+  int ctx = ctx_raw;
+  if (ctx < 0 || ctx > a.max_blocks * kBlock) {
+    if (lane == 0 && s == 0 && r == 0) flag_status(a.status, TQ_DEV_BAD_CONTEXT);
+    ctx = ctx < 0 ? 0 : a.max_blocks * kBlock;
+  }
+  const int nblk = (ctx + kBlock - 1) / kBlock;
+  const int j0 = (int)((int64_t)s * nblk / a.splits);
+  const int j1 = (int)((int64_t)(s + 1) * nblk / a.splits);
+  const int n_my = has ? j1 - j0 : 0;
+  BlockIds ids;
+  ids.init(a.block_table + (int64_t)b * a.max_blocks + j0, n_my, lane);
+
+  if (row0) {
+    rotate_row(warp, y0);
+    for (int row = warp + NW; row < nu * HPW; row += NW) {
+      float y[4];
+      load_rot_row(row, y);
+      rotate_row(row, y);
+    }
   }
 
   Ring ring;
@@ -860,8 +935,13 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     if (layout_ok) {
       // row e (pair byte, low nibble first) = f16x2(c[e & 15], c[e >> 4]) once per lane:
       // 16-byte word j of a row holds lanes 4j..4j+3 (j < 8: keys, j >= 8: values)
-      constexpr uint32_t MK = (1u << BK) - 1u, MV = (1u << BV) - 1u;
-      const float cl = lane < 16 ? a.cbk.c[lane & MK] : a.cbv.c[(lane - 16) & MV];
+      constexpr int MK = (1 << BK) - 1, MV = (1 << BV) - 1;
+      float cl = 0.0f;  // lane k < 16: key centroid k & MK, lane 16 + k: value centroid k & MV
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {  // uniform constant loads (a lane-indexed parameter read would serialize)
+        if (lane == k) cl = a.cbk.c[k & MK];
+        if (lane == 16 + k) cl = a.cbv.c[k & MV];
+      }
       uint4* tab = reinterpret_cast<uint4*>(gen(kLutAddr));
       for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
         const int e = i >> 4, vo = (i & 8) ? 16 : 0;
@@ -873,17 +953,6 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     }
   }
 
-  int ctx = ctx_raw;
-  if (ctx < 0 || ctx > a.max_blocks * kBlock) {
-    if (lane == 0 && s == 0 && r == 0) flag_status(a.status, TQ_DEV_BAD_CONTEXT);
-    ctx = ctx < 0 ? 0 : a.max_blocks * kBlock;
-  }
-  const int nblk = (ctx + kBlock - 1) / kBlock;
-  const int j0 = (int)((int64_t)s * nblk / a.splits);
-  const int j1 = (int)((int64_t)(s + 1) * nblk / a.splits);
-  const int n_my = has ? j1 - j0 : 0;
-  BlockIds ids;
-  ids.init(a.block_table + (int64_t)b * a.max_blocks + j0, n_my, lane);
 
   // per-warp constants: query fragments of column g_ (head 4 nt + g_ / 2, part g_ & 1)
   WarpConsts<NT> wc;
@@ -892,22 +961,38 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   wc.pt.init(g_, tig);
   wc.lk = kLutAddr | (4u * lane);
   wc.lv = wc.lk + 128u;
+  auto q_frags = [&]() {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    if (a.q_in_kernel == 1) {
-      rotate_q_quad(qv[nt], a.rot, tig, a.q_scale);
-    } else if (a.q_in_kernel == 2) {
+    for (int nt = 0; nt < NT; ++nt) {
+      if (q_shared) {
+        const int row = (unit - u0) * HPW + 4 * nt + (g_ >> 1);
+        if (has) {
+          const float4* src = reinterpret_cast<const float4*>(qs + row * kD + 32 * tig);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) qv[nt][k] *= a.q_scale;
+          for (int k = 0; k < 8; ++k) {
+            const float4 v = src[k];
+            qv[nt][4 * k] = v.x; qv[nt][4 * k + 1] = v.y; qv[nt][4 * k + 2] = v.z; qv[nt][4 * k + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) qv[nt][k] = 0.0f;
+        }
+      } else if (a.q_in_kernel == 1) {
+        rotate_q_quad(qv[nt], a.rot, tig, a.q_scale);
+      } else if (a.q_in_kernel == 2) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) qv[nt][k] *= a.q_scale;
+      }
+      const float iq = make_q_frags<KIND == 1>(qv[nt], g_ & 1, wc.bq[nt]);
+      wc.inv_qs[nt] = __shfl_sync(0xffffffffu, iq, 8 * tig);  // scale of head 4 nt + tig
+      wc.inv_us[nt] = 0.0f;
+      if constexpr (QJL) {
+        const float iu = make_q_frags<false>(uv[nt], g_ & 1, wc.bu[nt]);
+        wc.inv_us[nt] = __shfl_sync(0xffffffffu, iu, 8 * tig);
+      }
     }
-    const float iq = make_q_frags<KIND == 1>(qv[nt], g_ & 1, wc.bq[nt]);
-    wc.inv_qs[nt] = __shfl_sync(0xffffffffu, iq, 8 * tig);  // scale of head 4 nt + tig
-    wc.inv_us[nt] = 0.0f;
-    if constexpr (QJL) {
-      const float iu = make_q_frags<false>(uv[nt], g_ & 1, wc.bu[nt]);
-      wc.inv_us[nt] = __shfl_sync(0xffffffffu, iu, 8 * tig);
-    }
-  }
+  };
+  if (!q_shared) q_frags();
 
   // packed pages go in pairs of blocks: stages / 2 pair stages, one mbarrier each
   const int pstages = stages >= 2 ? stages / 2 : 1;
@@ -940,7 +1025,8 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt) st.acc[nt][mt][0] = st.acc[nt][mt][1] = st.acc[nt][mt][2] = st.acc[nt][mt][3] = 0.0f;
   }
-  __syncthreads();  // tables ready
+  __syncthreads();  // tables (and shared query rows) ready
+  if (q_shared) q_frags();
 
   int i = 0, stage = 0;
   uint32_t phase = 0u;
@@ -1060,11 +1146,7 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   __syncthreads();
 
   // ---- epilogue 2: one partial per (unit present in this CTA, head), all threads
-  const int c0 = blockIdx.x * NW;
-  const int c1 = min(c0 + NW, a.chunks);
   if (!layout_ok || c0 >= c1) return;  // uniform
-  const int u0 = c0 / a.splits;
-  const int nu = (c1 - 1) / a.splits - u0 + 1;
   for (int it = threadIdx.x; it < nu * HPW * 32; it += NW * 32) {
     const int ui = it / (HPW * 32), h = (it >> 5) % HPW, qd = it & 31;
     const int u = u0 + ui;
