@@ -99,6 +99,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// 2^k for an integer k, exactly (0 below the normal range, 2^127 above it).
+__device__ __forceinline__ float pow2i(int k) {
+  if (k < -126) return 0.0f;
+  return __uint_as_float((uint32_t)(min(k, 127) + 127) << 23);
+}
+
 // 2^x by the hardware approximation (relative error ~2^-22; 2^-inf = 0).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -273,34 +279,35 @@ __device__ __forceinline__ int tok_b(int tig) { return 2 * tig + 1 - (tig & 1); 
 // scale per head (max |q| scale < 2^14), or bf16.  Returns 1 / scale.
 template <bool BF16>
 __device__ __forceinline__ float make_q_frags(const float (&v)[32], int part, uint32_t (&bq)[8][2]) {
-  float scale = 1.0f;
+  float scale = 1.0f, inv_scale = 1.0f;
   if (!BF16) {
     float mx = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(v[i]));
     mx = quad_max(mx);  // the quad (same g_) holds one head
-    int e = 0;
-    if (mx > 0.0f) frexpf(mx, &e);
-    scale = ldexpf(1.0f, 14 - e);
+    // mx in [2^(e-1), 2^e): scale = 2^(14 - e) (1 for a zero or subnormal row)
+    const int ebits = (int)((__float_as_uint(mx) >> 23) & 0xFFu);
+    scale = ebits > 0 ? pow2i(140 - ebits) : 1.0f;
+    inv_scale = ebits > 0 ? pow2i(ebits - 140) : 1.0f;
   }
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    float x[4];
+  for (int c = 0; c < 8; ++c)
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float sv = v[4 * c + k] * scale;
-      const float hi = BF16 ? __bfloat162float(__float2bfloat16_rn(sv)) : __half2float(__float2half_rn(sv));
-      x[k] = part ? sv - hi : hi;
+    for (int j = 0; j < 2; ++j) {  // pair (4c + 2j, 4c + 2j + 1): hi = round(s), lo = s - hi
+      const float s0 = v[4 * c + 2 * j] * scale, s1 = v[4 * c + 2 * j + 1] * scale;
+      uint32_t hi;
+      float2 back;
+      if (BF16) {
+        hi = pack_bf162(s0, s1);
+        back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
+      } else {
+        hi = pack_half2(s0, s1);
+        back = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+      }
+      const uint32_t lo = BF16 ? pack_bf162(s0 - back.x, s1 - back.y) : pack_half2(s0 - back.x, s1 - back.y);
+      bq[c][j] = part ? lo : hi;
     }
-    if (BF16) {
-      bq[c][0] = pack_bf162(x[0], x[1]);
-      bq[c][1] = pack_bf162(x[2], x[3]);
-    } else {
-      bq[c][0] = pack_half2(x[0], x[1]);
-      bq[c][1] = pack_half2(x[2], x[3]);
-    }
-  }
-  return 1.0f / scale;
+  return inv_scale;
 }
 
 __device__ __forceinline__ void load_q(const float* qrow, bool valid, int tig, float (&v)[32]) {
@@ -400,7 +407,7 @@ __device__ __forceinline__ void softmax_tokens(SoftmaxState<NT>& st, const float
       const float bm = col_max(um[nt]);
       if (bm > st.M[nt] + kRescaleThreshold) {  // the same on the head's lanes
         const float newM = ceilf(bm);
-        const float alpha = (st.M[nt] == -INFINITY) ? 0.0f : ldexpf(1.0f, (int)(st.M[nt] - newM));
+        const float alpha = (st.M[nt] == -INFINITY) ? 0.0f : pow2i((int)(st.M[nt] - newM));
         st.l[nt] *= alpha;
         st.R[nt] *= alpha;  // acc R is the true sum: scale R, keep acc
         st.rR[nt] = st.R[nt] > 0.0f ? kPScale / st.R[nt] : 0.0f;
@@ -839,8 +846,12 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   const int nu = c1 > c0 ? (c1 - 1) / a.splits - u0 + 1 : 0;
   const uint32_t hi_rings = (uint32_t)NW > n_lo ? (uint32_t)NW - n_lo : 0u;
   const uint32_t qs_addr = (hi0 + hi_rings * ring_bytes + 15u) & ~15u;
-  const bool q_shared = a.q_in_kernel != 0 && layout_ok && qs_addr + (uint32_t)(nu * HPW * kD * 4) <= bars_addr;
-  float* qs = reinterpret_cast<float*>(gen(qs_addr));  // [nu * HPW][128]
+  const bool q_shared =
+      a.q_in_kernel != 0 && layout_ok && qs_addr + (uint32_t)(nu * HPW * (kD * 4 + 4)) <= bars_addr;
+  // per row: the key-side MMA fragments of the row's head (512 B, see rotate_row), then
+  // after all rows the rows' 1 / scale
+  uint32_t* qs = reinterpret_cast<uint32_t*>(gen(qs_addr));
+  float* qs_inv = reinterpret_cast<float*>(qs + nu * HPW * kD);
   // raw query coordinates 4 lane .. 4 lane + 3 of rotation row `row` (zeros when absent)
   auto load_rot_row = [&](int row, float (&y)[4]) {
     y[0] = y[1] = y[2] = y[3] = 0.0f;
@@ -876,7 +887,42 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
       }
     }
     const float f = a.q_in_kernel == 1 ? a.q_scale * 0.08838834764831845f : a.q_scale;
-    reinterpret_cast<float4*>(qs + row * kD)[lane] = make_float4(y[0] * f, y[1] * f, y[2] * f, y[3] * f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] *= f;
+    // fragments: lane l = 8 t + c holds coordinates 32 t + 4 c + {0..3}, i.e. words
+    // (c, j = 0, 1) of quarter t for both parts (fp16 hi and lo with a power-of-two
+    // scale per row, or bf16 hi and lo).  Segment (part, t) = 16 words [c][j]; its
+    // 16-byte chunk k sits at k ^ ((4 part + t) >> 1) so readers hit distinct banks.
+    float scale = 1.0f, inv_scale = 1.0f;
+    if (KIND == 0) {
+      float mx = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const int ebits = (int)((__float_as_uint(mx) >> 23) & 0xFFu);
+      scale = ebits > 0 ? pow2i(140 - ebits) : 1.0f;
+      inv_scale = ebits > 0 ? pow2i(ebits - 140) : 1.0f;
+    }
+    uint32_t hw[2], lw[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float s0 = y[2 * j] * scale, s1 = y[2 * j + 1] * scale;
+      float2 back;
+      if (KIND == 1) {
+        hw[j] = pack_bf162(s0, s1);
+        back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[j]));
+        lw[j] = pack_bf162(s0 - back.x, s1 - back.y);
+      } else {
+        hw[j] = pack_half2(s0, s1);
+        back = __half22float2(*reinterpret_cast<const __half2*>(&hw[j]));
+        lw[j] = pack_half2(s0 - back.x, s1 - back.y);
+      }
+    }
+    const int t = lane >> 3, c = lane & 7;
+    uint32_t* rowp = qs + row * kD;
+    *reinterpret_cast<uint2*>(rowp + 16 * t + 4 * ((c >> 1) ^ (t >> 1)) + 2 * (c & 1)) = make_uint2(hw[0], hw[1]);
+    *reinterpret_cast<uint2*>(rowp + 16 * (4 + t) + 4 * ((c >> 1) ^ ((4 + t) >> 1)) + 2 * (c & 1)) =
+        make_uint2(lw[0], lw[1]);
+    if (lane == 0) qs_inv[row] = inv_scale;
   };
   float y0[4];
   const bool row0 = q_shared && warp < nu * HPW;
@@ -931,6 +977,28 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncwarp();  // this warp's barriers are ready
 
+  // first copies as soon as the block ids are in; the code tables are built meanwhile.
+  // Packed pages go in pairs of blocks: stages / 2 pair stages, one mbarrier each
+  const int pstages = stages >= 2 ? stages / 2 : 1;
+  const int n_pairs = (n_my + 1) / 2;
+  PagePtrs pp;
+  pp.kbase = a.kpool + (int64_t)kvh * a.kpage;
+  pp.vbase = a.vpool + (int64_t)kvh * a.vpage;
+  pp.kstride = (int64_t)a.Hkv * a.kpage;
+  pp.vstride = (int64_t)a.Hkv * a.vpage;
+  uint32_t valid_mask = 0u;
+  if constexpr (KIND == 0) {
+    for (int k = 0; k < pstages && k < n_pairs; ++k) {
+      const bool hb = 2 * k + 1 < n_my;
+      const int ba = ids.get(2 * k, lane);
+      const int bb = hb ? ids.get(2 * k + 1, lane) : -1;
+      valid_mask |= issue_pair(ring, k, a, pp, ba, bb, hb, lane) << (2 * k);
+    }
+  } else {
+    for (int k = 0; k < stages && k < n_my; ++k)
+      if (issue_block(ring, k, a, ids.get(k, lane), kvh, lane)) valid_mask |= 1u << k;
+  }
+
   if constexpr (KIND == 0) {
     if (layout_ok) {
       // row e (pair byte, low nibble first) = f16x2(c[e & 15], c[e >> 4]) once per lane:
@@ -953,7 +1021,6 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     }
   }
 
-
   // per-warp constants: query fragments of column g_ (head 4 nt + g_ / 2, part g_ & 1)
   WarpConsts<NT> wc;
   wc.g_ = g_;
@@ -964,19 +1031,21 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   auto q_frags = [&]() {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      if (q_shared) {
-        const int row = (unit - u0) * HPW + 4 * nt + (g_ >> 1);
-        if (has) {
-          const float4* src = reinterpret_cast<const float4*>(qs + row * kD + 32 * tig);
+      if (q_shared) {  // fragments and scale prepared by the rotating warp
+        const int rbase = (unit - u0) * HPW + 4 * nt;
+        const int seg = 4 * (g_ & 1) + tig;
+        const uint4* src = reinterpret_cast<const uint4*>(qs + (rbase + (g_ >> 1)) * kD + 16 * seg);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float4 v = src[k];
-            qv[nt][4 * k] = v.x; qv[nt][4 * k + 1] = v.y; qv[nt][4 * k + 2] = v.z; qv[nt][4 * k + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) qv[nt][k] = 0.0f;
+        for (int k = 0; k < 4; ++k) {
+          const uint4 w = has ? src[k ^ (seg >> 1)] : make_uint4(0u, 0u, 0u, 0u);
+          wc.bq[nt][2 * k][0] = w.x;
+          wc.bq[nt][2 * k][1] = w.y;
+          wc.bq[nt][2 * k + 1][0] = w.z;
+          wc.bq[nt][2 * k + 1][1] = w.w;
         }
+        wc.inv_qs[nt] = has ? qs_inv[rbase + tig] : 1.0f;  // head 4 nt + tig
+        wc.inv_us[nt] = 0.0f;
+        continue;
       } else if (a.q_in_kernel == 1) {
         rotate_q_quad(qv[nt], a.rot, tig, a.q_scale);
       } else if (a.q_in_kernel == 2) {
@@ -993,27 +1062,6 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     }
   };
   if (!q_shared) q_frags();
-
-  // packed pages go in pairs of blocks: stages / 2 pair stages, one mbarrier each
-  const int pstages = stages >= 2 ? stages / 2 : 1;
-  const int n_pairs = (n_my + 1) / 2;
-  PagePtrs pp;
-  pp.kbase = a.kpool + (int64_t)kvh * a.kpage;
-  pp.vbase = a.vpool + (int64_t)kvh * a.vpage;
-  pp.kstride = (int64_t)a.Hkv * a.kpage;
-  pp.vstride = (int64_t)a.Hkv * a.vpage;
-  uint32_t valid_mask = 0u;
-  if constexpr (KIND == 0) {
-    for (int k = 0; k < pstages && k < n_pairs; ++k) {
-      const bool hb = 2 * k + 1 < n_my;
-      const int ba = ids.get(2 * k, lane);
-      const int bb = hb ? ids.get(2 * k + 1, lane) : -1;
-      valid_mask |= issue_pair(ring, k, a, pp, ba, bb, hb, lane) << (2 * k);
-    }
-  } else {
-    for (int k = 0; k < stages && k < n_my; ++k)
-      if (issue_block(ring, k, a, ids.get(k, lane), kvh, lane)) valid_mask |= 1u << k;
-  }
 
   SoftmaxState<NT> st;
 #pragma unroll
@@ -1159,7 +1207,7 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     float L = 0.0f;
     for (int w = wb; w < we; ++w) {
       const float mw = rm[w * HPW + h];
-      const float f = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
+      const float f = (mw == -INFINITY) ? 0.0f : pow2i((int)(mw - M));  // maxima are integral
       const float4 v = *reinterpret_cast<const float4*>(racc + (w * HPW + h) * kD + 4 * qd);
       acc.x = fmaf(v.x, f, acc.x);
       acc.y = fmaf(v.y, f, acc.y);
@@ -1219,7 +1267,7 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
         auto merge = [&](float m, float l, float v) {
           if (m == -INFINITY) return;
           const float nm = fmaxf(M, m);
-          const float fo = (M == -INFINITY) ? 0.0f : exp2f(M - nm), fn = exp2f(m - nm);
+          const float fo = (M == -INFINITY) ? 0.0f : pow2i((int)(M - nm)), fn = pow2i((int)(m - nm));
           y = y * fo + v * fn;
           L = L * fo + l * fn;
           M = nm;
@@ -1335,7 +1383,7 @@ __global__ void __launch_bounds__(128) k_combine(const float* __restrict__ part,
   const float M = fmaxf(fmaxf(stot[0], stot[1]), fmaxf(stot[2], stot[3]));
   for (int s = t; s < splits; s += blockDim.x) {
     const float ms = slot_live(unit, splits, s, um.nw) ? ml[(bh * splits + s) * 2] : -INFINITY;
-    const float f = (ms == -INFINITY) ? 0.0f : exp2f(ms - M);
+    const float f = (ms == -INFINITY) ? 0.0f : pow2i((int)(ms - M));  // maxima are integral
     sm[s] = f;
     sl[s] = f > 0.0f ? ml[(bh * splits + s) * 2 + 1] * f : 0.0f;
   }
