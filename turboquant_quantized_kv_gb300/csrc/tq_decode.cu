@@ -1225,15 +1225,18 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   }
   if (!a.fuse_combine) return;
 
-  // ---- epilogue 3: the CTA that completes a unit merges its slots and applies Pi^T
-  __threadfence();
+  // ---- epilogue 3: the CTA that completes a unit merges its slots and applies Pi^T.
+  // The partials of all threads are ordered before the count by the barrier and one
+  // release per unit; the completing CTA acquires the count before the barrier that
+  // lets its threads read the other CTAs' partials.
   __syncthreads();
   if (threadIdx.x < nu) {
     grid_dep_wait();  // the counters are zeroed by the preceding pass
     const int u = u0 + threadIdx.x;
     const int covered = min((u + 1) * a.splits, c1) - max(u * a.splits, c0);
-    const int done = atomicAdd(a.counters + u, covered) + covered;
-    const bool last = done == a.splits;
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(a.counters + u), "r"(covered) : "memory");
+    const bool last = old + covered == a.splits;
     if (last) a.counters[u] = 0;  // every chunk of the unit has counted: ready for the next call
     last_flag[threadIdx.x] = last ? 1 : 0;
   }
@@ -1241,7 +1244,6 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   float* xs = racc;  // [HPW][128] scratch of the inverse rotation (the partials above are written)
   for (int ui = 0; ui < nu; ++ui) {
     if (!last_flag[ui]) continue;  // uniform
-    __threadfence();
     const int u = u0 + ui;
     const int ub = u / per_b, ur = u - ub * per_b, ukvh = ur / a.ngroups, uhg = ur - ukvh * a.ngroups;
     const int ugc = min(HPW, a.g - uhg * HPW);
