@@ -138,7 +138,7 @@ def setup(torch, tq, steps_total, dev):
     ctx = torch.full((B,), T0, dtype=torch.int32, device=dev)
     slot_new = torch.empty(B, dtype=torch.int64, device=dev)
     ws_bytes = layers[0].workspace_bytes(B, HQ, mb, SPLITS)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)  # zero before first use
     return dict(layers=layers, bt=bt, bt_np=bt_np, mb=mb, nb=nb, q=q, knew=knew, vnew=vnew, out=out, ctx=ctx,
                 slot_new=slot_new, ws=ws, append_ms=append_ms, append_vectors=n_vec)
 

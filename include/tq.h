@@ -211,7 +211,9 @@ tq_status tq_quantize_rotated(const tq_cache_desc* desc, int which, const float*
 int tq_auto_splits(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks_per_seq);
 
 /* Workspace bytes tq_decode_attention needs for these sizes (num_splits = 0:
- * the automatic choice above).  0 on error. */
+ * the automatic choice above).  0 on error.  The first 64 KiB of every
+ * workspace (more only for shapes with over 16384 (sequence, query head)
+ * rows) hold per-(sequence, KV head) chunk counters at a fixed place. */
 size_t tq_workspace_bytes(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks_per_seq,
                           int num_splits);
 
@@ -220,9 +222,13 @@ size_t tq_workspace_bytes(const tq_cache_desc* desc, int batch, int num_q_heads,
  * block_table: device int32 [batch][max_blocks_per_seq]; context_lens: device
  * int32 [batch] (0 gives a zero output row); out: device
  * [batch][num_q_heads][head_dim] (out_dtype); workspace: device scratch of at
- * least tq_workspace_bytes(...) bytes, 256-byte aligned, contents need not be
- * initialised.  num_q_heads must be a multiple of num_kv_heads with at most
- * TQ_MAX_GROUP query heads per KV head.  num_splits: 0 = automatic, else the
+ * least tq_workspace_bytes(...) bytes, 256-byte aligned, all zero before the
+ * first call that uses it (e.g. cudaMemsetAsync once after allocating it).
+ * Every call leaves the counter region at zero again, so one workspace serves
+ * any sequence of calls, shapes and layers without clearing; memory that held
+ * anything else in between must be zero-filled again.  num_q_heads must be a
+ * multiple of num_kv_heads with at most TQ_MAX_GROUP query heads per KV head.
+ * num_splits: 0 = automatic, else the
  * number of contiguous context ranges each (sequence, KV head) is split into;
  * results agree for every split count up to fp32 rounding. */
 tq_status tq_decode_attention(const tq_cache_desc* desc, const void* q, int q_dtype, int batch,

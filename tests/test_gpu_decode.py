@@ -237,3 +237,29 @@ def test_late_max_jump_after_large_weight(cuda, tqlib):
     assert f["v_gamma"][40] > 4.0 * f["v_gamma"][90]
     ref = oa.decode_packed(q, kp, vp, ol, nb, Hkv, bt, ctx, sm)
     assert_close(out.cpu().numpy(), ref, TOL_F32, ctx)
+
+
+def test_workspace_reused_across_shapes(cuda, tqlib):
+    """One zero-filled workspace serves calls of different shapes and layers in
+    turn: the per-unit chunk counters return to zero after every call."""
+    tq = tqlib
+    sm = 1.0 / math.sqrt(D)
+    ws = cuda.zeros(8 << 20, dtype=cuda.uint8, device="cuda")
+    cases = [dict(B=2, Hq=8, Hkv=2, ctx=[300, 77], seed=31), dict(B=3, Hq=32, Hkv=4, ctx=[900, 5, 400], seed=32),
+             dict(B=2, Hq=8, Hkv=2, ctx=[300, 77], seed=31)]
+    for cs in cases:
+        out_ref, ref, layer = run_case(cuda, tq, B=cs["B"], Hq=cs["Hq"], Hkv=cs["Hkv"], ctx=cs["ctx"], seed=cs["seed"])
+        ctx = np.asarray(cs["ctx"], np.int32)
+        mb = int(math.ceil(ctx.max() / 16))
+        bt, _ = workloads.shuffled_block_table(cs["seed"] + 1, cs["B"], mb, num_blocks=cs["B"] * mb + 3)
+        q = to_dev(cuda, workloads.queries(cs["seed"] + 3, cs["B"], cs["Hq"], D, dtype="bf16"), bf16=True)
+        need = layer.workspace_bytes(cs["B"], cs["Hq"], mb)
+        assert need <= ws.numel()
+        for _ in range(2):
+            out = layer.decode(q, cuda.from_numpy(bt).cuda(), cuda.from_numpy(ctx).cuda(), sm_scale=sm,
+                               out_dtype=cuda.float32, workspace=ws)
+            cuda.cuda.synchronize()
+            assert tq.get_device_status() == 0
+            assert_close(out.cpu().numpy(), ref, TOL_BF16, ctx)
+        # the counter region is zero again after the calls
+        assert int(ws[:65536].count_nonzero().item()) == 0

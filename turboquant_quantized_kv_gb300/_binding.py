@@ -262,7 +262,7 @@ class Layer:
         if out is None:
             out = torch.empty(q.shape, dtype=q.dtype if out_dtype is None else out_dtype, device=q.device)
         if workspace is None:
-            workspace = torch.empty(self.workspace_bytes(bsz, hq, max_blocks, num_splits), dtype=torch.uint8,
+            workspace = torch.zeros(self.workspace_bytes(bsz, hq, max_blocks, num_splits), dtype=torch.uint8,
                                     device=q.device)
         _check(lib().tq_decode_attention(ctypes.byref(self.desc), _ptr(q, "q"), _dtype_code(q), bsz, hq,
                                          _ptr(block_table, "block_table"), max_blocks,

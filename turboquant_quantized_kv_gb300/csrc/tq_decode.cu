@@ -233,6 +233,7 @@ struct DecodeArgs {
   int q_bf16;
   int q_in_kernel;    // 0: read qrot; 1: rotate q here (Hadamard); 2: scale q here (no rotation)
   float q_scale;      // sm_scale * log2 e
+  int pdl;            // host side: launched as a programmatic dependent of the prep pass
   int Hq, g, ngroups;
   int splits;  // chunks per unit
   int chunks;  // units * splits
@@ -1231,7 +1232,7 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   // lets its threads read the other CTAs' partials.
   __syncthreads();
   if (threadIdx.x < nu) {
-    grid_dep_wait();  // the counters are zeroed by the preceding pass
+    grid_dep_wait();  // the counters may be zeroed by a preceding pass
     const int u = u0 + threadIdx.x;
     const int covered = min((u + 1) * a.splits, c1) - max(u * a.splits, c0);
     int old;
@@ -1444,7 +1445,7 @@ static cudaError_t run_decode_nt(DecodeArgs a, cudaStream_t st) {
   a.smem_bytes = optin;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   if (e != cudaSuccess) return e;
-  // programmatic dependent of the rotation / counter pass launched just before
+  // programmatic dependent of the rotation / counter pass when one was launched just before
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((a.chunks + NW - 1) / NW));
   cfg.blockDim = dim3(NW * 32);
@@ -1454,7 +1455,7 @@ static cudaError_t run_decode_nt(DecodeArgs a, cudaStream_t st) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.pdl ? 1 : 0;  // without the prep pass the previous kernel may be the append
   e = cudaLaunchKernelEx(&cfg, kern, a);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -1490,7 +1491,14 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   // dense rotations and S q' (QJL) take a separate mat-vec pass first
   const bool q_aligned = (reinterpret_cast<uintptr_t>(c.q) & 15) == 0;
   const int q_in_kernel = (!qjl && kind != ROTQ_DENSE && q_aligned) ? (kind == ROTQ_HADAMARD ? 1 : 2) : 0;
-  {
+  // The chunk counters stay zero between calls (the decode kernel resets each unit's
+  // counter when it completes the unit), so the separate pass is needed only for a
+  // q mat-vec or for counters that do not fit the fixed region at the start of the
+  // workspace (its contents must be zero before the first call).
+  const int g = c.num_q_heads / d.num_kv_heads;
+  const int64_t units = (int64_t)c.batch * d.num_kv_heads * ((g + (g <= 4 ? 3 : 7)) / (g <= 4 ? 4 : 8));
+  const bool prep = !q_in_kernel || (size_t)units * sizeof(int32_t) > kCounterRegionBytes;
+  if (prep) {
     const int64_t rot_rows = q_in_kernel ? 0 : rows;
     const int n_counters = (int)rows;  // >= batch * kv heads * head groups
     unsigned rgrid = (unsigned)((rot_rows + 3) / 4);
@@ -1523,6 +1531,7 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   a.q_bf16 = c.q_dtype == TQ_BF16 ? 1 : 0;
   a.q_in_kernel = q_in_kernel;
   a.q_scale = scale;
+  a.pdl = prep ? 1 : 0;
   a.Hq = c.num_q_heads;
   a.g = c.num_q_heads / d.num_kv_heads;
   a.ngroups = (a.g + (a.g <= 4 ? 3 : 7)) / (a.g <= 4 ? 4 : 8);  // head groups of 4 or 8 per warp

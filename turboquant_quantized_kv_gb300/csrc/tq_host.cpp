@@ -372,12 +372,15 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 DecodeWorkspace decode_workspace(int batch, int num_q_heads, int splits, int head_dim, bool qjl) {
   DecodeWorkspace w;
   const size_t bh = (size_t)batch * num_q_heads;
-  w.qrot_off = 0;
+  // the chunk counters come first, in a region of fixed size for every shape that fits
+  // it, so a workspace reused across shapes keeps its zeroed counters where they were
+  w.cnt_off = 0;
+  const size_t cnt_bytes = align256(bh * sizeof(int32_t));
+  w.qrot_off = cnt_bytes > kCounterRegionBytes ? cnt_bytes : kCounterRegionBytes;
   size_t qbytes = bh * head_dim * sizeof(float) * (qjl ? 2 : 1);
   w.part_off = align256(w.qrot_off + qbytes);
   w.ml_off = align256(w.part_off + bh * splits * head_dim * sizeof(float));
-  w.cnt_off = align256(w.ml_off + bh * splits * 2 * sizeof(float));
-  w.total = align256(w.cnt_off + bh * sizeof(int32_t));
+  w.total = align256(w.ml_off + bh * splits * 2 * sizeof(float));
   return w;
 }
 

@@ -34,12 +34,17 @@ int decode_warps(const tq_cache_desc& d, int g);
 
 // Workspace layout of decode (all offsets 256-byte aligned).
 struct DecodeWorkspace {
+  size_t cnt_off;    // int32 [units] finished-chunk counters, at offset 0 (see kCounterRegionBytes)
   size_t qrot_off;   // fp32 [batch][Hq][d]  rotated, scaled queries (+ QJL projections)
   size_t part_off;   // fp32 [batch][Hq][splits][d] partial accumulators
   size_t ml_off;     // fp32 [batch][Hq][splits][2] (running max, denominator)
-  size_t cnt_off;    // int32 [batch][Hq] finished-chunk counters (zeroed by the query prologue)
   size_t total;
 };
+
+// The counters occupy the first kCounterRegionBytes of every workspace (more only
+// for shapes with more than 16384 (sequence, query head) rows).  Decode calls leave
+// them at zero, so a workspace zero-filled once can serve any later call.
+constexpr size_t kCounterRegionBytes = 65536;
 DecodeWorkspace decode_workspace(int batch, int num_q_heads, int splits, int head_dim, bool qjl);
 
 // One validated decode call, as the launcher sees it.
