@@ -106,7 +106,7 @@ extern "C" {
 #define TQ_FORMAT_VERSION 1u
 #define TQ_BLOCK_SIZE 16
 #define TQ_HEAD_DIM 128
-#define TQ_MAX_GROUP 8 /* query heads per KV head handled by one decode CTA */
+#define TQ_MAX_GROUP 8 /* query heads one decode warp handles; larger GQA groups are split into groups of 8 */
 
 typedef enum {
   TQ_OK = 0,
@@ -227,7 +227,8 @@ size_t tq_workspace_bytes(const tq_cache_desc* desc, int batch, int num_q_heads,
  * Every call leaves the counter region at zero again, so one workspace serves
  * any sequence of calls, shapes and layers without clearing; memory that held
  * anything else in between must be zero-filled again.  num_q_heads must be a
- * multiple of num_kv_heads with at most TQ_MAX_GROUP query heads per KV head.
+ * multiple of num_kv_heads (any group size: a group above TQ_MAX_GROUP heads
+ * is split into warps of 8 heads that each stream the KV head's pages).
  * num_splits: 0 = automatic, else the
  * number of contiguous context ranges each (sequence, KV head) is split into;
  * results agree for every split count up to fp32 rounding. */
