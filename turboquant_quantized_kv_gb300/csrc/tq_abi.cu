@@ -71,10 +71,14 @@ tq_status tq_quantize_append(const tq_cache_desc* desc, const void* k, const voi
   if (!k && !v) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: both k and v are null");
   if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
     return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: k/v must be 16-byte aligned");
+  const tq_layer_format& f = desc->fmt;
+  if (f.kv_format == TQ_KV_PACKED &&
+      ((k && !cell_table_ok(desc->boundaries_k, (1 << f.bits_k) - 1)) ||
+       (v && !cell_table_ok(desc->boundaries_v, (1 << f.bits_v) - 1))))
+    return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_append: codebook boundaries closer than 1/63 apart");
   DeviceInfo di;
   if ((s = device_info(&di)) != TQ_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const tq_layer_format& f = desc->fmt;
   const bool same_tables = std::memcmp(desc->centroids_k, desc->centroids_v, sizeof(desc->centroids_k)) == 0 &&
                            std::memcmp(desc->boundaries_k, desc->boundaries_v, sizeof(desc->boundaries_k)) == 0;
   if (k && v && f.kv_format == TQ_KV_PACKED && f.bits_k == f.bits_v && !f.qjl_k && same_tables)  // one launch

@@ -64,6 +64,10 @@ struct DecodeCall {
   unsigned* status;
 };
 
+// True if the append quantizer's cell table can hold these (ascending) boundaries:
+// each boundary in a cell of its own (cells are 1/63 wide on [-1, 1]).
+bool cell_table_ok(const float* boundaries, int nb);
+
 // Kernel launchers (CUDA translation units).  All enqueue on `st` and return
 // the launch error, if any.
 // x_v != nullptr (packed layers, which = 0): the values are quantized in the same

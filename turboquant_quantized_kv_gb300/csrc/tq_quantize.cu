@@ -13,6 +13,9 @@
 // registers and 2 through quad shuffles.  A CTA of 256 threads handles tiles
 // of 64 vectors in a grid-stride loop.  Dense rotations and the QJL projection
 // are 128x128 mat-vecs against a padded copy of the matrix in shared memory.
+#include <cmath>
+#include <cstring>
+
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
@@ -48,6 +51,40 @@ constexpr int kPadQ = 36;            // padded quarter-row of a staged matrix (f
 constexpr size_t kTableBytes = 4096;
 constexpr size_t kTileBytes = (size_t)kTile * kTileStride * 4;
 constexpr size_t kMatBytes = (size_t)kD * 4 * kPadQ * 4;
+
+// Cell table of the quantizer for rotated coordinates (|y| <= 1 up to rounding).
+// cell(y) = round(63 y + 64) from the low bits of fmaf(y, 63, 1.5 * 2^23 + 64): a
+// monotone map of [-1, 1] onto cells 1..127, each narrower (1/63) than the
+// smallest gap between boundaries of the supported codebooks, so a cell holds at
+// most one boundary P.  For y in cell i, idx = #{beta <= y} = base_i + [y >= P_i]
+// exactly (the boundaries' own cells are computed with the same fmaf).  Entry =
+// {P, c[base]^2, c[base + 1]^2, base}; 8 interleaved copies (one per lane of a
+// quarter warp) so the lookups of a warp never conflict.
+constexpr int kQCells = 128;
+constexpr float kQScale = 63.0f;
+constexpr float kQMagic = 12582912.0f + 64.0f;  // 1.5 * 2^23 + 64
+constexpr size_t kLutQBytes = (size_t)kQCells * 8 * 16;
+
+__host__ __device__ __forceinline__ uint32_t qcell(float y) {
+#ifdef __CUDA_ARCH__
+  return __float_as_uint(fmaf(y, kQScale, kQMagic)) & (kQCells - 1);
+#else
+  const float t = std::fmaf(y, kQScale, kQMagic);
+  uint32_t u;
+  std::memcpy(&u, &t, 4);
+  return u & (kQCells - 1);
+#endif
+}
+
+// Host: every boundary of the table falls in its own cell, none in the end cells.
+bool cell_table_ok(const float* boundaries, int nb) {
+  for (int k = 0; k < nb; ++k) {
+    const uint32_t ck = qcell(boundaries[k]);
+    if (ck == 0u || ck == (uint32_t)(kQCells - 1)) return false;
+    if (k > 0 && ck == qcell(boundaries[k - 1])) return false;
+  }
+  return true;
+}
 
 // dst[r][q][k] = transpose ? src[32q + k][r] : src[r][32q + k]   (src row-major d x d)
 __device__ void stage_matrix(const float* __restrict__ src, float* dst, bool transpose) {
@@ -93,9 +130,12 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
   float* mag2 = reinterpret_cast<float*>(smem_raw);              // [H][32]
   float* ctab = mag2 + 8 * 32;                                   // [2H][32]
   uint32_t* signw = reinterpret_cast<uint32_t*>(ctab + 16 * 32);  // [4]
-  float* tile = reinterpret_cast<float*>(smem_raw + kTableBytes);
-  float* matP = reinterpret_cast<float*>(smem_raw + kTableBytes + kTileBytes);
-  float* matS = reinterpret_cast<float*>(smem_raw + kTableBytes + kTileBytes + (MODE == MODE_DENSE ? kMatBytes : 0));
+  constexpr bool LUTQ = MODE != MODE_GIVEN_Y;  // |y| <= 1 only for coordinates this kernel rotates
+  float4* qtab = reinterpret_cast<float4*>(smem_raw + kTableBytes);  // [kQCells][8]
+  unsigned char* const dyn = smem_raw + kTableBytes + (LUTQ ? kLutQBytes : 0);
+  float* tile = reinterpret_cast<float*>(dyn);
+  float* matP = reinterpret_cast<float*>(dyn + kTileBytes);
+  float* matS = reinterpret_cast<float*>(dyn + kTileBytes + (MODE == MODE_DENSE ? kMatBytes : 0));
 
   const int tid = threadIdx.x, lane = tid & 31, q = tid & 3, vl = tid >> 2;
   for (int i = tid; i < H * 32; i += kThreads) {
@@ -113,7 +153,26 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
   }
   if (MODE == MODE_DENSE) stage_matrix(a.rot, matP, /*transpose=*/true);  // out = Pi x
   if (QJL) stage_matrix(a.qjl, matS, /*transpose=*/true);                 // out = S r
+  if (LUTQ) {  // the host checked that no cell holds two boundaries (cell_table_ok)
+    if (tid < kQCells) {
+      constexpr int NB = (1 << BITS) - 1;  // boundaries
+      uint32_t base = 0u;
+      float P = INFINITY;
+      for (int k = 0; k < NB; ++k) {
+        const float bk = a.cb.b[k];
+        const uint32_t ck = qcell(bk);
+        if (ck < (uint32_t)tid) ++base;
+        if (ck == (uint32_t)tid) P = bk;
+      }
+      const float c0 = a.cb.c[min(base, (uint32_t)NB)];
+      const float c1 = a.cb.c[min(base + 1u, (uint32_t)NB)];
+      const float4 e = make_float4(P, c0 * c0, c1 * c1, __uint_as_float(base));
+#pragma unroll
+      for (int r = 0; r < 8; ++r) qtab[tid * 8 + r] = e;
+    }
+  }
   __syncthreads();
+  const float4* qrow = qtab + (lane & 7);
   const uint32_t sw = (MODE == MODE_HADAMARD) ? signw[q] : 0u;
   const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
 
@@ -153,12 +212,23 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
 
     uint32_t code[32];
     float c2 = 0.0f;
+    if constexpr (LUTQ) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float y = (MODE == MODE_GIVEN_Y) ? x[i] : x[i] * inv_n;
-      int mag;
-      code[i] = quantize_coord<BITS>(y, a.cb, &mag);
-      c2 += mag2[mag * 32 + lane];
+      for (int i = 0; i < 32; ++i) {
+        const float y = x[i] * inv_n;
+        const float4 e = qrow[qcell(y) * 8];
+        const bool up = y >= e.x;
+        code[i] = __float_as_uint(e.w) + (up ? 1u : 0u);
+        c2 += up ? e.z : e.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float y = (MODE == MODE_GIVEN_Y) ? x[i] : x[i] * inv_n;
+        int mag;
+        code[i] = quantize_coord<BITS>(y, a.cb, &mag);
+        c2 += mag2[mag * 32 + lane];
+      }
     }
     c2 = quad_sum(c2);
     float gamma;
@@ -355,6 +425,7 @@ template <int BITS, typename TIn, int MODE, bool QJL>
 static cudaError_t run_quantize(const QuantArgs& a, int ny, int num_sms, cudaStream_t st) {
   auto kern = k_quantize<BITS, TIn, MODE, QJL>;
   size_t smem = kTableBytes;
+  if (MODE != MODE_GIVEN_Y) smem += kLutQBytes;
   if (MODE == MODE_DENSE || QJL) smem += kTileBytes;
   if (MODE == MODE_DENSE) smem += kMatBytes;
   if (QJL) smem += kMatBytes;
