@@ -100,6 +100,42 @@ __device__ __forceinline__ void fwht128_quad(float (&x)[32], int q) {
   }
 }
 
+// The same transform with packed fp32 pairs (sm_100+ f32x2 arithmetic): bit 0 of
+// the coordinate inside each pair, bits 1..4 as pair butterflies, bits 5 and 6
+// across the quad as x <- partner + s x with s = -1 on the upper lane.
+__device__ __forceinline__ void fwht128_quad_f2(float (&x)[32], int q) {
+  float2 v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = make_float2(x[2 * j] + x[2 * j + 1], x[2 * j] - x[2 * j + 1]);
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if ((j & h) == 0) {
+        const float2 a = v[j], b = v[j + h];
+        v[j] = __fadd2_rn(a, b);
+        v[j + h] = __ffma2_rn(b, m1, a);
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m <= 2; m <<= 1) {
+    const float sgn = (q & m) ? -1.0f : 1.0f;
+    const float2 s2 = make_float2(sgn, sgn);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[j].x, m), __shfl_xor_sync(0xffffffffu, v[j].y, m));
+      v[j] = __ffma2_rn(v[j], s2, o);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    x[2 * j] = v[j].x;
+    x[2 * j + 1] = v[j].y;
+  }
+}
+
 __device__ __forceinline__ float quad_sum(float v) {
   v += __shfl_xor_sync(0xffffffffu, v, 1);
   v += __shfl_xor_sync(0xffffffffu, v, 2);
@@ -154,6 +190,16 @@ __device__ __forceinline__ uint32_t quantize_coord(float y, const Codebook& cb, 
 // Packs 32 codes (code k at bits [BITS k, BITS k + BITS)) into BITS words.
 template <int BITS>
 __device__ __forceinline__ void pack32(const uint32_t (&code)[32], uint32_t (&w)[BITS]) {
+  if constexpr (BITS == 4) {  // code pairs to bytes, bytes to words
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t by[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) by[j] = code[8 * k + 2 * j] + (code[8 * k + 2 * j + 1] << 4);
+      w[k] = __byte_perm(__byte_perm(by[0], by[1], 0x0040u), __byte_perm(by[2], by[3], 0x0040u), 0x5410u);
+    }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < BITS; ++i) w[i] = 0u;
 #pragma unroll

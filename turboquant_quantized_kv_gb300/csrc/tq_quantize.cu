@@ -189,16 +189,21 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
       n = __ldg(a.norms + vec);
     } else {
       load32<TIn>(reinterpret_cast<const TIn*>(x_in) + vec * kD + 32 * q, x);
-      float ss = 0.0f;
+      float2 ss2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) ss = fmaf(x[i], x[i], ss);
-      n = sqrtf(quad_sum(ss));
+      for (int i = 0; i < 16; ++i) {
+        const float2 xi = make_float2(x[2 * i], x[2 * i + 1]);
+        ss2 = __ffma2_rn(xi, xi, ss2);
+      }
+      n = sqrtf(quad_sum(ss2.x + ss2.y));
       if constexpr (MODE == MODE_HADAMARD) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = flip_sign(x[i], sw, i);
-        fwht128_quad(x, q);
+        fwht128_quad_f2(x, q);  // unnormalised: H D x = sqrt(d) Pi x
+        if constexpr (QJL) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] *= inv_sqrt_d;
+          for (int i = 0; i < 32; ++i) x[i] *= inv_sqrt_d;
+        }
       } else {
         __syncthreads();  // previous iteration is done with the tile
 #pragma unroll
@@ -207,20 +212,26 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
         matvec_padded(matP, tile + vl * kTileStride, q, x);
       }
     }
-    // y = (Pi x) / n; MODE_GIVEN_Y already holds y and uses it as is.
-    const float inv_n = (MODE == MODE_GIVEN_Y) ? 1.0f : (n > 0.0f ? 1.0f / n : 0.0f);
+    // y = (Pi x) / n; MODE_GIVEN_Y already holds y and uses it as is.  Without QJL the
+    // Hadamard path keeps H D x unnormalised and folds 1 / sqrt(d) in here.
+    constexpr bool kUnnorm = MODE == MODE_HADAMARD && !QJL;
+    const float inv_n = (MODE == MODE_GIVEN_Y) ? 1.0f : (n > 0.0f ? (kUnnorm ? inv_sqrt_d : 1.0f) / n : 0.0f);
 
     uint32_t code[32];
     float c2 = 0.0f;
     if constexpr (LUTQ) {
+      float2 c2v = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float y = x[i] * inv_n;
-        const float4 e = qrow[qcell(y) * 8];
-        const bool up = y >= e.x;
-        code[i] = __float_as_uint(e.w) + (up ? 1u : 0u);
-        c2 += up ? e.z : e.y;
+      for (int i = 0; i < 32; i += 2) {
+        const float2 y = __fmul2_rn(make_float2(x[i], x[i + 1]), make_float2(inv_n, inv_n));
+        const float4 e0 = qrow[qcell(y.x) * 8];
+        const float4 e1 = qrow[qcell(y.y) * 8];
+        const bool up0 = y.x >= e0.x, up1 = y.y >= e1.x;
+        code[i] = __float_as_uint(e0.w) + (up0 ? 1u : 0u);
+        code[i + 1] = __float_as_uint(e1.w) + (up1 ? 1u : 0u);
+        c2v = __fadd2_rn(c2v, make_float2(up0 ? e0.z : e0.y, up1 ? e1.z : e1.y));
       }
+      c2 = c2v.x + c2v.y;
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
