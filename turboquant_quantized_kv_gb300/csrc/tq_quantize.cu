@@ -53,28 +53,32 @@ constexpr size_t kTileBytes = (size_t)kTile * kTileStride * 4;
 constexpr size_t kMatBytes = (size_t)kD * 4 * kPadQ * 4;
 
 // Cell table of the quantizer for rotated coordinates (|y| <= 1 up to rounding).
-// cell(y) = round(63 y + 64) from the low bits of fmaf(y, 63, 1.5 * 2^23 + 64): a
-// monotone map of [-1, 1] onto cells 1..127, each narrower (1/63) than the
-// smallest gap between boundaries of the supported codebooks, so a cell holds at
-// most one boundary P.  For y in cell i, idx = #{beta <= y} = base_i + [y >= P_i]
-// exactly (the boundaries' own cells are computed with the same fmaf).  Entry =
-// {P, c[base]^2, c[base + 1]^2, base}; 8 interleaved copies (one per lane of a
-// quarter warp) so the lookups of a warp never conflict.
+// t = fmaf(y, 63, 1.5 * 2^16 + 64) has an ulp of 2^-7, so bits 7..13 of t are
+// cell(y) = floor(63 y + 64 + <2^-7 rounding>): a monotone map of [-1, 1] onto
+// cells 1..127, each narrower (1/63) than the smallest gap between boundaries of
+// the supported codebooks, so a cell holds at most one boundary P.  For y in cell
+// i, idx = #{beta <= y} = base_i + [y >= P_i] exactly (the boundaries' own cells
+// come from the same fmaf).  Entry = {P, c[base]^2, c[base + 1]^2, base}; 8
+// interleaved copies (one per lane of a quarter warp) make a 128-byte row per
+// cell, so bits 7..13 of t are the row offset: with the table 16 KB aligned, one
+// bitwise op turns t into the lane's entry address, and lookups never conflict.
 constexpr int kQCells = 128;
 constexpr float kQScale = 63.0f;
-constexpr float kQMagic = 12582912.0f + 64.0f;  // 1.5 * 2^23 + 64
+constexpr float kQMagic = 98304.0f + 64.0f;  // 1.5 * 2^16 + 64
 constexpr size_t kLutQBytes = (size_t)kQCells * 8 * 16;
+constexpr uint32_t kQRowMask = (uint32_t)(kQCells - 1) << 7;
 
-__host__ __device__ __forceinline__ uint32_t qcell(float y) {
+__host__ __device__ __forceinline__ uint32_t qcell_bits(float y) {
 #ifdef __CUDA_ARCH__
-  return __float_as_uint(fmaf(y, kQScale, kQMagic)) & (kQCells - 1);
+  return __float_as_uint(fmaf(y, kQScale, kQMagic));
 #else
   const float t = std::fmaf(y, kQScale, kQMagic);
   uint32_t u;
   std::memcpy(&u, &t, 4);
-  return u & (kQCells - 1);
+  return u;
 #endif
 }
+__host__ __device__ __forceinline__ uint32_t qcell(float y) { return (qcell_bits(y) & kQRowMask) >> 7; }
 
 // Host: every boundary of the table falls in its own cell, none in the end cells.
 bool cell_table_ok(const float* boundaries, int nb) {
@@ -116,6 +120,12 @@ __device__ __forceinline__ void matvec_padded(const float* Mp, const float* vin,
   }
 }
 
+__device__ __forceinline__ float4 lds128f(uint32_t addr) {
+  float4 v;
+  asm("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ float flip_sign(float v, uint32_t word, int bit) {
   return __uint_as_float(__float_as_uint(v) ^ ((word << (31 - bit)) & 0x80000000u));
 }
@@ -131,8 +141,11 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
   float* ctab = mag2 + 8 * 32;                                   // [2H][32]
   uint32_t* signw = reinterpret_cast<uint32_t*>(ctab + 16 * 32);  // [4]
   constexpr bool LUTQ = MODE != MODE_GIVEN_Y;  // |y| <= 1 only for coordinates this kernel rotates
-  float4* qtab = reinterpret_cast<float4*>(smem_raw + kTableBytes);  // [kQCells][8]
-  unsigned char* const dyn = smem_raw + kTableBytes + (LUTQ ? kLutQBytes : 0);
+  // the cell table starts at the first 16 KB aligned shared address past the small tables
+  const uint32_t smem_base = (uint32_t)__cvta_generic_to_shared(smem_raw);
+  const uint32_t qtab_addr = (smem_base + (uint32_t)kTableBytes + 16383u) & ~16383u;
+  float4* qtab = reinterpret_cast<float4*>(smem_raw + (qtab_addr - smem_base));  // [kQCells][8]
+  unsigned char* const dyn = LUTQ ? smem_raw + (qtab_addr - smem_base) + kLutQBytes : smem_raw + kTableBytes;
   float* tile = reinterpret_cast<float*>(dyn);
   float* matP = reinterpret_cast<float*>(dyn + kTileBytes);
   float* matS = reinterpret_cast<float*>(dyn + kTileBytes + (MODE == MODE_DENSE ? kMatBytes : 0));
@@ -172,8 +185,12 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
     }
   }
   __syncthreads();
-  const float4* qrow = qtab + (lane & 7);
+  const uint32_t qrow_addr = qtab_addr | (16u * (uint32_t)(lane & 7));
   const uint32_t sw = (MODE == MODE_HADAMARD) ? signw[q] : 0u;
+  // bf16 input, Hadamard: sign flips of coordinate pairs as masks on the packed bf16 words
+  uint32_t pmask[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) pmask[j] = ((sw >> (2 * j)) & 1u) << 15 | ((sw >> (2 * j + 1)) & 1u) << 31;
   const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
 
   const int64_t n_tiles = (a.n_vec + kTile - 1) / kTile;
@@ -188,7 +205,23 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
       load32<float>(a.y + vec * kD + 32 * q, x);
       n = __ldg(a.norms + vec);
     } else {
-      load32<TIn>(reinterpret_cast<const TIn*>(x_in) + vec * kD + 32 * q, x);
+      constexpr bool kBf16Signs = MODE == MODE_HADAMARD && sizeof(TIn) == 2;
+      if constexpr (kBf16Signs) {  // widen with the sign flips applied to the packed words
+        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const TIn*>(x_in) + vec * kD + 32 * q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = __ldg(src + k);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t f = w[e] ^ pmask[4 * k + e];
+            x[8 * k + 2 * e] = __uint_as_float(f << 16);
+            x[8 * k + 2 * e + 1] = __uint_as_float(f & 0xFFFF0000u);
+          }
+        }
+      } else {
+        load32<TIn>(reinterpret_cast<const TIn*>(x_in) + vec * kD + 32 * q, x);
+      }
       float2 ss2 = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -197,8 +230,10 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
       }
       n = sqrtf(quad_sum(ss2.x + ss2.y));
       if constexpr (MODE == MODE_HADAMARD) {
+        if constexpr (!kBf16Signs) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = flip_sign(x[i], sw, i);
+          for (int i = 0; i < 32; ++i) x[i] = flip_sign(x[i], sw, i);
+        }
         fwht128_quad_f2(x, q);  // unnormalised: H D x = sqrt(d) Pi x
         if constexpr (QJL) {
 #pragma unroll
@@ -224,8 +259,8 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
         const float2 y = __fmul2_rn(make_float2(x[i], x[i + 1]), make_float2(inv_n, inv_n));
-        const float4 e0 = qrow[qcell(y.x) * 8];
-        const float4 e1 = qrow[qcell(y.y) * 8];
+        const float4 e0 = lds128f((qcell_bits(y.x) & kQRowMask) | qrow_addr);
+        const float4 e1 = lds128f((qcell_bits(y.y) & kQRowMask) | qrow_addr);
         const bool up0 = y.x >= e0.x, up1 = y.y >= e1.x;
         code[i] = __float_as_uint(e0.w) + (up0 ? 1u : 0u);
         code[i + 1] = __float_as_uint(e1.w) + (up1 ? 1u : 0u);
@@ -436,7 +471,7 @@ template <int BITS, typename TIn, int MODE, bool QJL>
 static cudaError_t run_quantize(const QuantArgs& a, int ny, int num_sms, cudaStream_t st) {
   auto kern = k_quantize<BITS, TIn, MODE, QJL>;
   size_t smem = kTableBytes;
-  if (MODE != MODE_GIVEN_Y) smem += kLutQBytes;
+  if (MODE != MODE_GIVEN_Y) smem += 16384 + kLutQBytes;  // the cell table is 16 KB aligned
   if (MODE == MODE_DENSE || QJL) smem += kTileBytes;
   if (MODE == MODE_DENSE) smem += kMatBytes;
   if (QJL) smem += kMatBytes;
