@@ -130,8 +130,10 @@ __device__ __forceinline__ float flip_sign(float v, uint32_t word, int bit) {
   return __uint_as_float(__float_as_uint(v) ^ ((word << (31 - bit)) & 0x80000000u));
 }
 
+// Three CTAs per SM for the plain Hadamard path: the append is latency bound, so
+// residency matters more than the few registers the bound takes away.
 template <int BITS, typename TIn, int MODE, bool QJL>
-__global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
+__global__ void __launch_bounds__(kThreads, (MODE == MODE_HADAMARD && !QJL) ? 3 : 1) k_quantize(QuantArgs a) {
   const void* const x_in = blockIdx.y ? a.x_v : a.x;
   uint8_t* const pool = blockIdx.y ? a.pool_v : a.pool;
   extern __shared__ __align__(16) unsigned char smem_raw[];
