@@ -116,6 +116,75 @@ def test_append_zero_vector_and_bad_slot(cuda, tqlib):
     assert np.all(codes == 8) and gamma[0] == 0.0
 
 
+def _bf16_dev(cuda, bits):
+    return cuda.from_numpy(bits.view(np.int16)).cuda().view(cuda.bfloat16)
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_append_bf16_many_tiles_per_warp(cuda, tqlib, bits):
+    """8192 tokens x 8 heads of bf16 K and V in one paired launch (2 x 65536 vectors):
+    every warp of the staged kernel goes round its two-deep ring several times."""
+    tq = tqlib
+    H, n = 8, 8192
+    nb = n // 16 + 3
+    layer = tq.Layer(nb, H, bits_k=bits, bits_v=bits, seed=7, layer=3, fill=0xA5)
+    kb, vb = workloads.lognormal_channel_kv(12, n, H, D)
+    slots, slots_d = make_slots(cuda, n, nb, 13, skip_every=29)
+    layer.append(_bf16_dev(cuda, kb), _bf16_dev(cuda, vb), slots_d)
+    assert tq.get_device_status() == 0
+    pi = orot.hadamard_rotation_seeded(7, 3, D)
+    c32, b32 = ocb.codebook_fp32(D, bits)
+    keep = slots >= 0
+    written = np.zeros(nb * 16, bool)
+    written[slots[keep]] = True
+    for which, xb, pool in ((0, kb, layer.k_cache), (1, vb, layer.v_cache)):
+        host = pool.cpu().numpy()
+        fields = page_fields(layer, which, host)
+        x = oq.bf16_bits_to_f64(xb)
+        for h in range(H):
+            idx, gamma, y = oq.quantize(x[keep, h], pi, c32, b32)
+            codes, g_gpu = slot_fields(fields, slots[keep], h)
+            ok, _ = tie_band_ok(y, codes, idx, b32, 1e-5)
+            assert ok, "code mismatch outside the tie band"
+            same = np.all(codes == idx, axis=-1)
+            assert same.mean() > 0.99
+            assert np.all(np.abs(g_gpu[same] - gamma[same]) <= 1e-6 * np.abs(gamma[same]) + 1e-30)
+        rec = opack_record_view(host, nb, H, bits)
+        assert np.all(rec[~written.reshape(nb, 16)] == 0xA5)
+
+
+def test_append_misaligned_input_rejected(cuda, tqlib):
+    """k/v must be 16-byte aligned (include/tq.h): a bf16 input 2 bytes past a boundary is
+    refused before anything is launched, and the cache is left as it was."""
+    tq = tqlib
+    H, nb, n = 2, 4, 9
+    layer = tq.Layer(nb, H, fill=0x5A)
+    kb, _ = workloads.lognormal_channel_kv(5, n, H, D)
+    big = cuda.from_numpy(np.concatenate([np.zeros(1, np.int16), kb.view(np.int16).reshape(-1)])).cuda()
+    kt = big[1:].view(n, H, D).view(cuda.bfloat16)
+    assert kt.data_ptr() % 16 == 2
+    slots = cuda.arange(n, dtype=cuda.int64).cuda()
+    before = tq.launch_count()
+    with pytest.raises(tq.TQError, match="16-byte aligned"):
+        layer.append(kt, None, slots)
+    assert tq.launch_count() == before
+    assert np.all(layer.k_cache.cpu().numpy() == 0x5A)
+
+
+def test_append_bf16_zero_vector_and_bad_slot(cuda, tqlib):
+    tq = tqlib
+    layer = tq.Layer(4, 1)
+    x = np.zeros((2, 1, D), np.float32)
+    x[1, 0, 3] = 2.0
+    slots = cuda.tensor([5, 4 * 16 + 3], dtype=cuda.int64).cuda()  # second slot is out of range
+    layer.append(_bf16_dev(cuda, workloads.bf16_bits(x)), None, slots)
+    assert tq.get_device_status() & tq.TQ_DEV_BAD_SLOT
+    assert tq.get_device_status() == 0
+    fields = page_fields(layer, 0, layer.k_cache.cpu().numpy())
+    codes, gamma = slot_fields(fields, [5], 0)
+    assert np.all(codes == 8) and gamma[0] == 0.0
+
+
 def test_dense_rotation_append_matches_oracle(cuda, tqlib):
     tq = tqlib
     H, nb, n = 2, 12, 150

@@ -198,15 +198,15 @@ __device__ __forceinline__ void pack32(const uint32_t (&code)[32], uint32_t (&w)
       for (int j = 0; j < 4; ++j) by[j] = code[8 * k + 2 * j] + (code[8 * k + 2 * j + 1] << 4);
       w[k] = __byte_perm(__byte_perm(by[0], by[1], 0x0040u), __byte_perm(by[2], by[3], 0x0040u), 0x5410u);
     }
-    return;
-  }
+  } else {
 #pragma unroll
-  for (int i = 0; i < BITS; ++i) w[i] = 0u;
+    for (int i = 0; i < BITS; ++i) w[i] = 0u;
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    const int bit = BITS * k;
-    w[bit >> 5] |= code[k] << (bit & 31);
-    if ((bit & 31) + BITS > 32) w[(bit >> 5) + 1] |= code[k] >> (32 - (bit & 31));
+    for (int k = 0; k < 32; ++k) {
+      const int bit = BITS * k;
+      w[bit >> 5] |= code[k] << (bit & 31);
+      if ((bit & 31) + BITS > 32) w[(bit >> 5) + 1] |= code[k] >> (32 - (bit & 31));
+    }
   }
 }
 

@@ -16,6 +16,7 @@
 #include <cmath>
 #include <cstring>
 
+#include "tq_async.cuh"
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
@@ -331,6 +332,261 @@ __global__ void __launch_bounds__(kThreads, (MODE == MODE_HADAMARD && !QJL) ? 3 
   }
 }
 
+// ------------------------------------------------- bf16 Hadamard append, staged
+//
+// The same quantizer for bf16 inputs on the Hadamard path without QJL, laid out
+// so that one lane owns one whole vector: all seven butterfly stages of the FWHT
+// run in registers (no shuffles), on float pairs v[j] = (x_j, x_{j+64}) so that
+// six of them are packed fp32-pair operations.  Each warp streams tiles of 32
+// vectors through its own two-deep shared-memory ring with 2-D tensor copies
+// (two boxes of [32 vectors][64 coordinates], 128-byte swizzle: lane l reads
+// 16-byte chunk c of its row at chunk c ^ (l & 7), so no read conflicts), which
+// keeps the next tile's loads in flight while the current one is computed.
+// The cell entries shrink to 8 bytes {P, base} (one 64-bit read per
+// coordinate); the norm-correction sum sum_j c[idx_j]^2 is read per pair of
+// codes from a table of c[lo]^2 + c[hi]^2 indexed by the packed pair.
+constexpr int kTW = 8;                        // warps per CTA
+constexpr int kTStages = 2;                   // ring depth per warp
+constexpr uint32_t kTBox = 32 * 128;          // one box: 32 vectors x 64 bf16 coordinates
+constexpr uint32_t kTStage = 2 * kTBox;       // 32 whole vectors
+constexpr uint32_t kTCellBytes = 128 * 128;   // [cell][16 replicas] {P, base}
+constexpr uint32_t kTPairBytes = 256 * 128;   // [pair][32 replicas] c[lo]^2 + c[hi]^2
+constexpr uint32_t kTMiscBytes = 1024;        // sign masks (256 B) and mbarriers
+constexpr size_t kTSmem = 16384 + kTCellBytes + kTPairBytes + kTMiscBytes + (size_t)kTW * kTStages * kTStage;
+
+struct QuantTmaArgs {
+  CUtensorMap tm[2];  // [n_vec][128] bf16 keys / values: box [32][64], 128-byte swizzle
+  uint8_t* pool[2];
+  const int64_t* slots;
+  int64_t tiles;      // 32-vector tiles per tensor
+  uint32_t n_vec;     // vectors per tensor (n_tok * H)
+  int ny;             // tensors in this launch (1, or 2 for keys and values)
+  int H;
+  int page_bytes;
+  int64_t max_slot;
+  const float* rot;   // signs[128]
+  Codebook cb;
+  int norm_mode;
+  unsigned* status;
+};
+
+__device__ __forceinline__ uint4 lds128u(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float2 lds64f(uint32_t addr) {
+  float2 v;
+  asm("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float lds32f(uint32_t addr) {
+  float v;
+  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// Codes of the coordinate pair held in x (already H D x, unnormalised), scaled by s.
+__device__ __forceinline__ void quant_pair(float2 x, float2 s, uint32_t qrow, uint32_t& c0, uint32_t& c1) {
+  const float2 y = __fmul2_rn(x, s);
+  const float2 t = __ffma2_rn(y, make_float2(kQScale, kQScale), make_float2(kQMagic, kQMagic));
+  const float2 e0 = lds64f((__float_as_uint(t.x) & kQRowMask) | qrow);
+  const float2 e1 = lds64f((__float_as_uint(t.y) & kQRowMask) | qrow);
+  c0 = __float_as_uint(e0.y) + (y.x >= e0.x ? 1u : 0u);
+  c1 = __float_as_uint(e1.y) + (y.y >= e1.x ? 1u : 0u);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_constant__ QuantTmaArgs a) {
+  constexpr int R = 16 * BITS;             // record bytes
+  constexpr int NC = 1 << BITS;            // centroids
+  constexpr int NB = NC - 1;               // boundaries
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  const uint32_t cell_addr = (sbase + 16383u) & ~16383u;  // 16 KB aligned: address = (t & mask) | row
+  const uint32_t pair_addr = cell_addr + kTCellBytes;
+  const uint32_t misc_addr = pair_addr + kTPairBytes;
+  const uint32_t ring_addr = misc_addr + kTMiscBytes;     // 1 KB aligned (swizzled boxes)
+  auto gen = [&](uint32_t addr) { return smem_raw + (addr - sbase); };
+
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(gen(misc_addr + 256)) + w * kTStages;
+  const int64_t total = a.tiles * a.ny;
+  const int64_t gw = (int64_t)blockIdx.x * kTW + w, G = (int64_t)gridDim.x * kTW;
+  const int64_t n_my = gw < total ? (total - gw + G - 1) / G : 0;
+  const uint32_t ring = ring_addr + (uint32_t)w * kTStages * kTStage;
+
+  // lane 0: 32 vectors of tile `it` of this warp into stage s (both boxes on one barrier)
+  auto issue = [&](int64_t it, int s) {
+    const int64_t tile = gw + it * G;
+    const int kv = tile >= a.tiles ? 1 : 0;
+    const int row = (int)((tile - kv * a.tiles) * 32);
+    mbar_arrive_expect_tx(bar + s, kTStage);
+    tensor_copy_2d(ring + (uint32_t)s * kTStage, &a.tm[kv], 0, row, bar + s);
+    tensor_copy_2d(ring + (uint32_t)s * kTStage + kTBox, &a.tm[kv], 64, row, bar + s);
+  };
+  if (lane == 0) {
+    for (int s = 0; s < kTStages; ++s) mbar_init(bar + s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int s = 0; s < kTStages && s < n_my; ++s) issue(s, s);
+  }
+
+  // tables, built while the first copies are in flight
+  if (tid < 128) {  // cell table (the host checked that no cell holds two boundaries)
+    uint32_t base = 0u;
+    float P = INFINITY;
+    for (int k = 0; k < NB; ++k) {
+      const float bk = a.cb.b[k];
+      const uint32_t ck = qcell(bk);
+      if (ck < (uint32_t)tid) ++base;
+      if (ck == (uint32_t)tid) P = bk;
+    }
+    float2* row = reinterpret_cast<float2*>(gen(cell_addr + (uint32_t)tid * 128u));
+#pragma unroll
+    for (int r = 0; r < 16; ++r) row[r] = make_float2(P, __uint_as_float(base));
+  }
+  if (tid < NC * NC) {  // pair table: entry lo + NC * hi
+    const float lo = a.cb.c[tid & (NC - 1)], hi = a.cb.c[tid / NC];
+    const float v = lo * lo + hi * hi;
+    float4* row = reinterpret_cast<float4*>(gen(pair_addr + (uint32_t)tid * 128u));
+#pragma unroll
+    for (int r = 0; r < 8; ++r) row[r] = make_float4(v, v, v, v);
+  }
+  if (tid < 64) {  // sign flips of coordinates 2k, 2k+1 as a mask on their packed bf16 word
+    const uint32_t m = (__ldg(a.rot + 2 * tid) < 0.0f ? 0x8000u : 0u) | (__ldg(a.rot + 2 * tid + 1) < 0.0f ? 0x80000000u : 0u);
+    *reinterpret_cast<uint32_t*>(gen(misc_addr + 4u * (uint32_t)tid)) = m;
+  }
+  __syncthreads();
+
+  const uint32_t rowsw = ring + (uint32_t)lane * 128u + ((uint32_t)(lane & 7) << 4);  // row, swizzle bits
+  const uint32_t qrow = cell_addr | ((uint32_t)(lane & 15) << 3);
+  const uint32_t prow = pair_addr + ((uint32_t)lane << 2);
+  const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+
+  bool aborted = false;
+  int64_t it = 0;
+  for (; it < n_my; ++it) {
+    const int s = (int)(it % kTStages);
+    const uint32_t ph = (uint32_t)(it / kTStages) & 1u;
+    const int64_t tile = gw + it * G;
+    const int kv = tile >= a.tiles ? 1 : 0;
+    const uint32_t vec = (uint32_t)((tile - kv * a.tiles) * 32) + (uint32_t)lane;
+    const bool valid = vec < a.n_vec;
+    const uint32_t tok = valid ? vec / (uint32_t)a.H : 0u;
+    const int head = (int)(vec - tok * (uint32_t)a.H);
+    const int64_t slot = valid ? __ldg(a.slots + tok) : -1;
+
+    if (!mbar_wait(bar + s, ph)) {
+      if (lane == 0) flag_status(a.status, TQ_DEV_WAIT_TIMEOUT);
+      aborted = true;
+      break;
+    }
+    // widen with the sign flips applied: v[j] = (D x)_j, (D x)_{j+64}
+    float2 v[64];
+    const uint32_t sb = rowsw + (uint32_t)s * kTStage;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 d0 = lds128u(sb ^ ((uint32_t)c << 4));
+      const uint4 d1 = lds128u((sb + kTBox) ^ ((uint32_t)c << 4));
+      const uint4 p0 = lds128u(misc_addr + 16u * (uint32_t)c);
+      const uint4 p1 = lds128u(misc_addr + 128u + 16u * (uint32_t)c);
+      const uint32_t w0[4] = {d0.x ^ p0.x, d0.y ^ p0.y, d0.z ^ p0.z, d0.w ^ p0.w};
+      const uint32_t w1[4] = {d1.x ^ p1.x, d1.y ^ p1.y, d1.z ^ p1.z, d1.w ^ p1.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[8 * c + 2 * e] = make_float2(__uint_as_float(w0[e] << 16), __uint_as_float(w1[e] << 16));
+        v[8 * c + 2 * e + 1] = make_float2(__uint_as_float(w0[e] & 0xFFFF0000u), __uint_as_float(w1[e] & 0xFFFF0000u));
+      }
+    }
+    __syncwarp();  // every lane has its tile in registers: the stage may be refilled
+    if (lane == 0 && it + kTStages < n_my) {
+      fence_proxy_async();
+      issue(it + kTStages, s);
+    }
+
+    float2 ss2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < 64; ++j) ss2 = __ffma2_rn(v[j], v[j], ss2);
+    const float n = sqrtf(ss2.x + ss2.y);
+
+    // H D x, unnormalised: six stages over the bits of j, then the bit inside each pair
+#pragma unroll
+    for (int h = 1; h < 64; h <<= 1) {
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        if ((j & h) == 0) {
+          const float2 p = v[j], q = v[j + h];
+          v[j] = __fadd2_rn(p, q);
+          v[j + h] = __ffma2_rn(q, m1, p);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 64; ++j) v[j] = make_float2(v[j].x + v[j].y, v[j].x - v[j].y);
+
+    // y = Pi x / n = (H D x) / (sqrt(d) n)
+    const float inv_n = n > 0.0f ? inv_sqrt_d / n : 0.0f;
+    const float2 s2 = make_float2(inv_n, inv_n);
+    uint32_t wd[4 * BITS];  // the record, LSB-first
+    float c2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if constexpr (BITS == 4) {
+#pragma unroll
+      for (int j = 0; j < 64; j += 8) {
+        uint32_t bx[4], by[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t x0, y0, x1, y1;
+          quant_pair(v[j + 2 * k], s2, qrow, x0, y0);
+          quant_pair(v[j + 2 * k + 1], s2, qrow, x1, y1);
+          bx[k] = x0 | (x1 << 4);  // codes of coordinates j + 2k, j + 2k + 1
+          by[k] = y0 | (y1 << 4);  // ... and of the same plus 64
+          c2p[k] += lds32f(prow + (bx[k] << 7)) + lds32f(prow + (by[k] << 7));
+        }
+        wd[j / 8] = __byte_perm(__byte_perm(bx[0], bx[1], 0x0040), __byte_perm(bx[2], bx[3], 0x0040), 0x5410);
+        wd[8 + j / 8] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
+      }
+    } else {
+#pragma unroll
+      for (int jb = 0; jb < 64; jb += 32) {
+        uint32_t cx[32], cy[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) quant_pair(v[jb + i], s2, qrow, cx[i], cy[i]);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2)
+          c2p[(i >> 1) & 3] += lds32f(prow + ((cx[i] | (cx[i + 1] << BITS)) << 7)) +
+                               lds32f(prow + ((cy[i] | (cy[i + 1] << BITS)) << 7));
+        uint32_t wx[BITS], wy[BITS];
+        pack32<BITS>(cx, wx);
+        pack32<BITS>(cy, wy);
+#pragma unroll
+        for (int k = 0; k < BITS; ++k) {
+          wd[(jb / 32) * BITS + k] = wx[k];      // coordinates jb .. jb + 31
+          wd[(2 + jb / 32) * BITS + k] = wy[k];  // coordinates 64 + jb .. 64 + jb + 31
+        }
+      }
+    }
+    const float c2 = (c2p[0] + c2p[1]) + (c2p[2] + c2p[3]);
+    float gamma;
+    if (a.norm_mode == TQ_NORM_RAW) gamma = n;
+    else gamma = (n > 0.0f && c2 > 0.0f) ? n / sqrtf(c2) : 0.0f;
+
+    if (valid && slot >= a.max_slot) {
+      flag_status(a.status, TQ_DEV_BAD_SLOT);
+    } else if (valid && slot >= 0) {
+      uint8_t* page = a.pool[kv] + ((slot >> 4) * a.H + head) * (int64_t)a.page_bytes;
+      const int off = (int)(slot & 15);
+      uint4* rec = reinterpret_cast<uint4*>(page + off * R);
+#pragma unroll
+      for (int k = 0; k < BITS; ++k) rec[k] = make_uint4(wd[4 * k], wd[4 * k + 1], wd[4 * k + 2], wd[4 * k + 3]);
+      *reinterpret_cast<float*>(page + 16 * R + 4 * off) = gamma;
+    }
+  }
+  if (aborted && lane == 0) {  // let copies still in flight into this warp's ring land before exiting
+    for (int64_t k = it; k < n_my && k < it + kTStages; ++k) mbar_wait(bar + (int)(k % kTStages), (uint32_t)(k / kTStages) & 1u);
+  }
+}
+
 // bf16 layers: the append is a paged copy with rounding to bf16.
 template <typename TIn>
 __global__ void __launch_bounds__(256) k_append_bf16(const TIn* __restrict__ x, const int64_t* __restrict__ slots,
@@ -499,6 +755,82 @@ static cudaError_t dispatch_mode(const QuantArgs& a, int ny, int mode, bool qjl,
              : run_quantize<BITS, TIn, MODE_DENSE, false>(a, ny, num_sms, st);
 }
 
+// cuTensorMapEncodeTiled, fetched once through the runtime (no link-time libcuda dependency).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// [n_vec][128] bf16 rows, boxes of [32 rows][64 elements] with the 128-byte swizzle.
+static bool vec_tensor_map(CUtensorMap* m, const void* x, uint32_t n_vec) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)n_vec};
+  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BITS>
+static cudaError_t run_quantize_tma(const QuantTmaArgs& a, int num_sms, cudaStream_t st) {
+  auto kern = k_quantize_tma<BITS>;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t total = a.tiles * a.ny;
+  int64_t grid = (total + kTW - 1) / kTW;
+  if (grid > num_sms) grid = num_sms;
+  kern<<<(unsigned)grid, kTW * 32, kTSmem, st>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// The staged kernel takes bf16 Hadamard appends without QJL whose inputs TMA can
+// address (16-byte aligned, fewer than 2^31 vectors).  Returns false (nothing
+// launched) when the append is not of that kind.
+static bool try_quantize_tma(const tq_cache_desc& d, int which, const void* x, const void* x_v, int bits,
+                             const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms, cudaStream_t st,
+                             cudaError_t* err) {
+  const int64_t n_vec = n_tok * d.num_kv_heads;
+  if (n_vec <= 0 || n_vec >= ((int64_t)1 << 31)) return false;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (x_v && (reinterpret_cast<uintptr_t>(x_v) & 15u))) return false;
+  QuantTmaArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!vec_tensor_map(&a.tm[0], x, (uint32_t)n_vec)) return false;
+  if (x_v && !vec_tensor_map(&a.tm[1], x_v, (uint32_t)n_vec)) return false;
+  a.pool[0] = reinterpret_cast<uint8_t*>(which == 0 ? d.k_cache : d.v_cache);
+  a.pool[1] = reinterpret_cast<uint8_t*>(d.v_cache);
+  a.slots = slots;
+  a.tiles = (n_vec + 31) / 32;
+  a.n_vec = (uint32_t)n_vec;
+  a.ny = x_v ? 2 : 1;
+  a.H = d.num_kv_heads;
+  a.page_bytes = (int)page_bytes_of(d, which);
+  a.max_slot = d.num_blocks * kBlock;
+  a.rot = d.rotation;
+  a.cb = codebook_of(d, which);
+  a.norm_mode = d.fmt.norm_mode;
+  a.status = status;
+  switch (bits) {
+    case 2: *err = run_quantize_tma<2>(a, num_sms, st); break;
+    case 3: *err = run_quantize_tma<3>(a, num_sms, st); break;
+    default: *err = run_quantize_tma<4>(a, num_sms, st); break;
+  }
+  return true;
+}
+
 static QuantArgs quant_args(const tq_cache_desc& d, int which, const void* x, const float* y, const float* norms,
                             const int64_t* slots, int64_t n_tok, unsigned* status) {
   QuantArgs a;
@@ -541,6 +873,13 @@ cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, in
     count_launch();
     return cudaGetLastError();
   }
+  const int bits = which == 0 ? d.fmt.bits_k : d.fmt.bits_v;
+  const bool qjl = which == 0 && d.fmt.qjl_k && y == nullptr;
+  const int mode = y ? MODE_GIVEN_Y : (d.fmt.rot_kind == TQ_ROT_DENSE ? MODE_DENSE : MODE_HADAMARD);
+  if (mode == MODE_HADAMARD && !qjl && in_dtype == TQ_BF16) {
+    cudaError_t err = cudaSuccess;
+    if (try_quantize_tma(d, which, x, x_v, bits, slots, n_tok, status, num_sms, st, &err)) return err;
+  }
   QuantArgs a = quant_args(d, which, x, y, norms, slots, n_tok, status);
   int ny = 1;
   if (x_v) {  // values in the same launch (caller checked that the formats and tables agree)
@@ -548,9 +887,6 @@ cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, in
     a.pool_v = reinterpret_cast<uint8_t*>(d.v_cache);
     ny = 2;
   }
-  const int bits = which == 0 ? d.fmt.bits_k : d.fmt.bits_v;
-  const bool qjl = which == 0 && d.fmt.qjl_k && y == nullptr;
-  const int mode = y ? MODE_GIVEN_Y : (d.fmt.rot_kind == TQ_ROT_DENSE ? MODE_DENSE : MODE_HADAMARD);
   const bool f32 = in_dtype == TQ_F32;
   switch (bits) {
     case 2:
