@@ -120,12 +120,13 @@ def _bf16_dev(cuda, bits):
     return cuda.from_numpy(bits.view(np.int16)).cuda().view(cuda.bfloat16)
 
 
-@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 def test_append_bf16_many_tiles_per_warp(cuda, tqlib, bits):
-    """8192 tokens x 8 heads of bf16 K and V in one paired launch (2 x 65536 vectors):
-    every warp of the staged kernel goes round its two-deep ring several times."""
+    """8199 tokens x 8 heads of bf16 K and V in one paired launch (2 x 65592 vectors,
+    a ragged last tile): large appends take the staged kernel, every warp of which
+    refills its stage several times (the barrier phase flips from tile to tile)."""
     tq = tqlib
-    H, n = 8, 8192
+    H, n = 8, 8199
     nb = n // 16 + 3
     layer = tq.Layer(nb, H, bits_k=bits, bits_v=bits, seed=7, layer=3, fill=0xA5)
     kb, vb = workloads.lognormal_channel_kv(12, n, H, D)
@@ -151,6 +152,30 @@ def test_append_bf16_many_tiles_per_warp(cuda, tqlib, bits):
             assert np.all(np.abs(g_gpu[same] - gamma[same]) <= 1e-6 * np.abs(gamma[same]) + 1e-30)
         rec = opack_record_view(host, nb, H, bits)
         assert np.all(rec[~written.reshape(nb, 16)] == 0xA5)
+
+
+def test_append_bf16_keys_only_staged(cuda, tqlib):
+    """A keys-only append of 4100 tokens x 8 heads (32800 vectors, one tensor per launch)."""
+    tq = tqlib
+    H, n = 8, 4100
+    nb = n // 16 + 2
+    layer = tq.Layer(nb, H, bits_k=4, bits_v=3, seed=2, layer=5, fill=0x3C)
+    kb, _ = workloads.heavy_tail_kv(21, n, H, D)
+    slots, slots_d = make_slots(cuda, n, nb, 17)
+    layer.append(_bf16_dev(cuda, kb), None, slots_d)
+    assert tq.get_device_status() == 0
+    pi = orot.hadamard_rotation_seeded(2, 5, D)
+    c32, b32 = ocb.codebook_fp32(D, 4)
+    fields = page_fields(layer, 0, layer.k_cache.cpu().numpy())
+    x = oq.bf16_bits_to_f64(kb)
+    for h in range(H):
+        idx, gamma, y = oq.quantize(x[:, h], pi, c32, b32)
+        codes, g_gpu = slot_fields(fields, slots, h)
+        ok, _ = tie_band_ok(y, codes, idx, b32, 1e-5)
+        assert ok
+        same = np.all(codes == idx, axis=-1)
+        assert np.all(np.abs(g_gpu[same] - gamma[same]) <= 1e-6 * np.abs(gamma[same]) + 1e-30)
+    assert np.all(layer.v_cache.cpu().numpy() == 0x3C)  # values untouched
 
 
 def test_append_misaligned_input_rejected(cuda, tqlib):

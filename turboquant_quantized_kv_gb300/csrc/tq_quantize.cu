@@ -338,15 +338,16 @@ __global__ void __launch_bounds__(kThreads, (MODE == MODE_HADAMARD && !QJL) ? 3 
 // so that one lane owns one whole vector: all seven butterfly stages of the FWHT
 // run in registers (no shuffles), on float pairs v[j] = (x_j, x_{j+64}) so that
 // six of them are packed fp32-pair operations.  Each warp streams tiles of 32
-// vectors through its own two-deep shared-memory ring with 2-D tensor copies
+// vectors through its own shared-memory stage with 2-D tensor copies
 // (two boxes of [32 vectors][64 coordinates], 128-byte swizzle: lane l reads
-// 16-byte chunk c of its row at chunk c ^ (l & 7), so no read conflicts), which
-// keeps the next tile's loads in flight while the current one is computed.
+// 16-byte chunk c of its row at chunk c ^ (l & 7), so no read conflicts).  The
+// stage is refilled with the warp's next tile as soon as the current one is in
+// registers, so that tile's copy overlaps the current tile's arithmetic.
 // The cell entries shrink to 8 bytes {P, base} (one 64-bit read per
 // coordinate); the norm-correction sum sum_j c[idx_j]^2 is read per pair of
 // codes from a table of c[lo]^2 + c[hi]^2 indexed by the packed pair.
-constexpr int kTW = 8;                        // warps per CTA
-constexpr int kTStages = 2;                   // ring depth per warp
+constexpr int kTW = 12;                       // warps per CTA (3 per scheduler: 168 registers)
+constexpr int kTStages = 1;                   // tiles per warp ring: refilled as soon as unpacked
 constexpr uint32_t kTBox = 32 * 128;          // one box: 32 vectors x 64 bf16 coordinates
 constexpr uint32_t kTStage = 2 * kTBox;       // 32 whole vectors
 constexpr uint32_t kTCellBytes = 128 * 128;   // [cell][16 replicas] {P, base}
@@ -529,7 +530,7 @@ __global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_const
     const float inv_n = n > 0.0f ? inv_sqrt_d / n : 0.0f;
     const float2 s2 = make_float2(inv_n, inv_n);
     uint32_t wd[4 * BITS];  // the record, LSB-first
-    float c2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float2 c2p[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
     if constexpr (BITS == 4) {
 #pragma unroll
       for (int j = 0; j < 64; j += 8) {
@@ -541,7 +542,7 @@ __global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_const
           quant_pair(v[j + 2 * k + 1], s2, qrow, x1, y1);
           bx[k] = x0 | (x1 << 4);  // codes of coordinates j + 2k, j + 2k + 1
           by[k] = y0 | (y1 << 4);  // ... and of the same plus 64
-          c2p[k] += lds32f(prow + (bx[k] << 7)) + lds32f(prow + (by[k] << 7));
+          c2p[k & 1] = __fadd2_rn(c2p[k & 1], make_float2(lds32f(prow + (bx[k] << 7)), lds32f(prow + (by[k] << 7))));
         }
         wd[j / 8] = __byte_perm(__byte_perm(bx[0], bx[1], 0x0040), __byte_perm(bx[2], bx[3], 0x0040), 0x5410);
         wd[8 + j / 8] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
@@ -554,8 +555,8 @@ __global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_const
         for (int i = 0; i < 32; ++i) quant_pair(v[jb + i], s2, qrow, cx[i], cy[i]);
 #pragma unroll
         for (int i = 0; i < 32; i += 2)
-          c2p[(i >> 1) & 3] += lds32f(prow + ((cx[i] | (cx[i + 1] << BITS)) << 7)) +
-                               lds32f(prow + ((cy[i] | (cy[i + 1] << BITS)) << 7));
+          c2p[(i >> 1) & 1] = __fadd2_rn(c2p[(i >> 1) & 1], make_float2(lds32f(prow + ((cx[i] | (cx[i + 1] << BITS)) << 7)),
+                                                                       lds32f(prow + ((cy[i] | (cy[i + 1] << BITS)) << 7))));
         uint32_t wx[BITS], wy[BITS];
         pack32<BITS>(cx, wx);
         pack32<BITS>(cy, wy);
@@ -566,7 +567,7 @@ __global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_const
         }
       }
     }
-    const float c2 = (c2p[0] + c2p[1]) + (c2p[2] + c2p[3]);
+    const float c2 = (c2p[0].x + c2p[1].x) + (c2p[0].y + c2p[1].y);
     float gamma;
     if (a.norm_mode == TQ_NORM_RAW) gamma = n;
     else gamma = (n > 0.0f && c2 > 0.0f) ? n / sqrtf(c2) : 0.0f;
@@ -798,13 +799,17 @@ static cudaError_t run_quantize_tma(const QuantTmaArgs& a, int num_sms, cudaStre
 }
 
 // The staged kernel takes bf16 Hadamard appends without QJL whose inputs TMA can
-// address (16-byte aligned, fewer than 2^31 vectors).  Returns false (nothing
-// launched) when the append is not of that kind.
+// address (16-byte aligned, fewer than 2^31 vectors) and that are large enough
+// to amortise its per-CTA tables (at least kTmaMinVectors vectors in the launch;
+// a decode step's append of a few tokens is faster on the plain kernel).
+// Returns false (nothing launched) when the append is not of that kind.
+constexpr int64_t kTmaMinVectors = 24576;
 static bool try_quantize_tma(const tq_cache_desc& d, int which, const void* x, const void* x_v, int bits,
                              const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms, cudaStream_t st,
                              cudaError_t* err) {
   const int64_t n_vec = n_tok * d.num_kv_heads;
   if (n_vec <= 0 || n_vec >= ((int64_t)1 << 31)) return false;
+  if (n_vec * (x_v ? 2 : 1) < kTmaMinVectors) return false;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) || (x_v && (reinterpret_cast<uintptr_t>(x_v) & 15u))) return false;
   QuantTmaArgs a;
   std::memset(&a, 0, sizeof(a));
