@@ -232,6 +232,64 @@ def test_dense_rotation_append_matches_oracle(cuda, tqlib):
             assert np.all(np.abs(g_gpu[same] - gamma[same]) <= 2e-6 * gamma[same])
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_dense_rotation_append_tensor_cores_many_tiles(cuda, tqlib, bits):
+    """bf16 appends through a dense Pi run as a tensor-core GEMM over tiles of 128
+    vectors: 8199 tokens x 8 heads of K and V (2 x 65592 vectors, a ragged last
+    tile, several tiles per CTA so the ring and the accumulators are reused)."""
+    tq = tqlib
+    H, n = 8, 8199
+    nb = n // 16 + 3
+    layer = tq.Layer(nb, H, bits_k=bits, bits_v=bits, rot_kind=tq.TQ_ROT_DENSE, seed=8, layer=7, fill=0x69)
+    kb, vb = workloads.lognormal_channel_kv(31, n, H, D)
+    slots, slots_d = make_slots(cuda, n, nb, 19, skip_every=37)
+    layer.append(_bf16_dev(cuda, kb), _bf16_dev(cuda, vb), slots_d)
+    assert tq.get_device_status() == 0
+    pi = orot.dense_rotation_seeded(8, 7, D)
+    c32, b32 = ocb.codebook_fp32(D, bits)
+    keep = slots >= 0
+    written = np.zeros(nb * 16, bool)
+    written[slots[keep]] = True
+    rates = []
+    for which, xb, pool in ((0, kb, layer.k_cache), (1, vb, layer.v_cache)):
+        host = pool.cpu().numpy()
+        fields = page_fields(layer, which, host)
+        x = oq.bf16_bits_to_f64(xb)
+        for h in range(H):
+            idx, gamma, y = oq.quantize(x[keep, h], pi, c32, b32)
+            codes, g_gpu = slot_fields(fields, slots[keep], h)
+            ok, rate = tie_band_ok(y, codes, idx, b32, 1e-5)
+            assert ok, "code mismatch outside the tie band"
+            rates.append(rate)
+            same = np.all(codes == idx, axis=-1)
+            assert same.mean() > 0.99
+            assert np.all(np.abs(g_gpu[same] - gamma[same]) <= 2e-6 * gamma[same])
+        rec = opack_record_view(host, nb, H, bits)
+        assert np.all(rec[~written.reshape(nb, 16)] == 0x69)
+    print("dense tensor-core append: tie-band mismatch rate %.2e" % np.mean(rates))
+
+
+def test_dense_rotation_append_f32_input(cuda, tqlib):
+    """fp32 inputs through a dense Pi (the CUDA-core mat-vec kernel)."""
+    tq = tqlib
+    H, nb, n = 2, 10, 140
+    layer = tq.Layer(nb, H, rot_kind=tq.TQ_ROT_DENSE, seed=6, layer=1)
+    x = np.random.default_rng(40).standard_normal((n, H, D)).astype(np.float32)
+    slots, slots_d = make_slots(cuda, n, nb, 23)
+    layer.append(cuda.from_numpy(x).cuda(), None, slots_d)
+    assert tq.get_device_status() == 0
+    pi = orot.dense_rotation_seeded(6, 1, D)
+    c32, b32 = ocb.codebook_fp32(D, 4)
+    fields = page_fields(layer, 0, layer.k_cache.cpu().numpy())
+    for h in range(H):
+        idx, gamma, y = oq.quantize(x[:, h].astype(np.float64), pi, c32, b32)
+        codes, g_gpu = slot_fields(fields, slots, h)
+        ok, _ = tie_band_ok(y, codes, idx, b32, 1e-5)
+        assert ok
+        same = np.all(codes == idx, axis=-1)
+        assert np.all(np.abs(g_gpu[same] - gamma[same]) <= 2e-6 * gamma[same])
+
+
 def test_qjl_residual_matches_oracle(cuda, tqlib):
     tq = tqlib
     H, nb, n = 2, 10, 130

@@ -19,6 +19,7 @@
 #include "tq_async.cuh"
 #include "tq_device.cuh"
 #include "tq_internal.h"
+#include "tq_tcgen05.cuh"
 
 namespace tq {
 
@@ -387,6 +388,36 @@ __device__ __forceinline__ float lds32f(uint32_t addr) {
   return v;
 }
 
+// Tables of the one-lane-per-vector kernels (threads 0 .. max(128, NC^2) - 1 write):
+//   cell table, 128 rows of 16 replicas of {P, base} (8 B; the host checked that no
+//   cell holds two boundaries), at a 16 KB aligned shared address;
+//   pair table, NC^2 rows of 32 replicas of c[lo]^2 + c[hi]^2 for pair lo + NC * hi.
+template <int BITS>
+__device__ __forceinline__ void build_pair_cell_tables(const Codebook& cb, unsigned char* cell, unsigned char* pair) {
+  constexpr int NC = 1 << BITS, NB = NC - 1;
+  const int tid = threadIdx.x;
+  if (tid < 128) {
+    uint32_t base = 0u;
+    float P = INFINITY;
+    for (int k = 0; k < NB; ++k) {
+      const float bk = cb.b[k];
+      const uint32_t ck = qcell(bk);
+      if (ck < (uint32_t)tid) ++base;
+      if (ck == (uint32_t)tid) P = bk;
+    }
+    float2* row = reinterpret_cast<float2*>(cell + tid * 128);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) row[r] = make_float2(P, __uint_as_float(base));
+  }
+  if (tid < NC * NC) {
+    const float lo = cb.c[tid & (NC - 1)], hi = cb.c[tid / NC];
+    const float v = lo * lo + hi * hi;
+    float4* row = reinterpret_cast<float4*>(pair + tid * 128);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) row[r] = make_float4(v, v, v, v);
+  }
+}
+
 // Codes of the coordinate pair held in x (already H D x, unnormalised), scaled by s.
 __device__ __forceinline__ void quant_pair(float2 x, float2 s, uint32_t qrow, uint32_t& c0, uint32_t& c1) {
   const float2 y = __fmul2_rn(x, s);
@@ -400,8 +431,6 @@ __device__ __forceinline__ void quant_pair(float2 x, float2 s, uint32_t qrow, ui
 template <int BITS>
 __global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_constant__ QuantTmaArgs a) {
   constexpr int R = 16 * BITS;             // record bytes
-  constexpr int NC = 1 << BITS;            // centroids
-  constexpr int NB = NC - 1;               // boundaries
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const uint32_t sbase = smem_u32(smem_raw);
   const uint32_t cell_addr = (sbase + 16383u) & ~16383u;  // 16 KB aligned: address = (t & mask) | row
@@ -433,26 +462,7 @@ __global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_const
   }
 
   // tables, built while the first copies are in flight
-  if (tid < 128) {  // cell table (the host checked that no cell holds two boundaries)
-    uint32_t base = 0u;
-    float P = INFINITY;
-    for (int k = 0; k < NB; ++k) {
-      const float bk = a.cb.b[k];
-      const uint32_t ck = qcell(bk);
-      if (ck < (uint32_t)tid) ++base;
-      if (ck == (uint32_t)tid) P = bk;
-    }
-    float2* row = reinterpret_cast<float2*>(gen(cell_addr + (uint32_t)tid * 128u));
-#pragma unroll
-    for (int r = 0; r < 16; ++r) row[r] = make_float2(P, __uint_as_float(base));
-  }
-  if (tid < NC * NC) {  // pair table: entry lo + NC * hi
-    const float lo = a.cb.c[tid & (NC - 1)], hi = a.cb.c[tid / NC];
-    const float v = lo * lo + hi * hi;
-    float4* row = reinterpret_cast<float4*>(gen(pair_addr + (uint32_t)tid * 128u));
-#pragma unroll
-    for (int r = 0; r < 8; ++r) row[r] = make_float4(v, v, v, v);
-  }
+  build_pair_cell_tables<BITS>(a.cb, gen(cell_addr), gen(pair_addr));
   if (tid < 64) {  // sign flips of coordinates 2k, 2k+1 as a mask on their packed bf16 word
     const uint32_t m = (__ldg(a.rot + 2 * tid) < 0.0f ? 0x8000u : 0u) | (__ldg(a.rot + 2 * tid + 1) < 0.0f ? 0x80000000u : 0u);
     *reinterpret_cast<uint32_t*>(gen(misc_addr + 4u * (uint32_t)tid)) = m;
@@ -585,6 +595,244 @@ __global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_const
   }
   if (aborted && lane == 0) {  // let copies still in flight into this warp's ring land before exiting
     for (int64_t k = it; k < n_my && k < it + kTStages; ++k) mbar_wait(bar + (int)(k % kTStages), (uint32_t)(k / kTStages) & 1u);
+  }
+}
+
+// ------------------------------------- dense rotation append on tensor cores
+//
+// Batched appends of bf16 vectors through a dense Pi (Haar kind) are a GEMM:
+// Y = X Pi^T for tiles of 128 vectors, M = N = K = 128.  Pi is split into bf16
+// parts Pi = P_hi + P_lo + O(2^-16 |Pi|) (both K-major in shared memory, built
+// once per CTA), and every K step of 16 issues two tcgen05.mma of kind::f16
+// (X * P_hi^T, X * P_lo^T) into one fp32 accumulator of 128 tensor-memory
+// columns.  Roles: warp 0 streams X tiles with 2-D tensor copies (boxes of
+// [128 vectors][64 coordinates], 128-byte swizzle) into a 3-deep ring; one
+// thread of warp 1 issues the MMAs; 16 epilogue warps in four groups serve four
+// accumulators in turn (group e takes tiles e, e + 4, ...), one lane per vector
+// (its tensor-memory lane): the norm n = ||x|| from the vector's bf16 row in the
+// ring, then y = (Pi x) / n in chunks of 32 columns through the same cell-table
+// quantizer, pair table and packing as the FWHT kernels.
+constexpr int kGM = 128;                      // vectors per tile (MMA M)
+constexpr int kGStages = 3;                   // X tiles in the ring
+constexpr int kGAcc = 4;                      // accumulators (4 x 128 = 512 tensor-memory columns)
+constexpr int kGWarps = 2 + 4 * kGAcc;        // copy warp, MMA warp, 4 epilogue warps per accumulator
+constexpr uint32_t kGTile = kGM * kD * 2;     // 32 KB of bf16 vectors
+constexpr uint32_t kGMat = kD * kD * 2;       // 32 KB: one bf16 part of Pi
+// from the 16 KB aligned base: cell table 16 KB, pair table 32 KB, barriers 1 KB,
+// Pi parts 64 KB, ring 96 KB (every matrix 1 KB aligned)
+constexpr uint32_t kGOffPair = 16384, kGOffMisc = 49152, kGOffPi = 50176, kGOffX = kGOffPi + 2 * kGMat;
+constexpr size_t kGSmem = 16384 + (size_t)kGOffX + (size_t)kGStages * kGTile;
+
+struct QuantGemmArgs {
+  CUtensorMap tm[2];  // [n_vec][128] bf16 keys / values: box [128][64], 128-byte swizzle
+  uint8_t* pool[2];
+  const int64_t* slots;
+  int tiles;          // 128-vector tiles per tensor
+  uint32_t n_vec;     // vectors per tensor
+  int ny;
+  int H;
+  int page_bytes;
+  int64_t max_slot;
+  const float* rot;   // Pi [128][128] row-major (y = Pi x)
+  Codebook cb;
+  int norm_mode;
+  unsigned* status;
+};
+
+template <int BITS>
+__global__ void __launch_bounds__(kGWarps * 32, 1) k_quantize_dense_mma(const __grid_constant__ QuantGemmArgs a) {
+  constexpr int R = 16 * BITS;
+  constexpr uint32_t kIdesc = umma_idesc_bf16_f32(kGM, kD);
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  const uint32_t A0 = (sbase + 16383u) & ~16383u;
+  const uint32_t cell_addr = A0, pair_addr = A0 + kGOffPair, misc_addr = A0 + kGOffMisc;
+  const uint32_t pi_addr = A0 + kGOffPi, x_addr = A0 + kGOffX;
+  auto gen = [&](uint32_t addr) { return smem_raw + (addr - sbase); };
+  uint64_t* full = reinterpret_cast<uint64_t*>(gen(misc_addr));  // [kGStages] X tile landed
+  uint64_t* empty = full + kGStages;                              // [kGStages] MMAs and norms done with it
+  uint64_t* mdone = empty + kGStages;                             // [kGAcc] accumulator written
+  uint64_t* aempty = mdone + kGAcc;                               // [kGAcc] accumulator read out
+  const uint32_t tmem_slot = misc_addr + 512;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = a.tiles * a.ny;
+  const int n_my = (int)blockIdx.x < total ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1 + 4);  // the MMA commit and the 4 epilogue warps of the tile
+    }
+    for (int e = 0; e < kGAcc; ++e) {
+      mbar_init(mdone + e, 1);
+      mbar_init(aempty + e, 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+
+  build_pair_cell_tables<BITS>(a.cb, gen(cell_addr), gen(pair_addr));
+  // Pi -> bf16 parts, element (n = i, k = j) of B = Pi at box j / 64, row i, chunk (j % 64) / 8 ^ (i & 7)
+  for (int c = threadIdx.x; c < kD * kD / 8; c += blockDim.x) {
+    const int i = c >> 4, kc = c & 15;
+    const float4 p0 = __ldg(reinterpret_cast<const float4*>(a.rot + i * kD + 8 * kc));
+    const float4 p1 = __ldg(reinterpret_cast<const float4*>(a.rot + i * kD + 8 * kc) + 1);
+    const float v[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
+      const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * e] - __bfloat162float(h0));
+      const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1));
+      hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+    const uint32_t off = (uint32_t)(kc >> 3) * (kGMat / 2) + (uint32_t)i * 128u + ((uint32_t)((kc & 7) ^ (i & 7)) << 4);
+    *reinterpret_cast<uint4*>(gen(pi_addr + off)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(gen(pi_addr + kGMat + off)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+  fence_proxy_async();  // Pi parts (generic stores) are read by the tensor cores
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gen(tmem_slot));
+
+  if (warp == 0) {
+    if (lane == 0) {  // copies: tile i of this CTA into stage i % kGStages
+      int issued = 0;
+      for (int i = 0; i < n_my; ++i) {
+        const int s = i % kGStages;
+        if (i >= kGStages && !mbar_wait(empty + s, (uint32_t)((i / kGStages) - 1) & 1u)) {
+          flag_status(a.status, TQ_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+        const int kv = tile >= a.tiles ? 1 : 0;
+        const int row = (tile - kv * a.tiles) * kGM;
+        mbar_arrive_expect_tx(full + s, kGTile);
+        tensor_copy_2d(x_addr + (uint32_t)s * kGTile, &a.tm[kv], 0, row, full + s);
+        tensor_copy_2d(x_addr + (uint32_t)s * kGTile + kGTile / 2, &a.tm[kv], 64, row, full + s);
+        issued = i + 1;
+      }
+      // copies still in flight land before the CTA can exit (all of them on the normal path)
+      for (int i = issued - kGStages < 0 ? 0 : issued - kGStages; i < issued; ++i)
+        mbar_wait(full + i % kGStages, (uint32_t)(i / kGStages) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMAs of tile i into accumulator i % kGAcc
+      int issued = 0;
+      for (int i = 0; i < n_my; ++i) {
+        const int s = i % kGStages, e = i % kGAcc;
+        if (!mbar_wait(full + s, (uint32_t)(i / kGStages) & 1u) ||
+            (i >= kGAcc && !mbar_wait(aempty + e, (uint32_t)((i / kGAcc) - 1) & 1u))) {
+          flag_status(a.status, TQ_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)e * kD;
+        const uint32_t xs = x_addr + (uint32_t)s * kGTile;
+#pragma unroll
+        for (int kc = 0; kc < 8; ++kc) {  // K step of 16: box kc / 4, 32 bytes into the swizzled rows
+          const uint32_t ko = (uint32_t)(kc >> 2) * (kGTile / 2) + (uint32_t)(kc & 3) * 32u;
+          const uint32_t po = (uint32_t)(kc >> 2) * (kGMat / 2) + (uint32_t)(kc & 3) * 32u;
+          const uint64_t ad = umma_desc_sw128(xs + ko);
+          umma_bf16(d, ad, umma_desc_sw128(pi_addr + po), kIdesc, kc > 0);
+          umma_bf16(d, ad, umma_desc_sw128(pi_addr + kGMat + po), kIdesc, true);
+        }
+        umma_commit(smem_u32(empty + s));
+        umma_commit(smem_u32(mdone + e));
+        issued = i + 1;
+      }
+      if (issued > 0)  // every MMA has completed before tensor memory is released
+        mbar_wait(mdone + (issued - 1) % kGAcc, (uint32_t)((issued - 1) / kGAcc) & 1u);
+    }
+  } else {
+    const int grp = (warp - 2) >> 2;           // accumulator served
+    const int quad = warp & 3;                 // tensor-memory lanes 32 quad .. 32 quad + 31
+    const int r = quad * 32 + lane;            // row of the tile
+    const uint32_t qrow = cell_addr | ((uint32_t)(lane & 15) << 3);
+    const uint32_t prow = pair_addr + ((uint32_t)lane << 2);
+    const uint32_t xrow = x_addr + (uint32_t)r * 128u + ((uint32_t)(r & 7) << 4);  // with the swizzle bits
+    for (int i = grp; i < n_my; i += kGAcc) {
+      const int s = i % kGStages;
+      const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+      const int kv = tile >= a.tiles ? 1 : 0;
+      const uint32_t vec = (uint32_t)((tile - kv * a.tiles) * kGM + r);
+      const bool valid = vec < a.n_vec;
+      const uint32_t tok = valid ? vec / (uint32_t)a.H : 0u;
+      const int head = (int)(vec - tok * (uint32_t)a.H);
+      const int64_t slot = valid ? __ldg(a.slots + tok) : -1;
+      // the accumulator first: its MMAs consumed phase i / kGStages of full[s], so that
+      // phase is complete (and the next cannot start before this warp arrives on empty[s])
+      if (!mbar_wait(mdone + grp, (uint32_t)(i / kGAcc) & 1u) || !mbar_wait(full + s, (uint32_t)(i / kGStages) & 1u)) {
+        if (lane == 0) flag_status(a.status, TQ_DEV_WAIT_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      // n = ||x|| from the bf16 row
+      const uint32_t xb = xrow + (uint32_t)s * kGTile;
+      float2 ss2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 d0 = lds128u(xb ^ ((uint32_t)c << 4));
+        const uint4 d1 = lds128u((xb + kGTile / 2) ^ ((uint32_t)c << 4));
+        const uint32_t w[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 p = make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+          ss2 = __ffma2_rn(p, p, ss2);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);  // this warp is done with the X tile
+      const float n = sqrtf(ss2.x + ss2.y);
+      const float inv_n = n > 0.0f ? 1.0f / n : 0.0f;
+      const float2 s2 = make_float2(inv_n, inv_n);
+
+      uint32_t wd[4 * BITS];
+      float2 c2p = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {  // coordinates 32 ch .. 32 ch + 31
+        float y[32];
+        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)grp * kD + (uint32_t)ch * 32u, y);
+        uint32_t code[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) quant_pair(make_float2(y[j], y[j + 1]), s2, qrow, code[j], code[j + 1]);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          c2p = __fadd2_rn(c2p, make_float2(lds32f(prow + ((code[j] | (code[j + 1] << BITS)) << 7)),
+                                            lds32f(prow + ((code[j + 2] | (code[j + 3] << BITS)) << 7))));
+        uint32_t wc[BITS];
+        pack32<BITS>(code, wc);
+#pragma unroll
+        for (int k = 0; k < BITS; ++k) wd[ch * BITS + k] = wc[k];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(aempty + grp);  // accumulator read out
+
+      const float c2 = c2p.x + c2p.y;
+      float gamma;
+      if (a.norm_mode == TQ_NORM_RAW) gamma = n;
+      else gamma = (n > 0.0f && c2 > 0.0f) ? n / sqrtf(c2) : 0.0f;
+      if (valid && slot >= a.max_slot) {
+        flag_status(a.status, TQ_DEV_BAD_SLOT);
+      } else if (valid && slot >= 0) {
+        uint8_t* page = a.pool[kv] + ((slot >> 4) * a.H + head) * (int64_t)a.page_bytes;
+        const int off = (int)(slot & 15);
+        uint4* rec = reinterpret_cast<uint4*>(page + off * R);
+#pragma unroll
+        for (int k = 0; k < BITS; ++k) rec[k] = make_uint4(wd[4 * k], wd[4 * k + 1], wd[4 * k + 2], wd[4 * k + 3]);
+        *reinterpret_cast<float*>(page + 16 * R + 4 * off) = gamma;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -772,13 +1020,13 @@ static EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// [n_vec][128] bf16 rows, boxes of [32 rows][64 elements] with the 128-byte swizzle.
-static bool vec_tensor_map(CUtensorMap* m, const void* x, uint32_t n_vec) {
+// [n_vec][128] bf16 rows, boxes of [box_rows rows][64 elements] with the 128-byte swizzle.
+static bool vec_tensor_map(CUtensorMap* m, const void* x, uint32_t n_vec, uint32_t box_rows) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)n_vec};
   const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -813,8 +1061,8 @@ static bool try_quantize_tma(const tq_cache_desc& d, int which, const void* x, c
   if ((reinterpret_cast<uintptr_t>(x) & 15u) || (x_v && (reinterpret_cast<uintptr_t>(x_v) & 15u))) return false;
   QuantTmaArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!vec_tensor_map(&a.tm[0], x, (uint32_t)n_vec)) return false;
-  if (x_v && !vec_tensor_map(&a.tm[1], x_v, (uint32_t)n_vec)) return false;
+  if (!vec_tensor_map(&a.tm[0], x, (uint32_t)n_vec, 32)) return false;
+  if (x_v && !vec_tensor_map(&a.tm[1], x_v, (uint32_t)n_vec, 32)) return false;
   a.pool[0] = reinterpret_cast<uint8_t*>(which == 0 ? d.k_cache : d.v_cache);
   a.pool[1] = reinterpret_cast<uint8_t*>(d.v_cache);
   a.slots = slots;
@@ -832,6 +1080,53 @@ static bool try_quantize_tma(const tq_cache_desc& d, int which, const void* x, c
     case 2: *err = run_quantize_tma<2>(a, num_sms, st); break;
     case 3: *err = run_quantize_tma<3>(a, num_sms, st); break;
     default: *err = run_quantize_tma<4>(a, num_sms, st); break;
+  }
+  return true;
+}
+
+template <int BITS>
+static cudaError_t run_quantize_dense_mma(const QuantGemmArgs& a, int num_sms, cudaStream_t st) {
+  auto kern = k_quantize_dense_mma<BITS>;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+  if (e != cudaSuccess) return e;
+  const int total = a.tiles * a.ny;
+  const int grid = total < num_sms ? total : num_sms;
+  kern<<<(unsigned)grid, kGWarps * 32, kGSmem, st>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// bf16 appends through a dense Pi without QJL go to the tensor-core kernel (TMA
+// addressable inputs, fewer than 2^31 vectors).  Returns false (nothing
+// launched) for other appends.
+static bool try_quantize_dense_mma(const tq_cache_desc& d, int which, const void* x, const void* x_v, int bits,
+                                   const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms,
+                                   cudaStream_t st, cudaError_t* err) {
+  const int64_t n_vec = n_tok * d.num_kv_heads;
+  if (n_vec <= 0 || n_vec >= ((int64_t)1 << 31) - kGM) return false;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (x_v && (reinterpret_cast<uintptr_t>(x_v) & 15u))) return false;
+  if (reinterpret_cast<uintptr_t>(d.rotation) & 15u) return false;
+  QuantGemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!vec_tensor_map(&a.tm[0], x, (uint32_t)n_vec, kGM)) return false;
+  if (x_v && !vec_tensor_map(&a.tm[1], x_v, (uint32_t)n_vec, kGM)) return false;
+  a.pool[0] = reinterpret_cast<uint8_t*>(which == 0 ? d.k_cache : d.v_cache);
+  a.pool[1] = reinterpret_cast<uint8_t*>(d.v_cache);
+  a.slots = slots;
+  a.tiles = (int)((n_vec + kGM - 1) / kGM);
+  a.n_vec = (uint32_t)n_vec;
+  a.ny = x_v ? 2 : 1;
+  a.H = d.num_kv_heads;
+  a.page_bytes = (int)page_bytes_of(d, which);
+  a.max_slot = d.num_blocks * kBlock;
+  a.rot = d.rotation;
+  a.cb = codebook_of(d, which);
+  a.norm_mode = d.fmt.norm_mode;
+  a.status = status;
+  switch (bits) {
+    case 2: *err = run_quantize_dense_mma<2>(a, num_sms, st); break;
+    case 3: *err = run_quantize_dense_mma<3>(a, num_sms, st); break;
+    default: *err = run_quantize_dense_mma<4>(a, num_sms, st); break;
   }
   return true;
 }
@@ -884,6 +1179,10 @@ cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, in
   if (mode == MODE_HADAMARD && !qjl && in_dtype == TQ_BF16) {
     cudaError_t err = cudaSuccess;
     if (try_quantize_tma(d, which, x, x_v, bits, slots, n_tok, status, num_sms, st, &err)) return err;
+  }
+  if (mode == MODE_DENSE && !qjl && in_dtype == TQ_BF16) {
+    cudaError_t err = cudaSuccess;
+    if (try_quantize_dense_mma(d, which, x, x_v, bits, slots, n_tok, status, num_sms, st, &err)) return err;
   }
   QuantArgs a = quant_args(d, which, x, y, norms, slots, n_tok, status);
   int ny = 1;
