@@ -5,13 +5,15 @@ heads, head_dim 128, 32 layers, context 8192 (+1 token per step), bf16 K/V with
 per-(head, channel) lognormal(0, 1) scales, 4-bit keys and values with fp32
 norms, Hadamard rotation per layer, paged 16-token blocks under a shuffled block
 table.  A step appends one new token per sequence to every layer (quantize-
-append) and runs decode attention over every layer.  All inputs are synthetic
+append) and runs decode attention over every layer (one tq_append_decode call
+per layer: the decode kernel's prologue overlaps the append).  All inputs are synthetic
 and already resident in HBM; one step reads ~4.6 GB of packed cache, more
 than L2, so no flush is needed between steps.
 
 Reported: value = packed K/V bytes read by decode per step / step time (GB/s);
-roofline for the decode call; quantize-append vectors/s from the prefill;
-e2e through the public API with host buffers; the oracle's CPU throughput.
+roofline for the decode call; quantize-append vectors/s from the prefill and
+from the dense-rotation burst (36 layers x 11,000 tokens); e2e through the
+public API with host buffers; the oracle's CPU throughput.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
 """
@@ -143,6 +145,46 @@ def setup(torch, tq, steps_total, dev):
                 slot_new=slot_new, ws=ws, append_ms=append_ms, append_vectors=n_vec)
 
 
+def dense_burst(torch, tq, dev, peak):
+    """The burst append of the dense-rotation workload: 36 layers x 8 KV heads x 11,000
+    prefilled bf16 tokens, K and V scaled by a per-layer lambda ~ U(0.5, 4), a dense Haar
+    rotation per layer, 4-bit codes (6,336,000 vectors).  One untimed burst, then one
+    timed with CUDA events around all 36 layer calls (1.6 GB of inputs: larger than L2)."""
+    import workloads
+    n_layers, n_tok = 36, 11000
+    lam = workloads.layer_scales(36, n_layers)
+    gen = torch.Generator(device=dev).manual_seed(36)
+    nb = (n_tok + BLOCK - 1) // BLOCK + 1
+    layers = [tq.Layer(nb, HKV, bits_k=4, bits_v=4, rot_kind=tq.TQ_ROT_DENSE, seed=36, layer=l, device=dev)
+              for l in range(n_layers)]
+    ks = [(torch.randn(n_tok, HKV, D, generator=gen, device=dev) * float(lam[l])).to(torch.bfloat16)
+          for l in range(n_layers)]
+    vs = [(torch.randn(n_tok, HKV, D, generator=gen, device=dev) * float(lam[l])).to(torch.bfloat16)
+          for l in range(n_layers)]
+    slots = torch.arange(n_tok, dtype=torch.int64, device=dev)
+    for l in range(n_layers):
+        layers[l].append(ks[l], vs[l], slots)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = tq.launch_count()
+    e0.record()
+    for l in range(n_layers):
+        layers[l].append(ks[l], vs[l], slots)
+    e1.record()
+    torch.cuda.synchronize()
+    launches = tq.launch_count() - n0
+    ms = e0.elapsed_time(e1)
+    n_vec = 2 * n_layers * n_tok * HKV
+    gbs = n_vec * APPEND_BYTES_PER_VECTOR / (ms * 1e-3) / 1e9
+    status = tq.get_device_status()
+    del ks, vs, layers
+    torch.cuda.empty_cache()
+    return {"workload": "36 layers x 8 KV heads x 11000 tokens, bf16 K and V, dense Haar rotation per layer, 4-bit",
+            "vectors": n_vec, "ms": round(ms, 4), "vectors_per_s": round(n_vec / (ms * 1e-3), 1),
+            "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes_per_vector": APPEND_BYTES_PER_VECTOR,
+            "gpu_launches": launches, "device_status": status}
+
+
 def step_prepare(torch, st):
     """ctx += 1 is done after the step; the new token goes to position ctx."""
     ctx64 = st["ctx"].to(torch.int64)
@@ -157,6 +199,13 @@ def layer_append(st, l):
 
 def layer_decode(st, l):
     st["layers"][l].decode(st["q"][l], st["bt"], st["ctx"], out=st["out"][l], workspace=st["ws"], num_splits=SPLITS)
+
+
+def layer_step(st, l):
+    """Append the new token of every sequence, then decode (tq_append_decode: the decode's
+    prologue overlaps the append)."""
+    st["layers"][l].append_decode(st["knew"][l], st["vnew"][l], st["slot_new"], st["q"][l], st["bt"], st["ctx"],
+                                  out=st["out"][l], workspace=st["ws"], num_splits=SPLITS)
 
 
 def run_tq(args):
@@ -183,6 +232,8 @@ def run_tq(args):
     # events around the decode call of layer i % LAYERS (an event node inside a graph
     # costs microseconds, so each step carries one pair), and after the timed region
     # each copy's pair holds the duration of that decode call in its last replay.
+    # That layer makes the append and the decode as two calls, so that the events
+    # bracket the decode kernel alone; every other layer makes one tq_append_decode.
     torch.cuda.synchronize()
     for l in range(LAYERS):  # eager warm-up (module load, attributes) before capture
         layer_decode(st, l)
@@ -199,12 +250,13 @@ def run_tq(args):
         with torch.cuda.graph(g):
             step_prepare(torch, st)
             for l in range(LAYERS):
-                layer_append(st, l)
                 if l == lt:
+                    layer_append(st, l)
                     ev[0].record()
-                layer_decode(st, l)
-                if l == lt:
+                    layer_decode(st, l)
                     ev[1].record()
+                else:
+                    layer_step(st, l)
         if gi == 0:
             launches_per_step = tq.launch_count() - n_before  # libtq kernels in one step's graph
         graphs.append(g)
@@ -268,6 +320,7 @@ def run_tq(args):
 
     # end to end through the public API with host buffers (pinned), eager calls
     e2e = run_e2e(torch, st, args, stream) if args.e2e else None
+    dense = dense_burst(torch, tq, dev, peak) if args.dense_burst else None
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -283,6 +336,7 @@ def run_tq(args):
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind, "traffic": traffic},
         "append": {"vectors_per_s": round(app_vps, 1), "gbs": round(app_gbs, 1), "frac": round(app_gbs / peak, 4),
                    "vectors": st["append_vectors"], "bytes_per_vector": APPEND_BYTES_PER_VECTOR},
+        "append_dense_burst": dense,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
@@ -312,8 +366,7 @@ def run_e2e(torch, st, args, stream):
             st["knew"][l].copy_(hk[l], non_blocking=True)
             st["vnew"][l].copy_(hv[l], non_blocking=True)
             st["q"][l].copy_(hq[l], non_blocking=True)
-            layer_append(st, l)
-            layer_decode(st, l)
+            layer_step(st, l)
             ho[l].copy_(st["out"][l], non_blocking=True)
 
     for _ in range(2):
@@ -444,6 +497,8 @@ def main():
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-dense-burst", dest="dense_burst", action="store_false",
+                    help="skip the dense-rotation burst append (36 layers x 11000 tokens)")
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (profiling runs use fewer)")
     ap.add_argument("--splits", type=int, default=0, help="decode context splits (0 = library default)")
     args = ap.parse_args()

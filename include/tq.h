@@ -237,6 +237,21 @@ tq_status tq_decode_attention(const tq_cache_desc* desc, const void* q, int q_dt
                               const int32_t* context_lens, float sm_scale, void* out, int out_dtype,
                               void* workspace, size_t workspace_bytes, int num_splits, void* stream);
 
+/* One decode step of a layer: tq_quantize_append(desc, k, v, in_dtype,
+ * slot_mapping, n_tokens) followed by tq_decode_attention(desc, q, ...) on the
+ * same stream, with the same arguments, results and errors as those two calls
+ * made in that order (every argument of both is checked before anything is
+ * launched).  The decode kernel is launched as a programmatic dependent of the
+ * append: its prologue (context lengths, block ids, query rotation, code
+ * tables) runs while the append is still writing, and it waits for the append
+ * to finish before it reads any page.  q, block_table and context_lens are
+ * therefore read while the append runs; the append never writes them. */
+tq_status tq_append_decode(const tq_cache_desc* desc, const void* k, const void* v, int in_dtype,
+                           const int64_t* slot_mapping, int64_t n_tokens, const void* q, int q_dtype, int batch,
+                           int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                           const int32_t* context_lens, float sm_scale, void* out, int out_dtype, void* workspace,
+                           size_t workspace_bytes, int num_splits, void* stream);
+
 /* Dequantize records ([P2] "Incremental dequantization"): slots: device int64[n];
  * out: device [n][num_kv_heads][head_dim] (out_dtype) with
  * x_hat = gamma Pi^T c[idx] of the K (which = 0) or V (which = 1) pool

@@ -136,6 +136,28 @@ def test_descriptor_validation(tqlib):
     assert tq.launch_count() == launches0  # rejected and empty calls enqueue nothing
 
 
+def test_append_decode_checks_both_calls_before_launching(tqlib):
+    """tq_append_decode checks the append's and the decode's arguments before it
+    enqueues anything: an invalid decode part rejects the call with nothing launched."""
+    tq = tqlib
+    lib = tq.lib()
+    d = fake_desc(tq)
+    launches0 = tq.launch_count()
+    ws = ctypes.c_void_p(0x40000)
+
+    def call(k, n_tokens, hq, batch=2):
+        return lib.tq_append_decode(ctypes.byref(d), k, None, tq.TQ_F32, ctypes.c_void_p(0x2000), n_tokens,
+                                    ctypes.c_void_p(0x1000), tq.TQ_F32, batch, hq, ctypes.c_void_p(8), 4,
+                                    ctypes.c_void_p(8), 0.1, ctypes.c_void_p(0x1000), tq.TQ_F32, ws, 1 << 20, 1, None)
+
+    assert call(ctypes.c_void_p(0x1004), 4, 8) == tq.TQ_ERR_INVALID_ARG  # misaligned k
+    assert "tq_append_decode" in tq.last_error() and "aligned" in tq.last_error()
+    assert call(ctypes.c_void_p(0x1000), 4, 12) == tq.TQ_ERR_INVALID_ARG  # valid append, 12 % 8 != 0
+    assert "num_q_heads" in tq.last_error()
+    assert call(ctypes.c_void_p(0x1000), 0, 8, batch=0) == tq.TQ_OK  # nothing to append or decode
+    assert tq.launch_count() == launches0
+
+
 def test_make_args_rejected(tqlib):
     lib = tqlib.lib()
     c = (ctypes.c_float * 16)()

@@ -263,3 +263,39 @@ def test_workspace_reused_across_shapes(cuda, tqlib):
             assert_close(out.cpu().numpy(), ref, TOL_BF16, ctx)
         # the counter region is zero again after the calls
         assert int(ws[:65536].count_nonzero().item()) == 0
+
+
+@pytest.mark.parametrize("kind", ["hadamard", "dense", "qjl"])
+def test_append_decode_equals_separate_calls(cuda, tqlib, kind):
+    """tq_append_decode (the decode launched as a programmatic dependent of the append,
+    its prologue overlapping the append) gives bit-identical outputs and caches to
+    tq_quantize_append followed by tq_decode_attention, step after step."""
+    tq = tqlib
+    B, Hq, Hkv, T = 4, 16, 4, 320
+    mb = T // 16
+    bt, nb = workloads.shuffled_block_table(5, B, mb, num_blocks=B * mb + 2)
+    kb, vb = workloads.scaled_gaussian_kv(9, B * T, Hkv, D)
+    kb, vb = kb.reshape(B, T, Hkv, D), vb.reshape(B, T, Hkv, D)
+    kw = dict(bits_k=2 if kind == "qjl" else 4, bits_v=4, qjl=kind == "qjl",
+              rot_kind=tq.TQ_ROT_DENSE if kind == "dense" else tq.TQ_ROT_HADAMARD, seed=3, layer=1, qjl_seed=4)
+    la, lb = tq.Layer(nb, Hkv, **kw), tq.Layer(nb, Hkv, **kw)
+    ctx0 = np.array([200, 7, 150, 33], np.int32)
+    for layer in (la, lb):
+        fill_cache(cuda, layer, kb, vb, bt, ctx0, True)
+    bt_d = cuda.from_numpy(bt).cuda()
+    for step in range(3):
+        pos = ctx0 + step
+        slots = workloads.slot_mapping(bt, pos[:, None])[:, 0].astype(np.int64)
+        knew = to_dev(cuda, kb[np.arange(B), pos], True)
+        vnew = to_dev(cuda, vb[np.arange(B), pos], True)
+        slots_d = cuda.from_numpy(slots).cuda()
+        q = to_dev(cuda, workloads.queries(20 + step, B, Hq, D), True)
+        ctx_d = cuda.from_numpy(pos + 1).cuda()
+        out_a = la.append_decode(knew, vnew, slots_d, q, bt_d, ctx_d, out_dtype=cuda.float32)
+        lb.append(knew, vnew, slots_d)
+        out_b = lb.decode(q, bt_d, ctx_d, out_dtype=cuda.float32)
+        cuda.cuda.synchronize()
+        assert tq.get_device_status() == 0
+        assert np.array_equal(out_a.cpu().numpy(), out_b.cpu().numpy())
+        assert np.array_equal(la.k_cache.cpu().numpy(), lb.k_cache.cpu().numpy())
+        assert np.array_equal(la.v_cache.cpu().numpy(), lb.v_cache.cpu().numpy())

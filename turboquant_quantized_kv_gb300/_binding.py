@@ -70,6 +70,11 @@ _SIGNATURES = {
                                            ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
                                            ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                                            ctypes.c_int, ctypes.c_void_p]),
+    "tq_append_decode": (ctypes.c_int, [_D, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                        ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
+                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                        ctypes.c_int, ctypes.c_void_p]),
     "tq_dequantize": (ctypes.c_int, [_D, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                      ctypes.c_int, ctypes.c_void_p]),
     "tq_get_device_status": (ctypes.c_int, [ctypes.c_void_p, _P(ctypes.c_int32)]),
@@ -269,6 +274,31 @@ class Layer:
                                          _ptr(context_lens, "context_lens"), ctypes.c_float(sm_scale),
                                          _ptr(out, "out"), _dtype_code(out), _ptr(workspace, "workspace"),
                                          workspace.numel(), num_splits, _stream(stream)))
+        return out
+
+    def append_decode(self, k, v, slot_mapping, q, block_table, context_lens, sm_scale=None, out=None,
+                      out_dtype=None, num_splits=0, workspace=None, stream=None):
+        """append(k, v, slot_mapping) then decode(q, ...) in one call (tq_append_decode: the
+        decode's prologue overlaps the append).  Returns out."""
+        torch = _torch()
+        ref = k if k is not None else v
+        n = int(ref.shape[0]) if ref is not None else 0
+        bsz, hq, _ = q.shape
+        max_blocks = int(block_table.shape[1])
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.head_dim)
+        if out is None:
+            out = torch.empty(q.shape, dtype=q.dtype if out_dtype is None else out_dtype, device=q.device)
+        if workspace is None:
+            workspace = torch.zeros(self.workspace_bytes(bsz, hq, max_blocks, num_splits), dtype=torch.uint8,
+                                    device=q.device)
+        _check(lib().tq_append_decode(ctypes.byref(self.desc), _ptr(k, "k"), _ptr(v, "v"),
+                                      _dtype_code(ref) if ref is not None else TQ_BF16,
+                                      _ptr(slot_mapping, "slot_mapping"), n, _ptr(q, "q"), _dtype_code(q), bsz, hq,
+                                      _ptr(block_table, "block_table"), max_blocks,
+                                      _ptr(context_lens, "context_lens"), ctypes.c_float(sm_scale),
+                                      _ptr(out, "out"), _dtype_code(out), _ptr(workspace, "workspace"),
+                                      workspace.numel(), num_splits, _stream(stream)))
         return out
 
     def dequantize(self, which, slots, out_dtype=None, stream=None):

@@ -52,6 +52,106 @@ tq_status cuda_result(cudaError_t e, const char* what) {
 
 bool valid_dtype(int t) { return t == TQ_F32 || t == TQ_BF16; }
 
+// Checks of tq_quantize_append's arguments (n_tokens == 0 passes: nothing to do).
+tq_status check_append(const tq_cache_desc* desc, const void* k, const void* v, int in_dtype,
+                       const int64_t* slot_mapping, int64_t n_tokens, const char* fn) {
+  tq_status s = check_desc(desc);
+  if (s != TQ_OK) return s;
+  if (!valid_dtype(in_dtype)) return fail(TQ_ERR_INVALID_ARG, "%s: in_dtype %d", fn, in_dtype);
+  if (n_tokens < 0) return fail(TQ_ERR_INVALID_ARG, "%s: n_tokens < 0", fn);
+  if (n_tokens == 0) return TQ_OK;
+  if (!slot_mapping) return fail(TQ_ERR_INVALID_ARG, "%s: null slot_mapping", fn);
+  if (!k && !v) return fail(TQ_ERR_INVALID_ARG, "%s: both k and v are null", fn);
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
+    return fail(TQ_ERR_INVALID_ARG, "%s: k/v must be 16-byte aligned", fn);
+  const tq_layer_format& f = desc->fmt;
+  if (f.kv_format == TQ_KV_PACKED &&
+      ((k && !cell_table_ok(desc->boundaries_k, (1 << f.bits_k) - 1)) ||
+       (v && !cell_table_ok(desc->boundaries_v, (1 << f.bits_v) - 1))))
+    return fail(TQ_ERR_UNSUPPORTED, "%s: codebook boundaries closer than 1/63 apart", fn);
+  return TQ_OK;
+}
+
+// The launches of a checked append (n_tokens > 0): keys and values in one launch
+// when their formats and tables agree.
+tq_status run_append(const tq_cache_desc* desc, const void* k, const void* v, int in_dtype,
+                     const int64_t* slot_mapping, int64_t n_tokens, const DeviceInfo& di, cudaStream_t st) {
+  const tq_layer_format& f = desc->fmt;
+  const bool same_tables = std::memcmp(desc->centroids_k, desc->centroids_v, sizeof(desc->centroids_k)) == 0 &&
+                           std::memcmp(desc->boundaries_k, desc->boundaries_v, sizeof(desc->boundaries_k)) == 0;
+  if (k && v && f.kv_format == TQ_KV_PACKED && f.bits_k == f.bits_v && !f.qjl_k && same_tables)  // one launch
+    return cuda_result(launch_quantize(*desc, 0, k, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
+                                       di.num_sms, st, v),
+                       "quantize K+V");
+  tq_status s = TQ_OK;
+  if (k) {
+    s = cuda_result(launch_quantize(*desc, 0, k, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
+                                    di.num_sms, st), "quantize K");
+    if (s != TQ_OK) return s;
+  }
+  if (v)
+    s = cuda_result(launch_quantize(*desc, 1, v, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
+                                    di.num_sms, st), "quantize V");
+  return s;
+}
+
+// Split count of a decode call: num_splits clamped to [1, min(max_blocks, 256)], or
+// the automatic choice for 0.
+int resolve_splits(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks, int num_splits) {
+  if (num_splits > 0) return num_splits < max_blocks ? (num_splits > 256 ? 256 : num_splits) : (max_blocks > 256 ? 256 : max_blocks);
+  return tq_auto_splits(desc, batch, num_q_heads, max_blocks);
+}
+
+// Checks of tq_decode_attention's arguments and the call they describe (batch
+// == 0 passes with *c unset: nothing to do).
+tq_status prepare_decode(const tq_cache_desc* desc, const void* q, int q_dtype, int batch, int num_q_heads,
+                         const int32_t* block_table, int max_blocks_per_seq, const int32_t* context_lens,
+                         float sm_scale, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                         int num_splits, const char* fn, DecodeCall* c) {
+  tq_status s = check_desc(desc);
+  if (s != TQ_OK) return s;
+  if (batch < 0) return fail(TQ_ERR_INVALID_ARG, "%s: batch < 0", fn);
+  if (batch == 0) return TQ_OK;
+  if (batch > 65535) return fail(TQ_ERR_UNSUPPORTED, "%s: batch %d > 65535", fn, batch);
+  if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype))
+    return fail(TQ_ERR_INVALID_ARG, "%s: q_dtype %d / out_dtype %d", fn, q_dtype, out_dtype);
+  if (num_q_heads < 1 || num_q_heads % desc->num_kv_heads != 0)
+    return fail(TQ_ERR_INVALID_ARG, "%s: num_q_heads %d not a multiple of num_kv_heads %d", fn, num_q_heads,
+                desc->num_kv_heads);
+  if (!q || !block_table || !context_lens || !out)
+    return fail(TQ_ERR_INVALID_ARG, "%s: null q/block_table/context_lens/out", fn);
+  if (max_blocks_per_seq < 1) return fail(TQ_ERR_INVALID_ARG, "%s: max_blocks_per_seq < 1", fn);
+  if (num_splits < 0) return fail(TQ_ERR_INVALID_ARG, "%s: num_splits < 0", fn);
+  if (!(sm_scale == sm_scale)) return fail(TQ_ERR_INVALID_ARG, "%s: sm_scale is NaN", fn);
+  if (reinterpret_cast<uintptr_t>(q) & 15) return fail(TQ_ERR_INVALID_ARG, "%s: q must be 16-byte aligned", fn);
+  DeviceInfo di;
+  if ((s = device_info(&di)) != TQ_OK) return s;
+  const int splits = resolve_splits(desc, batch, num_q_heads, max_blocks_per_seq, num_splits);
+  if (splits < 1) return fail(TQ_ERR_INVALID_ARG, "%s: could not choose a split count", fn);
+  const bool qjl = desc->fmt.kv_format == TQ_KV_PACKED && desc->fmt.qjl_k;
+  const size_t need = decode_workspace(batch, num_q_heads, splits, desc->head_dim, qjl).total;
+  if (!workspace || workspace_bytes < need)
+    return fail(TQ_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", fn, workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(TQ_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
+  c->desc = desc;
+  c->q = q;
+  c->q_dtype = q_dtype;
+  c->batch = batch;
+  c->num_q_heads = num_q_heads;
+  c->block_table = block_table;
+  c->max_blocks = max_blocks_per_seq;
+  c->ctx_lens = context_lens;
+  c->sm_scale = sm_scale;
+  c->out = out;
+  c->out_dtype = out_dtype;
+  c->workspace = reinterpret_cast<uint8_t*>(workspace);
+  c->splits = splits;
+  c->status = di.status;
+  c->after_append = false;
+  return TQ_OK;
+}
+
 }  // namespace
 }  // namespace tq
 
@@ -62,40 +162,11 @@ extern "C" {
 tq_status tq_quantize_append(const tq_cache_desc* desc, const void* k, const void* v, int in_dtype,
                              const int64_t* slot_mapping, int64_t n_tokens, void* stream) {
   clear_error();
-  tq_status s = check_desc(desc);
-  if (s != TQ_OK) return s;
-  if (!valid_dtype(in_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: in_dtype %d", in_dtype);
-  if (n_tokens < 0) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: n_tokens < 0");
-  if (n_tokens == 0) return TQ_OK;
-  if (!slot_mapping) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: null slot_mapping");
-  if (!k && !v) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: both k and v are null");
-  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
-    return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append: k/v must be 16-byte aligned");
-  const tq_layer_format& f = desc->fmt;
-  if (f.kv_format == TQ_KV_PACKED &&
-      ((k && !cell_table_ok(desc->boundaries_k, (1 << f.bits_k) - 1)) ||
-       (v && !cell_table_ok(desc->boundaries_v, (1 << f.bits_v) - 1))))
-    return fail(TQ_ERR_UNSUPPORTED, "tq_quantize_append: codebook boundaries closer than 1/63 apart");
+  tq_status s = check_append(desc, k, v, in_dtype, slot_mapping, n_tokens, "tq_quantize_append");
+  if (s != TQ_OK || n_tokens == 0) return s;
   DeviceInfo di;
   if ((s = device_info(&di)) != TQ_OK) return s;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const bool same_tables = std::memcmp(desc->centroids_k, desc->centroids_v, sizeof(desc->centroids_k)) == 0 &&
-                           std::memcmp(desc->boundaries_k, desc->boundaries_v, sizeof(desc->boundaries_k)) == 0;
-  if (k && v && f.kv_format == TQ_KV_PACKED && f.bits_k == f.bits_v && !f.qjl_k && same_tables)  // one launch
-    return cuda_result(launch_quantize(*desc, 0, k, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
-                                       di.num_sms, st, v),
-                       "quantize K+V");
-  if (k) {
-    s = cuda_result(launch_quantize(*desc, 0, k, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
-                                    di.num_sms, st), "quantize K");
-    if (s != TQ_OK) return s;
-  }
-  if (v) {
-    s = cuda_result(launch_quantize(*desc, 1, v, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
-                                    di.num_sms, st), "quantize V");
-    if (s != TQ_OK) return s;
-  }
-  return TQ_OK;
+  return run_append(desc, k, v, in_dtype, slot_mapping, n_tokens, di, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tq_status tq_quantize_rotated(const tq_cache_desc* desc, int which, const float* y, const float* norms,
@@ -127,10 +198,6 @@ int tq_auto_splits(const tq_cache_desc* desc, int batch, int num_q_heads, int ma
   return auto_splits(di.num_sms, decode_warps(*desc, g), batch, desc->num_kv_heads * groups, max_blocks_per_seq);
 }
 
-static int resolve_splits(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks, int num_splits) {
-  if (num_splits > 0) return num_splits < max_blocks ? (num_splits > 256 ? 256 : num_splits) : (max_blocks > 256 ? 256 : max_blocks);
-  return tq_auto_splits(desc, batch, num_q_heads, max_blocks);
-}
 
 size_t tq_workspace_bytes(const tq_cache_desc* desc, int batch, int num_q_heads, int max_blocks_per_seq,
                           int num_splits) {
@@ -147,48 +214,35 @@ tq_status tq_decode_attention(const tq_cache_desc* desc, const void* q, int q_dt
                               float sm_scale, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
                               int num_splits, void* stream) {
   clear_error();
-  tq_status s = check_desc(desc);
-  if (s != TQ_OK) return s;
-  if (batch < 0) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: batch < 0");
-  if (batch == 0) return TQ_OK;
-  if (batch > 65535) return fail(TQ_ERR_UNSUPPORTED, "tq_decode_attention: batch %d > 65535", batch);
-  if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype))
-    return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: q_dtype %d / out_dtype %d", q_dtype, out_dtype);
-  if (num_q_heads < 1 || num_q_heads % desc->num_kv_heads != 0)
-    return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: num_q_heads %d not a multiple of num_kv_heads %d",
-                num_q_heads, desc->num_kv_heads);
-  if (!q || !block_table || !context_lens || !out)
-    return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: null q/block_table/context_lens/out");
-  if (max_blocks_per_seq < 1) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: max_blocks_per_seq < 1");
-  if (num_splits < 0) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: num_splits < 0");
-  if (!(sm_scale == sm_scale)) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: sm_scale is NaN");
-  if (reinterpret_cast<uintptr_t>(q) & 15) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: q must be 16-byte aligned");
-  DeviceInfo di;
-  if ((s = device_info(&di)) != TQ_OK) return s;
-  const int splits = resolve_splits(desc, batch, num_q_heads, max_blocks_per_seq, num_splits);
-  if (splits < 1) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: could not choose a split count");
-  const bool qjl = desc->fmt.kv_format == TQ_KV_PACKED && desc->fmt.qjl_k;
-  const size_t need = decode_workspace(batch, num_q_heads, splits, desc->head_dim, qjl).total;
-  if (!workspace || workspace_bytes < need)
-    return fail(TQ_ERR_WORKSPACE, "tq_decode_attention: workspace %zu bytes, need %zu", workspace_bytes, need);
-  if (reinterpret_cast<uintptr_t>(workspace) & 255)
-    return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: workspace must be 256-byte aligned");
   DecodeCall c;
-  c.desc = desc;
-  c.q = q;
-  c.q_dtype = q_dtype;
-  c.batch = batch;
-  c.num_q_heads = num_q_heads;
-  c.block_table = block_table;
-  c.max_blocks = max_blocks_per_seq;
-  c.ctx_lens = context_lens;
-  c.sm_scale = sm_scale;
-  c.out = out;
-  c.out_dtype = out_dtype;
-  c.workspace = reinterpret_cast<uint8_t*>(workspace);
-  c.splits = splits;
-  c.status = di.status;
+  tq_status s = prepare_decode(desc, q, q_dtype, batch, num_q_heads, block_table, max_blocks_per_seq, context_lens,
+                               sm_scale, out, out_dtype, workspace, workspace_bytes, num_splits, "tq_decode_attention",
+                               &c);
+  if (s != TQ_OK || batch == 0) return s;
   return cuda_result(launch_decode(c, reinterpret_cast<cudaStream_t>(stream)), "decode attention");
+}
+
+tq_status tq_append_decode(const tq_cache_desc* desc, const void* k, const void* v, int in_dtype,
+                           const int64_t* slot_mapping, int64_t n_tokens, const void* q, int q_dtype, int batch,
+                           int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                           const int32_t* context_lens, float sm_scale, void* out, int out_dtype, void* workspace,
+                           size_t workspace_bytes, int num_splits, void* stream) {
+  clear_error();
+  tq_status s = check_append(desc, k, v, in_dtype, slot_mapping, n_tokens, "tq_append_decode");
+  if (s != TQ_OK) return s;
+  DecodeCall c;
+  s = prepare_decode(desc, q, q_dtype, batch, num_q_heads, block_table, max_blocks_per_seq, context_lens, sm_scale,
+                     out, out_dtype, workspace, workspace_bytes, num_splits, "tq_append_decode", &c);
+  if (s != TQ_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (n_tokens > 0) {
+    DeviceInfo di;
+    if ((s = device_info(&di)) != TQ_OK) return s;
+    if ((s = run_append(desc, k, v, in_dtype, slot_mapping, n_tokens, di, st)) != TQ_OK) return s;
+    c.after_append = true;
+  }
+  if (batch == 0) return TQ_OK;
+  return cuda_result(launch_decode(c, st), "decode attention");
 }
 
 tq_status tq_dequantize(const tq_cache_desc* desc, int which, const int64_t* slots, int64_t n, void* out,

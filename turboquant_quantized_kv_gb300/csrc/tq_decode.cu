@@ -179,7 +179,8 @@ struct DecodeArgs {
   int q_bf16;
   int q_in_kernel;    // 0: read qrot; 1: rotate q here (Hadamard); 2: scale q here (no rotation)
   float q_scale;      // sm_scale * log2 e
-  int pdl;            // host side: launched as a programmatic dependent of the prep pass
+  int pdl;            // host side: launched as a programmatic dependent of the previous kernel
+  int overlap_append;  // 1: the previous kernel is this library's append; wait for it before the first page copy
   int Hq, g, ngroups;
   int splits;  // chunks per unit
   int chunks;  // units * splits
@@ -934,17 +935,22 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   pp.kstride = (int64_t)a.Hkv * a.kpage;
   pp.vstride = (int64_t)a.Hkv * a.vpage;
   uint32_t valid_mask = 0u;
-  if constexpr (KIND == 0) {
-    for (int k = 0; k < pstages && k < n_pairs; ++k) {
-      const bool hb = 2 * k + 1 < n_my;
-      const int ba = ids.get(2 * k, lane);
-      const int bb = hb ? ids.get(2 * k + 1, lane) : -1;
-      valid_mask |= issue_pair(ring, k, a, pp, ba, bb, hb, lane) << (2 * k);
+  auto first_copies = [&]() {
+    if constexpr (KIND == 0) {
+      for (int k = 0; k < pstages && k < n_pairs; ++k) {
+        const bool hb = 2 * k + 1 < n_my;
+        const int ba = ids.get(2 * k, lane);
+        const int bb = hb ? ids.get(2 * k + 1, lane) : -1;
+        valid_mask |= issue_pair(ring, k, a, pp, ba, bb, hb, lane) << (2 * k);
+      }
+    } else {
+      for (int k = 0; k < stages && k < n_my; ++k)
+        if (issue_block(ring, k, a, ids.get(k, lane), kvh, lane)) valid_mask |= 1u << k;
     }
-  } else {
-    for (int k = 0; k < stages && k < n_my; ++k)
-      if (issue_block(ring, k, a, ids.get(k, lane), kvh, lane)) valid_mask |= 1u << k;
-  }
+  };
+  // Launched as a programmatic dependent of the append (tq_append_decode): everything
+  // above and the code tables below overlap the append; pages only after it is done.
+  if (!a.overlap_append) first_copies();
 
   if constexpr (KIND == 0) {
     if (layout_ok) {
@@ -966,6 +972,11 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
         tab[i] = make_uint4(v, v, v, v);
       }
     }
+  }
+
+  if (a.overlap_append) {
+    grid_dep_wait();
+    first_copies();
   }
 
   // per-warp constants: query fragments of column g_ (head 4 nt + g_ / 2, part g_ & 1)
@@ -1401,7 +1412,7 @@ static cudaError_t run_decode_nt(DecodeArgs a, cudaStream_t st) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = a.pdl ? 1 : 0;  // without the prep pass the previous kernel may be the append
+  cfg.numAttrs = a.pdl ? 1 : 0;  // otherwise the previous kernel may be anything that writes the inputs
   e = cudaLaunchKernelEx(&cfg, kern, a);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -1477,7 +1488,10 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   a.q_bf16 = c.q_dtype == TQ_BF16 ? 1 : 0;
   a.q_in_kernel = q_in_kernel;
   a.q_scale = scale;
-  a.pdl = prep ? 1 : 0;
+  // programmatic dependent of the prep pass, or of the append of tq_append_decode (the
+  // prep pass itself is an ordinary launch, so it starts after the append has finished)
+  a.pdl = (prep || c.after_append) ? 1 : 0;
+  a.overlap_append = (c.after_append && !prep) ? 1 : 0;
   a.Hq = c.num_q_heads;
   a.g = c.num_q_heads / d.num_kv_heads;
   a.ngroups = (a.g + (a.g <= 4 ? 3 : 7)) / (a.g <= 4 ? 4 : 8);  // head groups of 4 or 8 per warp

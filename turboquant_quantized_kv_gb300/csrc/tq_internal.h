@@ -62,6 +62,7 @@ struct DecodeCall {
   uint8_t* workspace;
   int splits;
   unsigned* status;
+  bool after_append;  // enqueued right after this library's append on the same stream (tq_append_decode)
 };
 
 // True if the append quantizer's cell table can hold these (ascending) boundaries:

@@ -136,6 +136,7 @@ __device__ __forceinline__ float flip_sign(float v, uint32_t word, int bit) {
 // residency matters more than the few registers the bound takes away.
 template <int BITS, typename TIn, int MODE, bool QJL>
 __global__ void __launch_bounds__(kThreads, (MODE == MODE_HADAMARD && !QJL) ? 3 : 1) k_quantize(QuantArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // a dependent decode may start its prologue
   const void* const x_in = blockIdx.y ? a.x_v : a.x;
   uint8_t* const pool = blockIdx.y ? a.pool_v : a.pool;
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, (MODE == MODE_HADAMARD && !QJL) ? 3 
       const float c1 = a.cb.c[min(base + 1u, (uint32_t)NB)];
       const float4 e = make_float4(P, c0 * c0, c1 * c1, __uint_as_float(base));
 #pragma unroll
-      for (int r = 0; r < 8; ++r) qtab[tid * 8 + r] = e;
+      for (int r = 0; r < 8; ++r) qtab[tid * 8 + ((r + tid) & 7)] = e;  // rotated: no store conflicts
     }
   }
   __syncthreads();
@@ -407,14 +408,14 @@ __device__ __forceinline__ void build_pair_cell_tables(const Codebook& cb, unsig
     }
     float2* row = reinterpret_cast<float2*>(cell + tid * 128);
 #pragma unroll
-    for (int r = 0; r < 16; ++r) row[r] = make_float2(P, __uint_as_float(base));
+    for (int r = 0; r < 16; ++r) row[(r + tid) & 15] = make_float2(P, __uint_as_float(base));  // rotated: no conflicts
   }
   if (tid < NC * NC) {
     const float lo = cb.c[tid & (NC - 1)], hi = cb.c[tid / NC];
     const float v = lo * lo + hi * hi;
     float4* row = reinterpret_cast<float4*>(pair + tid * 128);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) row[r] = make_float4(v, v, v, v);
+    for (int r = 0; r < 8; ++r) row[(r + tid) & 7] = make_float4(v, v, v, v);
   }
 }
 
@@ -430,6 +431,7 @@ __device__ __forceinline__ void quant_pair(float2 x, float2 s, uint32_t qrow, ui
 
 template <int BITS>
 __global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_constant__ QuantTmaArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // a dependent decode may start its prologue
   constexpr int R = 16 * BITS;             // record bytes
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const uint32_t sbase = smem_u32(smem_raw);
@@ -641,6 +643,7 @@ struct QuantGemmArgs {
 
 template <int BITS>
 __global__ void __launch_bounds__(kGWarps * 32, 1) k_quantize_dense_mma(const __grid_constant__ QuantGemmArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // a dependent decode may start its prologue
   constexpr int R = 16 * BITS;
   constexpr uint32_t kIdesc = umma_idesc_bf16_f32(kGM, kD);
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -841,6 +844,7 @@ template <typename TIn>
 __global__ void __launch_bounds__(256) k_append_bf16(const TIn* __restrict__ x, const int64_t* __restrict__ slots,
                                                      int64_t n_vec, int H, int64_t max_slot, uint8_t* pool,
                                                      unsigned* status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // a dependent decode may start its prologue
   const int64_t n_chunks = n_vec * 16;  // 8 elements per chunk
   for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n_chunks; c += (int64_t)gridDim.x * blockDim.x) {
     const int64_t vec = c >> 4;
