@@ -476,8 +476,9 @@ __device__ __forceinline__ bool issue_block(const Ring& r, int stage, const Deco
       const uint8_t* srcv = a.vpool + ((int64_t)blk * a.Hkv + kvh) * a.vpage;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive_expect_tx(bar, (uint32_t)(a.kpage + a.vpage));
-      bulk_copy_g2s(dst, srck, (uint32_t)a.kpage, bar);
-      bulk_copy_g2s(dst + a.kpage, srcv, (uint32_t)a.vpage, bar);
+      const uint64_t pol = l2_evict_first_policy();  // pages are read once per call
+      bulk_copy_g2s_hint(dst, srck, (uint32_t)a.kpage, bar, pol);
+      bulk_copy_g2s_hint(dst + a.kpage, srcv, (uint32_t)a.vpage, bar, pol);
     } else {
       flag_status(a.status, TQ_DEV_BAD_BLOCK);
       mbar_arrive(bar);  // completes the phase without data
@@ -504,13 +505,15 @@ __device__ __forceinline__ uint32_t issue_pair(const Ring& r, int ps, const Deco
     uint8_t* dst = r.buf + ps * 2 * r.stage_bytes;
     if (!ok_a || (has_b && !ok_b)) flag_status(a.status, TQ_DEV_BAD_BLOCK);
     mbar_arrive_expect_tx(bar, (uint32_t)((ok_a ? r.stage_bytes : 0) + (ok_b ? r.stage_bytes : 0)));
+    const uint64_t pol = l2_evict_first_policy();  // pages are read once per call
     if (ok_a) {
-      bulk_copy_g2s(dst, pp.kbase + (int64_t)blk_a * pp.kstride, (uint32_t)a.kpage, bar);
-      bulk_copy_g2s(dst + a.kpage, pp.vbase + (int64_t)blk_a * pp.vstride, (uint32_t)a.vpage, bar);
+      bulk_copy_g2s_hint(dst, pp.kbase + (int64_t)blk_a * pp.kstride, (uint32_t)a.kpage, bar, pol);
+      bulk_copy_g2s_hint(dst + a.kpage, pp.vbase + (int64_t)blk_a * pp.vstride, (uint32_t)a.vpage, bar, pol);
     }
     if (ok_b) {
-      bulk_copy_g2s(dst + r.stage_bytes, pp.kbase + (int64_t)blk_b * pp.kstride, (uint32_t)a.kpage, bar);
-      bulk_copy_g2s(dst + r.stage_bytes + a.kpage, pp.vbase + (int64_t)blk_b * pp.vstride, (uint32_t)a.vpage, bar);
+      bulk_copy_g2s_hint(dst + r.stage_bytes, pp.kbase + (int64_t)blk_b * pp.kstride, (uint32_t)a.kpage, bar, pol);
+      bulk_copy_g2s_hint(dst + r.stage_bytes + a.kpage, pp.vbase + (int64_t)blk_b * pp.vstride, (uint32_t)a.vpage, bar,
+                         pol);
     }
   }
   return (ok_a ? 1u : 0u) | (ok_b ? 2u : 0u);
