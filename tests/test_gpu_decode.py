@@ -299,3 +299,98 @@ def test_append_decode_equals_separate_calls(cuda, tqlib, kind):
         assert np.array_equal(out_a.cpu().numpy(), out_b.cpu().numpy())
         assert np.array_equal(la.k_cache.cpu().numpy(), lb.k_cache.cpu().numpy())
         assert np.array_equal(la.v_cache.cpu().numpy(), lb.v_cache.cpu().numpy())
+
+
+def _sampled_err(tq, layer, out, q, bt, ctx, pairs, sm, g):
+    """Max relative error of out over the heads of sampled (sequence, KV head) pairs
+    against exact attention over the GPU's own cache (oracle gathers per pair)."""
+    kp, vp = layer.k_cache.cpu().numpy(), layer.v_cache.cpu().numpy()
+    nb, hkv = layer.num_blocks, layer.num_kv_heads
+    qx = q.float().cpu().numpy().astype(np.float64)
+    o = out.float().cpu().numpy()
+    errs = []
+    if not layer.packed:
+        for b, kvh in pairs:
+            k, v = oa.gather_bf16(kp.view(np.uint16), vp.view(np.uint16), nb, hkv, D, bt[b], int(ctx[b]), kvh)
+            for h in range(kvh * g, (kvh + 1) * g):
+                errs.append(max_rel_err(o[b, h][None], oa.softmax_attention(qx[b, h], k, v, sm)[None]))
+        return max(errs)
+    ol = oracle_layer(layer)
+    for b, kvh in pairs:
+        f = oa.gather_packed(kp, vp, ol, nb, hkv, D, bt[b], int(ctx[b]), kvh)
+        for h in range(kvh * g, (kvh + 1) * g):
+            if ol.qjl:
+                from oracle import qjl as oqjl
+                s = sm * oqjl.estimate(qx[b, h], ol.pi, ol.cb_k, f["k_idx"], f["k_gamma"], f["k_signs"], f["k_rho"],
+                                       ol.qjl_s)
+            else:
+                s = sm * (f["k_hat"] @ qx[b, h])
+            errs.append(max_rel_err(o[b, h][None], (oa.softmax_weights(s) @ f["v_hat"])[None]))
+    return max(errs)
+
+
+def _gpu_kv(torch, gen, n, hkv, heavy):
+    """bf16 [n, hkv, d] N(0, 1) K and V; heavy: each element replaced with probability
+    0.01 by an unscaled Student-t(3) draw (z / sqrt(chi2_3 / 3))."""
+    out = []
+    for _ in range(2):
+        x = torch.randn(n, hkv, D, generator=gen, device="cuda")
+        if heavy:
+            mask = torch.rand(n, hkv, D, generator=gen, device="cuda") < 0.01
+            chi = sum(torch.randn(n, hkv, D, generator=gen, device="cuda") ** 2 for _ in range(3))
+            t3 = torch.randn(n, hkv, D, generator=gen, device="cuda") / torch.sqrt(chi / 3.0)
+            x = torch.where(mask, t3, x)
+            del mask, chi, t3
+        out.append(x.to(torch.bfloat16))
+        del x
+    return out
+
+
+def test_config3_shape_full_size_sampled(cuda, tqlib):
+    """Batch 4, 64 query / 8 KV heads (groups of 8), context 131,072 (8192 blocks per
+    sequence), 3-bit keys / 4-bit values, N(0, 1) with 1 % Student-t(3) elements,
+    shuffled table; sampled (sequence, KV head) pairs of the full-size run."""
+    tq, torch = tqlib, cuda
+    B, Hq, Hkv, T = 4, 64, 8, 131072
+    bt, nb = workloads.shuffled_block_table(31, B, T // 16)
+    layer = tq.Layer(nb, Hkv, bits_k=3, bits_v=4, seed=3, layer=2)
+    gen = torch.Generator(device="cuda").manual_seed(33)
+    k, v = _gpu_kv(torch, gen, B * T, Hkv, heavy=True)
+    layer.append(k, v, torch.from_numpy(workloads.prefill_slots(bt, T)).cuda())
+    del k, v
+    ctx = np.full(B, T, np.int32)
+    q = torch.randn(B, Hq, D, generator=gen, device="cuda").to(torch.bfloat16)
+    out = layer.decode(q, torch.from_numpy(bt).cuda(), torch.from_numpy(ctx).cuda(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tq.get_device_status() == 0
+    err = _sampled_err(tq, layer, out, q, bt, ctx, ((0, 0), (3, 7)), 1 / math.sqrt(D), Hq // Hkv)
+    print("config 3 sampled max rel err %.3e" % err)
+    assert err <= TOL_BF16
+
+
+@pytest.mark.parametrize("variant", ["packed", "qjl", "bf16"])
+def test_config5_layers_full_size_sampled(cuda, tqlib, variant):
+    """Batch 8, 32 query / 8 KV heads, context 100,000 (6250 blocks per sequence) for
+    the three layer kinds of the mixed-precision model: a 4/4 packed layer, the
+    variant with 2-bit + QJL keys and 4-bit values, and a bf16 boundary layer."""
+    tq, torch = tqlib, cuda
+    B, Hq, Hkv, T = 8, 32, 8, 100000
+    bt, nb = workloads.shuffled_block_table(51, B, -(-T // 16))
+    if variant == "bf16":
+        layer = tq.Layer(nb, Hkv, kv_format="bf16")
+    elif variant == "qjl":
+        layer = tq.Layer(nb, Hkv, bits_k=2, bits_v=4, qjl=True, seed=5, layer=11, qjl_seed=9)
+    else:
+        layer = tq.Layer(nb, Hkv, seed=5, layer=11)
+    gen = torch.Generator(device="cuda").manual_seed(55)
+    k, v = _gpu_kv(torch, gen, B * T, Hkv, heavy=False)
+    layer.append(k, v, torch.from_numpy(workloads.prefill_slots(bt, T)).cuda())
+    del k, v
+    ctx = np.full(B, T, np.int32)
+    q = torch.randn(B, Hq, D, generator=gen, device="cuda").to(torch.bfloat16)
+    out = layer.decode(q, torch.from_numpy(bt).cuda(), torch.from_numpy(ctx).cuda(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tq.get_device_status() == 0
+    err = _sampled_err(tq, layer, out, q, bt, ctx, ((0, 1), (7, 6)), 1 / math.sqrt(D), Hq // Hkv)
+    print("config 5 %s sampled max rel err %.3e" % (variant, err))
+    assert err <= TOL_BF16
