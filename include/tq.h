@@ -37,6 +37,11 @@
  *  bf16 layers ([P1] §起動コマンド: the first and last two layers of dense
  *  models stay at full precision; [P4] layout table, 512 B per token and head)
  *  hold raw bf16 K/V and are attended without rotation.
+ *  k8v4 layers ([P1] §プリセット: FP8 keys with 4-bit TurboQuant values, the
+ *  error of the method coming almost entirely from the keys) store each key
+ *  coordinate as FP8 E4M3 (no rotation, no scale) and the values as above;
+ *  decode scores s_t = sm_scale <q, fp8(k_t)> with the raw query and keeps the
+ *  rotated-domain value sum and the one inverse rotation per query head.
  *
  * ------------------------------------------------------------------------
  * Readings of the pages (they leave these open; the library and the oracle
@@ -58,6 +63,10 @@
  *    max |delta c| < 1e-15; centroids emitted in fp32 with the upper half
  *    mirrored (c[2^b-1-i] = -c[i] exactly); boundaries
  *    beta_i = fp32(fp32(c_i + c_{i+1}) * 0.5).
+ *  FP8 keys (k8v4): E4M3 -- sign, 4 exponent bits with bias 7, 3 mantissa
+ *    bits, subnormals m 2^-9, no infinities, S.1111.111 = NaN, largest finite
+ *    448; encoding rounds to nearest, ties to even, and saturates finite
+ *    overflow and infinities to +-448 (NaN stays NaN).
  *  Packing: LSB-first bitstream; code j in bits [b j, b j + b) of the record,
  *    bit k of a record = bit (k mod 8) of byte (k div 8).  For b = 4 this is
  *    the 'codes[i] | codes[i+1] << 4' of [P4]'s worked example.
@@ -73,6 +82,8 @@
  *      keys with QJL add: [16 x d/8 sign bytes][16 x fp32 rho]
  *    d = 128: 1088 B (4-bit), 832 B (3-bit), 576 B (2-bit), 896 B (2-bit+QJL).
  *  bf16 pool: [num_blocks][num_kv_heads][16][d] bf16 (4096 B per page).
+ *  k8v4 key pool: [num_blocks][num_kv_heads][16][d] FP8 E4M3 bytes (2048 B
+ *  per page, nothing else); its value pool is a packed pool of bits_v.
  *  Pools must be 16-byte aligned.
  *
  * ------------------------------------------------------------------------
@@ -125,7 +136,7 @@ enum { TQ_F32 = 0, TQ_BF16 = 1 };
 enum { TQ_ROT_HADAMARD = 1, TQ_ROT_DENSE = 2, TQ_RNG_QJL = 3 };
 
 /* layer storage */
-enum { TQ_KV_PACKED = 0, TQ_KV_BF16 = 1 };
+enum { TQ_KV_PACKED = 0, TQ_KV_BF16 = 1, TQ_KV_K8V4 = 2 };
 
 /* norm handling */
 enum { TQ_NORM_CORRECTED = 0, TQ_NORM_RAW = 1 };
@@ -140,11 +151,11 @@ enum {
 };
 
 typedef struct {
-  int32_t kv_format; /* TQ_KV_PACKED or TQ_KV_BF16 */
-  int32_t bits_k;    /* packed: 2, 3 or 4 */
-  int32_t bits_v;    /* packed: 2, 3 or 4 */
-  int32_t qjl_k;     /* packed: 1 = keys carry the 1-bit QJL residual (m = head_dim) */
-  int32_t rot_kind;  /* packed: TQ_ROT_HADAMARD or TQ_ROT_DENSE */
+  int32_t kv_format; /* TQ_KV_PACKED, TQ_KV_BF16 or TQ_KV_K8V4 */
+  int32_t bits_k;    /* packed: 2, 3 or 4; k8v4: 8 (FP8 E4M3 keys) */
+  int32_t bits_v;    /* packed and k8v4: 2, 3 or 4 */
+  int32_t qjl_k;     /* packed: 1 = keys carry the 1-bit QJL residual (m = head_dim); k8v4: 0 */
+  int32_t rot_kind;  /* packed and k8v4 (values): TQ_ROT_HADAMARD or TQ_ROT_DENSE */
   int32_t norm_mode; /* TQ_NORM_CORRECTED or TQ_NORM_RAW */
 } tq_layer_format;
 

@@ -11,18 +11,21 @@ for every sequence b and query head h (KV head h // g, g = H_q / H_kv),
 
 with token t of sequence b stored at slot block_table[b][t // 16] * 16 + t % 16.
 bf16 layers ([P1] §起動コマンド: first/last two layers kept at full precision;
-[P4] layout table: 512 B/token/head) use the raw bf16 K and V.
+[P4] layout table: 512 B/token/head) use the raw bf16 K and V.  k8v4 layers
+([P1] §プリセット: FP8 keys, 4-bit values) use the FP8 E4M3 keys as stored
+(no rotation) with the raw query, and the decoded 4-bit values.
 
 This is exact softmax attention (max-subtracted, one pass over all tokens), no
 online/split evaluation.  Pinned by (tests/test_oracle_attention.py): one token
 gives o = v_hat; identical keys give the mean of v_hat; Pi = I and 8-bit
 codebook-free raw bf16 reduce to scipy.special.softmax attention; a
-hand-computed two-token case.
+hand-computed two-token case; the k8v4 gather returns exactly the encoded
+keys and the decoded values of the records it was handed.
 """
 
 import numpy as np
 
-from . import pack, qjl as qjl_mod
+from . import fp8, pack, qjl as qjl_mod
 from .quantize import bf16_bits_to_f64
 
 
@@ -135,6 +138,40 @@ def decode_bf16(q, k_pool_u16, v_pool_u16, num_blocks, num_kv_heads, block_table
             continue
         for kvh in range(num_kv_heads):
             k, v = gather_bf16(k_pool_u16, v_pool_u16, num_blocks, num_kv_heads, d, block_table[b], ctx, kvh)
+            for h in range(kvh * g, (kvh + 1) * g):
+                out[b, h] = softmax_attention(q[b, h], k, v, sm_scale)
+    return out
+
+
+def gather_k8v4(k_pool, v_pool, layer, num_blocks, num_kv_heads, d, block_table_row, ctx, head):
+    """One (sequence, kv head) of a k8v4 layer: FP8 E4M3 keys as stored (no rotation,
+    no scale) and the 4-bit (bits_v) TurboQuant values decoded to x_hat; [ctx, d] each."""
+    kp = pack.pool_pages(k_pool, num_blocks, num_kv_heads, fp8.page_bytes(d))
+    vp = pack.pool_pages(v_pool, num_blocks, num_kv_heads, pack.page_bytes(d, layer.bits_v))
+    slots = token_slots(block_table_row, ctx)
+    blocks = slots // pack.BLOCK
+    toks = slots % pack.BLOCK
+    krec = kp[blocks, head].reshape(ctx, pack.BLOCK, d)[np.arange(ctx), toks]
+    vf = pack.split_pages(vp[blocks, head], d, layer.bits_v)
+    sel = np.arange(ctx)
+    v_idx = vf[0][sel, toks]
+    v_gamma = vf[1][sel, toks]
+    return fp8.decode(krec), (layer.cb_v[v_idx] * v_gamma[:, None]) @ layer.pi
+
+
+def decode_k8v4(q, k_pool, v_pool, layer, num_blocks, num_kv_heads, block_table, context_lens, sm_scale):
+    """q [B, H_q, d] f64 -> out [B, H_q, d] f64 over a k8v4 layer: exact softmax
+    attention of the raw query against the FP8 keys, values from their codes."""
+    q = np.asarray(q, dtype=np.float64)
+    bsz, hq, d = q.shape
+    g = hq // num_kv_heads
+    out = np.zeros_like(q)
+    for b in range(bsz):
+        ctx = int(context_lens[b])
+        if ctx == 0:
+            continue
+        for kvh in range(num_kv_heads):
+            k, v = gather_k8v4(k_pool, v_pool, layer, num_blocks, num_kv_heads, d, block_table[b], ctx, kvh)
             for h in range(kvh * g, (kvh + 1) * g):
                 out[b, h] = softmax_attention(q[b, h], k, v, sm_scale)
     return out

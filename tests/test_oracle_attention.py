@@ -103,3 +103,40 @@ def test_bf16_layer_and_empty_context():
     vals = np.concatenate([vv[3, 1], vv[1, 1, :4]])
     assert np.allclose(out[0, 3], special.softmax(0.2 * keys @ q[0, 3]) @ vals, atol=1e-13)
     assert np.all(out[1] == 0.0)
+
+
+def test_k8v4_layer_is_plain_attention_over_fp8_keys():
+    """k8v4 pools built by hand (FP8 key records, 4-bit value records): the oracle's
+    decode equals scipy softmax attention of the raw query against the FP8-decoded
+    keys, with the decoded values; the gather returns the written key bytes."""
+    from oracle import fp8
+    d, heads, ctx, nb = 128, 2, 37, 5
+    g = np.random.default_rng(12)
+    pi = rotation.hadamard_rotation_seeded(4, 2, d)
+    bt = np.array([[3, 0, 4]], np.int32)
+    xk = g.standard_normal((1, 48, heads, d)) * 3.0
+    xv = g.standard_normal((1, 48, heads, d))
+    cv, bv = cb.codebook_fp32(d, 4)
+    kp = np.zeros(nb * heads * fp8.page_bytes(d), np.uint8)
+    vp = np.zeros(nb * heads * pack.page_bytes(d, 4), np.uint8)
+    slots = oa.token_slots(bt[0], ctx)
+    kbytes = fp8.encode(xk[0, :ctx])  # [ctx, heads, d]
+    for h in range(heads):
+        iv, gv, _ = oq.quantize(xv[0, :ctx, h], pi, cv, bv)
+        for t in range(ctx):
+            s = int(slots[t])
+            o = pack.page_offset(s // 16, h, heads, fp8.page_bytes(d)) + (s % 16) * d
+            kp[o: o + d] = kbytes[t, h]
+            pack.write_record(vp, s, h, heads, d, 4, iv[t], gv[t])
+    layer = oa.PackedLayer(pi, cv, cv, 4, 4)
+    q = g.standard_normal((1, 4, d))
+    out = oa.decode_k8v4(q, kp, vp, layer, nb, heads, bt, np.array([ctx]), 0.1)
+    for h in range(heads):
+        k, v = oa.gather_k8v4(kp, vp, layer, nb, heads, d, bt[0], ctx, h)
+        assert np.array_equal(fp8.encode(k), kbytes[:, h])
+        iv, gv, _ = oq.quantize(xv[0, :ctx, h], pi, cv, bv)
+        g32 = gv.astype(np.float32).astype(np.float64)  # the page holds gamma in fp32
+        assert np.allclose(v, oq.dequantize(iv, g32, pi, cv), rtol=0, atol=1e-12)
+        for hq in (2 * h, 2 * h + 1):
+            ref = special.softmax(0.1 * (fp8.decode(kbytes[:, h]) @ q[0, hq])) @ v
+            assert np.allclose(out[0, hq], ref, rtol=1e-12, atol=1e-12)
