@@ -167,3 +167,28 @@ def test_make_args_rejected(tqlib):
     out = (ctypes.c_float * 128)()
     assert lib.tq_make_rotation(tqlib.TQ_ROT_HADAMARD, 96, 0, 0, out) == tqlib.TQ_ERR_INVALID_ARG
     assert lib.tq_make_rotation(9, 128, 0, 0, out) == tqlib.TQ_ERR_INVALID_ARG
+
+
+def test_k8v4_descriptor(tqlib):
+    """k8v4 layers: FP8 key pages of 16 x 128 bytes, packed value pages; keys must be
+    declared 8-bit, without QJL; the key codebook is not used."""
+    tq = tqlib
+    lib = tq.lib()
+    d = fake_desc(tq, kv_format=tq.TQ_KV_K8V4, bits_k=8)
+    for i in range(16):
+        d.centroids_k[i] = 0.0  # ignored for FP8 keys
+    assert lib.tq_page_bytes(ctypes.byref(d), 0) == 2048
+    assert lib.tq_page_bytes(ctypes.byref(d), 1) == 1088
+    launches0 = tq.launch_count()
+
+    def append(desc):
+        return lib.tq_quantize_append(ctypes.byref(desc), ctypes.c_void_p(0x1000), None, tq.TQ_F32,
+                                      ctypes.c_void_p(0x2000), 4, None)
+
+    assert append(fake_desc(tq, kv_format=tq.TQ_KV_K8V4, bits_k=4)) == tq.TQ_ERR_INVALID_ARG
+    assert "bits_k" in tq.last_error()
+    assert append(fake_desc(tq, kv_format=tq.TQ_KV_K8V4, bits_k=8, qjl_k=1)) == tq.TQ_ERR_INVALID_ARG
+    bad = fake_desc(tq, kv_format=tq.TQ_KV_K8V4, bits_k=8)
+    bad.centroids_v[2] = bad.centroids_v[2] * 1.5  # breaks the value codebook
+    assert append(bad) == tq.TQ_ERR_INVALID_ARG
+    assert tq.launch_count() == launches0

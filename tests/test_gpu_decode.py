@@ -394,3 +394,25 @@ def test_config5_layers_full_size_sampled(cuda, tqlib, variant):
     err = _sampled_err(tq, layer, out, q, bt, ctx, ((0, 1), (7, 6)), 1 / math.sqrt(D), Hq // Hkv)
     print("config 5 %s sampled max rel err %.3e" % (variant, err))
     assert err <= TOL_BF16
+
+
+def test_config4_dense_layer_full_size(cuda, tqlib):
+    """One layer of the dense-rotation workload at full size: 11,000 prefilled bf16
+    tokens x 8 KV heads scaled by lambda = 2.7 through the tensor-core append (a ragged
+    last block), then batch-1 decode with 32 query heads; every KV head checked."""
+    tq, torch = tqlib, cuda
+    B, Hq, Hkv, T = 1, 32, 8, 11000
+    bt, nb = workloads.shuffled_block_table(41, B, -(-T // 16))
+    layer = tq.Layer(nb, Hkv, rot_kind=tq.TQ_ROT_DENSE, seed=36, layer=4)
+    gen = torch.Generator(device="cuda").manual_seed(44)
+    k, v = _gpu_kv(torch, gen, B * T, Hkv, heavy=False)
+    k, v = (k.float() * 2.7).to(torch.bfloat16), (v.float() * 2.7).to(torch.bfloat16)
+    layer.append(k, v, torch.from_numpy(workloads.prefill_slots(bt, T)).cuda())
+    ctx = np.full(B, T, np.int32)
+    q = torch.randn(B, Hq, D, generator=gen, device="cuda").to(torch.bfloat16)
+    out = layer.decode(q, torch.from_numpy(bt).cuda(), torch.from_numpy(ctx).cuda(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tq.get_device_status() == 0
+    err = _sampled_err(tq, layer, out, q, bt, ctx, tuple((0, h) for h in range(Hkv)), 1 / math.sqrt(D), Hq // Hkv)
+    print("config 4 layer max rel err %.3e" % err)
+    assert err <= TOL_BF16

@@ -12,6 +12,6 @@ from ._binding import (  # noqa: F401
     LIB_PATH, STATUS_NAMES,
     TQ_BF16, TQ_BLOCK_SIZE, TQ_DEV_BAD_BLOCK, TQ_DEV_BAD_CONTEXT, TQ_DEV_BAD_SLOT, TQ_DEV_WAIT_TIMEOUT,
     TQ_ERR_CUDA, TQ_ERR_DEVICE, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_VERSION, TQ_ERR_WORKSPACE,
-    TQ_F32, TQ_FORMAT_VERSION, TQ_HEAD_DIM, TQ_KV_BF16, TQ_KV_PACKED, TQ_MAX_GROUP, TQ_NORM_CORRECTED,
+    TQ_F32, TQ_FORMAT_VERSION, TQ_HEAD_DIM, TQ_KV_BF16, TQ_KV_K8V4, TQ_KV_PACKED, TQ_MAX_GROUP, TQ_NORM_CORRECTED,
     TQ_NORM_RAW, TQ_OK, TQ_RNG_QJL, TQ_ROT_DENSE, TQ_ROT_HADAMARD,
 )

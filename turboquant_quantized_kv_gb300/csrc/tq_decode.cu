@@ -27,6 +27,8 @@
 //                bf16 layers use the same skeleton with bf16 MMAs on raw pages.
 //   k_combine    CTA per (sequence, query head): log-sum-exp merge of the
 //                chunks and the inverse rotation.
+#include <cuda_fp8.h>
+
 #include <cfloat>
 
 #include "tq_async.cuh"
@@ -99,6 +101,12 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 // with `lbase` = 0x10000 | lane * 4 (+128) gives the address directly.
 constexpr uint32_t kLutAddr = 0x10000u;
 constexpr uint32_t kLutBytes = 0x10000u;
+
+// Two FP8 E4M3 values (low byte first) as an f16x2 word (exact: E4M3 is a subset of fp16).
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
 
 __device__ __forceinline__ uint32_t lut(uint32_t lbase, uint32_t w, int k) {
   return lds32(__byte_perm(w, lbase, 0x7604u | ((uint32_t)k << 4)));
@@ -545,9 +553,6 @@ __device__ __forceinline__ void packed_keys(const WarpConsts<NT>& wc, const uint
   // ---- keys: 8 k-chunks in KC independent accumulation chains per n-tile (the
   // two blocks of a step give the scheduler a second independent set)
   constexpr int KC = 2;
-  uint32_t kn[2][4];
-  load_quarter<BK>(sk + g_ * RK, tig, kn[0]);
-  load_quarter<BK>(sk + (g_ + 8) * RK, tig, kn[1]);
   float dk[NT][KC][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -555,14 +560,35 @@ __device__ __forceinline__ void packed_keys(const WarpConsts<NT>& wc, const uint
     for (int p = 0; p < KC; ++p)
 #pragma unroll
       for (int e = 0; e < 4; ++e) dk[nt][p][e] = 0.0f;
+  if constexpr (BK == 8) {
+    // FP8 E4M3 keys (k8v4): byte j of a record is coordinate j; word c of the lane's
+    // 32 bytes holds coordinates 32 tig + 4c .. 4c + 3, the same k order as the codes
+    const uint4* r0 = reinterpret_cast<const uint4*>(sk + g_ * RK + 32 * tig);
+    const uint4* r1 = reinterpret_cast<const uint4*>(sk + (g_ + 8) * RK + 32 * tig);
+    const uint4 p0 = r0[0], p1 = r0[1], p2 = r1[0], p3 = r1[1];
+    const uint32_t kw0[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const uint32_t kw1[8] = {p2.x, p2.y, p2.z, p2.w, p3.x, p3.y, p3.z, p3.w};
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const int wi = c >> 1, bi = 2 * (c & 1);
-    const uint32_t ak[4] = {lut(wc.lk, kn[0][wi], bi), lut(wc.lk, kn[1][wi], bi), lut(wc.lk, kn[0][wi], bi + 1),
-                            lut(wc.lk, kn[1][wi], bi + 1)};
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t ak[4] = {fp8x2_to_f16x2(kw0[c] & 0xFFFFu), fp8x2_to_f16x2(kw1[c] & 0xFFFFu),
+                              fp8x2_to_f16x2(kw0[c] >> 16), fp8x2_to_f16x2(kw1[c] >> 16)};
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-      mma_f16(dk[nt][c % KC], ak, wc.bq[nt][c][0], wc.bq[nt][c][1], dk[nt][c % KC]);
+      for (int nt = 0; nt < NT; ++nt)
+        mma_f16(dk[nt][c % KC], ak, wc.bq[nt][c][0], wc.bq[nt][c][1], dk[nt][c % KC]);
+    }
+  } else {
+    uint32_t kn[2][4];
+    load_quarter<BK>(sk + g_ * RK, tig, kn[0]);
+    load_quarter<BK>(sk + (g_ + 8) * RK, tig, kn[1]);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int wi = c >> 1, bi = 2 * (c & 1);
+      const uint32_t ak[4] = {lut(wc.lk, kn[0][wi], bi), lut(wc.lk, kn[1][wi], bi), lut(wc.lk, kn[0][wi], bi + 1),
+                              lut(wc.lk, kn[1][wi], bi + 1)};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma_f16(dk[nt][c % KC], ak, wc.bq[nt][c][0], wc.bq[nt][c][1], dk[nt][c % KC]);
+    }
   }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -596,7 +622,7 @@ __device__ __forceinline__ void packed_keys(const WarpConsts<NT>& wc, const uint
   }
   const float* gk = reinterpret_cast<const float*>(sk + 16 * RK);
   const float* gv = reinterpret_cast<const float*>(sv + 16 * RV);
-  const float gk0 = gk[g_], gk1 = gk[g_ + 8];
+  const float gk0 = BK == 8 ? 1.0f : gk[g_], gk1 = BK == 8 ? 1.0f : gk[g_ + 8];  // FP8 keys carry no norm
   const bool in0 = !MASKED || (valid && t0 + g_ < ctx), in1 = !MASKED || (valid && t0 + g_ + 8 < ctx);
   wv[o] = in0 ? gv[g_] : 0.0f;
   wv[o + 1] = in1 ? gv[g_ + 8] : 0.0f;
@@ -1387,15 +1413,21 @@ Codebook codebook_of(const tq_cache_desc& d, int which);
 // Warps per decode CTA (one CTA per SM, NW a multiple of 4): packed codes without
 // QJL run 16 warps at 128 registers for groups of up to 4 heads and 12 warps for 8;
 // the QJL variant and bf16 pages run 8 warps with more registers.
-constexpr int decode_nw(bool packed_plain, int nt) { return packed_plain ? (nt == 1 ? 16 : 12) : 8; }
+// Warps per decode CTA: 16 for packed pages with groups of <= 4 query heads, 12
+// for groups of 8 and for FP8 keys (larger stages: 12 four-stage rings fit), 8 for
+// QJL keys and bf16 pages.
+constexpr int decode_nw(bool packed_plain, int nt, bool fp8_keys = false) {
+  return packed_plain ? ((nt == 1 && !fp8_keys) ? 16 : 12) : 8;
+}
 
 int decode_warps(const tq_cache_desc& d, int g) {
-  return decode_nw(d.fmt.kv_format == TQ_KV_PACKED && !d.fmt.qjl_k, g <= 4 ? 1 : 2);
+  const bool k8 = d.fmt.kv_format == TQ_KV_K8V4;
+  return decode_nw((d.fmt.kv_format == TQ_KV_PACKED && !d.fmt.qjl_k) || k8, g <= 4 ? 1 : 2, k8);
 }
 
 template <int KIND, int BK, int BV, bool QJL, int NT>
 static cudaError_t run_decode_nt(DecodeArgs a, cudaStream_t st) {
-  constexpr int NW = decode_nw(KIND == 0 && !QJL, NT);
+  constexpr int NW = decode_nw(KIND == 0 && !QJL, NT, BK == 8);
   auto kern = k_decode<KIND, BK, BV, QJL, NT, NW>;
   int dev = 0, optin = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1439,18 +1471,22 @@ static cudaError_t dispatch_bv(const DecodeArgs& a, int bv, cudaStream_t st) {
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   const tq_cache_desc& d = *c.desc;
   const bool bf16 = d.fmt.kv_format == TQ_KV_BF16;
-  const bool qjl = !bf16 && d.fmt.qjl_k;
+  const bool k8 = d.fmt.kv_format == TQ_KV_K8V4;  // FP8 keys (unrotated) with packed values
+  const bool qjl = !bf16 && !k8 && d.fmt.qjl_k;
   const DecodeWorkspace ws = decode_workspace(c.batch, c.num_q_heads, c.splits, kD, qjl);
   float* qrot = reinterpret_cast<float*>(c.workspace + ws.qrot_off);
   float* uq = qjl ? qrot + (size_t)c.batch * c.num_q_heads * kD : nullptr;
+  // the output's inverse rotation is the values' rotation; the query is rotated like the
+  // keys, i.e. not at all for bf16 and FP8 keys
   const int kind = bf16 ? ROTQ_IDENTITY : (d.fmt.rot_kind == TQ_ROT_DENSE ? ROTQ_DENSE : ROTQ_HADAMARD);
+  const int kind_q = k8 ? ROTQ_IDENTITY : kind;
   const int64_t rows = (int64_t)c.batch * c.num_q_heads;
   const float scale = c.sm_scale * kLog2e;
   int* counters = reinterpret_cast<int*>(c.workspace + ws.cnt_off);
   // Hadamard and unrotated layers without QJL rotate q inside the decode kernel;
   // dense rotations and S q' (QJL) take a separate mat-vec pass first
   const bool q_aligned = (reinterpret_cast<uintptr_t>(c.q) & 15) == 0;
-  const int q_in_kernel = (!qjl && kind != ROTQ_DENSE && q_aligned) ? (kind == ROTQ_HADAMARD ? 1 : 2) : 0;
+  const int q_in_kernel = (!qjl && kind_q != ROTQ_DENSE && q_aligned) ? (kind_q == ROTQ_HADAMARD ? 1 : 2) : 0;
   // The chunk counters stay zero between calls (the decode kernel resets each unit's
   // counter when it completes the unit), so the separate pass is needed only for a
   // q mat-vec or for counters that do not fit the fixed region at the start of the
@@ -1464,10 +1500,10 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
     unsigned rgrid = (unsigned)((rot_rows + 3) / 4);
     if (rgrid == 0) rgrid = (unsigned)((n_counters + 127) / 128);
     if (c.q_dtype == TQ_F32)
-      k_rotate_q<float><<<rgrid, 128, 0, st>>>(reinterpret_cast<const float*>(c.q), rot_rows, kind, d.rotation,
+      k_rotate_q<float><<<rgrid, 128, 0, st>>>(reinterpret_cast<const float*>(c.q), rot_rows, kind_q, d.rotation,
                                                qjl ? d.qjl_proj : nullptr, scale, qrot, uq, counters, n_counters);
     else
-      k_rotate_q<__nv_bfloat16><<<rgrid, 128, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(c.q), rot_rows, kind,
+      k_rotate_q<__nv_bfloat16><<<rgrid, 128, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(c.q), rot_rows, kind_q,
                                                        d.rotation, qjl ? d.qjl_proj : nullptr, scale, qrot, uq,
                                                        counters, n_counters);
     count_launch();
@@ -1529,6 +1565,7 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
       switch (bk) {
         case 2: e = dispatch_bv<2, false>(a, bv, st); break;
         case 3: e = dispatch_bv<3, false>(a, bv, st); break;
+        case 8: e = dispatch_bv<8, false>(a, bv, st); break;  // FP8 keys (k8v4)
         default: e = dispatch_bv<4, false>(a, bv, st); break;
       }
     }

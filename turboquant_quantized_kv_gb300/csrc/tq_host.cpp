@@ -301,6 +301,7 @@ namespace tq {
 size_t page_bytes_of(const tq_cache_desc& d, int which) {
   const size_t blk = (size_t)d.block_size;
   if (d.fmt.kv_format == TQ_KV_BF16) return blk * (size_t)d.head_dim * 2;
+  if (d.fmt.kv_format == TQ_KV_K8V4 && which == 0) return blk * (size_t)d.head_dim;  // FP8 E4M3 keys
   const int bits = which == 0 ? d.fmt.bits_k : d.fmt.bits_v;
   size_t n = blk * (size_t)(d.head_dim * bits / 8) + blk * 4;
   if (which == 0 && d.fmt.qjl_k) n += blk * (size_t)(d.head_dim / 8) + blk * 4;
@@ -338,6 +339,17 @@ tq_status check_desc(const tq_cache_desc* d, bool need_data) {
   if (f.norm_mode != TQ_NORM_CORRECTED && f.norm_mode != TQ_NORM_RAW)
     return fail(TQ_ERR_INVALID_ARG, "norm_mode %d", f.norm_mode);
   if (f.kv_format == TQ_KV_BF16) return TQ_OK;
+  if (f.kv_format == TQ_KV_K8V4) {  // FP8 E4M3 keys, packed values
+    if (f.bits_k != 8) return fail(TQ_ERR_INVALID_ARG, "k8v4: bits_k %d must be 8", f.bits_k);
+    if (f.bits_v < 2 || f.bits_v > 4) return fail(TQ_ERR_INVALID_ARG, "k8v4: bits_v %d not in 2..4", f.bits_v);
+    if (f.qjl_k != 0) return fail(TQ_ERR_INVALID_ARG, "k8v4: keys carry no QJL residual");
+    if (f.rot_kind != TQ_ROT_HADAMARD && f.rot_kind != TQ_ROT_DENSE)
+      return fail(TQ_ERR_INVALID_ARG, "rot_kind %d", f.rot_kind);
+    if (need_data && !d->rotation) return fail(TQ_ERR_INVALID_ARG, "null rotation");
+    if (!table_ok(d->centroids_v, d->boundaries_v, f.bits_v))
+      return fail(TQ_ERR_INVALID_ARG, "value codebook is not increasing/antisymmetric with its midpoints");
+    return TQ_OK;
+  }
   if (f.kv_format != TQ_KV_PACKED) return fail(TQ_ERR_INVALID_ARG, "kv_format %d", f.kv_format);
   if (f.bits_k < 2 || f.bits_k > 4 || f.bits_v < 2 || f.bits_v > 4)
     return fail(TQ_ERR_INVALID_ARG, "bits_k %d / bits_v %d not in 2..4", f.bits_k, f.bits_v);

@@ -13,6 +13,8 @@
 // registers and 2 through quad shuffles.  A CTA of 256 threads handles tiles
 // of 64 vectors in a grid-stride loop.  Dense rotations and the QJL projection
 // are 128x128 mat-vecs against a padded copy of the matrix in shared memory.
+#include <cuda_fp8.h>
+
 #include <cmath>
 #include <cstring>
 
@@ -870,6 +872,63 @@ __global__ void __launch_bounds__(256) k_append_bf16(const TIn* __restrict__ x, 
   }
 }
 
+// k8v4 keys: each coordinate as FP8 E4M3 (nearest, ties to even, saturating at
+// +-448), 128-byte records, 16 per (block, KV head) page.  One thread per 16
+// coordinates (one 16-byte store).
+template <typename TIn>
+__global__ void __launch_bounds__(256) k_append_fp8(const TIn* __restrict__ x, const int64_t* __restrict__ slots,
+                                                    int64_t n_vec, int H, int64_t max_slot, uint8_t* pool,
+                                                    unsigned* status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // a dependent decode may start its prologue
+  const int64_t n_chunks = n_vec * 8;  // 16 coordinates per chunk
+  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n_chunks; c += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t vec = c >> 3;
+    const int part = (int)(c & 7);
+    const int64_t tok = vec / H;
+    const int head = (int)(vec - tok * H);
+    const int64_t slot = __ldg(slots + tok);
+    if (slot < 0) continue;
+    if (slot >= max_slot) {
+      if (part == 0) flag_status(status, TQ_DEV_BAD_SLOT);
+      continue;
+    }
+    const TIn* src = x + vec * kD + part * 16;
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+          make_float2(load_elem<TIn>(src + 4 * k), load_elem<TIn>(src + 4 * k + 1)), __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+          make_float2(load_elem<TIn>(src + 4 * k + 2), load_elem<TIn>(src + 4 * k + 3)), __NV_SATFINITE, __NV_E4M3);
+      w[k] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    uint8_t* page = pool + ((slot >> 4) * H + head) * (int64_t)(kBlock * kD);
+    *reinterpret_cast<uint4*>(page + (slot & 15) * kD + part * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <typename TOut>
+__global__ void __launch_bounds__(256) k_dequant_fp8(const uint8_t* __restrict__ pool, int H, int64_t max_slot,
+                                                     const int64_t* __restrict__ slots, int64_t n_vec, TOut* out,
+                                                     unsigned* status) {
+  const int64_t n = n_vec * kD;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t vec = e / kD;
+    const int j = (int)(e - vec * kD);
+    const int64_t tok = vec / H;
+    const int head = (int)(vec - tok * H);
+    const int64_t slot = __ldg(slots + tok);
+    float v = 0.0f;
+    if (slot >= 0 && slot < max_slot) {
+      const uint8_t b = pool[((slot >> 4) * H + head) * (int64_t)(kBlock * kD) + (slot & 15) * kD + j];
+      v = __half2float(__half(__nv_cvt_fp8_to_halfraw(b, __NV_E4M3)));
+    } else if (slot >= max_slot && j == 0) {
+      flag_status(status, TQ_DEV_BAD_SLOT);
+    }
+    store_elem<TOut>(out + e, v);
+  }
+}
+
 // Dequantize: x_hat = gamma Pi^T c[idx] (rotated-domain values, then the inverse rotation).
 template <int BITS, typename TOut, bool DENSE>
 __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t* __restrict__ pool, int page_bytes, int H,
@@ -1164,6 +1223,18 @@ cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, in
   const int64_t n_vec = n_tok * d.num_kv_heads;
   const int64_t max_slot = d.num_blocks * kBlock;
   uint8_t* pool = reinterpret_cast<uint8_t*>(which == 0 ? d.k_cache : d.v_cache);
+  if (d.fmt.kv_format == TQ_KV_K8V4 && which == 0) {  // FP8 keys
+    int64_t grid = (n_vec * 8 + 255) / 256;
+    if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
+    if (in_dtype == TQ_F32)
+      k_append_fp8<float><<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const float*>(x), slots, n_vec,
+                                                          d.num_kv_heads, max_slot, pool, status);
+    else
+      k_append_fp8<__nv_bfloat16><<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), slots,
+                                                                  n_vec, d.num_kv_heads, max_slot, pool, status);
+    count_launch();
+    return cudaGetLastError();
+  }
   if (d.fmt.kv_format == TQ_KV_BF16) {
     int64_t chunks = n_vec * 16;
     int64_t grid = (chunks + 255) / 256;
@@ -1249,6 +1320,20 @@ cudaError_t launch_dequant(const tq_cache_desc& d, int which, const int64_t* slo
                            int out_dtype, unsigned* status, int num_sms, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   const int64_t n_vec = n * d.num_kv_heads;
+  if (d.fmt.kv_format == TQ_KV_K8V4 && which == 0) {
+    const uint8_t* pool = reinterpret_cast<const uint8_t*>(d.k_cache);
+    int64_t grid = (n_vec * kD + 255) / 256;
+    if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
+    if (out_dtype == TQ_F32)
+      k_dequant_fp8<float><<<(unsigned)grid, 256, 0, st>>>(pool, d.num_kv_heads, d.num_blocks * kBlock, slots, n_vec,
+                                                          reinterpret_cast<float*>(out), status);
+    else
+      k_dequant_fp8<__nv_bfloat16><<<(unsigned)grid, 256, 0, st>>>(pool, d.num_kv_heads, d.num_blocks * kBlock, slots,
+                                                                  n_vec, reinterpret_cast<__nv_bfloat16*>(out),
+                                                                  status);
+    count_launch();
+    return cudaGetLastError();
+  }
   if (d.fmt.kv_format == TQ_KV_BF16) {
     const uint8_t* pool = reinterpret_cast<const uint8_t*>(which == 0 ? d.k_cache : d.v_cache);
     int64_t grid = (n_vec * kD + 255) / 256;
