@@ -12,8 +12,9 @@ than L2, so no flush is needed between steps.
 
 Reported: value = packed K/V bytes read by decode per step / step time (GB/s);
 roofline for the decode call; quantize-append vectors/s from the prefill and
-from the dense-rotation burst (36 layers x 11,000 tokens); e2e through the
-public API with host buffers; the oracle's CPU throughput.
+from the dense-rotation burst (36 layers x 11,000 tokens); decode GB/s of a
+k8v4 layer (FP8 keys, 4-bit values) at the same shape; e2e through the public
+API with host buffers; the oracle's CPU throughput.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
 """
@@ -185,6 +186,49 @@ def dense_burst(torch, tq, dev, peak):
             "gpu_launches": launches, "device_status": status}
 
 
+def decode_k8v4(torch, tq, dev, peak, reps=20):
+    """Decode on a k8v4 layer (FP8 E4M3 keys, 4-bit TurboQuant values) at the headline
+    shape (batch 16, 32/8 heads, context 8192, lognormal channels, shuffled table):
+    196 B per token and KV head (128 B of keys + 68 B value record), ~205.5 MB per
+    call, more than L2.  Median of `reps` calls timed with CUDA events."""
+    import workloads
+    mb = T0 // BLOCK + 1
+    bt_np, nb = workloads.shuffled_block_table(777, B, mb)
+    bt = torch.from_numpy(bt_np).to(dev)
+    layer = tq.Layer(nb, HKV, kv_format="k8v4", bits_v=4, seed=0, layer=0, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(778)
+    sk = torch.exp(torch.randn(HKV, D, generator=gen, device=dev))
+    sv = torch.exp(torch.randn(HKV, D, generator=gen, device=dev))
+    k = (torch.randn(B * T0, HKV, D, generator=gen, device=dev) * sk).to(torch.bfloat16)
+    v = (torch.randn(B * T0, HKV, D, generator=gen, device=dev) * sv).to(torch.bfloat16)
+    layer.append(k, v, torch.from_numpy(workloads.prefill_slots(bt_np, T0)).to(dev))
+    del k, v
+    q = torch.randn(B, HQ, D, generator=gen, device=dev).to(torch.bfloat16)
+    ctx = torch.full((B,), T0, dtype=torch.int32, device=dev)
+    out = torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(layer.workspace_bytes(B, HQ, mb), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        layer.decode(q, bt, ctx, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        layer.decode(q, bt, ctx, out=out, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    med = statistics.median(ms)
+    nbytes = B * HKV * T0 * (D + D * 4 // 8 + 4)
+    gbs = nbytes / (med * 1e-3) / 1e9
+    status = tq.get_device_status()
+    del layer
+    torch.cuda.empty_cache()
+    return {"workload": "k8v4 layer: B16 Hq32 Hkv8 d128 ctx8192, FP8 E4M3 keys + 4-bit values", "bytes": nbytes,
+            "ms": round(med, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "calls": reps,
+            "device_status": status}
+
+
 def step_prepare(torch, st):
     """ctx += 1 is done after the step; the new token goes to position ctx."""
     ctx64 = st["ctx"].to(torch.int64)
@@ -321,6 +365,7 @@ def run_tq(args):
     # end to end through the public API with host buffers (pinned), eager calls
     e2e = run_e2e(torch, st, args, stream) if args.e2e else None
     dense = dense_burst(torch, tq, dev, peak) if args.dense_burst else None
+    k8 = decode_k8v4(torch, tq, dev, peak) if args.k8v4 else None
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -337,6 +382,7 @@ def run_tq(args):
         "append": {"vectors_per_s": round(app_vps, 1), "gbs": round(app_gbs, 1), "frac": round(app_gbs / peak, 4),
                    "vectors": st["append_vectors"], "bytes_per_vector": APPEND_BYTES_PER_VECTOR},
         "append_dense_burst": dense,
+        "decode_k8v4": k8,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
@@ -497,6 +543,7 @@ def main():
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-k8v4", dest="k8v4", action="store_false", help="skip the k8v4 decode measurement")
     ap.add_argument("--no-dense-burst", dest="dense_burst", action="store_false",
                     help="skip the dense-rotation burst append (36 layers x 11000 tokens)")
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (profiling runs use fewer)")

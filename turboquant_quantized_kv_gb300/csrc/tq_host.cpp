@@ -366,12 +366,13 @@ tq_status check_desc(const tq_cache_desc* d, bool need_data) {
 }
 
 int auto_splits(int num_sms, int warps, int batch, int num_kv_heads, int max_blocks_per_seq) {
-  // One wave: about one chunk per decode warp of the GPU over (sequence, kv head
-  // group, split), each split keeping at least 8 blocks of context.
+  // One wave: at most one chunk per decode warp of the GPU over (sequence, kv head
+  // group, split) -- rounded down, since one chunk over makes a second wave of a
+  // few CTAs -- each split keeping at least 8 blocks of context.
   const long units = (long)batch * num_kv_heads;
   if (units <= 0 || max_blocks_per_seq <= 0) return 1;
   long target = (long)num_sms * warps;
-  long s = (target + units - 1) / units;
+  long s = target / units;
   long cap = (max_blocks_per_seq + 7) / 8;
   if (s > cap) s = cap;
   if (s < 1) s = 1;
