@@ -270,6 +270,41 @@ tq_status tq_append_decode(const tq_cache_desc* desc, const void* k, const void*
 tq_status tq_dequantize(const tq_cache_desc* desc, int which, const int64_t* slots, int64_t n, void* out,
                         int out_dtype, void* stream);
 
+/* ---- offload / restore ([P4]: LMCache copies BF16 and packed groups
+ * uninterpreted, restoring exactly what was stored, T(Q(X)) = Q(X), and the
+ * reader must know the format id and version of what it reads) -------------
+ *
+ * Image of n blocks of one layer (host memory, little-endian):
+ *   bytes 0..7 "TQKVIMG1"; 8..11 TQ_FORMAT_VERSION (uint32); 12..35 the layer
+ *   format (kv_format, bits_k, bits_v, qjl_k, rot_kind, norm_mode, int32);
+ *   36..47 head_dim, num_kv_heads, block_size (int32); 48..55 n (int64);
+ *   56..63 FNV-1a 64 of centroids_k[16], boundaries_k[15], centroids_v[16],
+ *   boundaries_v[15] as fp32 bytes; then the K pages of every KV head of the
+ *   listed blocks in the order listed, then their V pages in the same order.
+ * The rotation (and QJL projection) of the layer are not in the image: restore
+ * into a layer built with the same ones. */
+
+/* Bytes of the image of n_blocks blocks of this layer; 0 if invalid. */
+size_t tq_image_bytes(const tq_cache_desc* desc, int64_t n_blocks);
+
+/* Copies the pages of blocks[0..n) (host int32 array, each in [0, num_blocks))
+ * of both pools into image (host; pinned memory makes the copies asynchronous)
+ * after writing its header (written by the host before this call returns).
+ * Consecutive block ids are copied as one range.  image_bytes must be at least
+ * tq_image_bytes(desc, n).  Enqueued on the stream; the image is complete once
+ * the stream has reached this point. */
+tq_status tq_offload_blocks(const tq_cache_desc* desc, const int32_t* blocks, int64_t n, void* image,
+                            size_t image_bytes, void* stream);
+
+/* Checks the image header against the descriptor (magic, version, layer format,
+ * head_dim, num_kv_heads, block_size, n, codebook hash: TQ_ERR_VERSION for a
+ * version mismatch, TQ_ERR_INVALID_ARG for any other) and copies its pages into
+ * blocks[0..n) (host int32 array; the same or other blocks than were offloaded).
+ * Writes nothing else of the pools.  The image must stay valid until the
+ * stream has reached this point. */
+tq_status tq_restore_blocks(const tq_cache_desc* desc, const int32_t* blocks, int64_t n, const void* image,
+                            size_t image_bytes, void* stream);
+
 /* Bytes of the scratch array tq_decode_attention_static keeps on every device
  * that loads the library (held until the process exits). */
 #define TQ_STATIC_SCRATCH_BYTES (8u << 20)
