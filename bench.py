@@ -229,6 +229,32 @@ def decode_k8v4(torch, tq, dev, peak, reps=20):
             "device_status": status}
 
 
+def offload_restore(torch, st, reps=5):
+    """Offload every block of one benchmark layer (the pages of its K and V pools,
+    block ids in block-table order, i.e. shuffled) to a pinned host image and
+    restore them; median GB/s of each direction over `reps` rounds, timed with
+    CUDA events."""
+    layer = st["layers"][0]
+    blocks = st["bt_np"].reshape(-1)
+    image = layer.offload(blocks)
+    torch.cuda.synchronize()
+    nbytes = image.numel()
+    d2h, h2d = [], []
+    for _ in range(reps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        layer.offload(blocks, image=image)
+        e[1].record()
+        layer.restore(blocks, image)
+        e[2].record()
+        torch.cuda.synchronize()
+        d2h.append(nbytes / (e[0].elapsed_time(e[1]) * 1e-3) / 1e9)
+        h2d.append(nbytes / (e[1].elapsed_time(e[2]) * 1e-3) / 1e9)
+    return {"workload": "all %d blocks of one layer (K and V pages, shuffled ids) to a pinned host image and back"
+                        % blocks.size, "bytes": nbytes, "offload_gbs": round(statistics.median(d2h), 1),
+            "restore_gbs": round(statistics.median(h2d), 1)}
+
+
 def step_prepare(torch, st):
     """ctx += 1 is done after the step; the new token goes to position ctx."""
     ctx64 = st["ctx"].to(torch.int64)
@@ -366,6 +392,7 @@ def run_tq(args):
     e2e = run_e2e(torch, st, args, stream) if args.e2e else None
     dense = dense_burst(torch, tq, dev, peak) if args.dense_burst else None
     k8 = decode_k8v4(torch, tq, dev, peak) if args.k8v4 else None
+    off = offload_restore(torch, st) if args.offload else None
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -383,6 +410,7 @@ def run_tq(args):
                    "vectors": st["append_vectors"], "bytes_per_vector": APPEND_BYTES_PER_VECTOR},
         "append_dense_burst": dense,
         "decode_k8v4": k8,
+        "offload_restore": off,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
@@ -544,6 +572,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-k8v4", dest="k8v4", action="store_false", help="skip the k8v4 decode measurement")
+    ap.add_argument("--no-offload", dest="offload", action="store_false", help="skip the offload/restore measurement")
     ap.add_argument("--no-dense-burst", dest="dense_burst", action="store_false",
                     help="skip the dense-rotation burst append (36 layers x 11000 tokens)")
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (profiling runs use fewer)")

@@ -288,11 +288,11 @@ tq_status tq_dequantize(const tq_cache_desc* desc, int which, const int64_t* slo
 size_t tq_image_bytes(const tq_cache_desc* desc, int64_t n_blocks);
 
 /* Copies the pages of blocks[0..n) (host int32 array, each in [0, num_blocks))
- * of both pools into image (host; pinned memory makes the copies asynchronous)
- * after writing its header (written by the host before this call returns).
- * Consecutive block ids are copied as one range.  image_bytes must be at least
- * tq_image_bytes(desc, n).  Enqueued on the stream; the image is complete once
- * the stream has reached this point. */
+ * of both pools into image after writing its header (by the host, before this
+ * call returns).  image: pinned (or managed) host memory, 16-byte aligned: the
+ * pages are copied by a kernel through the image's device address.
+ * image_bytes must be at least tq_image_bytes(desc, n).  Enqueued on the
+ * stream; the image is complete once the stream has reached this point. */
 tq_status tq_offload_blocks(const tq_cache_desc* desc, const int32_t* blocks, int64_t n, void* image,
                             size_t image_bytes, void* stream);
 
@@ -300,8 +300,9 @@ tq_status tq_offload_blocks(const tq_cache_desc* desc, const int32_t* blocks, in
  * head_dim, num_kv_heads, block_size, n, codebook hash: TQ_ERR_VERSION for a
  * version mismatch, TQ_ERR_INVALID_ARG for any other) and copies its pages into
  * blocks[0..n) (host int32 array; the same or other blocks than were offloaded).
- * Writes nothing else of the pools.  The image must stay valid until the
- * stream has reached this point. */
+ * image: pinned (or managed) host memory as for tq_offload_blocks.  Writes
+ * nothing else of the pools.  The image must stay valid until the stream has
+ * reached this point. */
 tq_status tq_restore_blocks(const tq_cache_desc* desc, const int32_t* blocks, int64_t n, const void* image,
                             size_t image_bytes, void* stream);
 

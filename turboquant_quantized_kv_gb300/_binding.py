@@ -77,6 +77,11 @@ _SIGNATURES = {
                                         ctypes.c_int, ctypes.c_void_p]),
     "tq_dequantize": (ctypes.c_int, [_D, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                      ctypes.c_int, ctypes.c_void_p]),
+    "tq_image_bytes": (ctypes.c_size_t, [_D, ctypes.c_int64]),
+    "tq_offload_blocks": (ctypes.c_int, [_D, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
+                                         ctypes.c_void_p]),
+    "tq_restore_blocks": (ctypes.c_int, [_D, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
+                                         ctypes.c_void_p]),
     "tq_get_device_status": (ctypes.c_int, [ctypes.c_void_p, _P(ctypes.c_int32)]),
     "tq_last_error": (ctypes.c_char_p, []),
     "tq_format_version": (ctypes.c_uint32, []),
@@ -309,6 +314,33 @@ class Layer:
                                       _ptr(out, "out"), _dtype_code(out), _ptr(workspace, "workspace"),
                                       workspace.numel(), num_splits, _stream(stream)))
         return out
+
+    def image_bytes(self, n_blocks):
+        n = lib().tq_image_bytes(ctypes.byref(self.desc), int(n_blocks))
+        if n == 0:
+            raise TQError(TQ_ERR_INVALID_ARG, last_error() or "invalid descriptor")
+        return int(n)
+
+    def offload(self, blocks, image=None, stream=None):
+        """Host image (pinned uint8 tensor) of the pages of `blocks` (block ids), see
+        tq_offload_blocks.  The image is complete once the stream reaches this call."""
+        torch = _torch()
+        ids = np.ascontiguousarray(np.asarray(blocks, dtype=np.int32).reshape(-1))
+        if image is None:
+            image = torch.empty(self.image_bytes(ids.size), dtype=torch.uint8, pin_memory=True)
+        if image.is_cuda:
+            raise ValueError("image must be a host (pinned) tensor")
+        _check(lib().tq_offload_blocks(ctypes.byref(self.desc), ids.ctypes.data_as(ctypes.c_void_p), ids.size,
+                                       ctypes.c_void_p(image.data_ptr()), image.numel(), _stream(stream)))
+        return image
+
+    def restore(self, blocks, image, stream=None):
+        """Copies an image's pages into `blocks` (tq_restore_blocks)."""
+        ids = np.ascontiguousarray(np.asarray(blocks, dtype=np.int32).reshape(-1))
+        if image.is_cuda:
+            raise ValueError("image must be a host (pinned) tensor")
+        _check(lib().tq_restore_blocks(ctypes.byref(self.desc), ids.ctypes.data_as(ctypes.c_void_p), ids.size,
+                                       ctypes.c_void_p(image.data_ptr()), image.numel(), _stream(stream)))
 
     def dequantize(self, which, slots, out_dtype=None, stream=None):
         """x_hat [n, H_kv, d] of the K (which=0) or V (which=1) records at slots [n] (int64)."""
