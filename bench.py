@@ -255,6 +255,68 @@ def offload_restore(torch, st, reps=5):
             "restore_gbs": round(statistics.median(h2d), 1)}
 
 
+def incremental_dequant_baseline(torch, tq, st, dev, peak, reps=20):
+    """The incremental-dequant baseline the pages compare against: a bf16 running
+    cache (a bf16 layer) holding the dequantized keys and values of one benchmark
+    layer; per step the new token of every sequence is appended to the packed
+    layer, dequantized from it (tq_dequantize) and appended to the bf16 cache, and
+    decode runs over the bf16 cache (512 B per token and KV head).  Compared with
+    the fused step on the packed layer (tq_append_decode, 136 B per token and KV
+    head).  Medians of `reps` steps timed with CUDA events."""
+    import workloads
+    layer = st["layers"][0]
+    nb = st["nb"]
+    shadow = tq.Layer(nb, HKV, kv_format="bf16", device=dev)
+    # dequantize the whole context so far (prefill + the tokens of the timed steps) once
+    ctx_now = int(st["ctx"][0].item())
+    slots_all = torch.from_numpy(workloads.prefill_slots(st["bt_np"], ctx_now)).to(dev)
+    for i0 in range(0, slots_all.numel(), 1 << 16):
+        sl = slots_all[i0: i0 + (1 << 16)]
+        shadow.append(layer.dequantize(0, sl, out_dtype=torch.bfloat16), layer.dequantize(1, sl, out_dtype=torch.bfloat16),
+                      sl)
+    out = torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(shadow.workspace_bytes(B, HQ, st["mb"]), dtype=torch.uint8, device=dev)
+    q, knew, vnew, slot = st["q"][0], st["knew"][0], st["vnew"][0], st["slot_new"]
+    ctx = st["ctx"]
+
+    def baseline_step():
+        layer.append(knew, vnew, slot)
+        shadow.append(layer.dequantize(0, slot, out_dtype=torch.bfloat16), layer.dequantize(1, slot, out_dtype=torch.bfloat16),
+                      slot)
+        shadow.decode(q, st["bt"], ctx, out=out, workspace=ws)
+
+    def fused_step():
+        layer.append_decode(knew, vnew, slot, q, st["bt"], ctx, out=out, workspace=st["ws"], num_splits=SPLITS)
+
+    def bf16_decode():
+        shadow.decode(q, st["bt"], ctx, out=out, workspace=ws)
+
+    res = {}
+    for name, fn in (("baseline_step_ms", baseline_step), ("fused_step_ms", fused_step),
+                     ("bf16_decode_ms", bf16_decode)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        res[name] = round(statistics.median(ms), 4)
+    bf16_bytes = B * HKV * (int(ctx[0].item())) * 2 * D * 2
+    res["bf16_decode_gbs"] = round(bf16_bytes / (res["bf16_decode_ms"] * 1e-3) / 1e9, 1)
+    res["bf16_decode_frac"] = round(res["bf16_decode_gbs"] / peak, 4)
+    res["speedup_fused_vs_baseline"] = round(res["baseline_step_ms"] / res["fused_step_ms"], 3)
+    res["workload"] = ("one layer, B16 Hq32 Hkv8 d128 ctx8192: packed 4/4 cache + bf16 running cache of its "
+                       "dequantized contents; eager calls (launch gaps included)")
+    del shadow
+    torch.cuda.empty_cache()
+    return res
+
+
 def step_prepare(torch, st):
     """ctx += 1 is done after the step; the new token goes to position ctx."""
     ctx64 = st["ctx"].to(torch.int64)
@@ -393,6 +455,7 @@ def run_tq(args):
     dense = dense_burst(torch, tq, dev, peak) if args.dense_burst else None
     k8 = decode_k8v4(torch, tq, dev, peak) if args.k8v4 else None
     off = offload_restore(torch, st) if args.offload else None
+    incr = incremental_dequant_baseline(torch, tq, st, dev, peak) if args.incremental else None
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -411,6 +474,7 @@ def run_tq(args):
         "append_dense_burst": dense,
         "decode_k8v4": k8,
         "offload_restore": off,
+        "incremental_dequant_baseline": incr,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
@@ -573,6 +637,8 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-k8v4", dest="k8v4", action="store_false", help="skip the k8v4 decode measurement")
     ap.add_argument("--no-offload", dest="offload", action="store_false", help="skip the offload/restore measurement")
+    ap.add_argument("--no-incremental", dest="incremental", action="store_false",
+                    help="skip the incremental-dequant baseline measurement")
     ap.add_argument("--no-dense-burst", dest="dense_burst", action="store_false",
                     help="skip the dense-rotation burst append (36 layers x 11000 tokens)")
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (profiling runs use fewer)")

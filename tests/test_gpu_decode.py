@@ -416,3 +416,29 @@ def test_config4_dense_layer_full_size(cuda, tqlib):
     err = _sampled_err(tq, layer, out, q, bt, ctx, tuple((0, h) for h in range(Hkv)), 1 / math.sqrt(D), Hq // Hkv)
     print("config 4 layer max rel err %.3e" % err)
     assert err <= TOL_BF16
+
+
+def test_incremental_dequant_baseline_attends_the_same_tokens(cuda, tqlib):
+    """The incremental-dequant baseline (a bf16 running cache filled from
+    tq_dequantize, then bf16 decode) attends the same tokens as the fused decode on
+    the packed cache: equal up to the bf16 rounding of the dequantized values."""
+    tq, torch = tqlib, cuda
+    B, Hq, Hkv, T = 4, 16, 4, 700
+    bt, nb = workloads.shuffled_block_table(81, B, -(-T // 16))
+    layer = tq.Layer(nb, Hkv, seed=2, layer=6)
+    shadow = tq.Layer(nb, Hkv, kv_format="bf16")
+    kb, vb = workloads.scaled_gaussian_kv(82, B * T, Hkv, D)  # N(0, 1): logits of order 1
+    slots = torch.from_numpy(workloads.prefill_slots(bt, T)).cuda()
+    layer.append(torch.from_numpy(kb.view(np.int16)).cuda().view(torch.bfloat16),
+                 torch.from_numpy(vb.view(np.int16)).cuda().view(torch.bfloat16), slots)
+    shadow.append(layer.dequantize(0, slots, out_dtype=torch.bfloat16),
+                  layer.dequantize(1, slots, out_dtype=torch.bfloat16), slots)
+    q = torch.from_numpy(workloads.queries(83, B, Hq, D).view(np.int16)).cuda().view(torch.bfloat16)
+    ctx = torch.from_numpy(np.full(B, T, np.int32)).cuda()
+    bt_d = torch.from_numpy(bt).cuda()
+    o_packed = layer.decode(q, bt_d, ctx, out_dtype=torch.float32).cpu().numpy()
+    o_shadow = shadow.decode(q, bt_d, ctx, out_dtype=torch.float32).cpu().numpy()
+    assert tq.get_device_status() == 0
+    err = max_rel_err(o_shadow.reshape(-1, D), o_packed.reshape(-1, D))
+    print("incremental-dequant baseline vs fused: max rel err %.3e" % err)
+    assert err <= 1e-2  # bf16 rounding of the dequantized K/V; a wrong token would be O(1)
