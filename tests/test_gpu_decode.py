@@ -119,6 +119,12 @@ def test_qjl_keys(cuda, tqlib):
     assert_close(out, ref, TOL_BF16, [300, 129])
 
 
+def test_lmdeploy_layout_k3_qjl_v2(cuda, tqlib):
+    """LMDeploy's layout ([P1] §LMDeploy): 3-bit keys with the QJL residual, 2-bit values."""
+    out, ref, _ = run_case(cuda, tqlib, B=2, Hq=8, Hkv=2, ctx=[257, 90], bits_k=3, bits_v=2, qjl=True, seed=12)
+    assert_close(out, ref, TOL_BF16, [257, 90])
+
+
 def test_dense_rotation_layer(cuda, tqlib):
     out, ref, _ = run_case(cuda, tqlib, B=1, Hq=8, Hkv=2, ctx=[300], rot=tqlib.TQ_ROT_DENSE, seed=5, q_f32=True)
     assert_close(out, ref, TOL_BF16, [300])
