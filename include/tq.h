@@ -42,6 +42,27 @@
  *  coordinate as FP8 E4M3 (no rotation, no scale) and the values as above;
  *  decode scores s_t = sm_scale <q, fp8(k_t)> with the raw query and keeps the
  *  rotated-domain value sum and the one inverse rotation per query head.
+ *  Polar layers ([P3] "PolarQuant: 極座標変換で量子化定数を不要にする"): the
+ *  vector is rotated (Hadamard Pi), then turned into polar coordinates
+ *  recursively -- coordinate pairs give d/2 radii and d/2 angles, the radii
+ *  are paired again, ... -- until one radius and d - 1 angles remain; every
+ *  angle is quantized on one fixed uniform grid (no per-block constants) and
+ *  the radius is kept as fp16 (2 bytes per vector):
+ *      y = Pi x;  level 1: theta_{1,i} = atan2(y_{2i+1}, y_{2i}), i < d/2,
+ *      rho_{1,i} = |(y_{2i}, y_{2i+1})|;  level l >= 2:
+ *      theta_{l,i} = atan2(rho_{l-1,2i+1}, rho_{l-1,2i}) in [0, pi/2];
+ *      r = fp16(||x||) (round to nearest even).
+ *    Codes (b bits per angle): level 1 on the whole circle,
+ *      k = floor(phi / (2 pi / 2^b)), phi = theta + pi taken mod 2 pi in
+ *      [0, 2 pi) (theta = pi and theta = -pi give k = 0);
+ *    levels >= 2 on [0, pi/2]: k = min(floor(theta / (pi / 2^(b+1))), 2^b - 1).
+ *    A pair whose two entries are both zero has theta = 0.  Reconstruction
+ *    takes every angle at its cell's midpoint; coordinate j of the unit
+ *    direction is the product over levels l = 1..log2 d of cos(theta_hat) if
+ *    bit l-1 of j is 0, sin(theta_hat) if it is 1, for the level-l angle
+ *    number j >> l; x_hat = r Pi^T y_hat (||x_hat|| = r).  Decode scores are
+ *    s_t = sm_scale r_t <Pi q, y_hat_t>; values are summed in the rotated
+ *    domain as for the packed layers.
  *
  * ------------------------------------------------------------------------
  * Readings of the pages (they leave these open; the library and the oracle
@@ -84,6 +105,12 @@
  *  bf16 pool: [num_blocks][num_kv_heads][16][d] bf16 (4096 B per page).
  *  k8v4 key pool: [num_blocks][num_kv_heads][16][d] FP8 E4M3 bytes (2048 B
  *  per page, nothing else); its value pool is a packed pool of bits_v.
+ *  Polar pools (keys with bits_k, values with bits_v): one page per (block,
+ *  kv head) = [16 records of d*b/8 bytes][16 x fp16 radius]; record slot s
+ *  holds angle code s in the packed bitstream above, slots ordered by level
+ *  (level 1 angles 0..d/2-1, then level 2, ..., the last level's one angle at
+ *  slot d-2) and slot d-1 = 0.  d = 128: 1056 B (4-bit), 800 B (3-bit),
+ *  544 B (2-bit).
  *  Pools must be 16-byte aligned.
  *
  * ------------------------------------------------------------------------
@@ -136,7 +163,7 @@ enum { TQ_F32 = 0, TQ_BF16 = 1 };
 enum { TQ_ROT_HADAMARD = 1, TQ_ROT_DENSE = 2, TQ_RNG_QJL = 3 };
 
 /* layer storage */
-enum { TQ_KV_PACKED = 0, TQ_KV_BF16 = 1, TQ_KV_K8V4 = 2 };
+enum { TQ_KV_PACKED = 0, TQ_KV_BF16 = 1, TQ_KV_K8V4 = 2, TQ_KV_POLAR = 3 };
 
 /* norm handling */
 enum { TQ_NORM_CORRECTED = 0, TQ_NORM_RAW = 1 };
@@ -151,17 +178,19 @@ enum {
 };
 
 typedef struct {
-  int32_t kv_format; /* TQ_KV_PACKED, TQ_KV_BF16 or TQ_KV_K8V4 */
-  int32_t bits_k;    /* packed: 2, 3 or 4; k8v4: 8 (FP8 E4M3 keys) */
-  int32_t bits_v;    /* packed and k8v4: 2, 3 or 4 */
-  int32_t qjl_k;     /* packed: 1 = keys carry the 1-bit QJL residual (m = head_dim); k8v4: 0 */
-  int32_t rot_kind;  /* packed and k8v4 (values): TQ_ROT_HADAMARD or TQ_ROT_DENSE */
+  int32_t kv_format; /* TQ_KV_PACKED, TQ_KV_BF16, TQ_KV_K8V4 or TQ_KV_POLAR */
+  int32_t bits_k;    /* packed: 2, 3 or 4; k8v4: 8 (FP8 E4M3 keys); polar: 2, 3 or 4 bits per angle */
+  int32_t bits_v;    /* packed, k8v4 and polar: 2, 3 or 4 */
+  int32_t qjl_k;     /* packed: 1 = keys carry the 1-bit QJL residual (m = head_dim); k8v4, polar: 0 */
+  int32_t rot_kind;  /* packed and k8v4 (values): TQ_ROT_HADAMARD or TQ_ROT_DENSE; polar: TQ_ROT_HADAMARD */
   int32_t norm_mode; /* TQ_NORM_CORRECTED or TQ_NORM_RAW */
 } tq_layer_format;
 
 /* One descriptor per layer.  Codebooks travel by value; the tables must be
  * strictly increasing and antisymmetric (c[2^b-1-i] = -c[i], beta middle = 0),
- * as tq_make_codebook emits them.  Entries past 2^b (2^b - 1) are ignored. */
+ * as tq_make_codebook emits them.  Entries past 2^b (2^b - 1) are ignored.
+ * Polar and bf16 layers ignore the codebook fields (polar angle grids are
+ * fixed by the bit widths). */
 typedef struct {
   uint32_t format_version; /* TQ_FORMAT_VERSION */
   int32_t head_dim;        /* 128 */
