@@ -13,7 +13,8 @@ than L2, so no flush is needed between steps.
 Reported: value = packed K/V bytes read by decode per step / step time (GB/s);
 roofline for the decode call; quantize-append vectors/s from the prefill and
 from the dense-rotation burst (36 layers x 11,000 tokens); decode GB/s of a
-k8v4 layer (FP8 keys, 4-bit values) at the same shape; e2e through the public
+k8v4 layer (FP8 keys, 4-bit values) and the PolarQuant variant's append and
+decode (4-bit angles, fp16 radius) at the same shape; e2e through the public
 API with host buffers; the oracle's CPU throughput.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
@@ -227,6 +228,65 @@ def decode_k8v4(torch, tq, dev, peak, reps=20):
     return {"workload": "k8v4 layer: B16 Hq32 Hkv8 d128 ctx8192, FP8 E4M3 keys + 4-bit values", "bytes": nbytes,
             "ms": round(med, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "calls": reps,
             "device_status": status}
+
+
+def polar_layer(torch, tq, dev, peak, reps=20):
+    """The PolarQuant variant at the headline shape (batch 16, 32/8 heads, context
+    8192, lognormal channels, shuffled table, 4-bit angles): the prefill append of
+    2,097,152 vectors (256 B read + 66 B written each) and decode over 132 B per token
+    and KV head (~138.4 MB per call, more than L2).  Medians of CUDA-event timings."""
+    import workloads
+    mb = T0 // BLOCK + 1
+    bt_np, nb = workloads.shuffled_block_table(779, B, mb)
+    bt = torch.from_numpy(bt_np).to(dev)
+    layer = tq.Layer(nb, HKV, kv_format="polar", bits_k=4, bits_v=4, seed=0, layer=0, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(780)
+    sk = torch.exp(torch.randn(HKV, D, generator=gen, device=dev))
+    sv = torch.exp(torch.randn(HKV, D, generator=gen, device=dev))
+    k = (torch.randn(B * T0, HKV, D, generator=gen, device=dev) * sk).to(torch.bfloat16)
+    v = (torch.randn(B * T0, HKV, D, generator=gen, device=dev) * sv).to(torch.bfloat16)
+    slots = torch.from_numpy(workloads.prefill_slots(bt_np, T0)).to(dev)
+    for _ in range(3):
+        layer.append(k, v, slots)
+    torch.cuda.synchronize()
+    app = []
+    for _ in range(max(3, reps // 4)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        layer.append(k, v, slots)
+        e1.record()
+        torch.cuda.synchronize()
+        app.append(e0.elapsed_time(e1))
+    del k, v
+    q = torch.randn(B, HQ, D, generator=gen, device=dev).to(torch.bfloat16)
+    ctx = torch.full((B,), T0, dtype=torch.int32, device=dev)
+    out = torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(layer.workspace_bytes(B, HQ, mb), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        layer.decode(q, bt, ctx, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        layer.decode(q, bt, ctx, out=out, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    med = statistics.median(ms)
+    nbytes = B * HKV * T0 * 2 * (D * 4 // 8 + 2)
+    gbs = nbytes / (med * 1e-3) / 1e9
+    app_ms = statistics.median(app)
+    n_vec = 2 * B * T0 * HKV
+    app_gbs = n_vec * (2 * D + D * 4 // 8 + 2) / (app_ms * 1e-3) / 1e9
+    status = tq.get_device_status()
+    del layer
+    torch.cuda.empty_cache()
+    return {"workload": "polar layer: B16 Hq32 Hkv8 d128 ctx8192, 4-bit angles + fp16 radius (K and V)",
+            "decode_bytes": nbytes, "decode_ms": round(med, 4), "decode_gbs": round(gbs, 1),
+            "decode_frac": round(gbs / peak, 4), "append_vectors": n_vec, "append_ms": round(app_ms, 4),
+            "append_vectors_per_s": round(n_vec / (app_ms * 1e-3), 1), "append_gbs": round(app_gbs, 1),
+            "append_frac": round(app_gbs / peak, 4), "device_status": status}
 
 
 def offload_restore(torch, st, reps=5):
@@ -454,6 +514,7 @@ def run_tq(args):
     e2e = run_e2e(torch, st, args, stream) if args.e2e else None
     dense = dense_burst(torch, tq, dev, peak) if args.dense_burst else None
     k8 = decode_k8v4(torch, tq, dev, peak) if args.k8v4 else None
+    pol = polar_layer(torch, tq, dev, peak) if args.polar else None
     off = offload_restore(torch, st) if args.offload else None
     incr = incremental_dequant_baseline(torch, tq, st, dev, peak) if args.incremental else None
 
@@ -473,6 +534,7 @@ def run_tq(args):
                    "vectors": st["append_vectors"], "bytes_per_vector": APPEND_BYTES_PER_VECTOR},
         "append_dense_burst": dense,
         "decode_k8v4": k8,
+        "polar": pol,
         "offload_restore": off,
         "incremental_dequant_baseline": incr,
         "e2e": e2e,
@@ -637,6 +699,7 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-k8v4", dest="k8v4", action="store_false", help="skip the k8v4 decode measurement")
     ap.add_argument("--no-offload", dest="offload", action="store_false", help="skip the offload/restore measurement")
+    ap.add_argument("--no-polar", dest="polar", action="store_false", help="skip the PolarQuant-variant measurement")
     ap.add_argument("--no-incremental", dest="incremental", action="store_false",
                     help="skip the incremental-dequant baseline measurement")
     ap.add_argument("--no-dense-burst", dest="dense_burst", action="store_false",

@@ -192,3 +192,26 @@ def test_k8v4_descriptor(tqlib):
     bad.centroids_v[2] = bad.centroids_v[2] * 1.5  # breaks the value codebook
     assert append(bad) == tq.TQ_ERR_INVALID_ARG
     assert tq.launch_count() == launches0
+
+
+def test_polar_descriptor(tqlib):
+    """Polar layers: pages of 16 angle-code records + 16 fp16 radii; Hadamard only, no
+    QJL, 2..4 bits; the codebook fields are ignored."""
+    tq = tqlib
+    lib = tq.lib()
+    d = fake_desc(tq, kv_format=tq.TQ_KV_POLAR, bits_k=4, bits_v=3)
+    for i in range(16):
+        d.centroids_k[i] = d.centroids_v[i] = 0.0  # ignored
+    assert lib.tq_page_bytes(ctypes.byref(d), 0) == 1056
+    assert lib.tq_page_bytes(ctypes.byref(d), 1) == 800
+    assert lib.tq_page_bytes(ctypes.byref(fake_desc(tq, kv_format=tq.TQ_KV_POLAR, bits_k=2)), 0) == 544
+    launches0 = tq.launch_count()
+
+    def append(desc):
+        return lib.tq_quantize_append(ctypes.byref(desc), ctypes.c_void_p(0x1000), None, tq.TQ_F32,
+                                      ctypes.c_void_p(0x2000), 4, None)
+
+    assert append(fake_desc(tq, kv_format=tq.TQ_KV_POLAR, rot_kind=tq.TQ_ROT_DENSE)) == tq.TQ_ERR_UNSUPPORTED
+    assert append(fake_desc(tq, kv_format=tq.TQ_KV_POLAR, qjl_k=1)) == tq.TQ_ERR_INVALID_ARG
+    assert append(fake_desc(tq, kv_format=tq.TQ_KV_POLAR, bits_v=5)) == tq.TQ_ERR_INVALID_ARG
+    assert tq.launch_count() == launches0

@@ -23,7 +23,7 @@ TQ_MAX_GROUP = 8
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_WORKSPACE, TQ_ERR_CUDA, TQ_ERR_DEVICE, TQ_ERR_VERSION = range(7)
 TQ_F32, TQ_BF16 = 0, 1
 TQ_ROT_HADAMARD, TQ_ROT_DENSE, TQ_RNG_QJL = 1, 2, 3
-TQ_KV_PACKED, TQ_KV_BF16, TQ_KV_K8V4 = 0, 1, 2
+TQ_KV_PACKED, TQ_KV_BF16, TQ_KV_K8V4, TQ_KV_POLAR = 0, 1, 2, 3
 TQ_NORM_CORRECTED, TQ_NORM_RAW = 0, 1
 TQ_DEV_BAD_SLOT, TQ_DEV_BAD_BLOCK, TQ_DEV_BAD_CONTEXT, TQ_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
 
@@ -172,8 +172,9 @@ def _stream(stream):
 class Layer:
     """One layer of the paged cache: device pools, rotation and codebooks.
 
-    kv_format: "packed" (TurboQuant codes), "bf16" (boundary layers) or "k8v4"
-    (FP8 E4M3 keys with TurboQuant values of bits_v).
+    kv_format: "packed" (TurboQuant codes), "bf16" (boundary layers), "k8v4"
+    (FP8 E4M3 keys with TurboQuant values of bits_v) or "polar" (PolarQuant
+    angle codes of bits_k / bits_v bits with an fp16 radius; Hadamard only).
     The descriptor (`desc`) points at tensors owned by this object.
     """
 
@@ -184,19 +185,21 @@ class Layer:
         self.num_blocks = int(num_blocks)
         self.num_kv_heads = int(num_kv_heads)
         self.head_dim = TQ_HEAD_DIM
-        if kv_format not in ("packed", "bf16", "k8v4"):
-            raise ValueError("kv_format must be 'packed', 'bf16' or 'k8v4'")
+        if kv_format not in ("packed", "bf16", "k8v4", "polar"):
+            raise ValueError("kv_format must be 'packed', 'bf16', 'k8v4' or 'polar'")
         self.kv_format = kv_format
         self.packed = kv_format == "packed"
         self.k8v4 = kv_format == "k8v4"
-        coded_v = self.packed or self.k8v4  # values carry TurboQuant codes
+        self.polar = kv_format == "polar"
+        coded_v = self.packed or self.k8v4 or self.polar  # rotated, coded layers
         d = CacheDesc()
         d.format_version = TQ_FORMAT_VERSION
         d.head_dim = TQ_HEAD_DIM
         d.num_kv_heads = self.num_kv_heads
         d.block_size = TQ_BLOCK_SIZE
         d.num_blocks = self.num_blocks
-        d.fmt.kv_format = TQ_KV_PACKED if self.packed else (TQ_KV_K8V4 if self.k8v4 else TQ_KV_BF16)
+        d.fmt.kv_format = {"packed": TQ_KV_PACKED, "bf16": TQ_KV_BF16, "k8v4": TQ_KV_K8V4,
+                           "polar": TQ_KV_POLAR}[kv_format]
         if self.k8v4:
             bits_k = 8
         d.fmt.bits_k = bits_k if coded_v else 0
@@ -210,18 +213,20 @@ class Layer:
         self.explicit_rotation = rotation
         self.rotation_host = None
         self.qjl_host = None
+        self.cb_k = self.cb_v = None
         if coded_v:
             self.cb_k = make_codebook(bits_k) if self.packed else None
-            self.cb_v = make_codebook(bits_v)
+            self.cb_v = make_codebook(bits_v) if not self.polar else None
             if self.packed:
                 for i, v in enumerate(self.cb_k[0]):
                     d.centroids_k[i] = float(v)
                 for i, v in enumerate(self.cb_k[1]):
                     d.boundaries_k[i] = float(v)
-            for i, v in enumerate(self.cb_v[0]):
-                d.centroids_v[i] = float(v)
-            for i, v in enumerate(self.cb_v[1]):
-                d.boundaries_v[i] = float(v)
+            if self.cb_v is not None:
+                for i, v in enumerate(self.cb_v[0]):
+                    d.centroids_v[i] = float(v)
+                for i, v in enumerate(self.cb_v[1]):
+                    d.boundaries_v[i] = float(v)
             rot = make_rotation(rot_kind, seed, layer) if rotation is None else np.asarray(rotation, np.float32)
             self.rotation_host = rot
             self.rotation = torch.from_numpy(np.ascontiguousarray(rot)).to(device)

@@ -65,7 +65,8 @@ tq_status check_append(const tq_cache_desc* desc, const void* k, const void* v, 
   if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
     return fail(TQ_ERR_INVALID_ARG, "%s: k/v must be 16-byte aligned", fn);
   const tq_layer_format& f = desc->fmt;
-  const bool packed_k = f.kv_format == TQ_KV_PACKED, packed_v = f.kv_format != TQ_KV_BF16;
+  const bool packed_k = f.kv_format == TQ_KV_PACKED,
+             packed_v = f.kv_format == TQ_KV_PACKED || f.kv_format == TQ_KV_K8V4;  // codebook quantizers
   if ((k && packed_k && !cell_table_ok(desc->boundaries_k, (1 << f.bits_k) - 1)) ||
       (v && packed_v && !cell_table_ok(desc->boundaries_v, (1 << f.bits_v) - 1)))
     return fail(TQ_ERR_UNSUPPORTED, "%s: codebook boundaries closer than 1/63 apart", fn);

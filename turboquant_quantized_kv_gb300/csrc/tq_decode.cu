@@ -1421,6 +1421,7 @@ constexpr int decode_nw(bool packed_plain, int nt, bool fp8_keys = false) {
 }
 
 int decode_warps(const tq_cache_desc& d, int g) {
+  if (d.fmt.kv_format == TQ_KV_POLAR) return 8;  // two CTAs of four warps per SM
   const bool k8 = d.fmt.kv_format == TQ_KV_K8V4;
   return decode_nw((d.fmt.kv_format == TQ_KV_PACKED && !d.fmt.qjl_k) || k8, g <= 4 ? 1 : 2, k8);
 }
@@ -1470,6 +1471,7 @@ static cudaError_t dispatch_bv(const DecodeArgs& a, int bv, cudaStream_t st) {
 
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   const tq_cache_desc& d = *c.desc;
+  if (d.fmt.kv_format == TQ_KV_POLAR) return launch_polar_decode(c, st);
   const bool bf16 = d.fmt.kv_format == TQ_KV_BF16;
   const bool k8 = d.fmt.kv_format == TQ_KV_K8V4;  // FP8 keys (unrotated) with packed values
   const bool qjl = !bf16 && !k8 && d.fmt.qjl_k;

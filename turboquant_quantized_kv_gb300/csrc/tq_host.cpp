@@ -302,6 +302,8 @@ size_t page_bytes_of(const tq_cache_desc& d, int which) {
   const size_t blk = (size_t)d.block_size;
   if (d.fmt.kv_format == TQ_KV_BF16) return blk * (size_t)d.head_dim * 2;
   if (d.fmt.kv_format == TQ_KV_K8V4 && which == 0) return blk * (size_t)d.head_dim;  // FP8 E4M3 keys
+  if (d.fmt.kv_format == TQ_KV_POLAR)  // angle-code records + fp16 radii
+    return blk * (size_t)(d.head_dim * (which == 0 ? d.fmt.bits_k : d.fmt.bits_v) / 8) + blk * 2;
   const int bits = which == 0 ? d.fmt.bits_k : d.fmt.bits_v;
   size_t n = blk * (size_t)(d.head_dim * bits / 8) + blk * 4;
   if (which == 0 && d.fmt.qjl_k) n += blk * (size_t)(d.head_dim / 8) + blk * 4;
@@ -348,6 +350,14 @@ tq_status check_desc(const tq_cache_desc* d, bool need_data) {
     if (need_data && !d->rotation) return fail(TQ_ERR_INVALID_ARG, "null rotation");
     if (!table_ok(d->centroids_v, d->boundaries_v, f.bits_v))
       return fail(TQ_ERR_INVALID_ARG, "value codebook is not increasing/antisymmetric with its midpoints");
+    return TQ_OK;
+  }
+  if (f.kv_format == TQ_KV_POLAR) {  // PolarQuant angle codes, Hadamard rotation only
+    if (f.bits_k < 2 || f.bits_k > 4 || f.bits_v < 2 || f.bits_v > 4)
+      return fail(TQ_ERR_INVALID_ARG, "polar: bits_k %d / bits_v %d not in 2..4", f.bits_k, f.bits_v);
+    if (f.qjl_k != 0) return fail(TQ_ERR_INVALID_ARG, "polar: keys carry no QJL residual");
+    if (f.rot_kind != TQ_ROT_HADAMARD) return fail(TQ_ERR_UNSUPPORTED, "polar: rot_kind %d (Hadamard only)", f.rot_kind);
+    if (need_data && !d->rotation) return fail(TQ_ERR_INVALID_ARG, "null rotation");
     return TQ_OK;
   }
   if (f.kv_format != TQ_KV_PACKED) return fail(TQ_ERR_INVALID_ARG, "kv_format %d", f.kv_format);

@@ -79,5 +79,11 @@ cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, in
 cudaError_t launch_dequant(const tq_cache_desc& d, int which, const int64_t* slots, int64_t n, void* out,
                            int out_dtype, unsigned* status, int num_sms, cudaStream_t st);
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st);
+// Polar layers (tq_polar.cu); the generic launchers above route them here.
+cudaError_t launch_polar_append(const tq_cache_desc& d, int which, const void* x, int in_dtype,
+                                const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms, cudaStream_t st);
+cudaError_t launch_polar_dequant(const tq_cache_desc& d, int which, const int64_t* slots, int64_t n, void* out,
+                                 int out_dtype, unsigned* status, int num_sms, cudaStream_t st);
+cudaError_t launch_polar_decode(const DecodeCall& c, cudaStream_t st);
 
 }  // namespace tq

@@ -1,0 +1,498 @@
+// PolarQuant-variant layers of libtq (sm_103a): append, dequantize, decode.
+//
+// What is computed (lilting.ch TurboQuant article, "PolarQuant: 極座標変換で量子化
+// 定数を不要にする"): the Hadamard-rotated vector y = Pi x is turned into polar
+// form recursively -- coordinate pairs give radii and angles, radii are paired
+// again -- down to one radius and d - 1 angles; each angle is coded on a fixed
+// uniform grid (b bits, no per-block constants) and the radius is kept as fp16.
+// Grids and the record layout are specified in include/tq.h.
+//
+// Angle codes without trigonometry.  With squared radii s = rho^2 of a pair
+// (a, b) >= 0, theta >= e  <=>  b^2 >= a^2 tan^2(e) for e in [0, pi/2), so the
+// level-l (l >= 2) code is the number of grid edges e_k = k pi / 2^(b+1) with
+// s_b >= s_a tan^2(e_k): a branch-free binary search over a 2^b - 1 entry
+// table of tan^2 values.  Level 1 (the whole circle) first takes the quadrant
+// of (-y_{2i}, -y_{2i+1}) -- phi = theta + pi mod 2 pi -- from the signs, then
+// the same search inside the quadrant over 2^b / 4 cells.  Only squared sums
+// are carried up the levels: no sqrt, no atan2.
+//
+// Kernels:
+//   k_polar_append   4 lanes per vector (lane q holds y[32q, 32q + 32)): signs,
+//                    FWHT, 31 angles per lane, the last two levels from the
+//                    quad's four squared radii; codes are gathered so lane q
+//                    writes record bits [32 b q, 32 b (q + 1)).
+//   k_polar_decode   one warp per (sequence, KV head, head group, split) chunk;
+//                    pages stream through a 3-stage cp.async ring of two blocks
+//                    (32 tokens: lane = token).  Each lane rebuilds its key's
+//                    unit direction depth-first (product of cos / sin of the
+//                    midpoint angles, looked up in shared memory) and dots it
+//                    with the rotated queries; the value directions go through a
+//                    swizzled shared tile to a lane = coordinates layout for the
+//                    weighted sum.  One partial per (query head, split).
+//   k_polar_combine  CTA per (sequence, query head): log-sum-exp merge of the
+//                    splits and the inverse rotation Pi^T.
+//   k_polar_dequant  warp per vector: x_hat = r Pi^T y_hat.
+#include "tq_polar.cuh"
+
+namespace tq {
+static PolarGrid polar_grid(int bits) {
+  PolarGrid g = {};
+  const int n = 1 << bits, m = n / 4;
+  const double pi = 3.14159265358979323846;
+  const double w1 = 2.0 * pi / n, wh = 0.5 * pi / n;
+  for (int k = 1; k < m; ++k) {
+    const double t = std::tan(k * w1);
+    g.t1[k] = (float)(t * t);
+  }
+  for (int k = 1; k < n; ++k) {
+    const double t = std::tan(k * wh);
+    g.th[k] = (float)(t * t);
+  }
+  for (int k = 0; k < n; ++k) {
+    const double a1 = (k + 0.5) * w1 - pi, ah = (k + 0.5) * wh;
+    g.cs1[2 * k] = (float)std::cos(a1);
+    g.cs1[2 * k + 1] = (float)std::sin(a1);
+    g.csh[2 * k] = (float)std::cos(ah);
+    g.csh[2 * k + 1] = (float)std::sin(ah);
+  }
+  return g;
+}
+
+// #{k in 1..N-1 : sb >= sa * T[k]} for increasing T (N a power of two), by a
+// branch-free binary search; T in shared memory (distinct entries sit in
+// distinct banks, so lanes with different indices do not conflict).
+template <int N>
+__device__ __forceinline__ uint32_t edge_count(float sa, float sb, const float* T) {
+  uint32_t c = 0;
+#pragma unroll
+  for (int step = N / 2; step >= 1; step >>= 1)
+    if (sb >= sa * T[c + step]) c += step;
+  return c;
+}
+
+// Code of a level >= 2 angle from the squared radii of its pair.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_high(float sa, float sb, const float* th) {
+  if (sa == 0.0f && sb == 0.0f) return 0u;  // a pair of two zeros has angle 0
+  return edge_count<(1 << BITS)>(sa, sb, th);
+}
+
+// Code of a level-1 angle of the pair (x, y) = (y_{2i}, y_{2i+1}).
+template <int BITS>
+__device__ __forceinline__ uint32_t code_level1(float x, float y, const float* t1) {
+  constexpr uint32_t M = (1u << BITS) / 4;  // cells per quadrant
+  if (x == 0.0f && y == 0.0f) return (1u << BITS) / 2;  // theta = 0 -> phi = pi
+  // quadrant of (u, v) = (-x, -y): 0: u > 0, v >= 0; 1: u <= 0, v > 0; 2: u < 0, v <= 0; 3: u >= 0, v < 0
+  uint32_t quad;
+  if (x < 0.0f && y <= 0.0f) quad = 0;
+  else if (x >= 0.0f && y < 0.0f) quad = 1;
+  else if (x > 0.0f && y >= 0.0f) quad = 2;
+  else quad = 3;
+  const float xx = x * x, yy = y * y;
+  // rotated into the first quadrant: (u', v') = (u, v), (v, -u), (-u, -v), (-v, u)
+  const bool swap = quad & 1u;
+  const float su = swap ? yy : xx, sv = swap ? xx : yy;
+  uint32_t sub = 0;
+  if constexpr (M > 1) sub = edge_count<M>(su, sv, t1);
+  return quad * M + sub;
+}
+
+__device__ __forceinline__ uint16_t f16_bits(float v) { return __half_as_ushort(__float2half_rn(v)); }
+
+// ------------------------------------------------------------------ append
+
+struct PolarAppendArgs {
+  const void* x;          // [n_tok][H][d] fp32 or bf16
+  const int64_t* slots;   // [n_tok]
+  int64_t n_vec;          // n_tok * H
+  int H;
+  int64_t max_slot;
+  uint8_t* pool;
+  int page_bytes;
+  const float* signs;     // [d] +-1
+  unsigned* status;
+  PolarGrid grid;
+};
+
+// Lane q of a quad holds the 32 rotated coordinates [32q, 32q + 32) of one vector.
+template <int BITS, typename TIn>
+__global__ void __launch_bounds__(256) k_polar_append(PolarAppendArgs a) {
+  __shared__ float s_t1[4], s_th[16];
+  if (threadIdx.x < 4) s_t1[threadIdx.x] = a.grid.t1[threadIdx.x];
+  if (threadIdx.x < 16) s_th[threadIdx.x] = a.grid.th[threadIdx.x];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, q = lane & 3;
+  const int64_t nq = ((a.n_vec + 7) / 8) * 8;  // whole warps keep the quad shuffles convergent
+  for (int64_t v0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 2; v0 < nq;
+       v0 += ((int64_t)gridDim.x * blockDim.x) >> 2) {
+    const bool live = v0 < a.n_vec;
+    const int64_t vec = live ? v0 : a.n_vec - 1;
+    const int64_t tok = vec / a.H;
+    const int head = (int)(vec - tok * a.H);
+    const TIn* src = reinterpret_cast<const TIn*>(a.x) + vec * kD + 32 * q;
+    float y[32];
+    load32<TIn>(src, y);
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ss = fmaf(y[i], y[i], ss);
+    const float norm = sqrtf(quad_sum(ss));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) y[i] *= __ldg(a.signs + 32 * q + i);
+    fwht128_quad(y, q);  // unnormalised: angles do not depend on the scale
+    // level 1: 16 angles, squared radii
+    uint32_t c1[16];
+    float s[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      c1[i] = code_level1<BITS>(y[2 * i], y[2 * i + 1], s_t1);
+      s[i] = fmaf(y[2 * i], y[2 * i], y[2 * i + 1] * y[2 * i + 1]);
+    }
+    // levels 2..5 inside the lane: 8 + 4 + 2 + 1 angles
+    uint32_t c2[8], c3[4], c4[2], c5;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      c2[i] = code_high<BITS>(s[2 * i], s[2 * i + 1], s_th);
+      s[i] = s[2 * i] + s[2 * i + 1];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      c3[i] = code_high<BITS>(s[2 * i], s[2 * i + 1], s_th);
+      s[i] = s[2 * i] + s[2 * i + 1];
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      c4[i] = code_high<BITS>(s[2 * i], s[2 * i + 1], s_th);
+      s[i] = s[2 * i] + s[2 * i + 1];
+    }
+    c5 = code_high<BITS>(s[0], s[1], s_th);
+    const float s5 = s[0] + s[1];
+    // levels 6 and 7 from the quad's four squared radii (every lane computes them)
+    const int base = lane & ~3;
+    const float r0 = __shfl_sync(0xffffffffu, s5, base), r1 = __shfl_sync(0xffffffffu, s5, base + 1);
+    const float r2 = __shfl_sync(0xffffffffu, s5, base + 2), r3 = __shfl_sync(0xffffffffu, s5, base + 3);
+    const uint32_t c6a = code_high<BITS>(r0, r1, s_th), c6b = code_high<BITS>(r2, r3, s_th);
+    const uint32_t c7 = code_high<BITS>(r0 + r1, r2 + r3, s_th);
+
+    // per-lane packed pieces (LSB-first, BITS bits per code)
+    uint64_t p1 = 0;  // 16 level-1 codes
+#pragma unroll
+    for (int i = 0; i < 16; ++i) p1 |= (uint64_t)c1[i] << (BITS * i);
+    uint32_t p2 = 0;  // 8 level-2 codes
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p2 |= c2[i] << (BITS * i);
+    // level 3 (4), level 4 (2), level 5 (1) codes: 7 codes
+    uint32_t p3 = c3[0] | c3[1] << BITS | c3[2] << (2 * BITS) | c3[3] << (3 * BITS);
+    const uint32_t p4 = c4[0] | c4[1] << BITS;
+    // lane q writes record slots [32q, 32q + 32):
+    //   q = 0, 1: level-1 angles 32q .. 32q + 31 (from lanes 2q, 2q + 1)
+    //   q = 2:    level-2 angles 0 .. 31 (8 from each lane)
+    //   q = 3:    level 3 (16), level 4 (8), level 5 (4), level 6 (2), level 7 (1), 0
+    const uint64_t l1a = __shfl_sync(0xffffffffu, p1, base + ((2 * q) & 3));
+    const uint64_t l1b = __shfl_sync(0xffffffffu, p1, base + ((2 * q + 1) & 3));
+    uint32_t w2[4], w3[4], w4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w2[k] = __shfl_sync(0xffffffffu, p2, base + k);
+      w3[k] = __shfl_sync(0xffffffffu, p3, base + k);
+      w4[k] = __shfl_sync(0xffffffffu, p4, base + k);
+    }
+    const uint32_t w5[4] = {__shfl_sync(0xffffffffu, c5, base), __shfl_sync(0xffffffffu, c5, base + 1),
+                            __shfl_sync(0xffffffffu, c5, base + 2), __shfl_sync(0xffffffffu, c5, base + 3)};
+    // assemble the lane's 32 * BITS bits as 128-bit value (lo, hi)
+    unsigned __int128 chunk;
+    if (q < 2) {
+      chunk = (unsigned __int128)l1a | ((unsigned __int128)l1b << (16 * BITS));
+    } else if (q == 2) {
+      chunk = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) chunk |= (unsigned __int128)w2[k] << (8 * BITS * k);
+    } else {
+      chunk = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        chunk |= (unsigned __int128)w3[k] << (4 * BITS * k);          // slots 4k .. 4k+3
+        chunk |= (unsigned __int128)w4[k] << (BITS * (16 + 2 * k));  // slots 16 + 2k, +1
+        chunk |= (unsigned __int128)w5[k] << (BITS * (24 + k));      // slot 24 + k
+      }
+      chunk |= (unsigned __int128)c6a << (BITS * 28);
+      chunk |= (unsigned __int128)c6b << (BITS * 29);
+      chunk |= (unsigned __int128)c7 << (BITS * 30);
+    }
+    if (!live) continue;
+    const int64_t slot = __ldg(a.slots + tok);
+    if (slot < 0) continue;
+    if (slot >= a.max_slot) {
+      if (q == 0) flag_status(a.status, TQ_DEV_BAD_SLOT);
+      continue;
+    }
+    const int64_t blk = slot >> 4;
+    const int off = (int)(slot & 15);
+    uint8_t* page = a.pool + (blk * a.H + head) * (int64_t)a.page_bytes;
+    uint8_t* rec = page + off * (16 * BITS) + q * (4 * BITS);
+    const uint64_t lo = (uint64_t)chunk, hi = (uint64_t)(chunk >> 64);
+    if constexpr (BITS == 4) {
+      *reinterpret_cast<uint4*>(rec) = make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+    } else if constexpr (BITS == 3) {
+      uint32_t* r32 = reinterpret_cast<uint32_t*>(rec);
+      r32[0] = (uint32_t)lo;
+      r32[1] = (uint32_t)(lo >> 32);
+      r32[2] = (uint32_t)hi;
+    } else {
+      *reinterpret_cast<uint2*>(rec) = make_uint2((uint32_t)lo, (uint32_t)(lo >> 32));
+    }
+    if (q == 0) *reinterpret_cast<uint16_t*>(page + 16 * (16 * BITS) + 2 * off) = f16_bits(norm);
+  }
+}
+
+// CTA per (sequence, query head), thread t = coordinate t.
+template <typename TO>
+__global__ void __launch_bounds__(128) k_polar_combine(const float* __restrict__ part, const float* __restrict__ ml,
+                                                       int splits, const float* __restrict__ signs, TO* out) {
+  __shared__ float red[4], y[kD];
+  const int t = threadIdx.x;
+  const int64_t bh = blockIdx.x;
+  const float* mlr = ml + bh * splits * 2;
+  float mx = -INFINITY;
+  for (int s = t; s < splits; s += 128) mx = fmaxf(mx, mlr[2 * s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((t & 31) == 0) red[t >> 5] = mx;
+  __syncthreads();
+  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  float acc = 0.0f, L = 0.0f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < splits; ++s) {
+      const float ms = mlr[2 * s];
+      if (ms == -INFINITY) continue;  // empty chunk
+      const float f = exp2f(ms - M);
+      acc = fmaf(part[(bh * splits + s) * kD + t], f, acc);
+      L = fmaf(mlr[2 * s + 1], f, L);
+    }
+  }
+  y[t] = L > 0.0f ? acc / L : 0.0f;
+  __syncthreads();
+  for (int h = 1; h < kD; h <<= 1) {  // y <- H y
+    const bool lower = (t & h) == 0;
+    float u = 0.0f, v = 0.0f;
+    if (lower) { u = y[t]; v = y[t + h]; }
+    __syncthreads();
+    if (lower) { y[t] = u + v; y[t + h] = u - v; }
+    __syncthreads();
+  }
+  store_elem<TO>(out + bh * kD + t, y[t] * kInvSqrtD * __ldg(signs + t));
+}
+
+// ------------------------------------------------------------------ dequantize
+
+// Leaf writing a whole direction (times r) into a [32][128] tile row, quads at c ^ (v & 7).
+struct RowLeaf {
+  float4 buf;
+  float* row;
+  int sw;
+  template <int J>
+  __device__ __forceinline__ void at(float v) {
+    constexpr int k = J & 3;
+    if constexpr (k == 0) buf.x = v;
+    if constexpr (k == 1) buf.y = v;
+    if constexpr (k == 2) buf.z = v;
+    if constexpr (k == 3) {
+      buf.w = v;
+      *reinterpret_cast<float4*>(row + (((J >> 2) ^ sw) << 2)) = buf;
+    }
+  }
+};
+
+// Two warps per CTA; a warp takes 32 vectors: lane v rebuilds r * y_hat of vector v into the tile,
+// then the warp applies Pi^T = D H / sqrt(d) to each row (lane L: coordinates 4L..4L+3).
+template <int BITS, typename TO>
+__global__ void __launch_bounds__(64) k_polar_dequant(const uint8_t* __restrict__ pool, int H, int page_bytes,
+                                                       int64_t max_slot, const int64_t* __restrict__ slots,
+                                                       int64_t n_vec, const float* __restrict__ signs, TO* out,
+                                                       unsigned* status, PolarGrid grid) {
+  __shared__ float tabs[64];
+  __shared__ __align__(16) float tiles[2][32 * 128];
+  if (threadIdx.x < 32) {
+    tabs[threadIdx.x] = grid.cs1[threadIdx.x];
+    tabs[32 + threadIdx.x] = grid.csh[threadIdx.x];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* tile = tiles[warp];
+  float sg[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) sg[k] = __ldg(signs + 4 * lane + k) * kInvSqrtD;
+  const int64_t n_groups = (n_vec + 31) / 32;
+  for (int64_t grp = (int64_t)blockIdx.x * 2 + warp; grp < n_groups; grp += (int64_t)gridDim.x * 2) {
+    const int64_t vec = grp * 32 + lane;
+    float r = 0.0f;
+    uint32_t w[16] = {};
+    if (vec < n_vec) {
+      const int64_t tok = vec / H;
+      const int head = (int)(vec - tok * H);
+      const int64_t slot = __ldg(slots + tok);
+      if (slot >= max_slot) flag_status(status, TQ_DEV_BAD_SLOT);
+      if (slot >= 0 && slot < max_slot) {
+        const uint8_t* page = pool + ((slot >> 4) * H + head) * (int64_t)page_bytes;
+        const int off = (int)(slot & 15);
+        const uint4* rec = reinterpret_cast<const uint4*>(page + off * (16 * BITS));
+#pragma unroll
+        for (int c = 0; c < BITS; ++c) {
+          const uint4 v = __ldg(rec + c);
+          w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+        }
+        r = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(page + 16 * (16 * BITS) + 2 * off)));
+      }
+    }
+    RowLeaf rl;
+    rl.row = tile + lane * 128;
+    rl.sw = lane & 7;
+    expand<BITS, 7, 0>(w, r, tabs, tabs + 32, rl);
+    __syncwarp();
+    const int64_t rem = n_vec - grp * 32;
+    const int nv = rem < 32 ? (int)rem : 32;
+    for (int v = 0; v < nv; ++v) {
+      const float4 t4 = *reinterpret_cast<const float4*>(tile + v * 128 + ((lane ^ (v & 7)) << 2));
+      float y[4] = {t4.x, t4.y, t4.z, t4.w};
+      float a0 = y[0] + y[1], a1 = y[0] - y[1], a2 = y[2] + y[3], a3 = y[2] - y[3];
+      y[0] = a0 + a2; y[2] = a0 - a2; y[1] = a1 + a3; y[3] = a1 - a3;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float o = __shfl_xor_sync(0xffffffffu, y[k], m);
+          y[k] = upper ? (o - y[k]) : (y[k] + o);
+        }
+      }
+      TO* dst = out + (grp * 32 + v) * kD + 4 * lane;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) store_elem<TO>(dst + k, y[k] * sg[k]);
+    }
+    __syncwarp();
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+
+template <int BITS>
+static cudaError_t run_polar_append(const PolarAppendArgs& a, bool f32, int num_sms, cudaStream_t st) {
+  const int64_t threads = ((a.n_vec + 7) / 8) * 32;
+  int64_t grid = (threads + 255) / 256;
+  if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
+  if (grid < 1) grid = 1;
+  if (f32) k_polar_append<BITS, float><<<(unsigned)grid, 256, 0, st>>>(a);
+  else k_polar_append<BITS, __nv_bfloat16><<<(unsigned)grid, 256, 0, st>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_polar_append(const tq_cache_desc& d, int which, const void* x, int in_dtype,
+                                const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms, cudaStream_t st) {
+  if (n_tok <= 0) return cudaSuccess;
+  const int bits = which == 0 ? d.fmt.bits_k : d.fmt.bits_v;
+  PolarAppendArgs a;
+  a.x = x;
+  a.slots = slots;
+  a.n_vec = n_tok * d.num_kv_heads;
+  a.H = d.num_kv_heads;
+  a.max_slot = d.num_blocks * kBlock;
+  a.pool = reinterpret_cast<uint8_t*>(which == 0 ? d.k_cache : d.v_cache);
+  a.page_bytes = (int)page_bytes_of(d, which);
+  a.signs = d.rotation;
+  a.status = status;
+  a.grid = polar_grid(bits);
+  const bool f32 = in_dtype == TQ_F32;
+  switch (bits) {
+    case 2: return run_polar_append<2>(a, f32, num_sms, st);
+    case 3: return run_polar_append<3>(a, f32, num_sms, st);
+    default: return run_polar_append<4>(a, f32, num_sms, st);
+  }
+}
+
+template <int BITS, typename TO>
+static cudaError_t run_polar_dequant(const tq_cache_desc& d, int which, const int64_t* slots, int64_t n_vec,
+                                     TO* out, unsigned* status, int num_sms, cudaStream_t st) {
+  const int64_t groups = (n_vec + 31) / 32;
+  int64_t grid = (groups + 1) / 2;
+  if (grid > (int64_t)num_sms * 6) grid = (int64_t)num_sms * 6;
+  if (grid < 1) grid = 1;
+  k_polar_dequant<BITS, TO><<<(unsigned)grid, 64, 0, st>>>(
+      reinterpret_cast<const uint8_t*>(which == 0 ? d.k_cache : d.v_cache), d.num_kv_heads,
+      (int)page_bytes_of(d, which), d.num_blocks * kBlock, slots, n_vec, d.rotation, out, status,
+      polar_grid(which == 0 ? d.fmt.bits_k : d.fmt.bits_v));
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_polar_dequant(const tq_cache_desc& d, int which, const int64_t* slots, int64_t n, void* out,
+                                 int out_dtype, unsigned* status, int num_sms, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t n_vec = n * d.num_kv_heads;
+  const int bits = which == 0 ? d.fmt.bits_k : d.fmt.bits_v;
+  if (out_dtype == TQ_F32) {
+    float* o = reinterpret_cast<float*>(out);
+    switch (bits) {
+      case 2: return run_polar_dequant<2>(d, which, slots, n_vec, o, status, num_sms, st);
+      case 3: return run_polar_dequant<3>(d, which, slots, n_vec, o, status, num_sms, st);
+      default: return run_polar_dequant<4>(d, which, slots, n_vec, o, status, num_sms, st);
+    }
+  }
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+  switch (bits) {
+    case 2: return run_polar_dequant<2>(d, which, slots, n_vec, o, status, num_sms, st);
+    case 3: return run_polar_dequant<3>(d, which, slots, n_vec, o, status, num_sms, st);
+    default: return run_polar_dequant<4>(d, which, slots, n_vec, o, status, num_sms, st);
+  }
+}
+
+cudaError_t launch_polar_decode(const DecodeCall& c, cudaStream_t st) {
+  const tq_cache_desc& d = *c.desc;
+  const DecodeWorkspace ws = decode_workspace(c.batch, c.num_q_heads, c.splits, kD, false);
+  PolarDecodeArgs a;
+  a.kpool = reinterpret_cast<const uint8_t*>(d.k_cache);
+  a.vpool = reinterpret_cast<const uint8_t*>(d.v_cache);
+  a.kpage = (int)page_bytes_of(d, 0);
+  a.vpage = (int)page_bytes_of(d, 1);
+  a.Hkv = d.num_kv_heads;
+  a.Hq = c.num_q_heads;
+  a.g = c.num_q_heads / d.num_kv_heads;
+  const int nh = a.g <= 4 ? 4 : 8;
+  a.ngroups = (a.g + nh - 1) / nh;
+  a.splits = c.splits;
+  a.num_blocks = d.num_blocks;
+  a.block_table = c.block_table;
+  a.max_blocks = c.max_blocks;
+  a.ctx_lens = c.ctx_lens;
+  a.q = c.q;
+  a.q_bf16 = c.q_dtype == TQ_BF16 ? 1 : 0;
+  a.q_scale = c.sm_scale * kPolarLog2e * kInvSqrtD;
+  a.signs = d.rotation;
+  a.part = reinterpret_cast<float*>(c.workspace + ws.part_off);
+  a.ml = reinterpret_cast<float*>(c.workspace + ws.ml_off);
+  a.chunks = (int64_t)c.batch * d.num_kv_heads * a.ngroups * c.splits;
+  a.status = c.status;
+  const PolarGrid gk = polar_grid(d.fmt.bits_k), gv = polar_grid(d.fmt.bits_v);
+  for (int i = 0; i < 32; ++i) {
+    a.cs1k[i] = gk.cs1[i];
+    a.cshk[i] = gk.csh[i];
+    a.cs1v[i] = gv.cs1[i];
+    a.cshv[i] = gv.csh[i];
+  }
+  cudaError_t e;
+  switch (d.fmt.bits_k) {
+    case 2: e = polar_decode_bk<2>(a, d.fmt.bits_v, nh, st); break;
+    case 3: e = polar_decode_bk<3>(a, d.fmt.bits_v, nh, st); break;
+    default: e = polar_decode_bk<4>(a, d.fmt.bits_v, nh, st); break;
+  }
+  if (e != cudaSuccess) return e;
+  const unsigned cgrid = (unsigned)((int64_t)c.batch * c.num_q_heads);
+  if (c.out_dtype == TQ_F32)
+    k_polar_combine<float><<<cgrid, 128, 0, st>>>(a.part, a.ml, c.splits, d.rotation, reinterpret_cast<float*>(c.out));
+  else
+    k_polar_combine<__nv_bfloat16><<<cgrid, 128, 0, st>>>(a.part, a.ml, c.splits, d.rotation,
+                                                          reinterpret_cast<__nv_bfloat16*>(c.out));
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace tq

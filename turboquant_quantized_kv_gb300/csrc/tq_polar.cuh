@@ -1,0 +1,391 @@
+// Device code of the PolarQuant-variant layers shared by tq_polar.cu (append,
+// dequantize, combine, launch) and the decode translation units
+// tq_polar_decode_k{2,3,4}.cu (one per key bit width, so they build in parallel).
+// What the kernels compute and how is described at the top of tq_polar.cu.
+#pragma once
+
+#include <cfloat>
+#include <cmath>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+
+constexpr float kPolarLog2e = 1.4426950408889634f;
+constexpr float kInvSqrtD = 0.08838834764831845f;  // 1/sqrt(128)
+
+// Grid tables of one bit width, passed by value.
+struct PolarGrid {
+  float t1[4];     // level 1: tan^2 of the edges inside a quadrant, index 1..m-1 (m = 2^b / 4)
+  float th[16];    // levels >= 2: tan^2 of the edges k pi / 2^(b+1), index 1..2^b-1
+  float cs1[32];   // level 1 midpoints: (cos, sin) of theta_hat_k, k < 2^b, interleaved
+  float csh[32];   // levels >= 2: (cos, sin) of theta_hat_k
+};
+
+// ------------------------------------------------------------------ direction
+
+// Code in record slot SLOT of BITS-bit codes held as 32-bit words.
+template <int BITS, int SLOT>
+__device__ __forceinline__ uint32_t slot_code(const uint32_t (&w)[16]) {
+  constexpr int bit = BITS * SLOT, word = bit >> 5, sh = bit & 31;
+  uint32_t v = w[word] >> sh;
+  if constexpr (sh + BITS > 32) v |= w[word + 1] << (32 - sh);
+  return v & ((1u << BITS) - 1u);
+}
+
+// Depth-first expansion of the unit direction below node NODE of level LEVEL
+// (level 0 = coordinates): child 2 NODE takes val * cos(theta_hat), child
+// 2 NODE + 1 takes val * sin(theta_hat).  cs1 / csh: interleaved (cos, sin)
+// tables of the level-1 and the higher-level grids in shared memory.
+template <int BITS, int LEVEL, int NODE, typename Leaf>
+__device__ __forceinline__ void expand(const uint32_t (&w)[16], float val, const float* cs1, const float* csh,
+                                       Leaf& leaf) {
+  if constexpr (LEVEL == 0) {
+    leaf.template at<NODE>(val);
+  } else {
+    constexpr int slot = kD - (kD >> (LEVEL - 1)) + NODE;
+    const uint32_t code = slot_code<BITS, slot>(w);
+    const float2 cs = *reinterpret_cast<const float2*>((LEVEL == 1 ? cs1 : csh) + 2 * code);
+    expand<BITS, LEVEL - 1, 2 * NODE>(w, val * cs.x, cs1, csh, leaf);
+    expand<BITS, LEVEL - 1, 2 * NODE + 1>(w, val * cs.y, cs1, csh, leaf);
+  }
+}
+
+// ------------------------------------------------------------------ decode
+
+constexpr int kPolarNW = 4;          // warps per decode CTA (two CTAs per SM)
+constexpr int kPolarStages = 3;      // ring depth (stages of two blocks)
+constexpr int kPolarPage = 16 * 64 + 32;  // a page in shared memory: 16 records padded to 64 B + radii
+constexpr int kPolarStage = 4 * kPolarPage;  // K and V pages of two blocks
+
+struct PolarDecodeArgs {
+  const uint8_t* kpool;
+  const uint8_t* vpool;
+  int kpage, vpage;        // page bytes in the pools
+  int Hkv, Hq, g, ngroups, splits;
+  int64_t num_blocks;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* ctx_lens;
+  const void* q;
+  int q_bf16;
+  float q_scale;           // sm_scale * log2(e) / sqrt(d) (the FWHT is unnormalised)
+  const float* signs;
+  float* part;             // [B][Hq][splits][d]
+  float* ml;               // [B][Hq][splits][2]
+  int64_t chunks;
+  unsigned* status;
+  float cs1k[32], cshk[32], cs1v[32], cshv[32];
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Copies one page (16 records of 16*BITS bytes + 16 fp16 radii) into its shared
+// layout: record t at t * 64, its 16-byte chunk c at position c ^ ((t >> 1) & 3)
+// (conflict-free 16-byte reads of one record per lane), radii at 1024.
+template <int BITS>
+__device__ __forceinline__ void copy_page(uint8_t* dst, const uint8_t* src, int lane) {
+  constexpr int n_rec = 16 * BITS;  // record chunks
+  for (int ci = lane; ci < n_rec + 2; ci += 32) {
+    if (ci < n_rec) {
+      const int t = ci / BITS, c = ci - t * BITS;
+      cp_async16(dst + t * 64 + ((c ^ ((t >> 1) & 3)) << 4), src + 16 * ci);
+    } else {
+      cp_async16(dst + 1024 + 16 * (ci - n_rec), src + 16 * ci);
+    }
+  }
+}
+
+template <int BITS>
+__device__ __forceinline__ void load_record(const uint8_t* page, int t, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if (c < BITS) {
+      const uint4 v = *reinterpret_cast<const uint4*>(page + t * 64 + ((c ^ ((t >> 1) & 3)) << 4));
+      w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+    } else {
+      w[4 * c] = w[4 * c + 1] = w[4 * c + 2] = w[4 * c + 3] = 0u;
+    }
+  }
+}
+
+// Key leaf: s[h] += y_hat_j * q'_h[j]  (queries stored [j][NH]).
+template <int NH>
+struct KeyLeaf {
+  float s[NH];
+  const float* qs;
+  template <int J>
+  __device__ __forceinline__ void at(float v) {
+#pragma unroll
+    for (int h4 = 0; h4 < NH / 4; ++h4) {
+      const float4 qv = *reinterpret_cast<const float4*>(qs + J * NH + 4 * h4);
+      s[4 * h4] = fmaf(v, qv.x, s[4 * h4]);
+      s[4 * h4 + 1] = fmaf(v, qv.y, s[4 * h4 + 1]);
+      s[4 * h4 + 2] = fmaf(v, qv.z, s[4 * h4 + 2]);
+      s[4 * h4 + 3] = fmaf(v, qv.w, s[4 * h4 + 3]);
+    }
+  }
+};
+
+// Value leaf: coordinates of one half (64) of the direction, written to the
+// token's row of the shared tile in quads, quad c at position c ^ (t & 7).
+struct ValueLeaf {
+  float4 buf;
+  float* row;
+  int sw;
+  template <int J>
+  __device__ __forceinline__ void at(float v) {
+    constexpr int k = J & 3;
+    if constexpr (k == 0) buf.x = v;
+    if constexpr (k == 1) buf.y = v;
+    if constexpr (k == 2) buf.z = v;
+    if constexpr (k == 3) {
+      buf.w = v;
+      *reinterpret_cast<float4*>(row + ((((J & 63) >> 2) ^ sw) << 2)) = buf;
+    }
+  }
+};
+
+// One warp per chunk = (sequence b, KV head, head group, split s).  Lane t of a
+// stage handles token t of its two blocks.
+template <int BK, int BV, int NH>
+__global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeArgs a) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  float* tabs = reinterpret_cast<float*>(smem_raw);  // cs1k, cshk, cs1v, cshv
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < 32) {
+    tabs[threadIdx.x] = a.cs1k[threadIdx.x];
+    tabs[32 + threadIdx.x] = a.cshk[threadIdx.x];
+    tabs[64 + threadIdx.x] = a.cs1v[threadIdx.x];
+    tabs[96 + threadIdx.x] = a.cshv[threadIdx.x];
+  }
+  constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 64 * 4;
+  uint8_t* wbase = smem_raw + 512 + warp * kWarpBytes;
+  uint8_t* ring = wbase;
+  float* qs = reinterpret_cast<float*>(wbase + kPolarStages * kPolarStage);  // [128][NH]
+  float* wts = qs + 128 * NH;                                                  // [32][NH]
+  float* tile = wts + 32 * NH;                                                 // [32][64]
+  __syncthreads();
+  const int64_t chunk = (int64_t)blockIdx.x * kPolarNW + warp;
+  if (chunk >= a.chunks) return;
+  const int s = (int)(chunk % a.splits);
+  const int64_t unit = chunk / a.splits;
+  const int hg = (int)(unit % a.ngroups);
+  const int kvh = (int)((unit / a.ngroups) % a.Hkv);
+  const int b = (int)(unit / ((int64_t)a.ngroups * a.Hkv));
+  const int h0 = kvh * a.g + hg * NH;
+  const int nh = min(NH, a.g - hg * NH);
+  int ctx = __ldg(a.ctx_lens + b);
+  if (ctx < 0 || ctx > a.max_blocks * 16) {
+    if (lane == 0) flag_status(a.status, TQ_DEV_BAD_CONTEXT);
+    ctx = 0;
+  }
+  const int nblk = (ctx + 15) >> 4;
+  const int j0 = (int)((int64_t)s * nblk / a.splits), j1 = (int)((int64_t)(s + 1) * nblk / a.splits);
+
+  // rotated, scaled queries: q'[j][h] = scale * (H D q_h)_j
+  for (int h = 0; h < NH; ++h) {
+    float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (h < nh) {
+      const int64_t row = (int64_t)b * a.Hq + h0 + h;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = 4 * lane + k;
+        const float qv = a.q_bf16 ? load_elem(reinterpret_cast<const __nv_bfloat16*>(a.q) + row * kD + j)
+                                  : load_elem(reinterpret_cast<const float*>(a.q) + row * kD + j);
+        y[k] = qv * __ldg(a.signs + j);
+      }
+      float a0 = y[0] + y[1], a1 = y[0] - y[1], a2 = y[2] + y[3], a3 = y[2] - y[3];
+      y[0] = a0 + a2; y[2] = a0 - a2; y[1] = a1 + a3; y[3] = a1 - a3;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float o = __shfl_xor_sync(0xffffffffu, y[k], m);
+          y[k] = upper ? (o - y[k]) : (y[k] + o);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) qs[(4 * lane + k) * NH + h] = y[k] * a.q_scale;
+  }
+
+  const int n_my = j1 - j0;
+  const int n_st = (n_my + 1) >> 1;
+  const int32_t* bt = a.block_table + (int64_t)b * a.max_blocks;
+  // block id of block jb of the chunk's sequence, or -1 (past the chunk, or bad)
+  auto block_id = [&](int jb) -> int64_t {
+    if (jb >= j1) return -1;
+    const int64_t id = __ldg(bt + jb);
+    if (id < 0 || id >= a.num_blocks) {
+      flag_status(a.status, TQ_DEV_BAD_BLOCK);
+      return -1;
+    }
+    return id;
+  };
+  auto issue = [&](int st) {
+    if (st < n_st) {
+      uint8_t* dst = ring + (st % kPolarStages) * kPolarStage;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int64_t id = block_id(j0 + 2 * st + half);
+        if (id < 0) continue;
+        copy_page<BK>(dst + half * kPolarPage, a.kpool + (id * a.Hkv + kvh) * (int64_t)a.kpage, lane);
+        copy_page<BV>(dst + (2 + half) * kPolarPage, a.vpool + (id * a.Hkv + kvh) * (int64_t)a.vpage, lane);
+      }
+    }
+    cp_async_commit();
+  };
+  issue(0);
+  issue(1);
+
+  float M[NH], lsum[NH], acc[NH][4];
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    M[h] = -INFINITY;
+    lsum[h] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[h][k] = 0.0f;
+  }
+  const float* cs1k = tabs; const float* cshk = tabs + 32;
+  const float* cs1v = tabs + 64; const float* cshv = tabs + 96;
+  const int half = lane >> 4, t16 = lane & 15;
+
+  for (int st = 0; st < n_st; ++st) {
+    issue(st + 2);
+    cp_async_wait<2>();
+    __syncwarp();
+    const uint8_t* sbuf = ring + (st % kPolarStages) * kPolarStage;
+    const int jb = j0 + 2 * st + half;
+    const int pos = jb * 16 + t16;
+    bool valid = jb < j1 && pos < ctx;
+    if (valid) {  // the block id was checked when its pages were requested
+      const int64_t id = __ldg(bt + jb);
+      valid = id >= 0 && id < a.num_blocks;
+    }
+    // keys: logits in log2 units
+    const uint8_t* kp = sbuf + half * kPolarPage;
+    uint32_t w[16];
+    load_record<BK>(kp, t16, w);
+    const float rk = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(kp + 1024 + 2 * t16)));
+    KeyLeaf<NH> kl;
+    kl.qs = qs;
+#pragma unroll
+    for (int h = 0; h < NH; ++h) kl.s[h] = 0.0f;
+    expand<BK, 7, 0>(w, 1.0f, cs1k, cshk, kl);
+    float p[NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const float sc = valid ? kl.s[h] * rk : -INFINITY;
+      float mx = sc;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float mn = fmaxf(M[h], mx);
+      const float corr = (M[h] == -INFINITY) ? 0.0f : ex2(M[h] - mn);
+      p[h] = valid ? ex2(sc - mn) : 0.0f;
+      lsum[h] = lsum[h] * corr + p[h];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[h][k] *= corr;
+      M[h] = mn;
+    }
+    // values: weights p r_V per token, directions through the shared tile
+    const uint8_t* vp = sbuf + (2 + half) * kPolarPage;
+    load_record<BV>(vp, t16, w);
+    const float rv = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(vp + 1024 + 2 * t16)));
+#pragma unroll
+    for (int h = 0; h < NH; ++h) wts[lane * NH + h] = valid ? p[h] * rv : 0.0f;
+    const uint32_t c7 = slot_code<BV, kD - 2>(w);
+    const float2 cs7 = *reinterpret_cast<const float2*>(cshv + 2 * c7);
+#pragma unroll
+    for (int hv = 0; hv < 2; ++hv) {
+      ValueLeaf vl;
+      vl.row = tile + lane * 64;
+      vl.sw = lane & 7;
+      if (hv == 0) expand<BV, 6, 0>(w, cs7.x, cs1v, cshv, vl);
+      else expand<BV, 6, 1>(w, cs7.y, cs1v, cshv, vl);
+      __syncwarp();
+      // lane L: coordinates 64 hv + 2L, + 1 of every token
+      for (int t = 0; t < 32; ++t) {
+        const float2 v2 = *reinterpret_cast<const float2*>(tile + t * 64 + ((((lane >> 1) ^ (t & 7)) << 2) | ((lane & 1) << 1)));
+#pragma unroll
+        for (int h4 = 0; h4 < NH / 4; ++h4) {
+          const float4 wv = *reinterpret_cast<const float4*>(wts + t * NH + 4 * h4);
+          const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            acc[4 * h4 + k][2 * hv] = fmaf(wa[k], v2.x, acc[4 * h4 + k][2 * hv]);
+            acc[4 * h4 + k][2 * hv + 1] = fmaf(wa[k], v2.y, acc[4 * h4 + k][2 * hv + 1]);
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+  cp_async_wait<0>();
+
+  // partial of each live head: unnormalised acc, (max, denominator)
+  for (int h = 0; h < nh; ++h) {
+    float l = lsum[h];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    const int64_t slot = ((int64_t)b * a.Hq + h0 + h) * a.splits + s;
+    float* pr = a.part + slot * kD;
+    *reinterpret_cast<float2*>(pr + 2 * lane) = make_float2(acc[h][0], acc[h][1]);
+    *reinterpret_cast<float2*>(pr + 64 + 2 * lane) = make_float2(acc[h][2], acc[h][3]);
+    if (lane == 0) {
+      a.ml[2 * slot] = M[h];
+      a.ml[2 * slot + 1] = l;
+    }
+  }
+}
+
+template <int BK, int BV, int NH>
+cudaError_t run_polar_decode(const PolarDecodeArgs& a, cudaStream_t st) {
+  auto kern = k_polar_decode<BK, BV, NH>;
+  constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 64 * 4;
+  constexpr size_t smem = 512 + (size_t)kPolarNW * kWarpBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = (a.chunks + kPolarNW - 1) / kPolarNW;
+  kern<<<(unsigned)grid, kPolarNW * 32, smem, st>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// Decode launch of one key bit width (one translation unit per BK keeps the
+// build parallel): the value width and the heads per warp are dispatched here.
+template <int BK>
+cudaError_t polar_decode_bk(const PolarDecodeArgs& a, int bv, int nh, cudaStream_t st) {
+  if (nh == 4) {
+    switch (bv) {
+      case 2: return run_polar_decode<BK, 2, 4>(a, st);
+      case 3: return run_polar_decode<BK, 3, 4>(a, st);
+      default: return run_polar_decode<BK, 4, 4>(a, st);
+    }
+  }
+  switch (bv) {
+    case 2: return run_polar_decode<BK, 2, 8>(a, st);
+    case 3: return run_polar_decode<BK, 3, 8>(a, st);
+    default: return run_polar_decode<BK, 4, 8>(a, st);
+  }
+}
+extern template cudaError_t polar_decode_bk<2>(const PolarDecodeArgs&, int, int, cudaStream_t);
+extern template cudaError_t polar_decode_bk<3>(const PolarDecodeArgs&, int, int, cudaStream_t);
+extern template cudaError_t polar_decode_bk<4>(const PolarDecodeArgs&, int, int, cudaStream_t);
+
+}  // namespace tq

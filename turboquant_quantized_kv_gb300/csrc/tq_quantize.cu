@@ -1220,6 +1220,7 @@ cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, in
                             const float* norms, const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms,
                             cudaStream_t st, const void* x_v) {
   if (n_tok <= 0) return cudaSuccess;
+  if (d.fmt.kv_format == TQ_KV_POLAR) return launch_polar_append(d, which, x, in_dtype, slots, n_tok, status, num_sms, st);
   const int64_t n_vec = n_tok * d.num_kv_heads;
   const int64_t max_slot = d.num_blocks * kBlock;
   uint8_t* pool = reinterpret_cast<uint8_t*>(which == 0 ? d.k_cache : d.v_cache);
@@ -1319,6 +1320,7 @@ static cudaError_t dequant_bits(const tq_cache_desc& d, int which, const int64_t
 cudaError_t launch_dequant(const tq_cache_desc& d, int which, const int64_t* slots, int64_t n, void* out,
                            int out_dtype, unsigned* status, int num_sms, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
+  if (d.fmt.kv_format == TQ_KV_POLAR) return launch_polar_dequant(d, which, slots, n, out, out_dtype, status, num_sms, st);
   const int64_t n_vec = n * d.num_kv_heads;
   if (d.fmt.kv_format == TQ_KV_K8V4 && which == 0) {
     const uint8_t* pool = reinterpret_cast<const uint8_t*>(d.k_cache);
