@@ -70,30 +70,37 @@ __device__ __forceinline__ uint32_t edge_count(float sa, float sb, const float* 
   return c;
 }
 
-// Code of a level >= 2 angle from the squared radii of its pair.
+// Code of a level >= 2 angle from the squared radii of its pair.  sb <= 0 gives
+// code 0 (theta = 0, which also covers a pair of two zeros).
 template <int BITS>
 __device__ __forceinline__ uint32_t code_high(float sa, float sb, const float* th) {
-  if (sa == 0.0f && sb == 0.0f) return 0u;  // a pair of two zeros has angle 0
-  return edge_count<(1 << BITS)>(sa, sb, th);
+  return edge_count<(1 << BITS)>(sa, sb > 0.0f ? sb : -1.0f, th);
 }
 
-// Code of a level-1 angle of the pair (x, y) = (y_{2i}, y_{2i+1}).
+// Code of a level-1 angle of the pair (x, y) = (y_{2i}, y_{2i+1}); t1a, t1b = tan^2
+// of the first and third edges inside a quadrant (4-bit grids; the middle edge,
+// pi/4, is the exact test sv >= su).
 template <int BITS>
-__device__ __forceinline__ uint32_t code_level1(float x, float y, const float* t1) {
+__device__ __forceinline__ uint32_t code_level1(float x, float y, float t1a, float t1b) {
   constexpr uint32_t M = (1u << BITS) / 4;  // cells per quadrant
-  if (x == 0.0f && y == 0.0f) return (1u << BITS) / 2;  // theta = 0 -> phi = pi
-  // quadrant of (u, v) = (-x, -y): 0: u > 0, v >= 0; 1: u <= 0, v > 0; 2: u < 0, v <= 0; 3: u >= 0, v < 0
+  // quadrant of (u, v) = (-x, -y): 0: u > 0, v >= 0; 1: u <= 0, v > 0; 2: u < 0, v <= 0;
+  // 3: u >= 0, v < 0; a pair of two zeros has theta = 0, i.e. phi = pi: code 2M
   uint32_t quad;
   if (x < 0.0f && y <= 0.0f) quad = 0;
   else if (x >= 0.0f && y < 0.0f) quad = 1;
   else if (x > 0.0f && y >= 0.0f) quad = 2;
-  else quad = 3;
-  const float xx = x * x, yy = y * y;
+  else if (y > 0.0f) quad = 3;
+  else return 2 * M;
   // rotated into the first quadrant: (u', v') = (u, v), (v, -u), (-u, -v), (-v, u)
+  const float xx = x * x, yy = y * y;
   const bool swap = quad & 1u;
   const float su = swap ? yy : xx, sv = swap ? xx : yy;
   uint32_t sub = 0;
-  if constexpr (M > 1) sub = edge_count<M>(su, sv, t1);
+  if constexpr (M == 2) sub = sv >= su ? 1u : 0u;
+  if constexpr (M == 4) {
+    sub = sv >= su ? 2u : 0u;
+    sub += sv >= su * (sub ? t1b : t1a) ? 1u : 0u;
+  }
   return quad * M + sub;
 }
 
@@ -114,14 +121,39 @@ struct PolarAppendArgs {
   PolarGrid grid;
 };
 
+// The 32 record slots [32q, 32q + 32) of one vector, one code per byte (4 words),
+// packed to the BITS-bit bitstream: BITS words.
+template <int BITS>
+__device__ __forceinline__ void pack_slots(const uint32_t (&b)[8], uint32_t (&w)[BITS]) {
+  if constexpr (BITS == 4) {  // bytes b0..b3 -> nibble pairs, two input words per output word
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t t0 = b[2 * k] | (b[2 * k] >> 4), t1 = b[2 * k + 1] | (b[2 * k + 1] >> 4);
+      w[k] = __byte_perm(t0, t1, 0x6420u);
+    }
+  } else {
+    uint32_t code[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) code[i] = (b[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+    pack32<BITS>(code, w);
+  }
+}
+
 // Lane q of a quad holds the 32 rotated coordinates [32q, 32q + 32) of one vector.
+// The codes go through a per-vector byte array in shared memory (slot order), from
+// which lane q packs and stores record bits [32 BITS q, 32 BITS (q + 1)).
 template <int BITS, typename TIn>
 __global__ void __launch_bounds__(256) k_polar_append(PolarAppendArgs a) {
-  __shared__ float s_t1[4], s_th[16];
-  if (threadIdx.x < 4) s_t1[threadIdx.x] = a.grid.t1[threadIdx.x];
+  __shared__ float s_th[16];
+  __shared__ __align__(16) uint8_t s_codes[8][8][128];  // [warp][vector of the warp][slot]
   if (threadIdx.x < 16) s_th[threadIdx.x] = a.grid.th[threadIdx.x];
   __syncthreads();
   const int lane = threadIdx.x & 31, q = lane & 3;
+  uint8_t* rec_s = s_codes[threadIdx.x >> 5][lane >> 2];
+  const float t1a = a.grid.t1[1], t1b = a.grid.t1[3];
+  uint32_t sw = 0;  // sign flips of coordinates [32q, 32q + 32)
+#pragma unroll
+  for (int i = 0; i < 32; ++i) sw |= (__ldg(a.signs + 32 * q + i) < 0.0f ? 1u : 0u) << i;
   const int64_t nq = ((a.n_vec + 7) / 8) * 8;  // whole warps keep the quad shuffles convergent
   for (int64_t v0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 2; v0 < nq;
        v0 += ((int64_t)gridDim.x * blockDim.x) >> 2) {
@@ -131,37 +163,53 @@ __global__ void __launch_bounds__(256) k_polar_append(PolarAppendArgs a) {
     const int head = (int)(vec - tok * a.H);
     const TIn* src = reinterpret_cast<const TIn*>(a.x) + vec * kD + 32 * q;
     float y[32];
-    load32<TIn>(src, y);
+    if constexpr (sizeof(TIn) == 2) {  // sign flips applied to the packed bf16 words
+      const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = __ldg(p + i);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = 4 * i + k;  // word j: coordinates 2j, 2j + 1
+          const uint32_t f = wv[k] ^ (((sw >> (2 * j)) & 1u) << 15 | ((sw >> (2 * j + 1)) & 1u) << 31);
+          y[2 * j] = __uint_as_float(f << 16);
+          y[2 * j + 1] = __uint_as_float(f & 0xFFFF0000u);
+        }
+      }
+    } else {
+      load32<TIn>(src, y);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(__float_as_uint(y[i]) ^ (((sw >> i) & 1u) << 31));
+    }
     float ss = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) ss = fmaf(y[i], y[i], ss);
     const float norm = sqrtf(quad_sum(ss));
-#pragma unroll
-    for (int i = 0; i < 32; ++i) y[i] *= __ldg(a.signs + 32 * q + i);
-    fwht128_quad(y, q);  // unnormalised: angles do not depend on the scale
-    // level 1: 16 angles, squared radii
-    uint32_t c1[16];
+    fwht128_quad_f2(y, q);  // unnormalised: angles do not depend on the scale
+    // level 1: 16 angles (4 code bytes per word), squared radii
+    uint32_t b1[4] = {0u, 0u, 0u, 0u};
     float s[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      c1[i] = code_level1<BITS>(y[2 * i], y[2 * i + 1], s_t1);
+      b1[i >> 2] |= code_level1<BITS>(y[2 * i], y[2 * i + 1], t1a, t1b) << (8 * (i & 3));
       s[i] = fmaf(y[2 * i], y[2 * i], y[2 * i + 1] * y[2 * i + 1]);
     }
     // levels 2..5 inside the lane: 8 + 4 + 2 + 1 angles
-    uint32_t c2[8], c3[4], c4[2], c5;
+    uint32_t b2[2] = {0u, 0u}, b3 = 0u, b4 = 0u, c5;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      c2[i] = code_high<BITS>(s[2 * i], s[2 * i + 1], s_th);
+      b2[i >> 2] |= code_high<BITS>(s[2 * i], s[2 * i + 1], s_th) << (8 * (i & 3));
       s[i] = s[2 * i] + s[2 * i + 1];
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      c3[i] = code_high<BITS>(s[2 * i], s[2 * i + 1], s_th);
+      b3 |= code_high<BITS>(s[2 * i], s[2 * i + 1], s_th) << (8 * i);
       s[i] = s[2 * i] + s[2 * i + 1];
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      c4[i] = code_high<BITS>(s[2 * i], s[2 * i + 1], s_th);
+      b4 |= code_high<BITS>(s[2 * i], s[2 * i + 1], s_th) << (8 * i);
       s[i] = s[2 * i] + s[2 * i + 1];
     }
     c5 = code_high<BITS>(s[0], s[1], s_th);
@@ -172,52 +220,20 @@ __global__ void __launch_bounds__(256) k_polar_append(PolarAppendArgs a) {
     const float r2 = __shfl_sync(0xffffffffu, s5, base + 2), r3 = __shfl_sync(0xffffffffu, s5, base + 3);
     const uint32_t c6a = code_high<BITS>(r0, r1, s_th), c6b = code_high<BITS>(r2, r3, s_th);
     const uint32_t c7 = code_high<BITS>(r0 + r1, r2 + r3, s_th);
-
-    // per-lane packed pieces (LSB-first, BITS bits per code)
-    uint64_t p1 = 0;  // 16 level-1 codes
-#pragma unroll
-    for (int i = 0; i < 16; ++i) p1 |= (uint64_t)c1[i] << (BITS * i);
-    uint32_t p2 = 0;  // 8 level-2 codes
-#pragma unroll
-    for (int i = 0; i < 8; ++i) p2 |= c2[i] << (BITS * i);
-    // level 3 (4), level 4 (2), level 5 (1) codes: 7 codes
-    uint32_t p3 = c3[0] | c3[1] << BITS | c3[2] << (2 * BITS) | c3[3] << (3 * BITS);
-    const uint32_t p4 = c4[0] | c4[1] << BITS;
-    // lane q writes record slots [32q, 32q + 32):
-    //   q = 0, 1: level-1 angles 32q .. 32q + 31 (from lanes 2q, 2q + 1)
-    //   q = 2:    level-2 angles 0 .. 31 (8 from each lane)
-    //   q = 3:    level 3 (16), level 4 (8), level 5 (4), level 6 (2), level 7 (1), 0
-    const uint64_t l1a = __shfl_sync(0xffffffffu, p1, base + ((2 * q) & 3));
-    const uint64_t l1b = __shfl_sync(0xffffffffu, p1, base + ((2 * q + 1) & 3));
-    uint32_t w2[4], w3[4], w4[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      w2[k] = __shfl_sync(0xffffffffu, p2, base + k);
-      w3[k] = __shfl_sync(0xffffffffu, p3, base + k);
-      w4[k] = __shfl_sync(0xffffffffu, p4, base + k);
-    }
-    const uint32_t w5[4] = {__shfl_sync(0xffffffffu, c5, base), __shfl_sync(0xffffffffu, c5, base + 1),
-                            __shfl_sync(0xffffffffu, c5, base + 2), __shfl_sync(0xffffffffu, c5, base + 3)};
-    // assemble the lane's 32 * BITS bits as 128-bit value (lo, hi)
-    unsigned __int128 chunk;
-    if (q < 2) {
-      chunk = (unsigned __int128)l1a | ((unsigned __int128)l1b << (16 * BITS));
-    } else if (q == 2) {
-      chunk = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) chunk |= (unsigned __int128)w2[k] << (8 * BITS * k);
-    } else {
-      chunk = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        chunk |= (unsigned __int128)w3[k] << (4 * BITS * k);          // slots 4k .. 4k+3
-        chunk |= (unsigned __int128)w4[k] << (BITS * (16 + 2 * k));  // slots 16 + 2k, +1
-        chunk |= (unsigned __int128)w5[k] << (BITS * (24 + k));      // slot 24 + k
-      }
-      chunk |= (unsigned __int128)c6a << (BITS * 28);
-      chunk |= (unsigned __int128)c6b << (BITS * 29);
-      chunk |= (unsigned __int128)c7 << (BITS * 30);
-    }
+    // codes to the vector's byte array in slot order
+    *reinterpret_cast<uint4*>(rec_s + 16 * q) = make_uint4(b1[0], b1[1], b1[2], b1[3]);  // level 1
+    *reinterpret_cast<uint2*>(rec_s + 64 + 8 * q) = make_uint2(b2[0], b2[1]);            // level 2
+    *reinterpret_cast<uint32_t*>(rec_s + 96 + 4 * q) = b3;                               // level 3
+    *reinterpret_cast<uint16_t*>(rec_s + 112 + 2 * q) = (uint16_t)b4;                    // level 4
+    rec_s[120 + q] = (uint8_t)c5;                                                        // level 5
+    if (q == 0) *reinterpret_cast<uint32_t*>(rec_s + 124) = c6a | c6b << 8 | c7 << 16;  // 6, 7, pad
+    __syncwarp();
+    const uint4 lo = *reinterpret_cast<const uint4*>(rec_s + 32 * q);
+    const uint4 hi = *reinterpret_cast<const uint4*>(rec_s + 32 * q + 16);
+    __syncwarp();  // the array is rewritten by the next iteration
+    const uint32_t bytes[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t w[BITS];
+    pack_slots<BITS>(bytes, w);
     if (!live) continue;
     const int64_t slot = __ldg(a.slots + tok);
     if (slot < 0) continue;
@@ -229,20 +245,21 @@ __global__ void __launch_bounds__(256) k_polar_append(PolarAppendArgs a) {
     const int off = (int)(slot & 15);
     uint8_t* page = a.pool + (blk * a.H + head) * (int64_t)a.page_bytes;
     uint8_t* rec = page + off * (16 * BITS) + q * (4 * BITS);
-    const uint64_t lo = (uint64_t)chunk, hi = (uint64_t)(chunk >> 64);
     if constexpr (BITS == 4) {
-      *reinterpret_cast<uint4*>(rec) = make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+      *reinterpret_cast<uint4*>(rec) = make_uint4(w[0], w[1], w[2], w[3]);
     } else if constexpr (BITS == 3) {
       uint32_t* r32 = reinterpret_cast<uint32_t*>(rec);
-      r32[0] = (uint32_t)lo;
-      r32[1] = (uint32_t)(lo >> 32);
-      r32[2] = (uint32_t)hi;
+      r32[0] = w[0];
+      r32[1] = w[1];
+      r32[2] = w[2];
     } else {
-      *reinterpret_cast<uint2*>(rec) = make_uint2((uint32_t)lo, (uint32_t)(lo >> 32));
+      *reinterpret_cast<uint2*>(rec) = make_uint2(w[0], w[1]);
     }
     if (q == 0) *reinterpret_cast<uint16_t*>(page + 16 * (16 * BITS) + 2 * off) = f16_bits(norm);
   }
 }
+
+// ------------------------------------------------------------------ decode / combine
 
 // CTA per (sequence, query head), thread t = coordinate t.
 template <typename TO>
