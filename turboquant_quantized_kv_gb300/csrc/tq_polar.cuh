@@ -53,6 +53,24 @@ __device__ __forceinline__ void expand(const uint32_t (&w)[16], float val, const
   }
 }
 
+// The same expansion in packed fp32 pairs: every node's two children come from one
+// (val, val) * (cos, sin) product; level-1 nodes hand the coordinate pair
+// (y_hat_{2 NODE}, y_hat_{2 NODE + 1}) to leaf.pair<NODE>.
+template <int BITS, int LEVEL, int NODE, typename Leaf>
+__device__ __forceinline__ void expand2(const uint32_t (&w)[16], float val, const float* cs1, const float* csh,
+                                        Leaf& leaf) {
+  constexpr int slot = kD - (kD >> (LEVEL - 1)) + NODE;
+  const uint32_t code = slot_code<BITS, slot>(w);
+  const float2 cs = *reinterpret_cast<const float2*>((LEVEL == 1 ? cs1 : csh) + 2 * code);
+  const float2 ch = __fmul2_rn(make_float2(val, val), cs);
+  if constexpr (LEVEL == 1) {
+    leaf.template pair<NODE>(ch);
+  } else {
+    expand2<BITS, LEVEL - 1, 2 * NODE>(w, ch.x, cs1, csh, leaf);
+    expand2<BITS, LEVEL - 1, 2 * NODE + 1>(w, ch.y, cs1, csh, leaf);
+  }
+}
+
 // ------------------------------------------------------------------ decode
 
 constexpr int kPolarNW = 4;          // warps per decode CTA (two CTAs per SM)
@@ -123,47 +141,73 @@ __device__ __forceinline__ void load_record(const uint8_t* page, int t, uint32_t
   }
 }
 
-// Key leaf: s[h] += y_hat_j * q'_h[j]  (queries stored [j][NH]).
+// fp16 pair (low half = a, high half = b), each rounded to nearest.
+__device__ __forceinline__ uint32_t half2_bits(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// fp16 hi/lo split of a pair: hi = fp16(v), lo = fp16(v - hi); returns hi or lo.
+__device__ __forceinline__ uint32_t half2_part(float a, float b, bool lo) {
+  if (!lo) return half2_bits(a, b);
+  return half2_bits(a - __half2float(__float2half_rn(a)), b - __half2float(__float2half_rn(b)));
+}
+
+// Key leaf: s2[h] += (y_hat_{2i}, y_hat_{2i+1}) * (q'_{2i,h}, q'_{2i+1,h}) in packed
+// fp32 pairs (queries stored [pair][NH][2]); the logit of head h is s2[h].x + s2[h].y.
 template <int NH>
 struct KeyLeaf {
-  float s[NH];
+  float2 s2[NH];
   const float* qs;
-  template <int J>
-  __device__ __forceinline__ void at(float v) {
+  template <int I>
+  __device__ __forceinline__ void pair(float2 v) {
 #pragma unroll
-    for (int h4 = 0; h4 < NH / 4; ++h4) {
-      const float4 qv = *reinterpret_cast<const float4*>(qs + J * NH + 4 * h4);
-      s[4 * h4] = fmaf(v, qv.x, s[4 * h4]);
-      s[4 * h4 + 1] = fmaf(v, qv.y, s[4 * h4 + 1]);
-      s[4 * h4 + 2] = fmaf(v, qv.z, s[4 * h4 + 2]);
-      s[4 * h4 + 3] = fmaf(v, qv.w, s[4 * h4 + 3]);
+    for (int h2 = 0; h2 < NH / 2; ++h2) {
+      const float4 qv = *reinterpret_cast<const float4*>(qs + (I * NH + 2 * h2) * 2);
+      s2[2 * h2] = __ffma2_rn(v, make_float2(qv.x, qv.y), s2[2 * h2]);
+      s2[2 * h2 + 1] = __ffma2_rn(v, make_float2(qv.z, qv.w), s2[2 * h2 + 1]);
     }
   }
 };
 
-// Value leaf: coordinates of one half (64) of the direction, written to the
-// token's row of the shared tile in quads, quad c at position c ^ (t & 7).
-struct ValueLeaf {
-  float4 buf;
-  float* row;
+// Value leaf: the direction as fp16 in its token's row (256 B) of the [32][128]
+// tile: 16-byte chunk c (coordinates 8c .. 8c + 7) at position c ^ (row & 7), so
+// the chunk stores of a warp and the ldmatrix rows never share banks.
+struct HalfLeaf {
+  uint32_t h[4];
+  uint8_t* row;
   int sw;
-  template <int J>
-  __device__ __forceinline__ void at(float v) {
-    constexpr int k = J & 3;
-    if constexpr (k == 0) buf.x = v;
-    if constexpr (k == 1) buf.y = v;
-    if constexpr (k == 2) buf.z = v;
-    if constexpr (k == 3) {
-      buf.w = v;
-      *reinterpret_cast<float4*>(row + ((((J & 63) >> 2) ^ sw) << 2)) = buf;
-    }
+  template <int I>
+  __device__ __forceinline__ void pair(float2 v) {
+    h[I & 3] = half2_bits(v.x, v.y);
+    if constexpr ((I & 3) == 3)
+      *reinterpret_cast<uint4*>(row + (((I >> 2) ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
   }
 };
 
-// One warp per chunk = (sequence b, KV head, head group, split s).  Lane t of a
-// stage handles token t of its two blocks.
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&d)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One warp per chunk = (sequence b, KV head, head group, split s).  Per stage of
+// two blocks (32 tokens) lane t handles token t: it rebuilds the unit direction of
+// the key in fp32 pairs and dots it with the rotated queries (logits in fp32),
+// then rebuilds the value direction into an fp16 tile; acc^T (128 x 8 per n-tile)
+// += V_hat^T x W on tensor cores with W = p r_V split into fp16 hi / lo columns
+// (8 columns = 4 heads x {hi, lo}).  In the MMA layout lane (g, t) owns head
+// 4 nt + t, coordinates 16 mt + g and 16 mt + g + 8.
 template <int BK, int BV, int NH>
 __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeArgs a) {
+  constexpr int NT = NH / 4;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   float* tabs = reinterpret_cast<float*>(smem_raw);  // cs1k, cshk, cs1v, cshv
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -173,12 +217,12 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
     tabs[64 + threadIdx.x] = a.cs1v[threadIdx.x];
     tabs[96 + threadIdx.x] = a.cshv[threadIdx.x];
   }
-  constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 64 * 4;
+  constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 256;
   uint8_t* wbase = smem_raw + 512 + warp * kWarpBytes;
   uint8_t* ring = wbase;
-  float* qs = reinterpret_cast<float*>(wbase + kPolarStages * kPolarStage);  // [128][NH]
+  float* qs = reinterpret_cast<float*>(wbase + kPolarStages * kPolarStage);  // [64 pairs][NH][2]
   float* wts = qs + 128 * NH;                                                  // [32][NH]
-  float* tile = wts + 32 * NH;                                                 // [32][64]
+  uint8_t* tile = reinterpret_cast<uint8_t*>(wts + 32 * NH);                   // [32][256 B] fp16
   __syncthreads();
   const int64_t chunk = (int64_t)blockIdx.x * kPolarNW + warp;
   if (chunk >= a.chunks) return;
@@ -197,7 +241,7 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
   const int nblk = (ctx + 15) >> 4;
   const int j0 = (int)((int64_t)s * nblk / a.splits), j1 = (int)((int64_t)(s + 1) * nblk / a.splits);
 
-  // rotated, scaled queries: q'[j][h] = scale * (H D q_h)_j
+  // rotated, scaled queries: q'[j][h] = scale * (H D q_h)_j, stored by coordinate pair
   for (int h = 0; h < NH; ++h) {
     float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (h < nh) {
@@ -222,13 +266,16 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) qs[(4 * lane + k) * NH + h] = y[k] * a.q_scale;
+    for (int k = 0; k < 4; ++k) {
+      const int j = 4 * lane + k;
+      qs[((j >> 1) * NH + h) * 2 + (j & 1)] = y[k] * a.q_scale;
+    }
   }
+  __syncwarp();
 
   const int n_my = j1 - j0;
   const int n_st = (n_my + 1) >> 1;
   const int32_t* bt = a.block_table + (int64_t)b * a.max_blocks;
-  // block id of block jb of the chunk's sequence, or -1 (past the chunk, or bad)
   auto block_id = [&](int jb) -> int64_t {
     if (jb >= j1) return -1;
     const int64_t id = __ldg(bt + jb);
@@ -254,17 +301,29 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
   issue(0);
   issue(1);
 
-  float M[NH], lsum[NH], acc[NH][4];
+  float M[NH], lsum[NH], acc[8][NT][4];
 #pragma unroll
   for (int h = 0; h < NH; ++h) {
     M[h] = -INFINITY;
     lsum[h] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) acc[h][k] = 0.0f;
   }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[mt][nt][k] = 0.0f;
   const float* cs1k = tabs; const float* cshk = tabs + 32;
   const float* cs1v = tabs + 64; const float* cshv = tabs + 96;
   const int half = lane >> 4, t16 = lane & 15;
+  const int g = lane >> 2, tq = lane & 3;
+  HalfLeaf hl;
+  hl.row = tile + lane * 256;
+  hl.sw = lane & 7;
+  const uint32_t tile_u = (uint32_t)__cvta_generic_to_shared(tile);
+  const int mat = lane >> 3, mr = lane & 7;
+  // ldmatrix rows of the transposed value tiles (token 16 kt + mr + 8 (mat >> 1))
+  const uint32_t v_row = tile_u + (uint32_t)((mr + ((mat >> 1) << 3)) * 256);
 
   for (int st = 0; st < n_st; ++st) {
     issue(st + 2);
@@ -272,13 +331,12 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
     __syncwarp();
     const uint8_t* sbuf = ring + (st % kPolarStages) * kPolarStage;
     const int jb = j0 + 2 * st + half;
-    const int pos = jb * 16 + t16;
-    bool valid = jb < j1 && pos < ctx;
+    bool valid = jb < j1 && jb * 16 + t16 < ctx;
     if (valid) {  // the block id was checked when its pages were requested
       const int64_t id = __ldg(bt + jb);
       valid = id >= 0 && id < a.num_blocks;
     }
-    // keys: logits in log2 units
+    // keys: fp32 logits in log2 units
     const uint8_t* kp = sbuf + half * kPolarPage;
     uint32_t w[16];
     load_record<BK>(kp, t16, w);
@@ -286,70 +344,86 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
     KeyLeaf<NH> kl;
     kl.qs = qs;
 #pragma unroll
-    for (int h = 0; h < NH; ++h) kl.s[h] = 0.0f;
-    expand<BK, 7, 0>(w, 1.0f, cs1k, cshk, kl);
-    float p[NH];
+    for (int h = 0; h < NH; ++h) kl.s2[h] = make_float2(0.0f, 0.0f);
+    expand2<BK, 7, 0>(w, 1.0f, cs1k, cshk, kl);
+    const uint8_t* vp = sbuf + (2 + half) * kPolarPage;
+    const float rv = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(vp + 1024 + 2 * t16)));
+    float corr[NH];
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
-      const float sc = valid ? kl.s[h] * rk : -INFINITY;
+      const float sc = valid ? (kl.s2[h].x + kl.s2[h].y) * rk : -INFINITY;
       float mx = sc;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float mn = fmaxf(M[h], mx);
-      const float corr = (M[h] == -INFINITY) ? 0.0f : ex2(M[h] - mn);
-      p[h] = valid ? ex2(sc - mn) : 0.0f;
-      lsum[h] = lsum[h] * corr + p[h];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[h][k] *= corr;
+      corr[h] = (M[h] == -INFINITY) ? 0.0f : ex2(M[h] - mn);
+      const float p = valid ? ex2(sc - mn) : 0.0f;
+      lsum[h] = lsum[h] * corr[h] + p;
       M[h] = mn;
+      wts[lane * NH + h] = valid ? p * rv : 0.0f;
     }
-    // values: weights p r_V per token, directions through the shared tile
-    const uint8_t* vp = sbuf + (2 + half) * kPolarPage;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float c = corr[4 * nt + 0] * (tq == 0) + corr[4 * nt + 1] * (tq == 1) + corr[4 * nt + 2] * (tq == 2) +
+                      corr[4 * nt + 3] * (tq == 3);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[mt][nt][k] *= c;
+    }
+    // values: directions to the fp16 tile, then acc^T += V_hat^T W
     load_record<BV>(vp, t16, w);
-    const float rv = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(vp + 1024 + 2 * t16)));
+    expand2<BV, 7, 0>(w, 1.0f, cs1v, cshv, hl);
+    __syncwarp();
 #pragma unroll
-    for (int h = 0; h < NH; ++h) wts[lane * NH + h] = valid ? p[h] * rv : 0.0f;
-    const uint32_t c7 = slot_code<BV, kD - 2>(w);
-    const float2 cs7 = *reinterpret_cast<const float2*>(cshv + 2 * c7);
+    for (int kt = 0; kt < 2; ++kt) {
+      uint32_t bp[NT][2];
 #pragma unroll
-    for (int hv = 0; hv < 2; ++hv) {
-      ValueLeaf vl;
-      vl.row = tile + lane * 64;
-      vl.sw = lane & 7;
-      if (hv == 0) expand<BV, 6, 0>(w, cs7.x, cs1v, cshv, vl);
-      else expand<BV, 6, 1>(w, cs7.y, cs1v, cshv, vl);
-      __syncwarp();
-      // lane L: coordinates 64 hv + 2L, + 1 of every token
-      for (int t = 0; t < 32; ++t) {
-        const float2 v2 = *reinterpret_cast<const float2*>(tile + t * 64 + ((((lane >> 1) ^ (t & 7)) << 2) | ((lane & 1) << 1)));
-#pragma unroll
-        for (int h4 = 0; h4 < NH / 4; ++h4) {
-          const float4 wv = *reinterpret_cast<const float4*>(wts + t * NH + 4 * h4);
-          const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            acc[4 * h4 + k][2 * hv] = fmaf(wa[k], v2.x, acc[4 * h4 + k][2 * hv]);
-            acc[4 * h4 + k][2 * hv + 1] = fmaf(wa[k], v2.y, acc[4 * h4 + k][2 * hv + 1]);
-          }
-        }
+      for (int nt = 0; nt < NT; ++nt) {
+        const int hd = 4 * nt + (g >> 1), t0 = 16 * kt + 2 * tq;
+        bp[nt][0] = half2_part(wts[t0 * NH + hd], wts[(t0 + 1) * NH + hd], g & 1);
+        bp[nt][1] = half2_part(wts[(t0 + 8) * NH + hd], wts[(t0 + 9) * NH + hd], g & 1);
       }
-      __syncwarp();
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t af[4];
+        const int c = 2 * mt + (mat & 1);
+        ldsm_x4_t(v_row + (uint32_t)(kt * 16 * 256) + (uint32_t)((c ^ mr) << 4), af);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16(acc[mt][nt], af, bp[nt][0], bp[nt][1]);
+      }
     }
+    __syncwarp();  // tile and weights are rewritten by the next stage
   }
   cp_async_wait<0>();
 
-  // partial of each live head: unnormalised acc, (max, denominator)
-  for (int h = 0; h < nh; ++h) {
-    float l = lsum[h];
+  // partials: unnormalised acc of head 4 nt + tq (hi + lo columns), (max, denominator)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    const int64_t slot = ((int64_t)b * a.Hq + h0 + h) * a.splits + s;
-    float* pr = a.part + slot * kD;
-    *reinterpret_cast<float2*>(pr + 2 * lane) = make_float2(acc[h][0], acc[h][1]);
-    *reinterpret_cast<float2*>(pr + 64 + 2 * lane) = make_float2(acc[h][2], acc[h][3]);
-    if (lane == 0) {
-      a.ml[2 * slot] = M[h];
-      a.ml[2 * slot + 1] = l;
+  for (int h = 0; h < NH; ++h) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], o);
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = 4 * nt + tq;
+    if (h < nh) {
+      const int64_t slot = ((int64_t)b * a.Hq + h0 + h) * a.splits + s;
+      float* pr = a.part + slot * kD;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        pr[16 * mt + g] = acc[mt][nt][0] + acc[mt][nt][1];
+        pr[16 * mt + g + 8] = acc[mt][nt][2] + acc[mt][nt][3];
+      }
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      if (h < nh) {
+        const int64_t slot = ((int64_t)b * a.Hq + h0 + h) * a.splits + s;
+        a.ml[2 * slot] = M[h];
+        a.ml[2 * slot + 1] = lsum[h];
+      }
     }
   }
 }
@@ -357,7 +431,7 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
 template <int BK, int BV, int NH>
 cudaError_t run_polar_decode(const PolarDecodeArgs& a, cudaStream_t st) {
   auto kern = k_polar_decode<BK, BV, NH>;
-  constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 64 * 4;
+  constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 256;
   constexpr size_t smem = 512 + (size_t)kPolarNW * kWarpBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
