@@ -48,6 +48,13 @@ static PolarGrid polar_grid(int bits) {
     const double t = std::tan(k * wh);
     g.th[k] = (float)(t * t);
   }
+  // cell table over u = min / max of a pair's squared radii in [0, 1]: the edges with
+  // tan^2 <= 1 are at least 0.0097 apart (4 bits), so no cell of 1/256 holds two
+  for (int i = 0; i < 256; ++i) {
+    int c = 0;
+    for (int k = 1; k < n; ++k) c += (double)g.th[k] <= i / 256.0 ? 1 : 0;
+    g.ucell[i] = (uint8_t)c;
+  }
   for (int k = 0; k < n; ++k) {
     const double a1 = (k + 0.5) * w1 - pi, ah = (k + 0.5) * wh;
     g.cs1[2 * k] = (float)std::cos(a1);
@@ -70,27 +77,34 @@ __device__ __forceinline__ uint32_t edge_count(float sa, float sb, const float* 
   return c;
 }
 
-// Code of a level >= 2 angle from the squared radii of its pair.  sb <= 0 gives
-// code 0 (theta = 0, which also covers a pair of two zeros).
+// Code of a level >= 2 angle from the squared radii (sa, sb) of its pair:
+// #{k : sb >= sa tan^2(e_k)}.  With u = min / max in [0, 1] the count below pi/4 is
+// ucell[floor(256 u)] plus one more if u passes the next edge; above pi/4
+// (sb > sa) the angle is pi/2 - atan(sqrt u) and the count is mirrored.  A pair of
+// two zeros has angle 0 (u = 0, no mirror).
 template <int BITS>
-__device__ __forceinline__ uint32_t code_high(float sa, float sb, const float* th) {
-  return edge_count<(1 << BITS)>(sa, sb > 0.0f ? sb : -1.0f, th);
+__device__ __forceinline__ uint32_t code_high(float sa, float sb, const float* th, const uint8_t* ucell) {
+  constexpr uint32_t N = 1u << BITS;
+  const bool up = sb > sa;
+  const float lo = up ? sa : sb, hi = up ? sb : sa;
+  const float u = hi > 0.0f ? __fdividef(lo, hi) : 0.0f;
+  const uint32_t k0 = ucell[min((int)(u * 256.0f), 255)];
+  const uint32_t c = k0 + (u >= th[k0 + 1] ? 1u : 0u);
+  return up ? (N - 1u) - c : c;
 }
 
 // Code of a level-1 angle of the pair (x, y) = (y_{2i}, y_{2i+1}); t1a, t1b = tan^2
 // of the first and third edges inside a quadrant (4-bit grids; the middle edge,
-// pi/4, is the exact test sv >= su).
+// pi/4, is the exact test sv >= su).  Branch-free.
 template <int BITS>
 __device__ __forceinline__ uint32_t code_level1(float x, float y, float t1a, float t1b) {
   constexpr uint32_t M = (1u << BITS) / 4;  // cells per quadrant
   // quadrant of (u, v) = (-x, -y): 0: u > 0, v >= 0; 1: u <= 0, v > 0; 2: u < 0, v <= 0;
   // 3: u >= 0, v < 0; a pair of two zeros has theta = 0, i.e. phi = pi: code 2M
-  uint32_t quad;
-  if (x < 0.0f && y <= 0.0f) quad = 0;
-  else if (x >= 0.0f && y < 0.0f) quad = 1;
-  else if (x > 0.0f && y >= 0.0f) quad = 2;
-  else if (y > 0.0f) quad = 3;
-  else return 2 * M;
+  const uint32_t q1 = (x >= 0.0f && y < 0.0f) ? 1u : 0u;
+  const uint32_t q2 = (x > 0.0f && y >= 0.0f) ? 2u : 0u;
+  const uint32_t q3 = (x <= 0.0f && y > 0.0f) ? 3u : 0u;
+  const uint32_t quad = q1 | q2 | q3;
   // rotated into the first quadrant: (u', v') = (u, v), (v, -u), (-u, -v), (-v, u)
   const float xx = x * x, yy = y * y;
   const bool swap = quad & 1u;
@@ -101,7 +115,8 @@ __device__ __forceinline__ uint32_t code_level1(float x, float y, float t1a, flo
     sub = sv >= su ? 2u : 0u;
     sub += sv >= su * (sub ? t1b : t1a) ? 1u : 0u;
   }
-  return quad * M + sub;
+  const uint32_t code = quad * M + sub;
+  return (x == 0.0f && y == 0.0f) ? 2 * M : code;
 }
 
 __device__ __forceinline__ uint16_t f16_bits(float v) { return __half_as_ushort(__float2half_rn(v)); }
@@ -143,10 +158,12 @@ __device__ __forceinline__ void pack_slots(const uint32_t (&b)[8], uint32_t (&w)
 // The codes go through a per-vector byte array in shared memory (slot order), from
 // which lane q packs and stores record bits [32 BITS q, 32 BITS (q + 1)).
 template <int BITS, typename TIn>
-__global__ void __launch_bounds__(256) k_polar_append(PolarAppendArgs a) {
+__global__ void __launch_bounds__(256, 3) k_polar_append(PolarAppendArgs a) {
   __shared__ float s_th[16];
+  __shared__ uint8_t s_ucell[256];
   __shared__ __align__(16) uint8_t s_codes[8][8][128];  // [warp][vector of the warp][slot]
   if (threadIdx.x < 16) s_th[threadIdx.x] = a.grid.th[threadIdx.x];
+  s_ucell[threadIdx.x] = a.grid.ucell[threadIdx.x];  // 256 threads
   __syncthreads();
   const int lane = threadIdx.x & 31, q = lane & 3;
   uint8_t* rec_s = s_codes[threadIdx.x >> 5][lane >> 2];
@@ -199,27 +216,27 @@ __global__ void __launch_bounds__(256) k_polar_append(PolarAppendArgs a) {
     uint32_t b2[2] = {0u, 0u}, b3 = 0u, b4 = 0u, c5;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      b2[i >> 2] |= code_high<BITS>(s[2 * i], s[2 * i + 1], s_th) << (8 * (i & 3));
+      b2[i >> 2] |= code_high<BITS>(s[2 * i], s[2 * i + 1], s_th, s_ucell) << (8 * (i & 3));
       s[i] = s[2 * i] + s[2 * i + 1];
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      b3 |= code_high<BITS>(s[2 * i], s[2 * i + 1], s_th) << (8 * i);
+      b3 |= code_high<BITS>(s[2 * i], s[2 * i + 1], s_th, s_ucell) << (8 * i);
       s[i] = s[2 * i] + s[2 * i + 1];
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      b4 |= code_high<BITS>(s[2 * i], s[2 * i + 1], s_th) << (8 * i);
+      b4 |= code_high<BITS>(s[2 * i], s[2 * i + 1], s_th, s_ucell) << (8 * i);
       s[i] = s[2 * i] + s[2 * i + 1];
     }
-    c5 = code_high<BITS>(s[0], s[1], s_th);
+    c5 = code_high<BITS>(s[0], s[1], s_th, s_ucell);
     const float s5 = s[0] + s[1];
     // levels 6 and 7 from the quad's four squared radii (every lane computes them)
     const int base = lane & ~3;
     const float r0 = __shfl_sync(0xffffffffu, s5, base), r1 = __shfl_sync(0xffffffffu, s5, base + 1);
     const float r2 = __shfl_sync(0xffffffffu, s5, base + 2), r3 = __shfl_sync(0xffffffffu, s5, base + 3);
-    const uint32_t c6a = code_high<BITS>(r0, r1, s_th), c6b = code_high<BITS>(r2, r3, s_th);
-    const uint32_t c7 = code_high<BITS>(r0 + r1, r2 + r3, s_th);
+    const uint32_t c6a = code_high<BITS>(r0, r1, s_th, s_ucell), c6b = code_high<BITS>(r2, r3, s_th, s_ucell);
+    const uint32_t c7 = code_high<BITS>(r0 + r1, r2 + r3, s_th, s_ucell);
     // codes to the vector's byte array in slot order
     *reinterpret_cast<uint4*>(rec_s + 16 * q) = make_uint4(b1[0], b1[1], b1[2], b1[3]);  // level 1
     *reinterpret_cast<uint2*>(rec_s + 64 + 8 * q) = make_uint2(b2[0], b2[1]);            // level 2

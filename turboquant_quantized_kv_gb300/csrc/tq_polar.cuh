@@ -22,6 +22,7 @@ struct PolarGrid {
   float th[16];    // levels >= 2: tan^2 of the edges k pi / 2^(b+1), index 1..2^b-1
   float cs1[32];   // level 1 midpoints: (cos, sin) of theta_hat_k, k < 2^b, interleaved
   float csh[32];   // levels >= 2: (cos, sin) of theta_hat_k
+  uint8_t ucell[256];  // levels >= 2: #{k : th[k] <= i / 256}, at most one edge per cell
 };
 
 // ------------------------------------------------------------------ direction
@@ -209,7 +210,7 @@ template <int BK, int BV, int NH>
 __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeArgs a) {
   constexpr int NT = NH / 4;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  float* tabs = reinterpret_cast<float*>(smem_raw);  // cs1k, cshk, cs1v, cshv
+  __shared__ __align__(16) float tabs[128];  // cs1k, cshk, cs1v, cshv (static: lookups address code * 8 + constant)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x < 32) {
     tabs[threadIdx.x] = a.cs1k[threadIdx.x];
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
     tabs[96 + threadIdx.x] = a.cshv[threadIdx.x];
   }
   constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 256;
-  uint8_t* wbase = smem_raw + 512 + warp * kWarpBytes;
+  uint8_t* wbase = smem_raw + warp * kWarpBytes;
   uint8_t* ring = wbase;
   float* qs = reinterpret_cast<float*>(wbase + kPolarStages * kPolarStage);  // [64 pairs][NH][2]
   float* wts = qs + 128 * NH;                                                  // [32][NH]
@@ -432,7 +433,7 @@ template <int BK, int BV, int NH>
 cudaError_t run_polar_decode(const PolarDecodeArgs& a, cudaStream_t st) {
   auto kern = k_polar_decode<BK, BV, NH>;
   constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 256;
-  constexpr size_t smem = 512 + (size_t)kPolarNW * kWarpBytes;
+  constexpr size_t smem = (size_t)kPolarNW * kWarpBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = (a.chunks + kPolarNW - 1) / kPolarNW;
