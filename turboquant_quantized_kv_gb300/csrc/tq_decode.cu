@@ -1421,7 +1421,7 @@ constexpr int decode_nw(bool packed_plain, int nt, bool fp8_keys = false) {
 }
 
 int decode_warps(const tq_cache_desc& d, int g) {
-  if (d.fmt.kv_format == TQ_KV_POLAR) return 8;  // two CTAs of four warps per SM
+  if (d.fmt.kv_format == TQ_KV_POLAR) return g <= 4 ? 12 : 8;  // three (two) CTAs of four warps per SM
   const bool k8 = d.fmt.kv_format == TQ_KV_K8V4;
   return decode_nw((d.fmt.kv_format == TQ_KV_PACKED && !d.fmt.qjl_k) || k8, g <= 4 ? 1 : 2, k8);
 }

@@ -75,7 +75,7 @@ __device__ __forceinline__ void expand2(const uint32_t (&w)[16], float val, cons
 // ------------------------------------------------------------------ decode
 
 constexpr int kPolarNW = 4;          // warps per decode CTA (two CTAs per SM)
-constexpr int kPolarStages = 3;      // ring depth (stages of two blocks)
+constexpr int kPolarStages = 2;      // ring depth (stages of two blocks)
 constexpr int kPolarPage = 16 * 64 + 32;  // a page in shared memory: 16 records padded to 64 B + radii
 constexpr int kPolarStage = 4 * kPolarPage;  // K and V pages of two blocks
 
@@ -171,9 +171,10 @@ struct KeyLeaf {
   }
 };
 
-// Value leaf: the direction as fp16 in its token's row (256 B) of the [32][128]
-// tile: 16-byte chunk c (coordinates 8c .. 8c + 7) at position c ^ (row & 7), so
-// the chunk stores of a warp and the ldmatrix rows never share banks.
+// Value leaf: one half (64 coordinates) of the direction as fp16 in its token's
+// row (128 B) of the [32][64] tile: 16-byte chunk c (coordinates 8c .. 8c + 7 of
+// the half) at position c ^ (row & 7), so the chunk stores of a warp and the
+// ldmatrix rows never share banks.
 struct HalfLeaf {
   uint32_t h[4];
   uint8_t* row;
@@ -182,7 +183,7 @@ struct HalfLeaf {
   __device__ __forceinline__ void pair(float2 v) {
     h[I & 3] = half2_bits(v.x, v.y);
     if constexpr ((I & 3) == 3)
-      *reinterpret_cast<uint4*>(row + (((I >> 2) ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(row + ((((I >> 2) & 7) ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
   }
 };
 
@@ -202,12 +203,12 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], u
 // One warp per chunk = (sequence b, KV head, head group, split s).  Per stage of
 // two blocks (32 tokens) lane t handles token t: it rebuilds the unit direction of
 // the key in fp32 pairs and dots it with the rotated queries (logits in fp32),
-// then rebuilds the value direction into an fp16 tile; acc^T (128 x 8 per n-tile)
-// += V_hat^T x W on tensor cores with W = p r_V split into fp16 hi / lo columns
+// then rebuilds the value direction, one half of 64 coordinates at a time, into an
+// fp16 tile; acc^T (128 x 8 per n-tile) += V_hat^T x W on tensor cores with W = p r_V split into fp16 hi / lo columns
 // (8 columns = 4 heads x {hi, lo}).  In the MMA layout lane (g, t) owns head
 // 4 nt + t, coordinates 16 mt + g and 16 mt + g + 8.
 template <int BK, int BV, int NH>
-__global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeArgs a) {
+__global__ void __launch_bounds__(kPolarNW * 32, NH == 4 ? 3 : 2) k_polar_decode(PolarDecodeArgs a) {
   constexpr int NT = NH / 4;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ __align__(16) float tabs[128];  // cs1k, cshk, cs1v, cshv (static: lookups address code * 8 + constant)
@@ -218,12 +219,12 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
     tabs[64 + threadIdx.x] = a.cs1v[threadIdx.x];
     tabs[96 + threadIdx.x] = a.cshv[threadIdx.x];
   }
-  constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 256;
+  constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 128;
   uint8_t* wbase = smem_raw + warp * kWarpBytes;
   uint8_t* ring = wbase;
   float* qs = reinterpret_cast<float*>(wbase + kPolarStages * kPolarStage);  // [64 pairs][NH][2]
   float* wts = qs + 128 * NH;                                                  // [32][NH]
-  uint8_t* tile = reinterpret_cast<uint8_t*>(wts + 32 * NH);                   // [32][256 B] fp16
+  uint8_t* tile = reinterpret_cast<uint8_t*>(wts + 32 * NH);                   // [32][128 B] fp16
   __syncthreads();
   const int64_t chunk = (int64_t)blockIdx.x * kPolarNW + warp;
   if (chunk >= a.chunks) return;
@@ -300,7 +301,6 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
     cp_async_commit();
   };
   issue(0);
-  issue(1);
 
   float M[NH], lsum[NH], acc[8][NT][4];
 #pragma unroll
@@ -319,16 +319,16 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
   const int half = lane >> 4, t16 = lane & 15;
   const int g = lane >> 2, tq = lane & 3;
   HalfLeaf hl;
-  hl.row = tile + lane * 256;
+  hl.row = tile + lane * 128;
   hl.sw = lane & 7;
   const uint32_t tile_u = (uint32_t)__cvta_generic_to_shared(tile);
   const int mat = lane >> 3, mr = lane & 7;
   // ldmatrix rows of the transposed value tiles (token 16 kt + mr + 8 (mat >> 1))
-  const uint32_t v_row = tile_u + (uint32_t)((mr + ((mat >> 1) << 3)) * 256);
+  const uint32_t v_row = tile_u + (uint32_t)((mr + ((mat >> 1) << 3)) * 128);
 
   for (int st = 0; st < n_st; ++st) {
-    issue(st + 2);
-    cp_async_wait<2>();
+    issue(st + 1);
+    cp_async_wait<1>();
     __syncwarp();
     const uint8_t* sbuf = ring + (st % kPolarStages) * kPolarStage;
     const int jb = j0 + 2 * st + half;
@@ -363,38 +363,49 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
       M[h] = mn;
       wts[lane * NH + h] = valid ? p * rv : 0.0f;
     }
+    bool moved = false;  // warp-uniform: the running maxima are
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const float c = corr[4 * nt + 0] * (tq == 0) + corr[4 * nt + 1] * (tq == 1) + corr[4 * nt + 2] * (tq == 2) +
-                      corr[4 * nt + 3] * (tq == 3);
+    for (int h = 0; h < NH; ++h) moved |= corr[h] != 1.0f;
+    if (moved) {
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
+      for (int nt = 0; nt < NT; ++nt) {
+        const float c = tq == 0 ? corr[4 * nt] : tq == 1 ? corr[4 * nt + 1] : tq == 2 ? corr[4 * nt + 2] : corr[4 * nt + 3];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) acc[mt][nt][k] *= c;
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) acc[mt][nt][k] *= c;
+      }
     }
-    // values: directions to the fp16 tile, then acc^T += V_hat^T W
+    // values: directions to the fp16 tile one half at a time, then acc^T += V_hat^T W
     load_record<BV>(vp, t16, w);
-    expand2<BV, 7, 0>(w, 1.0f, cs1v, cshv, hl);
-    __syncwarp();
+    __syncwarp();  // weights of every token written
+    uint32_t bp[2][NT][2];
 #pragma unroll
-    for (int kt = 0; kt < 2; ++kt) {
-      uint32_t bp[NT][2];
+    for (int kt = 0; kt < 2; ++kt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int hd = 4 * nt + (g >> 1), t0 = 16 * kt + 2 * tq;
-        bp[nt][0] = half2_part(wts[t0 * NH + hd], wts[(t0 + 1) * NH + hd], g & 1);
-        bp[nt][1] = half2_part(wts[(t0 + 8) * NH + hd], wts[(t0 + 9) * NH + hd], g & 1);
+        bp[kt][nt][0] = half2_part(wts[t0 * NH + hd], wts[(t0 + 1) * NH + hd], g & 1);
+        bp[kt][nt][1] = half2_part(wts[(t0 + 8) * NH + hd], wts[(t0 + 9) * NH + hd], g & 1);
       }
+    const float2 cs7 = *reinterpret_cast<const float2*>(cshv + 2 * slot_code<BV, kD - 2>(w));
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        uint32_t af[4];
-        const int c = 2 * mt + (mat & 1);
-        ldsm_x4_t(v_row + (uint32_t)(kt * 16 * 256) + (uint32_t)((c ^ mr) << 4), af);
+    for (int hv = 0; hv < 2; ++hv) {
+      if (hv == 0) expand2<BV, 6, 0>(w, cs7.x, cs1v, cshv, hl);
+      else expand2<BV, 6, 1>(w, cs7.y, cs1v, cshv, hl);
+      __syncwarp();
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_f16(acc[mt][nt], af, bp[nt][0], bp[nt][1]);
-      }
+      for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+          uint32_t af[4];
+          const int c = 2 * m4 + (mat & 1);
+          ldsm_x4_t(v_row + (uint32_t)(kt * 16 * 128) + (uint32_t)((c ^ mr) << 4), af);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_f16(acc[4 * hv + m4][nt], af, bp[kt][nt][0], bp[kt][nt][1]);
+        }
+      __syncwarp();
     }
-    __syncwarp();  // tile and weights are rewritten by the next stage
   }
   cp_async_wait<0>();
 
@@ -432,7 +443,7 @@ __global__ void __launch_bounds__(kPolarNW * 32, 2) k_polar_decode(PolarDecodeAr
 template <int BK, int BV, int NH>
 cudaError_t run_polar_decode(const PolarDecodeArgs& a, cudaStream_t st) {
   auto kern = k_polar_decode<BK, BV, NH>;
-  constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 256;
+  constexpr int kWarpBytes = kPolarStages * kPolarStage + (128 + 32) * NH * 4 + 32 * 128;
   constexpr size_t smem = (size_t)kPolarNW * kWarpBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
