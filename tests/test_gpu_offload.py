@@ -29,7 +29,7 @@ def filled_layer(cuda, tq, kv, B=3, Hkv=4, T=200, seed=0):
     mb = -(-T // 16)
     bt, nb = workloads.shuffled_block_table(seed + 3, B, mb, num_blocks=B * mb + 5)
     kw = {"packed": dict(), "qjl": dict(bits_k=2, qjl=True, qjl_seed=4), "bf16": dict(kv_format="bf16"),
-          "k8v4": dict(kv_format="k8v4", bits_v=3)}[kv]
+          "k8v4": dict(kv_format="k8v4", bits_v=3), "polar": dict(kv_format="polar", bits_k=4, bits_v=3)}[kv]
     layer = tq.Layer(nb, Hkv, seed=seed + 1, layer=2, fill=0x11, **kw)
     kb, vb = workloads.scaled_gaussian_kv(seed + 5, B * T, Hkv, D, scale=3.0)
     k = cuda.from_numpy(kb.view(np.int16)).cuda().view(cuda.bfloat16)
@@ -42,7 +42,7 @@ def decode(cuda, layer, bt, ctx, q):
     return layer.decode(q, cuda.from_numpy(bt).cuda(), cuda.from_numpy(ctx).cuda(), out_dtype=cuda.float32).cpu().numpy()
 
 
-@pytest.mark.parametrize("kv", ["packed", "qjl", "bf16", "k8v4"])
+@pytest.mark.parametrize("kv", ["packed", "qjl", "bf16", "k8v4", "polar"])
 def test_offload_restore_round_trip(cuda, tqlib, kv):
     tq = tqlib
     layer, bt, nb, ctx = filled_layer(cuda, tq, kv)

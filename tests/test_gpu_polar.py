@@ -297,3 +297,34 @@ def test_polar_full_size_sampled(cuda, tqlib):
             w = np.exp(s - s.max())
             ref = (w / w.sum()) @ vh
             assert max_rel_err(out[b, h][None], ref[None]) <= TOL_BF16
+
+
+def test_polar_append_decode_fused_equals_separate_calls(cuda, tqlib):
+    """tq_append_decode on a polar layer: the same pages and the same output as
+    tq_quantize_append followed by tq_decode_attention."""
+    tq = tqlib
+    B, Hq, Hkv, T = 2, 8, 2, 150
+    mb = math.ceil((T + 1) / 16)
+    bt, nb = workloads.shuffled_block_table(31, B, mb, num_blocks=B * mb + 1)
+    kb, vb = workloads.lognormal_channel_kv(33, B * T, Hkv, D)
+    nk, nv = workloads.lognormal_channel_kv(34, B, Hkv, D)  # one new token per sequence
+    slots = cuda.from_numpy(workloads.prefill_slots(bt, T).astype(np.int64)).cuda()
+    new_slots = cuda.from_numpy(workloads.slot_mapping(bt, np.full((B, 1), T)).reshape(-1).astype(np.int64)).cuda()
+    ctx = cuda.from_numpy(np.full(B, T + 1, np.int32)).cuda()
+    q = dev_bf16(cuda, workloads.queries(35, B, Hq, D))
+    btd = cuda.from_numpy(bt).cuda()
+    outs, pools = [], []
+    for fused in (False, True):
+        layer = tq.Layer(nb, Hkv, kv_format="polar", bits_k=3, bits_v=4, seed=3, layer=1)
+        layer.append(dev_bf16(cuda, kb), dev_bf16(cuda, vb), slots)
+        if fused:
+            out = layer.append_decode(dev_bf16(cuda, nk), dev_bf16(cuda, nv), new_slots, q, btd, ctx,
+                                      out_dtype=cuda.float32)
+        else:
+            layer.append(dev_bf16(cuda, nk), dev_bf16(cuda, nv), new_slots)
+            out = layer.decode(q, btd, ctx, out_dtype=cuda.float32)
+        outs.append(out.cpu().numpy())
+        pools.append((layer.k_cache.cpu().numpy(), layer.v_cache.cpu().numpy()))
+    assert tq.get_device_status() == 0
+    assert np.array_equal(pools[0][0], pools[1][0]) and np.array_equal(pools[0][1], pools[1][1])
+    assert np.array_equal(outs[0], outs[1])
