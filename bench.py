@@ -42,6 +42,24 @@ METRIC = "decode-attn packed-KV GB/s"
 WORKLOAD = "llama3-8b-shaped GQA decode, B16 Hq32 Hkv8 d128 ctx8192, 32 layers, 4-bit K/V, Hadamard"
 
 
+def job_ms(ms_local, device=None):
+    """The job's timed-region length in ms: the maximum over ranks (the job ends with
+    its slowest rank); a single process returns its own."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms_local)
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank, world, ms_total):
+    """Whole-job throughput (units per second): the units all ranks processed (each
+    rank runs an independent replica of the same work) over the job's time."""
+    return units_per_rank * world / (ms_total * 1e-3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -474,11 +492,7 @@ def run_tq(args):
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = job_ms(t0.elapsed_time(t1), dev)
     ms_step = ms_total / args.steps
     # decode timings of the last min(ng, steps) timed steps, one layer each
     sampled = list(range(max(0, args.steps - ng), args.steps))
@@ -490,7 +504,7 @@ def run_tq(args):
         ctx_s = ctx_start + s_ + 1
         return B * HKV * ctx_s * BYTES_PER_TOKEN_HEAD + B * st["mb"] * 4 + 2 * B * HQ * D * 2
     bytes_steps = sum(LAYERS * call_bytes(s_) for s_ in range(args.steps))
-    value = bytes_steps * world / (ms_total * 1e-3) / 1e9
+    value = job_value(bytes_steps, world, ms_total) / 1e9
     peak, peak_kind = peaks()
     dec_avg_ms = statistics.mean(dec_ms)
     achieved = statistics.mean(call_bytes(s_) for s_ in sampled) / (dec_avg_ms * 1e-3) / 1e9
