@@ -8,30 +8,30 @@
 // Grids and the record layout are specified in include/tq.h.
 //
 // Angle codes without trigonometry.  With squared radii s = rho^2 of a pair
-// (a, b) >= 0, theta >= e  <=>  b^2 >= a^2 tan^2(e) for e in [0, pi/2), so the
+// (a, b) >= 0, theta >= e  <=>  b^2 >= a^2 tan^2(e) for e in [0, pi/2), so a
 // level-l (l >= 2) code is the number of grid edges e_k = k pi / 2^(b+1) with
-// s_b >= s_a tan^2(e_k): a branch-free binary search over a 2^b - 1 entry
-// table of tan^2 values.  Level 1 (the whole circle) first takes the quadrant
-// of (-y_{2i}, -y_{2i+1}) -- phi = theta + pi mod 2 pi -- from the signs, then
-// the same search inside the quadrant over 2^b / 4 cells.  Only squared sums
-// are carried up the levels: no sqrt, no atan2.
+// s_b >= s_a tan^2(e_k): with u = min / max of the two squared radii, a 256-cell
+// table over u gives the count below pi/4 up to one more edge test, mirrored
+// above pi/4.  Level 1 (the whole circle) takes the quadrant of
+// (-y_{2i}, -y_{2i+1}) -- phi = theta + pi mod 2 pi -- from the signs, then one
+// exact (pi/4) and one tan^2 test inside the quadrant.  Only squared sums are
+// carried up the levels: no sqrt, no atan2.
 //
 // Kernels:
-//   k_polar_append   4 lanes per vector (lane q holds y[32q, 32q + 32)): signs,
-//                    FWHT, 31 angles per lane, the last two levels from the
-//                    quad's four squared radii; codes are gathered so lane q
-//                    writes record bits [32 b q, 32 b (q + 1)).
-//   k_polar_decode   one warp per (sequence, KV head, head group, split) chunk;
-//                    pages stream through a 3-stage cp.async ring of two blocks
-//                    (32 tokens: lane = token).  Each lane rebuilds its key's
-//                    unit direction depth-first (product of cos / sin of the
-//                    midpoint angles, looked up in shared memory) and dots it
-//                    with the rotated queries; the value directions go through a
-//                    swizzled shared tile to a lane = coordinates layout for the
-//                    weighted sum.  One partial per (query head, split).
+//   k_polar_append   4 lanes per vector (lane q holds y[32q, 32q + 32)): signs on
+//                    the packed bf16 words, packed-pair FWHT, 31 angles per lane,
+//                    the last two levels from the quad's four squared radii;
+//                    codes are staged per vector in shared memory so lane q packs
+//                    and writes record bits [32 b q, 32 b (q + 1)).
+//   k_polar_decode   (tq_polar.cuh) one warp per (sequence, KV head, head group,
+//                    split) chunk; pages stream through a two-stage cp.async ring
+//                    of two blocks (32 tokens: lane = token).  Key logits in fp32
+//                    pairs from the depth-first rebuild of each key's unit
+//                    direction; value directions through an fp16 tile into
+//                    tensor-core MMAs.  One partial per (query head, split).
 //   k_polar_combine  CTA per (sequence, query head): log-sum-exp merge of the
 //                    splits and the inverse rotation Pi^T.
-//   k_polar_dequant  warp per vector: x_hat = r Pi^T y_hat.
+//   k_polar_dequant  warp per 32 vectors: x_hat = r Pi^T y_hat.
 #include "tq_polar.cuh"
 
 namespace tq {
@@ -63,18 +63,6 @@ static PolarGrid polar_grid(int bits) {
     g.csh[2 * k + 1] = (float)std::sin(ah);
   }
   return g;
-}
-
-// #{k in 1..N-1 : sb >= sa * T[k]} for increasing T (N a power of two), by a
-// branch-free binary search; T in shared memory (distinct entries sit in
-// distinct banks, so lanes with different indices do not conflict).
-template <int N>
-__device__ __forceinline__ uint32_t edge_count(float sa, float sb, const float* T) {
-  uint32_t c = 0;
-#pragma unroll
-  for (int step = N / 2; step >= 1; step >>= 1)
-    if (sb >= sa * T[c + step]) c += step;
-  return c;
 }
 
 // Code of a level >= 2 angle from the squared radii (sa, sb) of its pair:
