@@ -14,7 +14,8 @@ Reported: value = packed K/V bytes read by decode per step / step time (GB/s);
 roofline for the decode call; quantize-append vectors/s from the prefill and
 from the dense-rotation burst (36 layers x 11,000 tokens); decode GB/s of a
 k8v4 layer (FP8 keys, 4-bit values) and the PolarQuant variant's append and
-decode (4-bit angles, fp16 radius) at the same shape; e2e through the public
+decode (4-bit angles, fp16 radius) at the same shape; decode GB/s at the
+long-context shape (4 x 131,072 tokens, groups of 8, 3/4 bits); e2e through the public
 API with host buffers; the oracle's CPU throughput.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
@@ -246,6 +247,55 @@ def decode_k8v4(torch, tq, dev, peak, reps=20):
     return {"workload": "k8v4 layer: B16 Hq32 Hkv8 d128 ctx8192, FP8 E4M3 keys + 4-bit values", "bytes": nbytes,
             "ms": round(med, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "calls": reps,
             "device_status": status}
+
+
+def decode_long_context(torch, tq, dev, peak, reps=10):
+    """Decode at the long-context shape (batch 4, 64 query / 8 KV heads: groups of 8,
+    context 131,072, 3-bit keys / 4-bit values, Hadamard, bf16 with 1 % Student-t(3)
+    elements, shuffled table): 120 B per token and KV head, ~503.3 MB per call.
+    Median of `reps` calls timed with CUDA events."""
+    import workloads
+    b4, hq, hkv, t = 4, 64, 8, 131072
+    mb = t // BLOCK
+    bt_np, nb = workloads.shuffled_block_table(781, b4, mb)
+    bt = torch.from_numpy(bt_np).to(dev)
+    layer = tq.Layer(nb, hkv, bits_k=3, bits_v=4, seed=1, layer=0, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(782)
+    slots = torch.from_numpy(workloads.prefill_slots(bt_np, t)).to(dev)
+    for half in range(2):  # append in two halves (bf16 inputs of 1 GB each)
+        sl = slots[half * (b4 * t // 2):(half + 1) * (b4 * t // 2)]
+        n = sl.numel()
+        def heavy():  # N(0, 1) with 1 % of the elements replaced by Student-t(3) draws
+            x = torch.randn(n, hkv, D, generator=gen, device=dev)
+            m = torch.rand(n, hkv, D, generator=gen, device=dev) < 0.01
+            z = torch.randn(4, int(m.sum()), generator=gen, device=dev)
+            x[m] = z[0] / torch.sqrt((z[1] ** 2 + z[2] ** 2 + z[3] ** 2) / 3.0)
+            return x.to(torch.bfloat16)
+        layer.append(heavy(), heavy(), sl)
+    q = torch.randn(b4, hq, D, generator=gen, device=dev).to(torch.bfloat16)
+    ctx = torch.full((b4,), t, dtype=torch.int32, device=dev)
+    out = torch.empty(b4, hq, D, dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(layer.workspace_bytes(b4, hq, mb), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        layer.decode(q, bt, ctx, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        layer.decode(q, bt, ctx, out=out, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    med = statistics.median(ms)
+    nbytes = b4 * hkv * t * (D * 3 // 8 + 4 + D * 4 // 8 + 4)
+    gbs = nbytes / (med * 1e-3) / 1e9
+    status = tq.get_device_status()
+    del layer, ws
+    torch.cuda.empty_cache()
+    return {"workload": "long context: B4 Hq64 Hkv8 d128 ctx131072, 3-bit K / 4-bit V, 1% Student-t(3) elements",
+            "bytes": nbytes, "ms": round(med, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "calls": reps, "device_status": status}
 
 
 def polar_layer(torch, tq, dev, peak, reps=20):
@@ -528,6 +578,7 @@ def run_tq(args):
     e2e = run_e2e(torch, st, args, stream) if args.e2e else None
     dense = dense_burst(torch, tq, dev, peak) if args.dense_burst else None
     k8 = decode_k8v4(torch, tq, dev, peak) if args.k8v4 else None
+    lc = decode_long_context(torch, tq, dev, peak) if args.long_context else None
     pol = polar_layer(torch, tq, dev, peak) if args.polar else None
     off = offload_restore(torch, st) if args.offload else None
     incr = incremental_dequant_baseline(torch, tq, st, dev, peak) if args.incremental else None
@@ -548,6 +599,7 @@ def run_tq(args):
                    "vectors": st["append_vectors"], "bytes_per_vector": APPEND_BYTES_PER_VECTOR},
         "append_dense_burst": dense,
         "decode_k8v4": k8,
+        "decode_long_context": lc,
         "polar": pol,
         "offload_restore": off,
         "incremental_dequant_baseline": incr,
@@ -714,6 +766,8 @@ def main():
     ap.add_argument("--no-k8v4", dest="k8v4", action="store_false", help="skip the k8v4 decode measurement")
     ap.add_argument("--no-offload", dest="offload", action="store_false", help="skip the offload/restore measurement")
     ap.add_argument("--no-polar", dest="polar", action="store_false", help="skip the PolarQuant-variant measurement")
+    ap.add_argument("--no-long-context", dest="long_context", action="store_false",
+                    help="skip the long-context (131,072-token, groups of 8) decode measurement")
     ap.add_argument("--no-incremental", dest="incremental", action="store_false",
                     help="skip the incremental-dequant baseline measurement")
     ap.add_argument("--no-dense-burst", dest="dense_burst", action="store_false",
