@@ -242,7 +242,12 @@ tq_status tq_quantize_append(const tq_cache_desc* desc, const void* k, const voi
  * [n_tokens][num_kv_heads][head_dim] (y = Pi x / ||x||), norms: device fp32
  * [n_tokens][num_kv_heads] (||x||).  Writes codes and gamma of the K
  * (which = 0) or V (which = 1) pool exactly as tq_quantize_append would from
- * the same y (no QJL residual).  Packed layers only. */
+ * the same y (no QJL residual).  Packed layers only.  It runs the quantizer of
+ * the kernel a bf16 append of the same layer and size would run (the cell-table
+ * quantizer of the bulk kernels for dense layers and for Hadamard calls of at
+ * least 24,576 vectors, the boundary search of the per-quad kernel otherwise),
+ * so every append quantizer can be checked on exact inputs; all of them give
+ * the same codes for the same y. */
 tq_status tq_quantize_rotated(const tq_cache_desc* desc, int which, const float* y, const float* norms,
                               const int64_t* slot_mapping, int64_t n_tokens, void* stream);
 

@@ -55,6 +55,68 @@ def test_quantizer_bit_exact_given_rotated_coordinates(cuda, tqlib, bits):
     assert np.all(rec[~written.reshape(nb, 16)] == 0xA5)
 
 
+def planted_coordinates(b32):
+    """Rotated coordinates that sit on the quantizer's decision points: every
+    boundary and its fp32 neighbours, the edges (i - 64) / 63 of the bulk
+    kernels' 127 lookup cells and their neighbours, signed zeros, tiny values
+    and the ends of [-1, 1] (with the first value past them)."""
+    f32 = np.float32
+    b32 = np.asarray(b32, f32)
+    edges = ((np.arange(1, 128) - 64) / 63.0).astype(f32)
+    pts = [b32, np.nextafter(b32, f32(-2)), np.nextafter(b32, f32(2)),
+           edges, np.nextafter(edges, f32(-2)), np.nextafter(edges, f32(2)),
+           np.array([0.0, -0.0, 1e-30, -1e-30, 1e-45, -1e-45, 1.0, -1.0], f32),
+           np.array([np.nextafter(f32(1), f32(2)), np.nextafter(f32(-1), f32(-2))], f32)]
+    return np.concatenate(pts).astype(f32)
+
+
+@pytest.mark.parametrize("kind", ["hadamard_bulk", "dense"])
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_bulk_quantizer_bit_exact_given_rotated_coordinates(cuda, tqlib, bits, kind):
+    """The quantizer of the two bulk append kernels (the staged FWHT kernel for
+    Hadamard appends of >= 24,576 vectors, the tensor-core kernel for dense
+    layers) fed the oracle's y: codes equal the oracle's boundary count exactly,
+    including coordinates planted on every boundary, its fp32 neighbours and
+    the edges of the kernels' lookup cells."""
+    tq = tqlib
+    if kind == "hadamard_bulk":
+        H, nb, n = 8, 200, 3079  # 24,632 vectors: the bulk path, with a ragged last tile
+        layer = tq.Layer(nb, H, bits_k=bits, bits_v=bits, fill=0xA5)
+    else:
+        H, nb, n = 3, 40, 301
+        layer = tq.Layer(nb, H, bits_k=bits, bits_v=bits, fill=0xA5, rot_kind=tq.TQ_ROT_DENSE, seed=2, layer=3)
+    c32, b32 = ocb.codebook_fp32(D, bits)
+    g = np.random.default_rng(100 + bits)
+    x = g.standard_normal((n, H, D))
+    y = (x / np.linalg.norm(x, axis=-1, keepdims=True)).astype(np.float32)
+    flat = y.reshape(-1)
+    pts = planted_coordinates(b32)
+    # each planted value at several coordinates of different vectors (every position mod 128 is hit)
+    for r in range(4):
+        idx = (np.arange(pts.size) * 131 + r * 977) % flat.size
+        flat[idx] = pts
+    norms = (g.random((n, H)) * 10 + 0.1).astype(np.float32)
+    norms[5, 1] = 0.0
+    slots, slots_d = make_slots(cuda, n, nb, 11, skip_every=17)
+    layer.quantize_rotated(1, cuda.from_numpy(y).cuda(), cuda.from_numpy(norms).cuda(), slots_d)
+    cuda.cuda.synchronize()
+    assert tq.get_device_status() == 0
+    vp = layer.v_cache.cpu().numpy()
+    fields = page_fields(layer, 1, vp)
+    expect = oq.codes_from_y(y, b32)
+    keep = slots >= 0
+    for h in range(H):
+        codes, gamma = slot_fields(fields, slots[keep], h)
+        assert np.array_equal(codes, expect[keep, h]), (h, int(np.sum(codes != expect[keep, h])))
+        cn = np.sqrt(np.sum(c32.astype(np.float64)[expect[keep, h]] ** 2, axis=-1))
+        ref = norms[keep, h].astype(np.float64) / cn
+        assert np.all(np.abs(gamma - ref) <= 1e-6 * np.abs(ref))
+    written = np.zeros(nb * 16, bool)
+    written[slots[keep]] = True
+    rec = opack_record_view(vp, nb, H, bits)
+    assert np.all(rec[~written.reshape(nb, 16)] == 0xA5)
+
+
 def opack_record_view(pool, nb, H, bits):
     """uint8 [nb, 16, H, record+4] view of code records and gammas (for fill checks)."""
     from oracle import pack as opack

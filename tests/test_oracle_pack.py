@@ -24,29 +24,50 @@ def read_golden():
 
 
 def test_page_worked_example():
+    """The qiita page's worked example: eight 4-bit codes packed two per byte and
+    the scale 0.125 as a little-endian fp32 give the printed bytes, and the two
+    bf16 values give theirs."""
     g = read_golden()
     codes = [int(v) for v in g["codes"].split()]
     scale = float(g["scale"])
     packed4 = pack.pack_bits(codes, 4) + struct.pack("<f", scale)
     bf16 = workloads.bf16_bits(np.array([float(v) for v in g["bf16_values"].split()], np.float32))
-    bf16_bytes = bf16.astype("<u2").tobytes()
     assert packed4.hex() == g["packed4"]
-    assert bf16_bytes.hex() == g["bf16"]
-    # the page's arena: 0xA5 fill, bf16 at offset 0, packed4 at offset 16; save, clear, restore
-    arena = bytearray([int(g["fill"], 16)] * int(g["arena_bytes"]))
-    slots = {"bf16": (0, 4), "packed4": (16, 8)}
-    payload = {"bf16": bf16_bytes, "packed4": packed4}
-    for name, (o, n) in slots.items():
-        arena[o:o + n] = payload[name]
-    saved = {name: bytes(arena[o:o + n]) for name, (o, n) in slots.items()}
-    for o, n in slots.values():
-        arena[o:o + n] = bytes(n)
-    for name, (o, n) in slots.items():
-        arena[o:o + n] = saved[name]
-    assert all(bytes(arena[o:o + n]) == payload[name] for name, (o, n) in slots.items())
-    assert arena[4:16] == bytes([0xA5] * 12)
-    assert sum(map(len, saved.values())) == int(g["payload_bytes"])
+    assert bf16.astype("<u2").tobytes().hex() == g["bf16"]
+    assert len(packed4) + 2 * bf16.size == int(g["payload_bytes"])
     assert pack.unpack_bits(packed4[:4], 4, 8) == codes
+
+
+def test_page_example_through_the_pool_layout():
+    """The example's record written into a guard-filled pool with the oracle's
+    own page arithmetic: the code bytes and the scale land at the record's and
+    the norm's places with the printed bytes, a save / clear / restore of
+    exactly those two ranges reproduces them, and every other byte of the pool
+    keeps the guard fill."""
+    g = read_golden()
+    codes = [int(v) for v in g["codes"].split()]
+    scale = float(g["scale"])
+    fill = int(g["fill"], 16)
+    d, bits, heads, nblocks = len(codes), 4, 2, 3
+    pb = pack.page_bytes(d, bits)
+    pool = np.full(nblocks * heads * pb, fill, dtype=np.uint8)
+    slot, head = 1 * pack.BLOCK + 7, 1
+    pack.write_record(pool, slot, head, heads, d, bits, codes, scale)
+    base = pack.page_offset(slot // pack.BLOCK, head, heads, pb)
+    tok, rb = slot % pack.BLOCK, pack.record_bytes(d, bits)
+    ranges = [(base + tok * rb, rb), (base + pack.BLOCK * rb + 4 * tok, 4)]
+    written = b"".join(pool[o:o + n].tobytes() for o, n in ranges)
+    assert written.hex() == g["packed4"]
+    saved = [pool[o:o + n].copy() for o, n in ranges]
+    for o, n in ranges:
+        pool[o:o + n] = 0
+    for (o, n), data in zip(ranges, saved):
+        pool[o:o + n] = data
+    assert pack.read_record(pool, slot, head, heads, d, bits) == (codes, scale)
+    untouched = np.ones(pool.size, bool)
+    for o, n in ranges:
+        untouched[o:o + n] = False
+    assert np.all(pool[untouched] == fill)
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 8])

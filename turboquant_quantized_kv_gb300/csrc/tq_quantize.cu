@@ -431,6 +431,68 @@ __device__ __forceinline__ void quant_pair(float2 x, float2 s, uint32_t qrow, ui
   c1 = __float_as_uint(e1.y) + (y.y >= e1.x ? 1u : 0u);
 }
 
+// The record of one vector held as coordinate pairs v[j] = (x_j, x_{j+64}) (the
+// staged kernel's layout after its FWHT), scaled by s2: the LSB-first record
+// words of the codes, and ||c[idx]||^2 summed through the pair table (returned).
+template <int BITS>
+__device__ __forceinline__ float cell_record_split(const float2 (&v)[64], float2 s2, uint32_t qrow, uint32_t prow,
+                                                   uint32_t (&wd)[4 * BITS]) {
+  float2 c2p[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+  if constexpr (BITS == 4) {
+#pragma unroll
+    for (int j = 0; j < 64; j += 8) {
+      uint32_t bx[4], by[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t x0, y0, x1, y1;
+        quant_pair(v[j + 2 * k], s2, qrow, x0, y0);
+        quant_pair(v[j + 2 * k + 1], s2, qrow, x1, y1);
+        bx[k] = x0 | (x1 << 4);  // codes of coordinates j + 2k, j + 2k + 1
+        by[k] = y0 | (y1 << 4);  // ... and of the same plus 64
+        c2p[k & 1] = __fadd2_rn(c2p[k & 1], make_float2(lds32f(prow + (bx[k] << 7)), lds32f(prow + (by[k] << 7))));
+      }
+      wd[j / 8] = __byte_perm(__byte_perm(bx[0], bx[1], 0x0040), __byte_perm(bx[2], bx[3], 0x0040), 0x5410);
+      wd[8 + j / 8] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
+    }
+  } else {
+#pragma unroll
+    for (int jb = 0; jb < 64; jb += 32) {
+      uint32_t cx[32], cy[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) quant_pair(v[jb + i], s2, qrow, cx[i], cy[i]);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2)
+        c2p[(i >> 1) & 1] = __fadd2_rn(c2p[(i >> 1) & 1], make_float2(lds32f(prow + ((cx[i] | (cx[i + 1] << BITS)) << 7)),
+                                                                     lds32f(prow + ((cy[i] | (cy[i + 1] << BITS)) << 7))));
+      uint32_t wx[BITS], wy[BITS];
+      pack32<BITS>(cx, wx);
+      pack32<BITS>(cy, wy);
+#pragma unroll
+      for (int k = 0; k < BITS; ++k) {
+        wd[(jb / 32) * BITS + k] = wx[k];      // coordinates jb .. jb + 31
+        wd[(2 + jb / 32) * BITS + k] = wy[k];  // coordinates 64 + jb .. 64 + jb + 31
+      }
+    }
+  }
+  return (c2p[0].x + c2p[1].x) + (c2p[0].y + c2p[1].y);
+}
+
+// Codes of the 32 consecutive coordinates y[0..32) of one vector (a chunk of the
+// tensor-core kernel's accumulator columns), scaled by s2: their BITS record
+// words, and their c[idx]^2 added to c2p through the pair table.
+template <int BITS>
+__device__ __forceinline__ void cell_chunk32(const float (&y)[32], float2 s2, uint32_t qrow, uint32_t prow,
+                                             uint32_t (&wc)[BITS], float2& c2p) {
+  uint32_t code[32];
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) quant_pair(make_float2(y[j], y[j + 1]), s2, qrow, code[j], code[j + 1]);
+#pragma unroll
+  for (int j = 0; j < 32; j += 4)
+    c2p = __fadd2_rn(c2p, make_float2(lds32f(prow + ((code[j] | (code[j + 1] << BITS)) << 7)),
+                                      lds32f(prow + ((code[j + 2] | (code[j + 3] << BITS)) << 7))));
+  pack32<BITS>(code, wc);
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_constant__ QuantTmaArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // a dependent decode may start its prologue
@@ -544,44 +606,7 @@ __global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_const
     const float inv_n = n > 0.0f ? inv_sqrt_d / n : 0.0f;
     const float2 s2 = make_float2(inv_n, inv_n);
     uint32_t wd[4 * BITS];  // the record, LSB-first
-    float2 c2p[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-    if constexpr (BITS == 4) {
-#pragma unroll
-      for (int j = 0; j < 64; j += 8) {
-        uint32_t bx[4], by[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t x0, y0, x1, y1;
-          quant_pair(v[j + 2 * k], s2, qrow, x0, y0);
-          quant_pair(v[j + 2 * k + 1], s2, qrow, x1, y1);
-          bx[k] = x0 | (x1 << 4);  // codes of coordinates j + 2k, j + 2k + 1
-          by[k] = y0 | (y1 << 4);  // ... and of the same plus 64
-          c2p[k & 1] = __fadd2_rn(c2p[k & 1], make_float2(lds32f(prow + (bx[k] << 7)), lds32f(prow + (by[k] << 7))));
-        }
-        wd[j / 8] = __byte_perm(__byte_perm(bx[0], bx[1], 0x0040), __byte_perm(bx[2], bx[3], 0x0040), 0x5410);
-        wd[8 + j / 8] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
-      }
-    } else {
-#pragma unroll
-      for (int jb = 0; jb < 64; jb += 32) {
-        uint32_t cx[32], cy[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) quant_pair(v[jb + i], s2, qrow, cx[i], cy[i]);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2)
-          c2p[(i >> 1) & 1] = __fadd2_rn(c2p[(i >> 1) & 1], make_float2(lds32f(prow + ((cx[i] | (cx[i + 1] << BITS)) << 7)),
-                                                                       lds32f(prow + ((cy[i] | (cy[i + 1] << BITS)) << 7))));
-        uint32_t wx[BITS], wy[BITS];
-        pack32<BITS>(cx, wx);
-        pack32<BITS>(cy, wy);
-#pragma unroll
-        for (int k = 0; k < BITS; ++k) {
-          wd[(jb / 32) * BITS + k] = wx[k];      // coordinates jb .. jb + 31
-          wd[(2 + jb / 32) * BITS + k] = wy[k];  // coordinates 64 + jb .. 64 + jb + 31
-        }
-      }
-    }
-    const float c2 = (c2p[0].x + c2p[1].x) + (c2p[0].y + c2p[1].y);
+    const float c2 = cell_record_split<BITS>(v, s2, qrow, prow, wd);
     float gamma;
     if (a.norm_mode == TQ_NORM_RAW) gamma = n;
     else gamma = (n > 0.0f && c2 > 0.0f) ? n / sqrtf(c2) : 0.0f;
@@ -801,15 +826,8 @@ __global__ void __launch_bounds__(kGWarps * 32, 1) k_quantize_dense_mma(const __
       for (int ch = 0; ch < 4; ++ch) {  // coordinates 32 ch .. 32 ch + 31
         float y[32];
         tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)grp * kD + (uint32_t)ch * 32u, y);
-        uint32_t code[32];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) quant_pair(make_float2(y[j], y[j + 1]), s2, qrow, code[j], code[j + 1]);
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          c2p = __fadd2_rn(c2p, make_float2(lds32f(prow + ((code[j] | (code[j + 1] << BITS)) << 7)),
-                                            lds32f(prow + ((code[j + 2] | (code[j + 3] << BITS)) << 7))));
         uint32_t wc[BITS];
-        pack32<BITS>(code, wc);
+        cell_chunk32<BITS>(y, s2, qrow, prow, wc, c2p);
 #pragma unroll
         for (int k = 0; k < BITS; ++k) wd[ch * BITS + k] = wc[k];
       }
@@ -838,6 +856,76 @@ __global__ void __launch_bounds__(kGWarps * 32, 1) k_quantize_dense_mma(const __
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// The quantizer of the two bulk append kernels on given rotated coordinates:
+// tq_quantize_rotated runs it whenever a bf16 append of the same layer and size
+// would run k_quantize_tma (SPLIT: Hadamard layers, at least kTmaMinVectors
+// vectors) or k_quantize_dense_mma (!SPLIT: dense layers), so that those
+// kernels' cell-table quantizer, pair-table norm and packing can be checked on
+// exact inputs.  One lane per vector; y is read from global memory in the
+// layout the bulk kernel holds it in registers.  y is clamped to [-1, 1] before
+// the lookup, which changes no code (every boundary lies inside (-1, 1)) and
+// keeps the cell index in range for any input.
+__device__ __forceinline__ float clamp_unit(float y) { return fminf(fmaxf(y, -1.0f), 1.0f); }
+
+constexpr size_t kCellSmem = 16384 + kTCellBytes + kTPairBytes;
+
+template <int BITS, bool SPLIT>
+__global__ void __launch_bounds__(256) k_quantize_given_y_cells(QuantArgs a) {
+  constexpr int R = 16 * BITS;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  const uint32_t cell_addr = (sbase + 16383u) & ~16383u;  // 16 KB aligned: address = (t & mask) | row
+  const uint32_t pair_addr = cell_addr + kTCellBytes;
+  build_pair_cell_tables<BITS>(a.cb, smem_raw + (cell_addr - sbase), smem_raw + (pair_addr - sbase));
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const uint32_t qrow = cell_addr | ((uint32_t)(lane & 15) << 3);
+  const uint32_t prow = pair_addr + ((uint32_t)lane << 2);
+  const float2 one = make_float2(1.0f, 1.0f);
+  for (int64_t vec = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; vec < a.n_vec;
+       vec += (int64_t)gridDim.x * blockDim.x) {
+    const float* yr = a.y + vec * kD;
+    const float n = __ldg(a.norms + vec);
+    uint32_t wd[4 * BITS];
+    float c2;
+    if constexpr (SPLIT) {
+      float2 v[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) v[j] = make_float2(clamp_unit(__ldg(yr + j)), clamp_unit(__ldg(yr + 64 + j)));
+      c2 = cell_record_split<BITS>(v, one, qrow, prow, wd);
+    } else {
+      float2 c2p = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        float y[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] = clamp_unit(__ldg(yr + 32 * ch + j));
+        uint32_t wc[BITS];
+        cell_chunk32<BITS>(y, one, qrow, prow, wc, c2p);
+#pragma unroll
+        for (int k = 0; k < BITS; ++k) wd[ch * BITS + k] = wc[k];
+      }
+      c2 = c2p.x + c2p.y;
+    }
+    float gamma;
+    if (a.norm_mode == TQ_NORM_RAW) gamma = n;
+    else gamma = (n > 0.0f && c2 > 0.0f) ? n / sqrtf(c2) : 0.0f;
+    const int64_t tok = vec / a.H;
+    const int head = (int)(vec - tok * a.H);
+    const int64_t slot = __ldg(a.slots + tok);
+    if (slot >= a.max_slot) {
+      flag_status(a.status, TQ_DEV_BAD_SLOT);
+    } else if (slot >= 0) {
+      uint8_t* page = a.pool + ((slot >> 4) * a.H + head) * (int64_t)a.page_bytes;
+      const int off = (int)(slot & 15);
+      uint4* rec = reinterpret_cast<uint4*>(page + off * R);
+#pragma unroll
+      for (int k = 0; k < BITS; ++k) rec[k] = make_uint4(wd[4 * k], wd[4 * k + 1], wd[4 * k + 2], wd[4 * k + 3]);
+      *reinterpret_cast<float*>(page + 16 * R + 4 * off) = gamma;
+    }
   }
 }
 
@@ -1194,6 +1282,18 @@ static bool try_quantize_dense_mma(const tq_cache_desc& d, int which, const void
   return true;
 }
 
+template <int BITS, bool SPLIT>
+static cudaError_t run_given_y_cells(const QuantArgs& a, int num_sms, cudaStream_t st) {
+  auto kern = k_quantize_given_y_cells<BITS, SPLIT>;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCellSmem);
+  if (e != cudaSuccess) return e;
+  int64_t grid = (a.n_vec + 255) / 256;
+  if (grid > (int64_t)num_sms * 3) grid = (int64_t)num_sms * 3;
+  kern<<<(unsigned)grid, 256, kCellSmem, st>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
 static QuantArgs quant_args(const tq_cache_desc& d, int which, const void* x, const float* y, const float* norms,
                             const int64_t* slots, int64_t n_tok, unsigned* status) {
   QuantArgs a;
@@ -1252,6 +1352,15 @@ cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, in
   const int bits = which == 0 ? d.fmt.bits_k : d.fmt.bits_v;
   const bool qjl = which == 0 && d.fmt.qjl_k && y == nullptr;
   const int mode = y ? MODE_GIVEN_Y : (d.fmt.rot_kind == TQ_ROT_DENSE ? MODE_DENSE : MODE_HADAMARD);
+  if (mode == MODE_GIVEN_Y && (d.fmt.rot_kind == TQ_ROT_DENSE || n_vec >= kTmaMinVectors)) {
+    const QuantArgs a = quant_args(d, which, nullptr, y, norms, slots, n_tok, status);
+    const bool split = d.fmt.rot_kind != TQ_ROT_DENSE;
+    switch (bits) {
+      case 2: return split ? run_given_y_cells<2, true>(a, num_sms, st) : run_given_y_cells<2, false>(a, num_sms, st);
+      case 3: return split ? run_given_y_cells<3, true>(a, num_sms, st) : run_given_y_cells<3, false>(a, num_sms, st);
+      default: return split ? run_given_y_cells<4, true>(a, num_sms, st) : run_given_y_cells<4, false>(a, num_sms, st);
+    }
+  }
   if (mode == MODE_HADAMARD && !qjl && in_dtype == TQ_BF16) {
     cudaError_t err = cudaSuccess;
     if (try_quantize_tma(d, which, x, x_v, bits, slots, n_tok, status, num_sms, st, &err)) return err;

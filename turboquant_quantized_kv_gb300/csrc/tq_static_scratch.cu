@@ -13,9 +13,14 @@
 // the array's name as a device address, so the first call on each device looks
 // the address up with cudaGetSymbolAddress (with that device current) and
 // caches it; make that first call before any stream capture.  The call then
-// runs the ordinary decode path with the array as its workspace.  Nothing in
-// the scratch has to start at zero (every word the decode reads was written
-// earlier in the same call), so no clearing is done.  All calls on a device
+// runs the ordinary decode path with the array as its workspace.  That path
+// needs the per-unit chunk counters at the start of its workspace to be zero
+// when a call begins.  A __device__ array is zero-filled when the module is
+// loaded, and every decode call leaves the counters it used at zero again
+// (the CTA that completes a unit resets its counter, also in a call whose
+// bounded wait gave up), so the array never needs clearing; everything else in
+// it is written before it is read within a call.  Keep the array a
+// zero-initialised __device__ object for that reason.  All calls on a device
 // share the one array: calls whose work overlaps on the GPU (different streams,
 // or several host threads) race on it and give wrong results.
 #include <cuda_runtime.h>
