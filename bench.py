@@ -87,7 +87,7 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -153,6 +153,10 @@ def setup(torch, tq, steps_total, dev):
     torch.cuda.synchronize()
     append_ms = [a.elapsed_time(b) for a, b in ev]
     n_vec = 2 * B * T0 * HKV
+    # a sample of the prefill keys and their slots (layer 0), for the tie-band report
+    tie_tok = 2048
+    tie_x = kpre[:tie_tok].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    tie_slots = slots_pre[:tie_tok].cpu().numpy()
     del kpre, vpre
     q = [torch.randn(B, HQ, D, generator=gen, device=dev).to(torch.bfloat16) for _ in range(LAYERS)]
     knew = [torch.randn(B, HKV, D, generator=gen, device=dev).to(torch.bfloat16) for _ in range(LAYERS)]
@@ -162,20 +166,28 @@ def setup(torch, tq, steps_total, dev):
     slot_new = torch.empty(B, dtype=torch.int64, device=dev)
     ws_bytes = layers[0].workspace_bytes(B, HQ, mb, SPLITS)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)  # zero before first use
-    return dict(layers=layers, bt=bt, bt_np=bt_np, mb=mb, nb=nb, q=q, knew=knew, vnew=vnew, out=out, ctx=ctx,
+    return dict(tie_x=tie_x, tie_slots=tie_slots,
+                layers=layers, bt=bt, bt_np=bt_np, mb=mb, nb=nb, q=q, knew=knew, vnew=vnew, out=out, ctx=ctx,
                 slot_new=slot_new, ws=ws, append_ms=append_ms, append_vectors=n_vec)
 
 
-def dense_burst(torch, tq, dev, peak):
-    """The burst append of the dense-rotation workload: 36 layers x 8 KV heads x 11,000
-    prefilled bf16 tokens, K and V scaled by a per-layer lambda ~ U(0.5, 4), a dense Haar
-    rotation per layer, 4-bit codes (6,336,000 vectors).  One untimed burst, then one
-    timed with CUDA events around all 36 layer calls (1.6 GB of inputs: larger than L2)."""
+def dense_workload(torch, tq, dev, peak, decode_steps=256):
+    """The dense-rotation workload: 36 layers x 8 KV heads x 11,000 prefilled bf16
+    tokens, K and V scaled by a per-layer lambda ~ U(0.5, 4), a dense Haar rotation
+    per layer, 4-bit codes.
+
+    Burst append: 6,336,000 vectors; one untimed burst, then one timed with CUDA
+    events around all 36 layer calls (1.6 GB of inputs: larger than L2).
+    Decode phase: `decode_steps` incremental steps at batch 1 with 32 query heads;
+    a step appends one new token to every layer and decodes every layer
+    (tq_append_decode per layer, the step captured as one CUDA graph), reading
+    36 x 8 x ctx x 136 B of packed cache (~431 MB per step, above L2); timed with
+    CUDA events around all steps."""
     import workloads
     n_layers, n_tok = 36, 11000
     lam = workloads.layer_scales(36, n_layers)
     gen = torch.Generator(device=dev).manual_seed(36)
-    nb = (n_tok + BLOCK - 1) // BLOCK + 1
+    nb = (n_tok + decode_steps + 8 + BLOCK - 1) // BLOCK + 1
     layers = [tq.Layer(nb, HKV, bits_k=4, bits_v=4, rot_kind=tq.TQ_ROT_DENSE, seed=36, layer=l, device=dev)
               for l in range(n_layers)]
     ks = [(torch.randn(n_tok, HKV, D, generator=gen, device=dev) * float(lam[l])).to(torch.bfloat16)
@@ -198,12 +210,173 @@ def dense_burst(torch, tq, dev, peak):
     n_vec = 2 * n_layers * n_tok * HKV
     gbs = n_vec * APPEND_BYTES_PER_VECTOR / (ms * 1e-3) / 1e9
     status = tq.get_device_status()
-    del ks, vs, layers
+    del ks, vs
+    burst = {"workload": "36 layers x 8 KV heads x 11000 tokens, bf16 K and V, dense Haar rotation per layer, 4-bit",
+             "vectors": n_vec, "ms": round(ms, 4), "vectors_per_s": round(n_vec / (ms * 1e-3), 1),
+             "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes_per_vector": APPEND_BYTES_PER_VECTOR,
+             "gpu_launches": launches, "device_status": status}
+
+    # decode phase: batch 1, one block table (the identity: the burst filled slots 0..n_tok-1)
+    hq = 32
+    bt = torch.arange(nb, dtype=torch.int32, device=dev).reshape(1, nb)
+    ctx = torch.full((1,), n_tok, dtype=torch.int32, device=dev)
+    slot = torch.empty(1, dtype=torch.int64, device=dev)
+    q = [torch.randn(1, hq, D, generator=gen, device=dev).to(torch.bfloat16) for _ in range(n_layers)]
+    kn = [(torch.randn(1, HKV, D, generator=gen, device=dev) * float(lam[l])).to(torch.bfloat16)
+          for l in range(n_layers)]
+    vn = [(torch.randn(1, HKV, D, generator=gen, device=dev) * float(lam[l])).to(torch.bfloat16)
+          for l in range(n_layers)]
+    out = [torch.empty(1, hq, D, dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
+    ws = torch.zeros(layers[0].workspace_bytes(1, hq, nb), dtype=torch.uint8, device=dev)
+
+    def step():
+        slot.copy_(ctx.to(torch.int64))  # identity table: the new token's slot is its position
+        ctx.add_(1)
+        for l in range(n_layers):
+            layers[l].append_decode(kn[l], vn[l], slot, q[l], bt, ctx, out=out[l], workspace=ws)
+
+    for l in range(n_layers):  # eager warm-up before capture
+        layers[l].decode(q[l], bt, ctx, out=out[l], workspace=ws)
+    torch.cuda.synchronize()
+    ctx0 = ctx.clone()
+    g = torch.cuda.CUDAGraph()
+    n0 = tq.launch_count()
+    with torch.cuda.graph(g):
+        step()
+    per_step_launches = tq.launch_count() - n0
+    ctx.copy_(ctx0)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    c_start = int(ctx[0].item())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(decode_steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    dms = e0.elapsed_time(e1)
+    nbytes = sum(n_layers * HKV * (c_start + i + 1) * BYTES_PER_TOKEN_HEAD for i in range(decode_steps))
+    dgbs = nbytes / (dms * 1e-3) / 1e9
+    dec = {"workload": "36 dense-rotation layers x 8 KV heads x ~11000 tokens, batch 1, 32 query heads, %d "
+                       "incremental steps (append + decode of every layer per step, CUDA graph)" % decode_steps,
+           "steps": decode_steps, "bytes_per_step": nbytes // decode_steps, "ms_per_step": round(dms / decode_steps, 4),
+           "gbs": round(dgbs, 1), "frac": round(dgbs / peak, 4), "gpu_launches": per_step_launches * decode_steps,
+           "device_status": tq.get_device_status()}
+    del layers, ws, q, kn, vn, out
     torch.cuda.empty_cache()
-    return {"workload": "36 layers x 8 KV heads x 11000 tokens, bf16 K and V, dense Haar rotation per layer, 4-bit",
-            "vectors": n_vec, "ms": round(ms, 4), "vectors_per_s": round(n_vec / (ms * 1e-3), 1),
-            "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes_per_vector": APPEND_BYTES_PER_VECTOR,
-            "gpu_launches": launches, "device_status": status}
+    return burst, dec
+
+
+def mixed62(torch, tq, dev, peak, steps=6):
+    """The mixed-precision cache: 62 layers where layers 0, 1, 60 and 61 keep bf16 K/V
+    and the other 58 hold 4-bit TurboQuant codes, 8 KV heads, batch 8, 32 query
+    heads, 100,000-token contexts (bf16 N(0, 1) inputs, identity block tables).  A
+    step appends one token per sequence to every layer and decodes every layer
+    (tq_append_decode per layer, one CUDA graph): 58 x 870.4 MB + 4 x 3.277 GB =
+    63.6 GB of cache read per step.  Also one layer of the QJL variant (2-bit keys
+    + 1-bit QJL residual, 4-bit values: 124 B per token and KV head, ~793.6 MB)
+    timed alone.  CUDA events around all steps / calls."""
+    n_layers, b8, hq, t = 62, 8, 32, 100000
+    bf16_ids = (0, 1, 60, 61)
+    gen = torch.Generator(device=dev).manual_seed(62)
+    mb = (t + steps + 8 + BLOCK - 1) // BLOCK + 1
+    nb = b8 * mb
+    bt = torch.arange(nb, dtype=torch.int32, device=dev).reshape(b8, mb)
+    slots_pre = (torch.arange(b8, device=dev, dtype=torch.int64)[:, None] * (mb * BLOCK)
+                 + torch.arange(t, device=dev, dtype=torch.int64)[None, :]).reshape(-1)
+    layers = []
+    for l in range(n_layers):
+        if l in bf16_ids:
+            layers.append(tq.Layer(nb, HKV, kv_format="bf16", device=dev))
+        else:
+            layers.append(tq.Layer(nb, HKV, bits_k=4, bits_v=4, seed=62, layer=l, device=dev))
+    chunk = 1 << 18  # tokens per append call (bf16 inputs of 512 MB for K and V)
+    for i0 in range(0, b8 * t, chunk):
+        sl = slots_pre[i0:i0 + chunk]
+        k = torch.randn(sl.numel(), HKV, D, generator=gen, device=dev).to(torch.bfloat16)
+        v = torch.randn(sl.numel(), HKV, D, generator=gen, device=dev).to(torch.bfloat16)
+        for layer in layers:  # the same tokens in every layer (different rotations per layer)
+            layer.append(k, v, sl)
+        del k, v
+    torch.cuda.synchronize()
+    ctx = torch.full((b8,), t, dtype=torch.int32, device=dev)
+    slot = torch.empty(b8, dtype=torch.int64, device=dev)
+    q = [torch.randn(b8, hq, D, generator=gen, device=dev).to(torch.bfloat16) for _ in range(n_layers)]
+    kn = torch.randn(b8, HKV, D, generator=gen, device=dev).to(torch.bfloat16)
+    vn = torch.randn(b8, HKV, D, generator=gen, device=dev).to(torch.bfloat16)
+    out = [torch.empty(b8, hq, D, dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
+    ws = torch.zeros(max(layer.workspace_bytes(b8, hq, mb) for layer in layers), dtype=torch.uint8, device=dev)
+    row0 = torch.arange(b8, device=dev, dtype=torch.int64) * (mb * BLOCK)
+
+    def step():
+        slot.copy_(row0 + ctx.to(torch.int64))
+        ctx.add_(1)
+        for l in range(n_layers):
+            layers[l].append_decode(kn, vn, slot, q[l], bt, ctx, out=out[l], workspace=ws)
+
+    for l in range(n_layers):
+        layers[l].decode(q[l], bt, ctx, out=out[l], workspace=ws)
+    torch.cuda.synchronize()
+    ctx0 = ctx.clone()
+    g = torch.cuda.CUDAGraph()
+    n0 = tq.launch_count()
+    with torch.cuda.graph(g):
+        step()
+    per_step_launches = tq.launch_count() - n0
+    ctx.copy_(ctx0)
+    g.replay()
+    torch.cuda.synchronize()
+    c_start = int(ctx[0].item())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    per_tok = 58 * BYTES_PER_TOKEN_HEAD + 4 * 2 * D * 2  # bytes per token and KV head over all layers
+    nbytes = sum(b8 * HKV * (c_start + i + 1) * per_tok for i in range(steps))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res = {"workload": "62 layers (0, 1, 60, 61 bf16; 58 x 4-bit), B8 Hq32 Hkv8 d128 ctx100000, append + decode "
+                       "of every layer per step (CUDA graph)", "steps": steps, "bytes_per_step": nbytes // steps,
+           "ms_per_step": round(ms / steps, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+           "gpu_launches": per_step_launches * steps, "device_status": tq.get_device_status()}
+    del layers, out, q
+    torch.cuda.empty_cache()
+
+    # one layer of the QJL variant: 2-bit keys + QJL residual, 4-bit values
+    layer = tq.Layer(nb, HKV, bits_k=2, bits_v=4, qjl=True, seed=62, layer=2, device=dev)
+    for i0 in range(0, b8 * t, chunk):
+        sl = slots_pre[i0:i0 + chunk]
+        k = torch.randn(sl.numel(), HKV, D, generator=gen, device=dev).to(torch.bfloat16)
+        v = torch.randn(sl.numel(), HKV, D, generator=gen, device=dev).to(torch.bfloat16)
+        layer.append(k, v, sl)
+        del k, v
+    ctx.fill_(t)
+    qq = torch.randn(b8, hq, D, generator=gen, device=dev).to(torch.bfloat16)
+    oo = torch.empty(b8, hq, D, dtype=torch.bfloat16, device=dev)
+    wq = torch.zeros(layer.workspace_bytes(b8, hq, mb), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        layer.decode(qq, bt, ctx, out=oo, workspace=wq)
+    torch.cuda.synchronize()
+    ms_q = []
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        layer.decode(qq, bt, ctx, out=oo, workspace=wq)
+        e1.record()
+        torch.cuda.synchronize()
+        ms_q.append(e0.elapsed_time(e1))
+    mq = statistics.median(ms_q)
+    qbytes = b8 * HKV * t * (D * 2 // 8 + 4 + D // 8 + 4 + D * 4 // 8 + 4)
+    res["qjl_layer"] = {"workload": "one layer, 2-bit keys + 1-bit QJL residual (m = 128), 4-bit values, B8 Hq32 "
+                                    "Hkv8 ctx100000", "bytes": qbytes, "ms": round(mq, 4),
+                        "gbs": round(qbytes / (mq * 1e-3) / 1e9, 1),
+                        "frac": round(qbytes / (mq * 1e-3) / 1e9 / peak, 4), "device_status": tq.get_device_status()}
+    del layer, wq
+    torch.cuda.empty_cache()
+    return res
 
 
 def decode_k8v4(torch, tq, dev, peak, reps=20):
@@ -487,45 +660,24 @@ def run_tq(args):
     st = setup(torch, tq, args.warmup + 2 * args.steps + 4, dev)
     stream = torch.cuda.current_stream()
 
-    # The step (slot bookkeeping, then append + decode of every layer) is one CUDA
-    # graph.  NG copies of it are replayed in turn; copy i holds one pair of timing
-    # events around the decode call of layer i % LAYERS (an event node inside a graph
-    # costs microseconds, so each step carries one pair), and after the timed region
-    # each copy's pair holds the duration of that decode call in its last replay.
-    # That layer makes the append and the decode as two calls, so that the events
-    # bracket the decode kernel alone; every other layer makes one tq_append_decode.
+    # The step (slot bookkeeping, then append + decode of every layer) is one CUDA graph.
     torch.cuda.synchronize()
     for l in range(LAYERS):  # eager warm-up (module load, attributes) before capture
         layer_decode(st, l)
     torch.cuda.synchronize()
-    ng = max(1, min(LAYERS, args.steps))
-    graphs, dec_ev = [], []
     ctx_save = st["ctx"].clone()
-    launches_per_step = 0
-    for gi in range(ng):
-        ev = (torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
-        lt = gi % LAYERS
-        g = torch.cuda.CUDAGraph()
-        n_before = tq.launch_count()
-        with torch.cuda.graph(g):
-            step_prepare(torch, st)
-            for l in range(LAYERS):
-                if l == lt:
-                    layer_append(st, l)
-                    ev[0].record()
-                    layer_decode(st, l)
-                    ev[1].record()
-                else:
-                    layer_step(st, l)
-        if gi == 0:
-            launches_per_step = tq.launch_count() - n_before  # libtq kernels in one step's graph
-        graphs.append(g)
-        dec_ev.append(ev)
+    g = torch.cuda.CUDAGraph()
+    n_before = tq.launch_count()
+    with torch.cuda.graph(g):
+        step_prepare(torch, st)
+        for l in range(LAYERS):
+            layer_step(st, l)
+    launches_per_step = tq.launch_count() - n_before  # libtq kernels in one step's graph
     st["ctx"].copy_(ctx_save)
     torch.cuda.synchronize()
 
     for w in range(args.warmup):
-        graphs[w % ng].replay()
+        g.replay()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -535,29 +687,41 @@ def run_tq(args):
     clocks = ClockSampler(local)
     clocks.start()
     torch.cuda.synchronize()
-    first = args.warmup % ng  # graph of timed step 0
     t0.record(stream)
     for s_ in range(args.steps):
-        graphs[(first + s_) % ng].replay()
+        g.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     ms_total = job_ms(t0.elapsed_time(t1), dev)
     ms_step = ms_total / args.steps
-    # decode timings of the last min(ng, steps) timed steps, one layer each
-    sampled = list(range(max(0, args.steps - ng), args.steps))
-    dec_ms = [dec_ev[(first + s_) % ng][0].elapsed_time(dec_ev[(first + s_) % ng][1]) for s_ in sampled]
     status = tq.get_device_status()
     # algorithmic bytes: every decode call of the timed steps reads ctx tokens x H_kv
     # records of 136 B (4-bit K + V + fp32 norms) per sequence, plus block table, q, out
-    def call_bytes(s_):
-        ctx_s = ctx_start + s_ + 1
+    def call_bytes(ctx_s):
         return B * HKV * ctx_s * BYTES_PER_TOKEN_HEAD + B * st["mb"] * 4 + 2 * B * HQ * D * 2
-    bytes_steps = sum(LAYERS * call_bytes(s_) for s_ in range(args.steps))
+    bytes_steps = sum(LAYERS * call_bytes(ctx_start + s_ + 1) for s_ in range(args.steps))
     value = job_value(bytes_steps, world, ms_total) / 1e9
     peak, peak_kind = peaks()
-    dec_avg_ms = statistics.mean(dec_ms)
-    achieved = statistics.mean(call_bytes(s_) for s_ in sampled) / (dec_avg_ms * 1e-3) / 1e9
+    # the decode kernel alone: a graph of the decode calls of all layers (no appends, the
+    # context as the timed steps left it), replayed; CUDA events around each replay
+    gd = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gd):
+        for l in range(LAYERS):
+            layer_decode(st, l)
+    for _ in range(3):
+        gd.replay()
+    torch.cuda.synchronize()
+    rep_ms = []
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gd.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        rep_ms.append(e0.elapsed_time(e1))
+    dec_avg_ms = statistics.median(rep_ms) / LAYERS
+    achieved = call_bytes(int(st["ctx"][0].item())) / (dec_avg_ms * 1e-3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if os.path.exists(tpath):  # counters from one ncu capture, valid only for the kernel source they came from
@@ -576,7 +740,8 @@ def run_tq(args):
 
     # end to end through the public API with host buffers (pinned), eager calls
     e2e = run_e2e(torch, st, args, stream) if args.e2e else None
-    dense = dense_burst(torch, tq, dev, peak) if args.dense_burst else None
+    dense, dense_dec = dense_workload(torch, tq, dev, peak) if args.dense_burst else (None, None)
+    mixed = mixed62(torch, tq, dev, peak) if args.mixed else None
     k8 = decode_k8v4(torch, tq, dev, peak) if args.k8v4 else None
     lc = decode_long_context(torch, tq, dev, peak) if args.long_context else None
     pol = polar_layer(torch, tq, dev, peak) if args.polar else None
@@ -592,12 +757,16 @@ def run_tq(args):
                    "context": T0, "layers": LAYERS, "bits_k": 4, "bits_v": 4, "block_size": BLOCK,
                    "splits": st["layers"][0].auto_splits(B, HQ, st["mb"]) if SPLITS == 0 else SPLITS,
                    "l2": "inputs larger than L2 (~4.6 GB of packed cache per step)", "parallelism": "replicas"},
-        "roofline": {"kernel": "tq_decode_attention (rotate-q + split-K decode + combine)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_kind, "traffic": traffic},
+        "roofline": {"kernel": "k_decode (tq_decode_attention: split-K decode with the merge and inverse rotation "
+                               "fused)", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind, "traffic": traffic,
+                     "timing": "graph of the %d layers' decode calls, median of 10 replays / %d (%.2f us per call)"
+                               % (LAYERS, LAYERS, dec_avg_ms * 1e3)},
         "append": {"vectors_per_s": round(app_vps, 1), "gbs": round(app_gbs, 1), "frac": round(app_gbs / peak, 4),
                    "vectors": st["append_vectors"], "bytes_per_vector": APPEND_BYTES_PER_VECTOR},
         "append_dense_burst": dense,
+        "decode_vlm_b1": dense_dec,
+        "decode_mixed62": mixed,
         "decode_k8v4": k8,
         "decode_long_context": lc,
         "polar": pol,
@@ -610,6 +779,7 @@ def run_tq(args):
     }
     if rank == 0 and args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(st, args)
+        line["append_tie_band"] = tie_band(st)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -719,6 +889,37 @@ def cpu_baseline(st, args):
                       % (n_units, cores), "seconds": round(dt, 2)}
 
 
+def tie_band(st):
+    """Codes of the benchmark's own prefill keys against the oracle's: 2,048 tokens x 8
+    KV heads of layer 0 (bf16 inputs, Hadamard rotation of seed 0, 4-bit codes), the
+    oracle quantizing the same bf16 vectors in fp64 and the GPU's codes read from its
+    pages.  Reports the fraction of coordinates whose codes differ and the largest
+    distance |y - beta| between the oracle's rotated coordinate and the boundary
+    separating the two codes among them (the parity rule allows 1e-5).  Part of the
+    CPU leg, the one place the benchmark runs the oracle."""
+    import numpy as np
+    from oracle import codebook as ocb, pack as opack, quantize as oq, rotation as orot
+    c4, b4 = ocb.codebook_fp32(D, 4)
+    x = oq.bf16_bits_to_f64(st["tie_x"])  # [tok][H][d]
+    pi = orot.hadamard_rotation_seeded(0, 0, D)
+    idx, _, y = oq.quantize(x, pi, c4, b4)
+    layer = st["layers"][0]
+    pool = layer.k_cache.cpu().numpy()
+    pages = opack.pool_pages(pool, layer.num_blocks, HKV, opack.page_bytes(D, 4))
+    slots = st["tie_slots"]
+    codes, _ = opack.split_pages(pages[slots // BLOCK], D, 4)  # [tok][H][16][d]
+    gpu = codes[np.arange(slots.size), :, slots % BLOCK]       # [tok][H][d]
+    mism = gpu != idx
+    worst = 0.0
+    if mism.any():
+        lo = np.minimum(gpu, idx)[mism]
+        beta = np.asarray(b4, np.float64)[np.clip(lo, 0, len(b4) - 1)]
+        worst = float(np.max(np.abs(y[mism] - beta)))
+    return {"sample": "%d prefill tokens x %d KV heads of layer 0 (%d coordinates)" % (slots.size, HKV, mism.size),
+            "mismatch_rate": float(mism.mean()), "mismatches": int(mism.sum()), "max_abs_y_minus_beta": worst,
+            "tau": 1e-5}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -771,7 +972,10 @@ def main():
     ap.add_argument("--no-incremental", dest="incremental", action="store_false",
                     help="skip the incremental-dequant baseline measurement")
     ap.add_argument("--no-dense-burst", dest="dense_burst", action="store_false",
-                    help="skip the dense-rotation burst append (36 layers x 11000 tokens)")
+                    help="skip the dense-rotation workload (burst append of 36 layers x 11000 tokens, then "
+                         "batch-1 decode steps)")
+    ap.add_argument("--no-mixed", dest="mixed", action="store_false",
+                    help="skip the 62-layer mixed bf16 / 4-bit step (B8, 100,000 tokens, 64 GB of cache)")
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (profiling runs use fewer)")
     ap.add_argument("--splits", type=int, default=0, help="decode context splits (0 = library default)")
     args = ap.parse_args()

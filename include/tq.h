@@ -357,7 +357,11 @@ tq_status tq_restore_blocks(const tq_cache_desc* desc, const int32_t* blocks, in
  * device looks up the array's device address (cudaGetSymbolAddress, that
  * device current): make it before any stream capture.  Allocates nothing.
  * All calls on a device share the array; calls that overlap on the GPU (other
- * streams, other host threads) race on it. */
+ * streams, other host threads) race on it.  The array's counter region starts
+ * at zero (the array is zero-filled when the library loads) and every call
+ * leaves it at zero: the decode kernels contain no wait that can give up, and a
+ * call that flags TQ_DEV_BAD_BLOCK or TQ_DEV_BAD_CONTEXT still completes every
+ * (sequence, KV head) unit, so one faulty call does not disturb later ones. */
 tq_status tq_decode_attention_static(const tq_cache_desc* desc, const void* q, int q_dtype, int batch,
                                      int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
                                      const int32_t* context_lens, float sm_scale, void* out, int out_dtype,

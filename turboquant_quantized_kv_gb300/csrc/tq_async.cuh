@@ -51,6 +51,12 @@ __device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, u
       : "memory");
 }
 
+// Starts bringing [src, src + bytes) into L2 (16-byte aligned, a multiple of 16 bytes);
+// nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Waits for the grid this one was launched as a programmatic dependent of (no-op
 // for an ordinary launch).
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -79,6 +85,41 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t it = 0; it < (1u << 30); ++it) {
     if (mbar_try(addr, parity)) return true;
     if ((it & 63) == 63 && global_ns() - t0 > 1000000000ull) return false;
+  }
+  return false;
+}
+
+// Non-blocking test of an mbarrier phase (each thread may test its own barrier).
+__device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// try_wait that may suspend the thread for up to `ns` nanoseconds while the phase
+// is incomplete (a suspended warp takes no issue slots).
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t addr, uint32_t parity, uint32_t ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(addr), "r"(parity), "r"(ns)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait on an mbarrier phase that suspends between tests instead of
+// spinning: gives up after ~1 s (returns false).
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t addr, uint32_t parity) {
+  if (mbar_try_sleep(addr, parity, 20000u)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_sleep(addr, parity, 20000u)) return true;
+    if (global_ns() - t0 > 1000000000ull) return false;
   }
   return false;
 }

@@ -10,23 +10,29 @@
 //   and o = Pi^T (acc / l) once per query head.  Dequantized K/V never reach HBM.
 //
 // Kernels and launch shapes:
-//   k_rotate_q   warp per (sequence, query head): FWHT or dense mat-vec.
-//   k_decode     one CTA per SM (16 warps; 8 for QJL keys and bf16 pages).  The context of every (sequence, KV
-//                head, head group) unit is cut into `splits` equal chunks and
-//                each warp owns one chunk: one balanced wave.  A warp streams
-//                its blocks' K and V pages into its own 4-deep shared-memory
-//                ring with 1-D bulk copies (cp.async.bulk, completion on an
-//                mbarrier).  Codes become fp16 mma.sync m16n8k16 fragments
-//                through byte-indexed tables in shared memory (one f16x2
-//                entry per pair of codes, replicated per lane so lookups never
-//                conflict): logits^T = Q'(16 rows = 8 heads x {hi, lo} fp16
-//                split) x K_hat^T, then acc^T += V_hat^T x P'^T with
-//                P'_t = 2^(u_t - M) gamma'_t / W_block (<= 1) and W_block
-//                folded back in fp32.  At the end the warps of a CTA that share
-//                a unit merge through shared memory and one partial is written.
-//                bf16 layers use the same skeleton with bf16 MMAs on raw pages.
-//   k_combine    CTA per (sequence, query head): log-sum-exp merge of the
-//                chunks and the inverse rotation.
+//   k_rotate_q   warp per (sequence, query head): dense mat-vec or S q' (dense and
+//                QJL layers only; Hadamard layers rotate the query inside k_decode).
+//   k_decode     one CTA per SM (16 warps for groups of <= 4 query heads, 12 for
+//                groups of 8 and FP8 keys, 8 for QJL keys and bf16 pages).  The
+//                block-table row of every (sequence, KV head, head group) unit is
+//                cut into `splits` equal chunks and each warp owns one chunk: one
+//                balanced wave.  A warp streams its chunk's K and V pages into its
+//                own ring of shared-memory stages (two 16-token blocks per stage)
+//                with 16-byte cp.async copies, one stage ahead of the one it
+//                computes on.  Codes become fp16 mma.sync m16n8k16 fragments
+//                through byte-indexed tables in shared memory (one f16x2 entry per
+//                pair of codes, replicated per lane so lookups never conflict):
+//                logits = K_hat (16 tokens) x Q'^T (4 heads x {hi, lo} fp16 split),
+//                online softmax in base 2, then acc += V_hat^T x P' in the rotated
+//                domain.  At the end the warps of a CTA that share a unit merge
+//                through shared memory and one partial per (unit, head) goes to the
+//                workspace; the CTA that completes a unit (an acq_rel counter)
+//                merges the unit's partials and applies Pi^T, one warp per head
+//                row.  bf16 layers use the same skeleton with bf16 MMAs on raw pages.
+//   k_combine    CTA per (sequence, query head): log-sum-exp merge of the chunks and
+//                the inverse rotation, when the decode kernel cannot finish the job
+//                itself (dense Pi, more than 128 splits).
+
 #include <cuda_fp8.h>
 
 #include <cfloat>
@@ -37,7 +43,6 @@
 
 namespace tq {
 
-constexpr int kMaxStages = 4;
 constexpr int kMaxFusedSplits = 128;  // the decode kernel merges its own chunks up to this split count
 constexpr float kRescaleThreshold = 20.0f;  // log2 units before the running max is refreshed
 constexpr float kLog2e = 1.4426950408889634f;
@@ -192,7 +197,6 @@ struct DecodeArgs {
   int Hq, g, ngroups;
   int splits;  // chunks per unit
   int chunks;  // units * splits
-  int stages;  // ring depth per warp
   int smem_bytes;  // dynamic shared memory of the launch
   int fuse_combine;  // 0: k_combine finishes; 1: decode finishes (identity); 2: decode finishes (Hadamard)
   int* counters;     // [units] chunks finished per unit (zeroed by k_rotate_q)
@@ -440,8 +444,8 @@ struct PTranspose {
 };
 
 // Block-table entries of one warp's chunk, read 32 at a time into a register
-// (lane k holds entry 32 r + k) with the next 32 already in flight, so issuing a
-// copy never waits on a global load.  Indices must be requested in increasing order.
+// (lane k holds entry 32 r + k) with the next 32 already in flight, so a request
+// never waits on a global load.  Indices must be requested in increasing order.
 struct BlockIds {
   const int32_t* row;  // block table row + j0
   int n, round;
@@ -463,69 +467,6 @@ struct BlockIds {
     return __shfl_sync(0xffffffffu, cur, k & 31);
   }
 };
-
-// Per-warp ring of (K page, V page) stages fed by bulk copies.
-struct Ring {
-  uint8_t* buf;   // stages x (kpage + vpage)
-  uint64_t* bar;  // stages
-  int stage_bytes;
-};
-
-// Issues the copies of block j of sequence b into `stage` (lane 0 only).
-// Returns true (on every lane) if the block id was valid and copies were issued.
-__device__ __forceinline__ bool issue_block(const Ring& r, int stage, const DecodeArgs& a, int blk, int kvh,
-                                            int lane) {
-  const bool ok = blk >= 0 && (int64_t)blk < a.num_blocks;
-  if (lane == 0) {
-    uint64_t* bar = r.bar + stage;
-    if (ok) {
-      uint8_t* dst = r.buf + stage * r.stage_bytes;
-      const uint8_t* srck = a.kpool + ((int64_t)blk * a.Hkv + kvh) * a.kpage;
-      const uint8_t* srcv = a.vpool + ((int64_t)blk * a.Hkv + kvh) * a.vpage;
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(bar, (uint32_t)(a.kpage + a.vpage));
-      const uint64_t pol = l2_evict_first_policy();  // pages are read once per call
-      bulk_copy_g2s_hint(dst, srck, (uint32_t)a.kpage, bar, pol);
-      bulk_copy_g2s_hint(dst + a.kpage, srcv, (uint32_t)a.vpage, bar, pol);
-    } else {
-      flag_status(a.status, TQ_DEV_BAD_BLOCK);
-      mbar_arrive(bar);  // completes the phase without data
-    }
-  }
-  return ok;
-}
-
-// Issues blocks blk_a and (if has_b) blk_b into the two slots of pair stage `ps`
-// (one mbarrier for both; lane 0).  kbase / vbase: this warp's KV head in the pools,
-// stride: bytes between blocks.  Returns bit 0 / bit 1 = block a / b valid.
-struct PagePtrs {
-  const uint8_t* kbase;
-  const uint8_t* vbase;
-  int64_t kstride, vstride;
-};
-
-__device__ __forceinline__ uint32_t issue_pair(const Ring& r, int ps, const DecodeArgs& a, const PagePtrs& pp,
-                                               int blk_a, int blk_b, bool has_b, int lane) {
-  const bool ok_a = blk_a >= 0 && (int64_t)blk_a < a.num_blocks;
-  const bool ok_b = has_b && blk_b >= 0 && (int64_t)blk_b < a.num_blocks;
-  if (lane == 0) {
-    uint64_t* bar = r.bar + ps;
-    uint8_t* dst = r.buf + ps * 2 * r.stage_bytes;
-    if (!ok_a || (has_b && !ok_b)) flag_status(a.status, TQ_DEV_BAD_BLOCK);
-    mbar_arrive_expect_tx(bar, (uint32_t)((ok_a ? r.stage_bytes : 0) + (ok_b ? r.stage_bytes : 0)));
-    const uint64_t pol = l2_evict_first_policy();  // pages are read once per call
-    if (ok_a) {
-      bulk_copy_g2s_hint(dst, pp.kbase + (int64_t)blk_a * pp.kstride, (uint32_t)a.kpage, bar, pol);
-      bulk_copy_g2s_hint(dst + a.kpage, pp.vbase + (int64_t)blk_a * pp.vstride, (uint32_t)a.vpage, bar, pol);
-    }
-    if (ok_b) {
-      bulk_copy_g2s_hint(dst + r.stage_bytes, pp.kbase + (int64_t)blk_b * pp.kstride, (uint32_t)a.kpage, bar, pol);
-      bulk_copy_g2s_hint(dst + r.stage_bytes + a.kpage, pp.vbase + (int64_t)blk_b * pp.vstride, (uint32_t)a.vpage, bar,
-                         pol);
-    }
-  }
-  return (ok_a ? 1u : 0u) | (ok_b ? 2u : 0u);
-}
 
 // ------------------------------------------------------------ block compute
 
@@ -742,59 +683,74 @@ __device__ __forceinline__ bool slot_live(int unit, int splits, int s, int nw) {
   return s == 0 || ((int64_t)unit * splits + s) % nw == 0;
 }
 
-// In-place inverse Hadamard rotation of head rows spread over the CTA: thread t
-// holds coordinate c = t % 128 of row t / 128 (y), xs is [rows][128] scratch.
-// Returns Pi^T y = D H y / sqrt(d) at coordinate c.  Every thread of the CTA calls it.
-__device__ __forceinline__ float inv_hadamard_cta(float y, int c, float* xs_row, const float* rot) {
-  const int lane = c & 31;
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {  // bits 0..4 of the coordinate: lanes of one warp
-    const float o = __shfl_xor_sync(0xffffffffu, y, m);
-    y = (lane & m) ? (o - y) : (y + o);
-  }
-  xs_row[c] = y;
-  __syncthreads();
-  const int ch = c >> 5;  // bits 5, 6: the four warps of the row
-  float r = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float z = xs_row[lane + 32 * j];
-    r += (__popc(ch & j) & 1) ? -z : z;
-  }
-  __syncthreads();
-  return r * 0.08838834764831845f * __ldg(rot + c);
-}
-
 // KIND 0: packed codes (BK, BV, QJL); KIND 1: bf16 pages.  NT n-tiles of 4 heads
 // per warp, NW warps per CTA, one CTA per SM holding all of the SM's shared memory.
+// Each warp owns one chunk (a split of one unit's context) and streams its pages
+// into its own ring of P stages of SB blocks (K page, V page per block) with
+// 16-byte cp.async copies (the load/store path, not the bulk-copy engine: with
+// pages of about 1 KB the bulk-copy engine cannot keep enough bytes in flight),
+// P - 1 stages ahead of the one it computes on.
 // Shared layout (absolute shared addresses; base = start of the dynamic window):
 //   packed: rings of warps [0, n_lo) in [base, 0x10000), code tables in
 //           [0x10000, 0x20000), rings of the other warps from 0x20000;
-//   bf16:   rings from base.  mbarriers at the top.  The merge scratch of the
-//   epilogue reuses the rings above the tables (drained by then).
+//   bf16:   rings from base.  The merge scratch of the epilogue reuses the rings
+//   above the tables (drained by then).
+template <int KIND, int BK, int BV, bool QJL, int NT>
+__host__ __device__ constexpr int decode_stage_blocks() {
+  return KIND == 0 ? 2 : 1;
+}
+template <int KIND, int BK, int BV, bool QJL, int NT>
+__host__ __device__ constexpr int decode_ring_stages() {
+  return KIND == 1 ? 3 : ((NT == 1 && !QJL) || BK == 8 ? 2 : 3);
+}
+
+// Bytes of a K and a V page of the layer formats the decode kernel takes (they
+// agree with page_bytes_of; the launcher checks).
+template <int KIND, int BK, bool QJL>
+__host__ __device__ constexpr int decode_kpage() {
+  return KIND == 1 ? kBlock * kD * 2 : (BK == 8 ? kBlock * kD : kBlock * (kD * BK / 8 + 4) + (QJL ? kBlock * (kD / 8 + 4) : 0));
+}
+template <int KIND, int BV>
+__host__ __device__ constexpr int decode_vpage() {
+  return KIND == 1 ? kBlock * kD * 2 : kBlock * (kD * BV / 8 + 4);
+}
+
+// 16-byte global -> shared copy on the load/store path (cp.async, L2 evict-first).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 template <int KIND, int BK, int BV, bool QJL, int NT, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   constexpr int HPW = 4 * NT;  // heads per warp
+  constexpr int SB = decode_stage_blocks<KIND, BK, BV, QJL, NT>();
+  constexpr int PMAX = decode_ring_stages<KIND, BK, BV, QJL, NT>();
+  constexpr int KPAGE = decode_kpage<KIND, BK, QJL>(), VPAGE = decode_vpage<KIND, BV>();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g_ = lane >> 2, tig = lane & 3;
-  const int stage_bytes = a.kpage + a.vpage;
+  constexpr uint32_t blk_bytes = (uint32_t)(KPAGE + VPAGE);
+  const uint32_t stage_bytes = SB * blk_bytes;
   const uint32_t base = smem_u32(smem_raw);
-  const uint32_t bars_addr = (base + (uint32_t)a.smem_bytes - (uint32_t)(NW * kMaxStages * 8)) & ~15u;
+  const uint32_t top = (base + (uint32_t)a.smem_bytes) & ~15u;
   const uint32_t lo0 = (base + 127u) & ~127u;
   const uint32_t hi0 = KIND == 0 ? kLutAddr + kLutBytes : lo0;
-  // the deepest ring (<= a.stages) of which NW copies fit below and above the tables
-  int stages = a.stages;
+  // the deepest ring (P <= PMAX stages) of which NW copies fit below and above the tables
+  int P = PMAX;
   uint32_t ring_bytes = 0u, n_lo = 0u, n_hi = 0u;
-  for (;; --stages) {
-    ring_bytes = (uint32_t)(stages * stage_bytes);
+  for (;; --P) {
+    ring_bytes = (uint32_t)P * stage_bytes;
     n_lo = (KIND == 0 && kLutAddr > lo0) ? (kLutAddr - lo0) / ring_bytes : 0u;
-    n_hi = bars_addr > hi0 ? (bars_addr - hi0) / ring_bytes : 0u;
-    if (n_lo + n_hi >= (uint32_t)NW || stages == 1) break;
+    n_hi = top > hi0 ? (top - hi0) / ring_bytes : 0u;
+    if (n_lo + n_hi >= (uint32_t)NW || P == 1) break;
   }
   const uint32_t red_bytes = (uint32_t)(NW * HPW * kD + 2 * NW * HPW + NW) * 4u;
-  const bool layout_ok = (KIND == 1 || (base <= kLutAddr && kLutAddr + kLutBytes <= bars_addr)) &&
-                         n_lo + n_hi >= (uint32_t)NW && hi0 + red_bytes <= bars_addr;
+  const bool layout_ok = (KIND == 1 || (base <= kLutAddr && kLutAddr + kLutBytes <= top)) &&
+                         n_lo + n_hi >= (uint32_t)NW && hi0 + red_bytes <= top;
   auto gen = [&](uint32_t addr) { return smem_raw + (addr - base); };
 
   if (!layout_ok && threadIdx.x == 0 && blockIdx.x == 0) flag_status(a.status, TQ_DEV_LAYOUT);
@@ -811,8 +767,8 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   const int head0 = kvh * a.g + hg * HPW;
   const int gc = min(HPW, a.g - hg * HPW);
 
-  // ---- prologue: start the long-latency loads first (context length, query rows),
-  // build the code tables while they are in flight, then the block ids and copies
+  // ---- prologue: the long-latency loads first (context length, query rows), then
+  // the block ids and the first copies, the code tables while those are in flight
   const int ctx_raw = has ? __ldg(a.ctx_lens + b) : 0;
 
   // CTA-shared query rotation (q_in_kernel != 0): the rows of this CTA's units are
@@ -823,8 +779,7 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   const int nu = c1 > c0 ? (c1 - 1) / a.splits - u0 + 1 : 0;
   const uint32_t hi_rings = (uint32_t)NW > n_lo ? (uint32_t)NW - n_lo : 0u;
   const uint32_t qs_addr = (hi0 + hi_rings * ring_bytes + 15u) & ~15u;
-  const bool q_shared =
-      a.q_in_kernel != 0 && layout_ok && qs_addr + (uint32_t)(nu * HPW * (kD * 4 + 4)) <= bars_addr;
+  const bool q_shared = a.q_in_kernel != 0 && layout_ok && qs_addr + (uint32_t)(nu * HPW * (kD * 4 + 4)) <= top;
   // per row: the key-side MMA fragments of the row's head (512 B, see rotate_row), then
   // after all rows the rows' 1 / scale
   uint32_t* qs = reinterpret_cast<uint32_t*>(gen(qs_addr));
@@ -923,17 +878,102 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     }
   }
 
+  // code tables, in two halves: the first while the context length and the query rows
+  // are in flight, the second while the block ids are
+  uint4* tab = reinterpret_cast<uint4*>(gen(kLutAddr));
+  float cl = 0.0f;  // lane k < 16: key centroid k & MK, lane 16 + k: value centroid k & MV
+  if constexpr (KIND == 0) {
+    constexpr int MK = (1 << BK) - 1, MV = (1 << BV) - 1;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {  // uniform constant loads (a lane-indexed parameter read would serialize)
+      if (lane == k) cl = a.cbk.c[k & MK];
+      if (lane == 16 + k) cl = a.cbv.c[k & MV];
+    }
+  }
+  // rows [e0, e1) of the tables: row e (pair byte, low nibble first) = f16x2(c[e & 15],
+  // c[e >> 4]) once per lane; 16-byte word j of a row holds lanes 4j..4j+3 (j < 8: keys,
+  // j >= 8: values)
+  auto build_tables = [&](int e0, int e1) {
+    if constexpr (KIND == 0) {
+      if (layout_ok) {
+        for (int i = e0 * 16 + (int)threadIdx.x; i < e1 * 16; i += NW * 32) {
+          const int e = i >> 4, vo = (i & 8) ? 16 : 0;
+          const float lo = __shfl_sync(0xffffffffu, cl, vo + (e & 15));
+          const float hi = __shfl_sync(0xffffffffu, cl, vo + (e >> 4));
+          const uint32_t v = pack_half2(lo, hi);
+          tab[i] = make_uint4(v, v, v, v);
+        }
+      }
+    }
+  };
+  build_tables(0, 128);
+
+  // Splits cut the block-table row (max_blocks entries), not the context, so the block
+  // ids can be read before the context length arrives; a split past the context is
+  // empty.  (The longest sequences set the kernel's length either way.)
+  const int j0 = (int)((int64_t)s * a.max_blocks / a.splits);
+  const int j1r = (int)((int64_t)(s + 1) * a.max_blocks / a.splits);
+  BlockIds ids;
+  ids.init(a.block_table + (int64_t)b * a.max_blocks + j0, has ? j1r - j0 : 0, lane);
+  build_tables(128, 256);
   int ctx = ctx_raw;
   if (ctx < 0 || ctx > a.max_blocks * kBlock) {
     if (lane == 0 && s == 0 && r == 0) flag_status(a.status, TQ_DEV_BAD_CONTEXT);
     ctx = ctx < 0 ? 0 : a.max_blocks * kBlock;
   }
   const int nblk = (ctx + kBlock - 1) / kBlock;
-  const int j0 = (int)((int64_t)s * nblk / a.splits);
-  const int j1 = (int)((int64_t)(s + 1) * nblk / a.splits);
-  const int n_my = has ? j1 - j0 : 0;
-  BlockIds ids;
-  ids.init(a.block_table + (int64_t)b * a.max_blocks + j0, n_my, lane);
+  const int n_my = has ? max(0, min(j1r, nblk) - j0) : 0;
+  const int n_stages = (n_my + SB - 1) / SB;
+
+  // copies of stage k (blocks SB k .. SB k + SB - 1 of the chunk) into slot `slot` of this
+  // warp's ring, one cp.async group per stage (an empty group past the end); returns the
+  // mask of the blocks copied (a block id out of range is recorded and skipped)
+  const uint32_t rw = (uint32_t)warp;
+  const uint32_t ring = rw < n_lo ? lo0 + rw * ring_bytes : hi0 + (rw - n_lo) * ring_bytes;
+  const uint8_t* kbase = a.kpool + (int64_t)kvh * KPAGE;
+  const uint8_t* vbase = a.vpool + (int64_t)kvh * VPAGE;
+  const int64_t kstride = (int64_t)a.Hkv * KPAGE, vstride = (int64_t)a.Hkv * VPAGE;
+  const uint64_t pol = l2_evict_first_policy();  // pages are read once per call
+  auto copy_stage = [&](int k, int slot) -> uint32_t {
+    uint32_t m = 0u;
+    if (k < n_stages) {
+#pragma unroll
+      for (int e = 0; e < SB; ++e) {
+        const int j = SB * k + e;
+        if (j < n_my) {  // warp-uniform
+          const int blk = ids.get(j, lane);
+          if (blk >= 0 && (int64_t)blk < a.num_blocks) {
+            m |= 1u << e;
+            // lane copies 16-byte chunks lane, lane + 32, ... of the K page, then of the V page
+            const uint32_t d = ring + (uint32_t)slot * stage_bytes + (uint32_t)e * blk_bytes + 16u * (uint32_t)lane;
+            const uint8_t* ks = kbase + (int64_t)blk * kstride + 16 * lane;
+            const uint8_t* vs = vbase + (int64_t)blk * vstride + 16 * lane;
+#pragma unroll
+            for (int c = 0; c < KPAGE; c += 512)
+              if (c + 512 <= KPAGE || 16 * lane < KPAGE - c) cp_async16(d + (uint32_t)c, ks + c, pol);
+#pragma unroll
+            for (int c = 0; c < VPAGE; c += 512)
+              if (c + 512 <= VPAGE || 16 * lane < VPAGE - c) cp_async16(d + (uint32_t)(KPAGE + c), vs + c, pol);
+          } else if (lane == 0) {
+            flag_status(a.status, TQ_DEV_BAD_BLOCK);
+          }
+        }
+      }
+    }
+    cp_async_commit();
+    return m;
+  };
+  // waits until this lane's copies of the oldest stage in flight have landed
+  auto wait_oldest = [&]() {
+    switch (P) {  // the group count of wait_group is an immediate
+      case 6: cp_async_wait<5>(); break;
+      case 5: cp_async_wait<4>(); break;
+      case 4: cp_async_wait<3>(); break;
+      case 3: cp_async_wait<2>(); break;
+      case 2: cp_async_wait<1>(); break;
+      default: cp_async_wait<0>(); break;
+    }
+  };
 
   if (row0) {
     rotate_row(warp, y0);
@@ -944,69 +984,13 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     }
   }
 
-  Ring ring;
-  ring.stage_bytes = stage_bytes;
-  const uint32_t rw = (uint32_t)warp;
-  ring.buf = gen(rw < n_lo ? lo0 + rw * ring_bytes : hi0 + (rw - n_lo) * ring_bytes);
-  ring.bar = reinterpret_cast<uint64_t*>(gen(bars_addr)) + warp * kMaxStages;
-  if (lane == 0)
-    for (int k = 0; k < stages; ++k) mbar_init(ring.bar + k, 1);
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  __syncwarp();  // this warp's barriers are ready
+  // first copies as soon as the block ids are in.  Launched as a programmatic dependent
+  // of the append (tq_append_decode): everything above overlaps the append; pages only
+  // after it is done.
+  uint32_t vm = 0u;  // SB bits per slot: blocks present
+  if (a.overlap_append) grid_dep_wait();
+  for (int k = 0; k < P; ++k) vm |= copy_stage(k, k) << (SB * k);
 
-  // first copies as soon as the block ids are in; the code tables are built meanwhile.
-  // Packed pages go in pairs of blocks: stages / 2 pair stages, one mbarrier each
-  const int pstages = stages >= 2 ? stages / 2 : 1;
-  const int n_pairs = (n_my + 1) / 2;
-  PagePtrs pp;
-  pp.kbase = a.kpool + (int64_t)kvh * a.kpage;
-  pp.vbase = a.vpool + (int64_t)kvh * a.vpage;
-  pp.kstride = (int64_t)a.Hkv * a.kpage;
-  pp.vstride = (int64_t)a.Hkv * a.vpage;
-  uint32_t valid_mask = 0u;
-  auto first_copies = [&]() {
-    if constexpr (KIND == 0) {
-      for (int k = 0; k < pstages && k < n_pairs; ++k) {
-        const bool hb = 2 * k + 1 < n_my;
-        const int ba = ids.get(2 * k, lane);
-        const int bb = hb ? ids.get(2 * k + 1, lane) : -1;
-        valid_mask |= issue_pair(ring, k, a, pp, ba, bb, hb, lane) << (2 * k);
-      }
-    } else {
-      for (int k = 0; k < stages && k < n_my; ++k)
-        if (issue_block(ring, k, a, ids.get(k, lane), kvh, lane)) valid_mask |= 1u << k;
-    }
-  };
-  // Launched as a programmatic dependent of the append (tq_append_decode): everything
-  // above and the code tables below overlap the append; pages only after it is done.
-  if (!a.overlap_append) first_copies();
-
-  if constexpr (KIND == 0) {
-    if (layout_ok) {
-      // row e (pair byte, low nibble first) = f16x2(c[e & 15], c[e >> 4]) once per lane:
-      // 16-byte word j of a row holds lanes 4j..4j+3 (j < 8: keys, j >= 8: values)
-      constexpr int MK = (1 << BK) - 1, MV = (1 << BV) - 1;
-      float cl = 0.0f;  // lane k < 16: key centroid k & MK, lane 16 + k: value centroid k & MV
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {  // uniform constant loads (a lane-indexed parameter read would serialize)
-        if (lane == k) cl = a.cbk.c[k & MK];
-        if (lane == 16 + k) cl = a.cbv.c[k & MV];
-      }
-      uint4* tab = reinterpret_cast<uint4*>(gen(kLutAddr));
-      for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
-        const int e = i >> 4, vo = (i & 8) ? 16 : 0;
-        const float lo = __shfl_sync(0xffffffffu, cl, vo + (e & 15));
-        const float hi = __shfl_sync(0xffffffffu, cl, vo + (e >> 4));
-        const uint32_t v = pack_half2(lo, hi);
-        tab[i] = make_uint4(v, v, v, v);
-      }
-    }
-  }
-
-  if (a.overlap_append) {
-    grid_dep_wait();
-    first_copies();
-  }
 
   // per-warp constants: query fragments of column g_ (head 4 nt + g_ / 2, part g_ & 1)
   WarpConsts<NT> wc;
@@ -1063,93 +1047,62 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   __syncthreads();  // tables (and shared query rows) ready
   if (q_shared) q_frags();
 
-  int i = 0, stage = 0;
-  uint32_t phase = 0u;
-  bool aborted = false;
-  if constexpr (KIND == 0) {
-    // two blocks (32 tokens) per step: keys of both, one softmax update, values of both
-    for (; i < n_pairs; ++i) {
-      if (!mbar_wait(ring.bar + stage, phase)) {
-        if (lane == 0) flag_status(a.status, TQ_DEV_WAIT_TIMEOUT);
-        aborted = true;
-        break;
-      }
-      const uint32_t m = (valid_mask >> (2 * stage)) & 3u;
-      if (m) {
-        const uint8_t* sa = ring.buf + stage * 2 * stage_bytes;
-        const uint8_t* sb = sa + stage_bytes;
-        const int t0 = (j0 + 2 * i) * kBlock;
-        float u[NT][4], wv[4];
-        if (m == 3u && t0 + 2 * kBlock <= ctx) {  // both blocks whole: no masks
-          packed_keys<NT, BK, BV, QJL, 4, false>(wc, sa, sa + a.kpage, t0, ctx, true, a.qjl_coef, 0, u, wv);
-          packed_keys<NT, BK, BV, QJL, 4, false>(wc, sb, sb + a.kpage, t0 + kBlock, ctx, true, a.qjl_coef, 2, u, wv);
-        } else {
-          packed_keys<NT, BK, BV, QJL, 4, true>(wc, sa, sa + a.kpage, t0, ctx, (m & 1u) != 0, a.qjl_coef, 0, u, wv);
-          packed_keys<NT, BK, BV, QJL, 4, true>(wc, sb, sb + a.kpage, t0 + kBlock, ctx, (m & 2u) != 0, a.qjl_coef, 2,
-                                                u, wv);
-        }
-        uint32_t pk[NT][2], pl[NT][2];
-        softmax_tokens<NT, false, 4>(st, u, wv, pk, pl);
-        uint32_t pka[NT], pkb[NT];
+  int slot = 0;
+  for (int i = 0; i < n_stages; ++i) {
+    wait_oldest();  // this lane's copies of stage i have landed
+    __syncwarp();   // ... and every lane's
+    const uint32_t m = (vm >> (SB * slot)) & ((1u << SB) - 1u);
+    const uint8_t* sa = gen(ring + (uint32_t)slot * stage_bytes);
+    if constexpr (KIND == 0) {
+      if constexpr (SB == 2) {  // two blocks (32 tokens) per stage: keys of both, one softmax update, values of both
+        if (m) {
+          const uint8_t* sb = sa + blk_bytes;
+          const int t0 = (j0 + 2 * i) * kBlock;
+          float u[NT][4], wv[4];
+          if (m == 3u && t0 + 2 * kBlock <= ctx) {  // both blocks whole: no masks
+            packed_keys<NT, BK, BV, QJL, 4, false>(wc, sa, sa + KPAGE, t0, ctx, true, a.qjl_coef, 0, u, wv);
+            packed_keys<NT, BK, BV, QJL, 4, false>(wc, sb, sb + KPAGE, t0 + kBlock, ctx, true, a.qjl_coef, 2, u, wv);
+          } else {
+            packed_keys<NT, BK, BV, QJL, 4, true>(wc, sa, sa + KPAGE, t0, ctx, (m & 1u) != 0, a.qjl_coef, 0, u, wv);
+            packed_keys<NT, BK, BV, QJL, 4, true>(wc, sb, sb + KPAGE, t0 + kBlock, ctx, (m & 2u) != 0, a.qjl_coef,
+                                                  2, u, wv);
+          }
+          uint32_t pk[NT][2], pl[NT][2];
+          softmax_tokens<NT, false, 4>(st, u, wv, pk, pl);
+          uint32_t pka[NT], pkb[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          pka[nt] = pk[nt][0];
-          pkb[nt] = pk[nt][1];
+          for (int nt = 0; nt < NT; ++nt) {
+            pka[nt] = pk[nt][0];
+            pkb[nt] = pk[nt][1];
+          }
+          packed_values<NT, BV>(st, wc, sa + KPAGE, pka);
+          packed_values<NT, BV>(st, wc, sb + KPAGE, pkb);
         }
-        packed_values<NT, BV>(st, wc, sa + a.kpage, pka);
-        packed_values<NT, BV>(st, wc, sb + a.kpage, pkb);
-      }
-      __syncwarp();
-      if (i + pstages < n_pairs) {
-        const int k = i + pstages;
-        const bool hb = 2 * k + 1 < n_my;
-        const int ba = ids.get(2 * k, lane);
-        const int bb = hb ? ids.get(2 * k + 1, lane) : -1;
-        valid_mask = (valid_mask & ~(3u << (2 * stage))) | (issue_pair(ring, stage, a, pp, ba, bb, hb, lane) << (2 * stage));
-      }
-      if (++stage == pstages) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
-  } else {
-    for (; i < n_my; ++i) {
-      if (!mbar_wait(ring.bar + stage, phase)) {
-        if (lane == 0) flag_status(a.status, TQ_DEV_WAIT_TIMEOUT);
-        aborted = true;
-        break;
-      }
-      if (valid_mask & (1u << stage)) {
-        const uint8_t* sk = ring.buf + stage * stage_bytes;
-        const uint8_t* sv = sk + a.kpage;
-        bf16_block<NT>(st, wc, sk, sv, (j0 + i) * kBlock, ctx);
-      }
-      __syncwarp();
-      if (i + stages < n_my) {
-        if (issue_block(ring, stage, a, ids.get(i + stages, lane), kvh, lane)) valid_mask |= 1u << stage;
-        else valid_mask &= ~(1u << stage);
-      }
-      if (++stage == stages) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
-  }
-  if (aborted) {  // drain copies still in flight into this warp's ring before the smem is reused
-    const int nst = KIND == 0 ? pstages : stages;
-    const int nun = KIND == 0 ? n_pairs : n_my;
-    int stg = stage;
-    uint32_t ph = phase;
-    for (int k = i; k < nun && k < i + nst; ++k) {
-      mbar_wait(ring.bar + stg, ph);
-      if (++stg == nst) { stg = 0; ph ^= 1u; }
-    }
+      } else {  // one block (16 tokens) per stage
+        if (m) {
+          const int t0 = (j0 + i) * kBlock;
+          float u[NT][2], wv[2];
+          if (t0 + kBlock <= ctx) {
+            packed_keys<NT, BK, BV, QJL, 2, false>(wc, sa, sa + KPAGE, t0, ctx, true, a.qjl_coef, 0, u, wv);
+          } else {
+            packed_keys<NT, BK, BV, QJL, 2, true>(wc, sa, sa + KPAGE, t0, ctx, true, a.qjl_coef, 0, u, wv);
+          }
+          uint32_t pk[NT][1], pl[NT][1];
+          softmax_tokens<NT, false, 2>(st, u, wv, pk, pl);
+          uint32_t pka[NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      st.M[nt] = -INFINITY;
-      st.l[nt] = 0.0f;
+          for (int nt = 0; nt < NT; ++nt) pka[nt] = pk[nt][0];
+          packed_values<NT, BV>(st, wc, sa + KPAGE, pka);
+        }
+      }
+    } else {
+      if (m) bf16_block<NT>(st, wc, sa, sa + KPAGE, (j0 + i) * kBlock, ctx);
     }
+    __syncwarp();  // every lane is done with the slot
+    vm = (vm & ~(((1u << SB) - 1u) << (SB * slot))) | (copy_stage(i + P, slot) << (SB * slot));
+    if (++slot == P) slot = 0;
   }
+  cp_async_wait<0>();  // (only empty groups remain)
 
   // ---- epilogue 1: per-warp results to shared memory (true sums, l over the head's lanes)
 #pragma unroll
@@ -1228,55 +1181,73 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     last_flag[threadIdx.x] = last ? 1 : 0;
   }
   __syncthreads();
-  float* xs = racc;  // [HPW][128] scratch of the inverse rotation (the partials above are written)
-  for (int ui = 0; ui < nu; ++ui) {
-    if (!last_flag[ui]) continue;  // uniform
+  // one warp per (completed unit, head) row; lane holds coordinates 4 lane .. 4 lane + 3:
+  // merge the unit's live slots, divide by the denominator, apply Pi^T in registers
+  for (int rr = warp; rr < nu * HPW; rr += NW) {
+    const int ui = rr / HPW, h = rr - (rr / HPW) * HPW;
+    if (!last_flag[ui]) continue;  // warp-uniform
     const int u = u0 + ui;
     const int ub = u / per_b, ur = u - ub * per_b, ukvh = ur / a.ngroups, uhg = ur - ukvh * a.ngroups;
-    const int ugc = min(HPW, a.g - uhg * HPW);
-    const int64_t hrow0 = (int64_t)ub * a.Hq + ukvh * a.g + uhg * HPW;
-    for (int o0 = 0; o0 < HPW * kD; o0 += NW * 32) {  // uniform trip count; rows of 128 threads
-      const int o = o0 + threadIdx.x;
-      const int h = o >> 7, c = o & (kD - 1);
-      float y = 0.0f;
-      if (h < ugc) {
-        // live slots: 0, then f1, f1 + NW, ... (the first chunk of the unit on each later CTA)
-        const int f1 = NW - (int)(((int64_t)u * a.splits) % NW);
-        float m4[4], l4[4], v4[4];
+    if (h >= min(HPW, a.g - uhg * HPW)) continue;
+    const int64_t hrow = (int64_t)ub * a.Hq + ukvh * a.g + uhg * HPW + h;
+    // live slots: 0, then f1, f1 + NW, ... (the first chunk of the unit on each later CTA)
+    const int f1 = NW - (int)(((int64_t)u * a.splits) % NW);
+    float m4[4], l4[4];
+    float4 v4[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {  // the loads of up to four slots in flight together
-          const int s2 = k == 0 ? 0 : f1 + (k - 1) * NW;
-          const int64_t row = (hrow0 + h) * a.splits + s2;
-          const bool in = s2 < a.splits;
-          m4[k] = in ? __ldcg(a.ml + row * 2) : -INFINITY;
-          l4[k] = in ? __ldcg(a.ml + row * 2 + 1) : 0.0f;
-          v4[k] = in ? __ldcg(a.part + row * kD + c) : 0.0f;
-        }
-        float M = -INFINITY, L = 0.0f;
-        auto merge = [&](float m, float l, float v) {
-          if (m == -INFINITY) return;
-          const float nm = fmaxf(M, m);
-          const float fo = (M == -INFINITY) ? 0.0f : pow2i((int)(M - nm)), fn = pow2i((int)(m - nm));
-          y = y * fo + v * fn;
-          L = L * fo + l * fn;
-          M = nm;
-        };
+    for (int k = 0; k < 4; ++k) {  // the loads of up to four slots in flight together
+      const int s2 = k == 0 ? 0 : f1 + (k - 1) * NW;
+      const int64_t row = hrow * a.splits + s2;
+      const bool in = s2 < a.splits;
+      m4[k] = in ? __ldcg(a.ml + row * 2) : -INFINITY;
+      l4[k] = in ? __ldcg(a.ml + row * 2 + 1) : 0.0f;
+      v4[k] = in ? __ldcg(reinterpret_cast<const float4*>(a.part + row * kD) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float M = -INFINITY, L = 0.0f;
+    auto merge = [&](float m, float l, const float4& v) {
+      if (m == -INFINITY) return;
+      const float nm = fmaxf(M, m);
+      const float fo = (M == -INFINITY) ? 0.0f : pow2i((int)(M - nm)), fn = pow2i((int)(m - nm));
+      y[0] = y[0] * fo + v.x * fn;
+      y[1] = y[1] * fo + v.y * fn;
+      y[2] = y[2] * fo + v.z * fn;
+      y[3] = y[3] * fo + v.w * fn;
+      L = L * fo + l * fn;
+      M = nm;
+    };
 #pragma unroll
-        for (int k = 0; k < 4; ++k) merge(m4[k], l4[k], v4[k]);
-        for (int s2 = f1 + 3 * NW; s2 < a.splits; s2 += NW) {  // more than four slots
-          const int64_t row = (hrow0 + h) * a.splits + s2;
-          merge(__ldcg(a.ml + row * 2), __ldcg(a.ml + row * 2 + 1), __ldcg(a.part + row * kD + c));
+    for (int k = 0; k < 4; ++k) merge(m4[k], l4[k], v4[k]);
+    for (int s2 = f1 + 3 * NW; s2 < a.splits; s2 += NW) {  // more than four slots
+      const int64_t row = hrow * a.splits + s2;
+      merge(__ldcg(a.ml + row * 2), __ldcg(a.ml + row * 2 + 1),
+            __ldcg(reinterpret_cast<const float4*>(a.part + row * kD) + lane));
+    }
+    const float inv_l = L > 0.0f ? 1.0f / L : 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] *= inv_l;
+    if (a.fuse_combine == 2) {  // Pi^T y = D H y / sqrt(d): bits 0, 1 in the lane, bits 2..6 across lanes
+      const float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
+      y[0] = t0 + t2; y[2] = t0 - t2; y[1] = t1 + t3; y[3] = t1 - t3;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float o = __shfl_xor_sync(0xffffffffu, y[k], m);
+          y[k] = upper ? (o - y[k]) : (y[k] + o);
         }
-        y = L > 0.0f ? y / L : 0.0f;
       }
-      if (a.fuse_combine == 2) y = inv_hadamard_cta(y, c, xs + (o >> 7) * kD, a.rot);
-      if (h < ugc) {
-        const int64_t orow = (hrow0 + h) * kD + c;
-        if (a.out_bf16)
-          reinterpret_cast<__nv_bfloat16*>(a.out)[orow] = __float2bfloat16_rn(y);
-        else
-          reinterpret_cast<float*>(a.out)[orow] = y;
-      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) y[k] *= 0.08838834764831845f * __ldg(a.rot + 4 * lane + k);
+    }
+    const int64_t orow = hrow * kD + 4 * lane;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (a.out_bf16)
+        reinterpret_cast<__nv_bfloat16*>(a.out)[orow + k] = __float2bfloat16_rn(y[k]);
+      else
+        reinterpret_cast<float*>(a.out)[orow + k] = y[k];
     }
   }
 }
@@ -1410,12 +1381,9 @@ __global__ void __launch_bounds__(128) k_combine(const float* __restrict__ part,
 
 Codebook codebook_of(const tq_cache_desc& d, int which);
 
-// Warps per decode CTA (one CTA per SM, NW a multiple of 4): packed codes without
-// QJL run 16 warps at 128 registers for groups of up to 4 heads and 12 warps for 8;
-// the QJL variant and bf16 pages run 8 warps with more registers.
-// Warps per decode CTA: 16 for packed pages with groups of <= 4 query heads, 12
-// for groups of 8 and for FP8 keys (larger stages: 12 four-stage rings fit), 8 for
-// QJL keys and bf16 pages.
+// Warps per decode CTA (one CTA per SM): 16 for packed pages with groups of <= 4
+// query heads, 12 for groups of 8 and for FP8 keys (larger stages), 8 for QJL keys
+// and bf16 pages (more registers).
 constexpr int decode_nw(bool packed_plain, int nt, bool fp8_keys = false) {
   return packed_plain ? ((nt == 1 && !fp8_keys) ? 16 : 12) : 8;
 }
@@ -1429,6 +1397,7 @@ int decode_warps(const tq_cache_desc& d, int g) {
 template <int KIND, int BK, int BV, bool QJL, int NT>
 static cudaError_t run_decode_nt(DecodeArgs a, cudaStream_t st) {
   constexpr int NW = decode_nw(KIND == 0 && !QJL, NT, BK == 8);
+  if (a.kpage != decode_kpage<KIND, BK, QJL>() || a.vpage != decode_vpage<KIND, BV>()) return cudaErrorInvalidValue;
   auto kern = k_decode<KIND, BK, BV, QJL, NT, NW>;
   int dev = 0, optin = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1550,9 +1519,6 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   a.rot = d.rotation;
   a.out = c.out;
   a.out_bf16 = c.out_dtype == TQ_BF16 ? 1 : 0;
-  // ring depth: at most 4 stages (3 for bf16 pages, 8 KB per block); the kernel
-  // takes the deepest that fits its warps
-  a.stages = bf16 ? 3 : 4;
   if (bf16) {
     e = run_decode<1, 4, 4, false>(a, st);
   } else {

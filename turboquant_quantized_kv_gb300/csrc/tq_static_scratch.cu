@@ -17,9 +17,10 @@
 // needs the per-unit chunk counters at the start of its workspace to be zero
 // when a call begins.  A __device__ array is zero-filled when the module is
 // loaded, and every decode call leaves the counters it used at zero again
-// (the CTA that completes a unit resets its counter, also in a call whose
-// bounded wait gave up), so the array never needs clearing; everything else in
-// it is written before it is read within a call.  Keep the array a
+// (the CTA that completes a unit resets its counter; the decode kernel has no
+// wait that can give up, and a call that flags a bad block id or context length
+// still completes every unit), so the array never needs clearing; everything
+// else in it is written before it is read within a call.  Keep the array a
 // zero-initialised __device__ object for that reason.  All calls on a device
 // share the one array: calls whose work overlaps on the GPU (different streams,
 // or several host threads) race on it and give wrong results.
