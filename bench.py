@@ -176,8 +176,9 @@ def dense_workload(torch, tq, dev, peak, decode_steps=256):
     tokens, K and V scaled by a per-layer lambda ~ U(0.5, 4), a dense Haar rotation
     per layer, 4-bit codes.
 
-    Burst append: 6,336,000 vectors; one untimed burst, then one timed with CUDA
-    events around all 36 layer calls (1.6 GB of inputs: larger than L2).
+    Burst append: 6,336,000 vectors in one batched call (tq_quantize_append_layers);
+    one untimed burst, then one timed with CUDA events around the call (1.6 GB of
+    inputs: larger than L2).
     Decode phase: `decode_steps` incremental steps at batch 1 with 32 query heads;
     a step appends one new token to every layer and decodes every layer
     (tq_append_decode per layer, the step captured as one CUDA graph), reading
@@ -195,14 +196,12 @@ def dense_workload(torch, tq, dev, peak, decode_steps=256):
     vs = [(torch.randn(n_tok, HKV, D, generator=gen, device=dev) * float(lam[l])).to(torch.bfloat16)
           for l in range(n_layers)]
     slots = torch.arange(n_tok, dtype=torch.int64, device=dev)
-    for l in range(n_layers):
-        layers[l].append(ks[l], vs[l], slots)
+    tq.append_layers(layers, ks, vs, slots)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n0 = tq.launch_count()
     e0.record()
-    for l in range(n_layers):
-        layers[l].append(ks[l], vs[l], slots)
+    tq.append_layers(layers, ks, vs, slots)  # one batched append of all 36 layers
     e1.record()
     torch.cuda.synchronize()
     launches = tq.launch_count() - n0
@@ -740,7 +739,7 @@ def run_tq(args):
 
     # end to end through the public API with host buffers (pinned), eager calls
     e2e = run_e2e(torch, st, args, stream) if args.e2e else None
-    dense, dense_dec = dense_workload(torch, tq, dev, peak) if args.dense_burst else (None, None)
+    dense, dense_dec = dense_workload(torch, tq, dev, peak, args.vlm_steps) if args.dense_burst else (None, None)
     mixed = mixed62(torch, tq, dev, peak) if args.mixed else None
     k8 = decode_k8v4(torch, tq, dev, peak) if args.k8v4 else None
     lc = decode_long_context(torch, tq, dev, peak) if args.long_context else None
@@ -974,6 +973,8 @@ def main():
     ap.add_argument("--no-dense-burst", dest="dense_burst", action="store_false",
                     help="skip the dense-rotation workload (burst append of 36 layers x 11000 tokens, then "
                          "batch-1 decode steps)")
+    ap.add_argument("--vlm-steps", type=int, default=256,
+                    help="batch-1 decode steps of the dense-rotation workload (profiling runs use fewer)")
     ap.add_argument("--no-mixed", dest="mixed", action="store_false",
                     help="skip the 62-layer mixed bf16 / 4-bit step (B8, 100,000 tokens, 64 GB of cache)")
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (profiling runs use fewer)")

@@ -238,6 +238,21 @@ size_t tq_page_bytes(const tq_cache_desc* desc, int which);
 tq_status tq_quantize_append(const tq_cache_desc* desc, const void* k, const void* v, int in_dtype,
                              const int64_t* slot_mapping, int64_t n_tokens, void* stream);
 
+/* Quantize-on-append of the same tokens into several layers at once (a batched
+ * prefill): descs: host array of n_layers descriptors of distinct caches; k, v:
+ * host arrays of n_layers device pointers, [n_tokens][num_kv_heads][head_dim]
+ * of in_dtype per layer (either array may be NULL to append only the other);
+ * slot_mapping, n_tokens: as tq_quantize_append, shared by all layers.  The
+ * result equals n_layers tq_quantize_append calls in order.  Every layer is
+ * checked before anything is launched.  Since the layers share no memory that
+ * the appends write, each layer's kernel after the first is launched as a
+ * programmatic dependent of the previous one and may start while it finishes;
+ * the inputs must therefore be ready when the call is enqueued (written by work
+ * that precedes the call on the stream), as for any kernel. */
+tq_status tq_quantize_append_layers(const tq_cache_desc* const* descs, int n_layers, const void* const* k,
+                                    const void* const* v, int in_dtype, const int64_t* slot_mapping,
+                                    int64_t n_tokens, void* stream);
+
 /* The quantizer alone, fed rotated unit coordinates: y: device fp32
  * [n_tokens][num_kv_heads][head_dim] (y = Pi x / ||x||), norms: device fp32
  * [n_tokens][num_kv_heads] (||x||).  Writes codes and gamma of the K

@@ -411,3 +411,37 @@ def test_dequantize_matches_oracle(cuda, tqlib, rot):
             ref = oq.dequantize(codes, gamma, pi, c32)
             err = np.max(np.abs(out[:, h] - ref), axis=-1) / np.max(np.abs(ref), axis=-1)
             assert np.max(err) < 1e-5
+
+
+@pytest.mark.parametrize("kind", ["dense_bulk", "hadamard_bulk", "small_mixed"])
+def test_append_layers_equals_per_layer_appends(cuda, tqlib, kind):
+    """tq_quantize_append_layers (the layers after the first launched as programmatic
+    dependents of the previous layer's kernel, without waiting for it) writes exactly
+    the pages of one tq_quantize_append per layer: the tensor-core and staged bulk
+    kernels, and a small append over a mix of packed, QJL, dense and bf16 layers."""
+    tq, torch = tqlib, cuda
+    H = 8
+    if kind == "small_mixed":
+        n, nb = 37, 8
+        fmts = [dict(seed=1, layer=0), dict(kv_format="bf16"), dict(bits_k=2, bits_v=4, qjl=True, seed=1, layer=2),
+                dict(rot_kind=tq.TQ_ROT_DENSE, seed=1, layer=3), dict(bits_k=3, bits_v=3, seed=1, layer=4)]
+    else:
+        n, nb = 3100, 200  # 24,800 vectors per tensor: the bulk kernels
+        rk = tq.TQ_ROT_DENSE if kind == "dense_bulk" else tq.TQ_ROT_HADAMARD
+        fmts = [dict(rot_kind=rk, seed=7, layer=l, bits_k=b, bits_v=b) for l, b in enumerate((4, 3, 2, 4))]
+    slots, slots_d = make_slots(cuda, n, nb, 5, skip_every=11)
+    gen = torch.Generator(device="cuda").manual_seed(9)
+    ks = [torch.randn(n, H, D, generator=gen, device="cuda").to(torch.bfloat16) for _ in fmts]
+    vs = [torch.randn(n, H, D, generator=gen, device="cuda").to(torch.bfloat16) for _ in fmts]
+    batched = [tq.Layer(nb, H, fill=0xA5, **f) for f in fmts]
+    single = [tq.Layer(nb, H, fill=0xA5, **f) for f in fmts]
+    tq.append_layers(batched, ks, vs, slots_d)
+    for ly, k, v in zip(single, ks, vs):
+        ly.append(k, v, slots_d)
+    torch.cuda.synchronize()
+    assert tq.get_device_status() == 0
+    for a, b in zip(batched, single):
+        assert torch.equal(a.k_cache, b.k_cache) and torch.equal(a.v_cache, b.v_cache)
+    # a shared cache is rejected before anything is launched
+    with pytest.raises(tq.TQError):
+        tq.append_layers([batched[0], batched[0]], ks[:2], vs[:2], slots_d)

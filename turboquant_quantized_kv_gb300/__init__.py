@@ -8,7 +8,8 @@ in libtq's CUDA kernels; this package only marshals arguments.
 """
 
 from ._binding import (  # noqa: F401
-    CacheDesc, Layer, LayerFormat, TQError, get_device_status, last_error, launch_count, lib, make_codebook,
+    CacheDesc, Layer, LayerFormat, TQError, append_layers, get_device_status, last_error, launch_count, lib,
+    make_codebook,
     make_rotation,
     LIB_PATH, STATUS_NAMES,
     TQ_BF16, TQ_BLOCK_SIZE, TQ_DEV_BAD_BLOCK, TQ_DEV_BAD_CONTEXT, TQ_DEV_BAD_SLOT, TQ_DEV_WAIT_TIMEOUT,

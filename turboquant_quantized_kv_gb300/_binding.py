@@ -62,6 +62,8 @@ _SIGNATURES = {
     "tq_page_bytes": (ctypes.c_size_t, [_D, ctypes.c_int]),
     "tq_quantize_append": (ctypes.c_int, [_D, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                           ctypes.c_int64, ctypes.c_void_p]),
+    "tq_quantize_append_layers": (ctypes.c_int, [_P(_D), ctypes.c_int, _P(ctypes.c_void_p), _P(ctypes.c_void_p),
+                                                 ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
     "tq_quantize_rotated": (ctypes.c_int, [_D, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                            ctypes.c_int64, ctypes.c_void_p]),
     "tq_auto_splits": (ctypes.c_int, [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
@@ -355,6 +357,20 @@ class Layer:
         _check(lib().tq_dequantize(ctypes.byref(self.desc), which, _ptr(slots, "slots"), int(slots.shape[0]),
                                    _ptr(out, "out"), _dtype_code(out), _stream(stream)))
         return out
+
+
+def append_layers(layers, ks, vs, slot_mapping, stream=None):
+    """Quantize-on-append of the same tokens into several layers (tq_quantize_append_layers):
+    ks[l], vs[l] [n_tokens, H_kv, d] are layer l's inputs (either list may be None)."""
+    n_layers = len(layers)
+    descs = (ctypes.POINTER(CacheDesc) * n_layers)(*[ctypes.pointer(ly.desc) for ly in layers])
+    def ptrs(ts, name):
+        if ts is None:
+            return None
+        return (ctypes.c_void_p * n_layers)(*[_ptr(t, name) for t in ts])
+    ref = (ks if ks is not None else vs)[0]
+    _check(lib().tq_quantize_append_layers(descs, n_layers, ptrs(ks, "k"), ptrs(vs, "v"), _dtype_code(ref),
+                                           _ptr(slot_mapping, "slot_mapping"), int(ref.shape[0]), _stream(stream)))
 
 
 def get_device_status(stream=None):

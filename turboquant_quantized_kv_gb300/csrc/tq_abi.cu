@@ -76,23 +76,24 @@ tq_status check_append(const tq_cache_desc* desc, const void* k, const void* v, 
 // The launches of a checked append (n_tokens > 0): keys and values in one launch
 // when their formats and tables agree.
 tq_status run_append(const tq_cache_desc* desc, const void* k, const void* v, int in_dtype,
-                     const int64_t* slot_mapping, int64_t n_tokens, const DeviceInfo& di, cudaStream_t st) {
+                     const int64_t* slot_mapping, int64_t n_tokens, const DeviceInfo& di, cudaStream_t st,
+                     bool pdl = false) {
   const tq_layer_format& f = desc->fmt;
   const bool same_tables = std::memcmp(desc->centroids_k, desc->centroids_v, sizeof(desc->centroids_k)) == 0 &&
                            std::memcmp(desc->boundaries_k, desc->boundaries_v, sizeof(desc->boundaries_k)) == 0;
   if (k && v && f.kv_format == TQ_KV_PACKED && f.bits_k == f.bits_v && !f.qjl_k && same_tables)  // one launch
     return cuda_result(launch_quantize(*desc, 0, k, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
-                                       di.num_sms, st, v),
+                                       di.num_sms, st, v, pdl),
                        "quantize K+V");
   tq_status s = TQ_OK;
   if (k) {
     s = cuda_result(launch_quantize(*desc, 0, k, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
-                                    di.num_sms, st), "quantize K");
+                                    di.num_sms, st, nullptr, pdl), "quantize K");
     if (s != TQ_OK) return s;
   }
   if (v)
     s = cuda_result(launch_quantize(*desc, 1, v, in_dtype, nullptr, nullptr, slot_mapping, n_tokens, di.status,
-                                    di.num_sms, st), "quantize V");
+                                    di.num_sms, st, nullptr, pdl || k != nullptr), "quantize V");
   return s;
 }
 
@@ -168,6 +169,35 @@ tq_status tq_quantize_append(const tq_cache_desc* desc, const void* k, const voi
   DeviceInfo di;
   if ((s = device_info(&di)) != TQ_OK) return s;
   return run_append(desc, k, v, in_dtype, slot_mapping, n_tokens, di, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tq_status tq_quantize_append_layers(const tq_cache_desc* const* descs, int n_layers, const void* const* k,
+                                    const void* const* v, int in_dtype, const int64_t* slot_mapping,
+                                    int64_t n_tokens, void* stream) {
+  clear_error();
+  if (n_layers < 0) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append_layers: n_layers < 0");
+  if (n_layers == 0) return TQ_OK;
+  if (!descs) return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append_layers: null descriptor array");
+  for (int l = 0; l < n_layers; ++l) {  // every layer is checked before anything is launched
+    tq_status s = check_append(descs[l], k ? k[l] : nullptr, v ? v[l] : nullptr, in_dtype, slot_mapping, n_tokens,
+                               "tq_quantize_append_layers");
+    if (s != TQ_OK) return s;
+    for (int m = 0; m < l; ++m)
+      if (descs[m]->k_cache == descs[l]->k_cache || descs[m]->v_cache == descs[l]->v_cache)
+        return fail(TQ_ERR_INVALID_ARG, "tq_quantize_append_layers: layers %d and %d share a cache", m, l);
+  }
+  if (n_tokens == 0) return TQ_OK;
+  DeviceInfo di;
+  tq_status s = device_info(&di);
+  if (s != TQ_OK) return s;
+  for (int l = 0; l < n_layers; ++l) {
+    // after the first layer: launched as programmatic dependents, without waiting for the
+    // previous layer's kernel (other caches, other inputs)
+    s = run_append(descs[l], k ? k[l] : nullptr, v ? v[l] : nullptr, in_dtype, slot_mapping, n_tokens, di,
+                   reinterpret_cast<cudaStream_t>(stream), l > 0);
+    if (s != TQ_OK) return s;
+  }
+  return TQ_OK;
 }
 
 tq_status tq_quantize_rotated(const tq_cache_desc* desc, int which, const float* y, const float* norms,

@@ -198,7 +198,7 @@ struct DecodeArgs {
   int splits;  // chunks per unit
   int chunks;  // units * splits
   int smem_bytes;  // dynamic shared memory of the launch
-  int fuse_combine;  // 0: k_combine finishes; 1: decode finishes (identity); 2: decode finishes (Hadamard)
+  int fuse_combine;  // 0: k_combine finishes; the decode finishes with 1: identity, 2: Hadamard, 3: dense Pi^T
   int* counters;     // [units] chunks finished per unit (zeroed by k_rotate_q)
   const float* rot;  // Hadamard signs (fuse_combine == 2)
   void* out;
@@ -862,24 +862,26 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
 
   float qv[NT][32];
   float uv[QJL ? NT : 1][32];
-  if (!q_shared) {
+  // this warp's query rows: raw (rotated below) or, after the first copies, the rows the
+  // preceding rotation pass wrote
+  auto load_q_rows = [&](bool from_pass) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int hq = 4 * nt + (g_ >> 1);
       const bool hv = has && hq < gc;
       const int64_t row = (int64_t)b * a.Hq + head0 + (hv ? hq : 0);
-      if (a.q_in_kernel) {
+      if (!from_pass) {
         load_q_raw(a.q, a.q_bf16 != 0, row, hv, tig, qv[nt]);
       } else {
-        grid_dep_wait();  // qrot comes from the preceding rotation pass
         load_q(a.qrot + row * kD, hv, tig, qv[nt]);
+        if constexpr (QJL) load_q(a.uqjl + row * kD, hv, tig, uv[nt]);
       }
-      if constexpr (QJL) load_q(a.uqjl + row * kD, hv, tig, uv[nt]);
     }
-  }
+  };
+  if (!q_shared && a.q_in_kernel) load_q_rows(false);
 
-  // code tables, in two halves: the first while the context length and the query rows
-  // are in flight, the second while the block ids are
+  // code tables while the context length, the query rows and the block ids are in
+  // flight
   uint4* tab = reinterpret_cast<uint4*>(gen(kLutAddr));
   float cl = 0.0f;  // lane k < 16: key centroid k & MK, lane 16 + k: value centroid k & MV
   if constexpr (KIND == 0) {
@@ -906,8 +908,6 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
       }
     }
   };
-  build_tables(0, 128);
-
   // Splits cut the block-table row (max_blocks entries), not the context, so the block
   // ids can be read before the context length arrives; a split past the context is
   // empty.  (The longest sequences set the kernel's length either way.)
@@ -915,7 +915,8 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   const int j1r = (int)((int64_t)(s + 1) * a.max_blocks / a.splits);
   BlockIds ids;
   ids.init(a.block_table + (int64_t)b * a.max_blocks + j0, has ? j1r - j0 : 0, lane);
-  build_tables(128, 256);
+  build_tables(0, 256);
+
   int ctx = ctx_raw;
   if (ctx < 0 || ctx > a.max_blocks * kBlock) {
     if (lane == 0 && s == 0 && r == 0) flag_status(a.status, TQ_DEV_BAD_CONTEXT);
@@ -990,6 +991,10 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   uint32_t vm = 0u;  // SB bits per slot: blocks present
   if (a.overlap_append) grid_dep_wait();
   for (int k = 0; k < P; ++k) vm |= copy_stage(k, k) << (SB * k);
+  if (!q_shared && !a.q_in_kernel) {  // the pages do not depend on the rotation pass; its rows do
+    grid_dep_wait();
+    load_q_rows(true);
+  }
 
 
   // per-warp constants: query fragments of column g_ (head 4 nt + g_ / 2, part g_ & 1)
@@ -1181,6 +1186,20 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     last_flag[threadIdx.x] = last ? 1 : 0;
   }
   __syncthreads();
+  // a dense Pi for the inverse rotation: staged row-major in the code-table region (free
+  // now) when this CTA completes a unit; lanes then read distinct banks of one row
+  const float* pim = reinterpret_cast<const float*>(gen(kLutAddr));
+  if constexpr (KIND == 0) {
+    if (a.fuse_combine == 3) {
+      bool any = false;
+      for (int ui = 0; ui < nu; ++ui) any |= last_flag[ui] != 0;
+      if (any) {  // uniform
+        for (int e = threadIdx.x; e < kD * kD / 4; e += NW * 32)
+          reinterpret_cast<float4*>(gen(kLutAddr))[e] = __ldg(reinterpret_cast<const float4*>(a.rot) + e);
+        __syncthreads();
+      }
+    }
+  }
   // one warp per (completed unit, head) row; lane holds coordinates 4 lane .. 4 lane + 3:
   // merge the unit's live slots, divide by the denominator, apply Pi^T in registers
   for (int rr = warp; rr < nu * HPW; rr += NW) {
@@ -1240,6 +1259,21 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) y[k] *= 0.08838834764831845f * __ldg(a.rot + 4 * lane + k);
+    } else if (a.fuse_combine == 3) {  // Pi^T y for a dense Pi: (Pi^T y)_c = sum_j Pi[j][c] y_j
+      float o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int j4 = 0; j4 < 32; ++j4) {
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          const float yj = __shfl_sync(0xffffffffu, y[k2], j4);  // y_j, j = 4 j4 + k2
+          const float4 p = reinterpret_cast<const float4*>(pim + (4 * j4 + k2) * kD)[lane];
+          o[0] = fmaf(p.x, yj, o[0]);
+          o[1] = fmaf(p.y, yj, o[1]);
+          o[2] = fmaf(p.z, yj, o[2]);
+          o[3] = fmaf(p.w, yj, o[3]);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) y[k] = o[k];
     }
     const int64_t orow = hrow * kD + 4 * lane;
 #pragma unroll
@@ -1256,24 +1290,60 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
 
 enum { ROTQ_IDENTITY = 0, ROTQ_HADAMARD = 1, ROTQ_DENSE = 2 };
 
-// One warp per (sequence, query head).  qrot = Pi q * scale; uq = S qrot (QJL).
-// Also zeroes the decode's per-unit chunk counters.  The decode kernel that follows
-// is launched as its programmatic dependent: it may start right away and waits for
-// this grid (griddepcontrol.wait) only where it reads qrot / uq or the counters.
+// One warp per (sequence, query head), 16 per CTA.  qrot = Pi q * scale; uq = S qrot
+// (QJL).  Also zeroes the decode's per-unit chunk counters.  The decode kernel that
+// follows is launched as its programmatic dependent: it may start right away and waits
+// for this grid (griddepcontrol.wait) only where it reads qrot / uq or the counters.
+// A dense Pi and S are staged once per CTA in shared memory, M[c][j] at row c, column
+// j ^ (c & 31), so that lane l forming outputs l + 32 k reads 32 distinct banks.
+constexpr int kRotWarps = 16;
+
+// out[k] = (M x)_{lane + 32 k} from the staged M; x_j is held by lane j >> 2 at x4[j & 3]
+// (4-per-lane layout) when four_per_lane, else by lane j & 31 at x4[j >> 5].
+__device__ __forceinline__ void staged_matvec(const float* M, const float (&x4)[4], bool four_per_lane, int lane,
+                                              float (&out)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) out[k] = 0.0f;
+#pragma unroll 4
+  for (int j = 0; j < kD; ++j) {
+    const float xj = four_per_lane ? __shfl_sync(0xffffffffu, j & 1 ? (j & 2 ? x4[3] : x4[1]) : (j & 2 ? x4[2] : x4[0]), j >> 2)
+                                   : __shfl_sync(0xffffffffu, j & 64 ? (j & 32 ? x4[3] : x4[2]) : (j & 32 ? x4[1] : x4[0]),
+                                                 j & 31);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) out[k] = fmaf(M[(lane + 32 * k) * kD + (j ^ lane)], xj, out[k]);
+  }
+}
+
+__device__ __forceinline__ void stage_swizzled(const float* __restrict__ src, float* M) {
+  for (int e = threadIdx.x; e < kD * kD / 4; e += blockDim.x) {  // float4 e of row c = e / 32
+    const int c = e >> 5, j = 4 * (e & 31);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(src) + e);
+    float* row = M + c * kD;
+    const int sw = c & 31;
+    row[(j + 0) ^ sw] = v.x;
+    row[(j + 1) ^ sw] = v.y;
+    row[(j + 2) ^ sw] = v.z;
+    row[(j + 3) ^ sw] = v.w;
+  }
+}
+
 template <typename TQ>
-__global__ void __launch_bounds__(128) k_rotate_q(const TQ* __restrict__ q, int64_t n_rows, int kind,
-                                                  const float* __restrict__ rot, const float* __restrict__ S,
-                                                  float scale, float* qrot, float* uq, int* counters, int n_counters) {
+__global__ void __launch_bounds__(kRotWarps * 32) k_rotate_q(const TQ* __restrict__ q, int64_t n_rows, int kind,
+                                                             const float* __restrict__ rot,
+                                                             const float* __restrict__ S, float scale, float* qrot,
+                                                             float* uq, int* counters, int n_counters) {
+  extern __shared__ __align__(16) float mat[];  // [128][128] staged Pi or S (dense and QJL only)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_counters; i += gridDim.x * blockDim.x) counters[i] = 0;
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (row >= n_rows) return;
-  const TQ* src = q + row * kD;
+  const int64_t row = (int64_t)blockIdx.x * kRotWarps + (threadIdx.x >> 5);
+  const bool live = row < n_rows;
+  const TQ* src = q + (live ? row : 0) * kD;
   float x[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) x[k] = load_elem<TQ>(src + 4 * lane + k);
+  for (int k = 0; k < 4; ++k) x[k] = live ? load_elem<TQ>(src + 4 * lane + k) : 0.0f;
   float y[4];
+  bool y_strided = false;  // y in the lane + 32 k layout (else coordinates 4 lane .. 4 lane + 3)
   if (kind == ROTQ_HADAMARD) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) y[k] = x[k] * __ldg(rot + 4 * lane + k);
@@ -1292,28 +1362,34 @@ __global__ void __launch_bounds__(128) k_rotate_q(const TQ* __restrict__ q, int6
 #pragma unroll
     for (int k = 0; k < 4; ++k) y[k] *= 0.08838834764831845f * scale;
   } else if (kind == ROTQ_DENSE) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) y[k] = 0.0f;
-    for (int j = 0; j < kD; ++j) {
-      const float xj = __shfl_sync(0xffffffffu, x[j & 3], j >> 2);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) y[k] = fmaf(__ldg(rot + (4 * lane + k) * kD + j), xj, y[k]);
-    }
+    stage_swizzled(rot, mat);
+    __syncthreads();
+    staged_matvec(mat, x, true, lane, y);
+    y_strided = true;
 #pragma unroll
     for (int k = 0; k < 4; ++k) y[k] *= scale;
   } else {
 #pragma unroll
     for (int k = 0; k < 4; ++k) y[k] = x[k] * scale;
   }
-  *reinterpret_cast<float4*>(qrot + row * kD + 4 * lane) = make_float4(y[0], y[1], y[2], y[3]);
-  if (S) {
-    float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int j = 0; j < kD; ++j) {
-      const float yj = __shfl_sync(0xffffffffu, y[j & 3], j >> 2);
+  if (live) {
+    if (y_strided) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) z[k] = fmaf(__ldg(S + (4 * lane + k) * kD + j), yj, z[k]);
+      for (int k = 0; k < 4; ++k) qrot[row * kD + lane + 32 * k] = y[k];
+    } else {
+      *reinterpret_cast<float4*>(qrot + row * kD + 4 * lane) = make_float4(y[0], y[1], y[2], y[3]);
     }
-    *reinterpret_cast<float4*>(uq + row * kD + 4 * lane) = make_float4(z[0], z[1], z[2], z[3]);
+  }
+  if (S) {
+    if (kind == ROTQ_DENSE) __syncthreads();  // every warp is done with the staged Pi
+    stage_swizzled(S, mat);
+    __syncthreads();
+    float z[4];
+    staged_matvec(mat, y, !y_strided, lane, z);
+    if (live) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) uq[row * kD + lane + 32 * k] = z[k];
+    }
   }
 }
 
@@ -1468,15 +1544,26 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   if (prep) {
     const int64_t rot_rows = q_in_kernel ? 0 : rows;
     const int n_counters = (int)rows;  // >= batch * kv heads * head groups
-    unsigned rgrid = (unsigned)((rot_rows + 3) / 4);
-    if (rgrid == 0) rgrid = (unsigned)((n_counters + 127) / 128);
-    if (c.q_dtype == TQ_F32)
-      k_rotate_q<float><<<rgrid, 128, 0, st>>>(reinterpret_cast<const float*>(c.q), rot_rows, kind_q, d.rotation,
-                                               qjl ? d.qjl_proj : nullptr, scale, qrot, uq, counters, n_counters);
-    else
-      k_rotate_q<__nv_bfloat16><<<rgrid, 128, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(c.q), rot_rows, kind_q,
-                                                       d.rotation, qjl ? d.qjl_proj : nullptr, scale, qrot, uq,
-                                                       counters, n_counters);
+    unsigned rgrid = (unsigned)((rot_rows + kRotWarps - 1) / kRotWarps);
+    if (rgrid == 0) rgrid = (unsigned)((n_counters + kRotWarps * 32 - 1) / (kRotWarps * 32));
+    const bool staged = rot_rows > 0 && (kind_q == ROTQ_DENSE || qjl);
+    const size_t smem = staged ? (size_t)kD * kD * sizeof(float) : 0;
+    cudaError_t ea = cudaSuccess;
+    if (c.q_dtype == TQ_F32) {
+      if (staged) ea = cudaFuncSetAttribute(k_rotate_q<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (ea == cudaSuccess)
+        k_rotate_q<float><<<rgrid, kRotWarps * 32, smem, st>>>(reinterpret_cast<const float*>(c.q), rot_rows, kind_q,
+                                                              d.rotation, qjl ? d.qjl_proj : nullptr, scale, qrot, uq,
+                                                              counters, n_counters);
+    } else {
+      if (staged)
+        ea = cudaFuncSetAttribute(k_rotate_q<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (ea == cudaSuccess)
+        k_rotate_q<__nv_bfloat16><<<rgrid, kRotWarps * 32, smem, st>>>(
+            reinterpret_cast<const __nv_bfloat16*>(c.q), rot_rows, kind_q, d.rotation, qjl ? d.qjl_proj : nullptr,
+            scale, qrot, uq, counters, n_counters);
+    }
+    if (ea != cudaSuccess) return ea;
     count_launch();
   }
   cudaError_t e = cudaGetLastError();
@@ -1513,8 +1600,12 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   a.cbv = codebook_of(d, 1);
   a.qjl_coef = 1.2533141373155003f / (float)kD;  // sqrt(pi/2) / m
   a.status = c.status;
-  // the decode kernel finishes the job itself unless the inverse rotation is a dense mat-vec
-  a.fuse_combine = (kind == ROTQ_DENSE || c.splits > kMaxFusedSplits) ? 0 : (kind == ROTQ_HADAMARD ? 2 : 1);
+  // the decode kernel finishes the job itself (merge and inverse rotation) unless the
+  // splits are too many for its merge or the dense rotation's rows are not 16-byte aligned
+  const bool rot_aligned = (reinterpret_cast<uintptr_t>(d.rotation) & 15) == 0;
+  a.fuse_combine = (c.splits > kMaxFusedSplits || (kind == ROTQ_DENSE && !rot_aligned))
+                       ? 0
+                       : (kind == ROTQ_HADAMARD ? 2 : (kind == ROTQ_DENSE ? 3 : 1));
   a.counters = counters;
   a.rot = d.rotation;
   a.out = c.out;

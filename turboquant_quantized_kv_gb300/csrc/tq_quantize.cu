@@ -1184,17 +1184,35 @@ static bool vec_tensor_map(CUtensorMap* m, const void* x, uint32_t n_vec, uint32
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launches kern<<<grid, block, smem, st>>>(args); with pdl, as a programmatic dependent
+// of the kernel before it on the stream (it may start while that kernel finishes).
+template <typename Args>
+static cudaError_t launch_maybe_pdl(void (*kern)(Args), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                                    const Args& args, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args);
+  count_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int BITS>
-static cudaError_t run_quantize_tma(const QuantTmaArgs& a, int num_sms, cudaStream_t st) {
+static cudaError_t run_quantize_tma(const QuantTmaArgs& a, int num_sms, cudaStream_t st, bool pdl) {
   auto kern = k_quantize_tma<BITS>;
   const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTSmem);
   if (e != cudaSuccess) return e;
   const int64_t total = a.tiles * a.ny;
   int64_t grid = (total + kTW - 1) / kTW;
   if (grid > num_sms) grid = num_sms;
-  kern<<<(unsigned)grid, kTW * 32, kTSmem, st>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_maybe_pdl(kern, (unsigned)grid, kTW * 32, kTSmem, st, a, pdl);
 }
 
 // The staged kernel takes bf16 Hadamard appends without QJL whose inputs TMA can
@@ -1205,7 +1223,7 @@ static cudaError_t run_quantize_tma(const QuantTmaArgs& a, int num_sms, cudaStre
 constexpr int64_t kTmaMinVectors = 24576;
 static bool try_quantize_tma(const tq_cache_desc& d, int which, const void* x, const void* x_v, int bits,
                              const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms, cudaStream_t st,
-                             cudaError_t* err) {
+                             cudaError_t* err, bool pdl) {
   const int64_t n_vec = n_tok * d.num_kv_heads;
   if (n_vec <= 0 || n_vec >= ((int64_t)1 << 31)) return false;
   if (n_vec * (x_v ? 2 : 1) < kTmaMinVectors) return false;
@@ -1228,31 +1246,29 @@ static bool try_quantize_tma(const tq_cache_desc& d, int which, const void* x, c
   a.norm_mode = d.fmt.norm_mode;
   a.status = status;
   switch (bits) {
-    case 2: *err = run_quantize_tma<2>(a, num_sms, st); break;
-    case 3: *err = run_quantize_tma<3>(a, num_sms, st); break;
-    default: *err = run_quantize_tma<4>(a, num_sms, st); break;
+    case 2: *err = run_quantize_tma<2>(a, num_sms, st, pdl); break;
+    case 3: *err = run_quantize_tma<3>(a, num_sms, st, pdl); break;
+    default: *err = run_quantize_tma<4>(a, num_sms, st, pdl); break;
   }
   return true;
 }
 
 template <int BITS>
-static cudaError_t run_quantize_dense_mma(const QuantGemmArgs& a, int num_sms, cudaStream_t st) {
+static cudaError_t run_quantize_dense_mma(const QuantGemmArgs& a, int num_sms, cudaStream_t st, bool pdl) {
   auto kern = k_quantize_dense_mma<BITS>;
   const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
   if (e != cudaSuccess) return e;
   const int total = a.tiles * a.ny;
   const int grid = total < num_sms ? total : num_sms;
-  kern<<<(unsigned)grid, kGWarps * 32, kGSmem, st>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_maybe_pdl(kern, (unsigned)grid, kGWarps * 32, kGSmem, st, a, pdl);
 }
 
 // bf16 appends through a dense Pi without QJL go to the tensor-core kernel (TMA
-// addressable inputs, fewer than 2^31 vectors).  Returns false (nothing
-// launched) for other appends.
+// addressable inputs, fewer than 2^31 vectors); it is also the faster one for a
+// decode step's few tokens.  Returns false (nothing launched) for other appends.
 static bool try_quantize_dense_mma(const tq_cache_desc& d, int which, const void* x, const void* x_v, int bits,
                                    const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms,
-                                   cudaStream_t st, cudaError_t* err) {
+                                   cudaStream_t st, cudaError_t* err, bool pdl) {
   const int64_t n_vec = n_tok * d.num_kv_heads;
   if (n_vec <= 0 || n_vec >= ((int64_t)1 << 31) - kGM) return false;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) || (x_v && (reinterpret_cast<uintptr_t>(x_v) & 15u))) return false;
@@ -1275,9 +1291,9 @@ static bool try_quantize_dense_mma(const tq_cache_desc& d, int which, const void
   a.norm_mode = d.fmt.norm_mode;
   a.status = status;
   switch (bits) {
-    case 2: *err = run_quantize_dense_mma<2>(a, num_sms, st); break;
-    case 3: *err = run_quantize_dense_mma<3>(a, num_sms, st); break;
-    default: *err = run_quantize_dense_mma<4>(a, num_sms, st); break;
+    case 2: *err = run_quantize_dense_mma<2>(a, num_sms, st, pdl); break;
+    case 3: *err = run_quantize_dense_mma<3>(a, num_sms, st, pdl); break;
+    default: *err = run_quantize_dense_mma<4>(a, num_sms, st, pdl); break;
   }
   return true;
 }
@@ -1318,7 +1334,7 @@ static QuantArgs quant_args(const tq_cache_desc& d, int which, const void* x, co
 
 cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, int in_dtype, const float* y,
                             const float* norms, const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms,
-                            cudaStream_t st, const void* x_v) {
+                            cudaStream_t st, const void* x_v, bool pdl) {
   if (n_tok <= 0) return cudaSuccess;
   if (d.fmt.kv_format == TQ_KV_POLAR) return launch_polar_append(d, which, x, in_dtype, slots, n_tok, status, num_sms, st);
   const int64_t n_vec = n_tok * d.num_kv_heads;
@@ -1363,11 +1379,11 @@ cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, in
   }
   if (mode == MODE_HADAMARD && !qjl && in_dtype == TQ_BF16) {
     cudaError_t err = cudaSuccess;
-    if (try_quantize_tma(d, which, x, x_v, bits, slots, n_tok, status, num_sms, st, &err)) return err;
+    if (try_quantize_tma(d, which, x, x_v, bits, slots, n_tok, status, num_sms, st, &err, pdl)) return err;
   }
   if (mode == MODE_DENSE && !qjl && in_dtype == TQ_BF16) {
     cudaError_t err = cudaSuccess;
-    if (try_quantize_dense_mma(d, which, x, x_v, bits, slots, n_tok, status, num_sms, st, &err)) return err;
+    if (try_quantize_dense_mma(d, which, x, x_v, bits, slots, n_tok, status, num_sms, st, &err, pdl)) return err;
   }
   QuantArgs a = quant_args(d, which, x, y, norms, slots, n_tok, status);
   int ny = 1;
