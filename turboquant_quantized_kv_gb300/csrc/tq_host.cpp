@@ -378,15 +378,16 @@ tq_status check_desc(const tq_cache_desc* d, bool need_data) {
 int auto_splits(int num_sms, int warps, int batch, int num_kv_heads, int max_blocks_per_seq) {
   // One wave: at most one chunk per decode warp of the GPU over (sequence, kv head
   // group, split) -- rounded down, since one chunk over makes a second wave of a
-  // few CTAs -- each split keeping at least 8 blocks of context.
+  // few CTAs -- each split keeping at least 4 blocks of the table (two stages of the
+  // decode's ring), and at most 128 splits (the most the decode kernel merges itself).
   const long units = (long)batch * num_kv_heads;
   if (units <= 0 || max_blocks_per_seq <= 0) return 1;
   long target = (long)num_sms * warps;
   long s = target / units;
-  long cap = (max_blocks_per_seq + 7) / 8;
+  long cap = (max_blocks_per_seq + 3) / 4;
   if (s > cap) s = cap;
   if (s < 1) s = 1;
-  if (s > 256) s = 256;
+  if (s > 128) s = 128;
   return (int)s;
 }
 
