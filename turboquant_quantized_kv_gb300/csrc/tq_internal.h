@@ -74,8 +74,10 @@ bool cell_table_ok(const float* boundaries, int nb);
 // x_v != nullptr (packed layers, which = 0): the values are quantized in the same
 // launch; the caller guarantees the K and V formats agree (bits, no QJL).
 // pdl: the bulk kernels (staged FWHT, tensor-core dense) are launched as programmatic
-// dependents of the kernel before them and do not wait for it -- only for a kernel
-// that shares no memory the launch touches (the previous layer of a batched append).
+// dependents of the kernel before them and touch memory without waiting for it -- only
+// for a kernel that shares no memory the launch touches (the previous layer of a
+// batched append, the keys of the same append); they wait for it before completing,
+// so work queued after them still finds both grids done.
 cudaError_t launch_quantize(const tq_cache_desc& d, int which, const void* x, int in_dtype, const float* y,
                             const float* norms, const int64_t* slots, int64_t n_tok, unsigned* status, int num_sms,
                             cudaStream_t st, const void* x_v = nullptr, bool pdl = false);

@@ -625,6 +625,10 @@ __global__ void __launch_bounds__(kTW * 32, 1) k_quantize_tma(const __grid_const
   if (aborted && lane == 0) {  // let copies still in flight into this warp's ring land before exiting
     for (int64_t k = it; k < n_my && k < it + kTStages; ++k) mbar_wait(bar + (int)(k % kTStages), (uint32_t)(k / kTStages) & 1u);
   }
+  // Launched as a programmatic dependent (a batched append, or values after keys), this
+  // grid touches no memory of the grid before it, but it must not complete before that
+  // grid does: work queued after it relies on both.  (No-op for an ordinary launch.)
+  grid_dep_wait();
 }
 
 // ------------------------------------- dense rotation append on tensor cores
@@ -857,6 +861,7 @@ __global__ void __launch_bounds__(kGWarps * 32, 1) k_quantize_dense_mma(const __
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  grid_dep_wait();  // complete only after a grid this one is a programmatic dependent of
 }
 
 // The quantizer of the two bulk append kernels on given rotated coordinates:
