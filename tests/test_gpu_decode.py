@@ -462,3 +462,25 @@ def test_incremental_dequant_baseline_attends_the_same_tokens(cuda, tqlib):
     err = max_rel_err(o_shadow.reshape(-1, D), o_packed.reshape(-1, D))
     print("incremental-dequant baseline vs fused: max rel err %.3e" % err)
     assert err <= 1e-2  # bf16 rounding of the dequantized K/V; a wrong token would be O(1)
+
+
+def test_padded_block_table_splits_the_context(cuda, tqlib):
+    """A block-table row far wider than the context (a table padded to a maximum
+    length, the padding set to -1 so that reading it would be flagged) is split over
+    the context: with the same split count the output equals, bit for bit, the one
+    for a table cut to the longest context, and matches the oracle."""
+    tq = tqlib
+    B, Hq, Hkv, S = 3, 8, 2, 6
+    ctx = np.array([517, 300, 64], np.int32)
+    out_t, ref, layer = run_case(cuda, tq, B=B, Hq=Hq, Hkv=Hkv, ctx=ctx, seed=9, num_splits=S)
+    assert_close(out_t, ref, TOL_BF16, ctx)
+    mb = int(math.ceil(ctx.max() / 16))
+    bt, _ = workloads.shuffled_block_table(10, B, mb, num_blocks=B * mb + 3)  # the table run_case used
+    padded = np.full((B, 8 * mb), -1, np.int32)
+    padded[:, :mb] = bt
+    qf = workloads.queries(9 + 3, B, Hq, D, dtype="bf16")
+    out_p = layer.decode(to_dev(cuda, qf, bf16=True), cuda.from_numpy(padded).cuda(), cuda.from_numpy(ctx).cuda(),
+                         sm_scale=1.0 / math.sqrt(D), out_dtype=cuda.float32, num_splits=S)
+    cuda.cuda.synchronize()
+    assert tq.get_device_status() == 0
+    assert np.array_equal(out_p.cpu().numpy(), out_t)

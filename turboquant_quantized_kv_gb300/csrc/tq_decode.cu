@@ -15,8 +15,9 @@
 //   k_decode     one CTA per SM (16 warps for groups of <= 4 query heads, 12 for
 //                groups of 8 and FP8 keys, 8 for QJL keys and bf16 pages).  The
 //                block-table row of every (sequence, KV head, head group) unit is
-//                cut into `splits` equal chunks and each warp owns one chunk: one
-//                balanced wave.  A warp streams its chunk's K and V pages into its
+//                cut into `splits` equal chunks (the context instead, when the row
+//                is much wider than it) and each warp owns one chunk: one balanced
+//                wave.  A warp streams its chunk's K and V pages into its
 //                own ring of shared-memory stages (two 16-token blocks per stage)
 //                with 16-byte cp.async copies, one stage ahead of the one it
 //                computes on.  Codes become fp16 mma.sync m16n8k16 fragments
@@ -910,9 +911,10 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   };
   // Splits cut the block-table row (max_blocks entries), not the context, so the block
   // ids can be read before the context length arrives; a split past the context is
-  // empty.  (The longest sequences set the kernel's length either way.)
-  const int j0 = (int)((int64_t)s * a.max_blocks / a.splits);
-  const int j1r = (int)((int64_t)(s + 1) * a.max_blocks / a.splits);
+  // empty.  (The longest sequences set the kernel's length either way.)  Rows much
+  // wider than the context are re-split below.
+  int j0 = (int)((int64_t)s * a.max_blocks / a.splits);
+  int j1r = (int)((int64_t)(s + 1) * a.max_blocks / a.splits);
   BlockIds ids;
   ids.init(a.block_table + (int64_t)b * a.max_blocks + j0, has ? j1r - j0 : 0, lane);
   build_tables(0, 256);
@@ -923,6 +925,14 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     ctx = ctx < 0 ? 0 : a.max_blocks * kBlock;
   }
   const int nblk = (ctx + kBlock - 1) / kBlock;
+  // A row much wider than the sequence's context (a table padded to a maximum length)
+  // would leave most of the unit's splits past the context and the few others with all
+  // of it: split the context instead and read those block ids (warp-uniform).
+  if (has && 4 * nblk < 3 * a.max_blocks) {
+    j0 = (int)((int64_t)s * nblk / a.splits);
+    j1r = (int)((int64_t)(s + 1) * nblk / a.splits);
+    ids.init(a.block_table + (int64_t)b * a.max_blocks + j0, j1r - j0, lane);
+  }
   const int n_my = has ? max(0, min(j1r, nblk) - j0) : 0;
   const int n_stages = (n_my + SB - 1) / SB;
 
@@ -1213,6 +1223,16 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     const int f1 = NW - (int)(((int64_t)u * a.splits) % NW);
     float m4[4], l4[4];
     float4 v4[4];
+    // the signs of the inverse FWHT, loaded with the slots
+    float4 sgn = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (a.fuse_combine == 2) {
+      if ((reinterpret_cast<uintptr_t>(a.rot) & 15u) == 0u) {
+        sgn = __ldg(reinterpret_cast<const float4*>(a.rot) + lane);
+      } else {
+        sgn = make_float4(__ldg(a.rot + 4 * lane), __ldg(a.rot + 4 * lane + 1), __ldg(a.rot + 4 * lane + 2),
+                          __ldg(a.rot + 4 * lane + 3));
+      }
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {  // the loads of up to four slots in flight together
       const int s2 = k == 0 ? 0 : f1 + (k - 1) * NW;
@@ -1257,8 +1277,10 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
           y[k] = upper ? (o - y[k]) : (y[k] + o);
         }
       }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) y[k] *= 0.08838834764831845f * __ldg(a.rot + 4 * lane + k);
+      y[0] *= 0.08838834764831845f * sgn.x;
+      y[1] *= 0.08838834764831845f * sgn.y;
+      y[2] *= 0.08838834764831845f * sgn.z;
+      y[3] *= 0.08838834764831845f * sgn.w;
     } else if (a.fuse_combine == 3) {  // Pi^T y for a dense Pi: (Pi^T y)_c = sum_j Pi[j][c] y_j
       float o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       for (int j4 = 0; j4 < 32; ++j4) {
@@ -1276,12 +1298,22 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
       for (int k = 0; k < 4; ++k) y[k] = o[k];
     }
     const int64_t orow = hrow * kD + 4 * lane;
+    if (a.out_bf16) {
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out) + orow;
+      if ((reinterpret_cast<uintptr_t>(a.out) & 7u) == 0u) {  // one 8-byte store
+        *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf162(y[0], y[1]), pack_bf162(y[2], y[3]));
+      } else {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (a.out_bf16)
-        reinterpret_cast<__nv_bfloat16*>(a.out)[orow + k] = __float2bfloat16_rn(y[k]);
-      else
-        reinterpret_cast<float*>(a.out)[orow + k] = y[k];
+        for (int k = 0; k < 4; ++k) o[k] = __float2bfloat16_rn(y[k]);
+      }
+    } else {
+      float* o = reinterpret_cast<float*>(a.out) + orow;
+      if ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) {  // one 16-byte store
+        *reinterpret_cast<float4*>(o) = make_float4(y[0], y[1], y[2], y[3]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] = y[k];
+      }
     }
   }
 }
