@@ -12,8 +12,9 @@
 // Kernels and launch shapes:
 //   k_rotate_q   warp per (sequence, query head): dense mat-vec or S q' (dense and
 //                QJL layers only; Hadamard layers rotate the query inside k_decode).
-//   k_decode     one CTA per SM (16 warps for groups of <= 4 query heads, 12 for
-//                groups of 8 and FP8 keys, 8 for QJL keys and bf16 pages).  The
+//   k_decode     one CTA per SM (16 warps for groups of <= 4 query heads, also with
+//                QJL keys; 12 for groups of 8 and FP8 keys; 8 for QJL keys with
+//                groups of 8 and for bf16 pages).  The
 //                block-table row of every (sequence, KV head, head group) unit is
 //                cut into `splits` equal chunks (the context instead, when the row
 //                is much wider than it) and each warp owns one chunk: one balanced
@@ -1492,19 +1493,22 @@ Codebook codebook_of(const tq_cache_desc& d, int which);
 // Warps per decode CTA (one CTA per SM): 16 for packed pages with groups of <= 4
 // query heads, 12 for groups of 8 and for FP8 keys (larger stages), 8 for QJL keys
 // and bf16 pages (more registers).
-constexpr int decode_nw(bool packed_plain, int nt, bool fp8_keys = false) {
-  return packed_plain ? ((nt == 1 && !fp8_keys) ? 16 : 12) : 8;
+constexpr int decode_nw(bool packed_plain, int nt, bool fp8_keys = false, bool qjl = false) {
+  // QJL keys with groups of <= 4 heads fit 16 warps' registers (128 each, rings of two
+  // stages); with groups of 8, and for bf16 pages, 8 warps
+  return packed_plain ? ((nt == 1 && !fp8_keys) ? 16 : 12) : ((qjl && nt == 1) ? 16 : 8);
 }
 
 int decode_warps(const tq_cache_desc& d, int g) {
   if (d.fmt.kv_format == TQ_KV_POLAR) return g <= 4 ? 12 : 8;  // three (two) CTAs of four warps per SM
   const bool k8 = d.fmt.kv_format == TQ_KV_K8V4;
-  return decode_nw((d.fmt.kv_format == TQ_KV_PACKED && !d.fmt.qjl_k) || k8, g <= 4 ? 1 : 2, k8);
+  const bool qjl = d.fmt.kv_format == TQ_KV_PACKED && d.fmt.qjl_k;
+  return decode_nw((d.fmt.kv_format == TQ_KV_PACKED && !d.fmt.qjl_k) || k8, g <= 4 ? 1 : 2, k8, qjl);
 }
 
 template <int KIND, int BK, int BV, bool QJL, int NT>
 static cudaError_t run_decode_nt(DecodeArgs a, cudaStream_t st) {
-  constexpr int NW = decode_nw(KIND == 0 && !QJL, NT, BK == 8);
+  constexpr int NW = decode_nw(KIND == 0 && !QJL, NT, BK == 8, QJL);
   if (a.kpage != decode_kpage<KIND, BK, QJL>() || a.vpage != decode_vpage<KIND, BV>()) return cudaErrorInvalidValue;
   auto kern = k_decode<KIND, BK, BV, QJL, NT, NW>;
   int dev = 0, optin = 0;
