@@ -786,23 +786,34 @@ def run_tq(args):
 
 
 def run_e2e(torch, st, args, stream):
-    """Public API, host buffers: per step H2D of the new K/V tokens and queries of
-    every layer from pinned memory, append + decode per layer, D2H of all outputs."""
-    hk = [t.cpu().pin_memory() for t in st["knew"]]
-    hv = [t.cpu().pin_memory() for t in st["vnew"]]
-    hq = [t.cpu().pin_memory() for t in st["q"]]
-    ho = [torch.empty(B, HQ, D, dtype=torch.bfloat16).pin_memory() for _ in range(LAYERS)]
-    h2d = sum(t.numel() * t.element_size() for t in hk + hv + hq)
-    d2h = sum(t.numel() * t.element_size() for t in ho)
+    """Public API, host buffers: per step one H2D copy of the new K/V tokens and queries
+    of every layer from pinned memory (one staging buffer), append + decode per layer
+    through Layer.append_decode, and one D2H copy of all layers' outputs."""
+    parts = [t for l in range(LAYERS) for t in (st["knew"][l], st["vnew"][l], st["q"][l])]
+    sizes = [t.numel() for t in parts]
+    h_in = torch.empty(sum(sizes), dtype=torch.bfloat16).pin_memory()
+    off = 0
+    for t, n in zip(parts, sizes):
+        h_in[off:off + n].copy_(t.reshape(-1).cpu())
+        off += n
+    d_in = torch.empty_like(h_in, device=st["q"][0].device)
+    views, off = [], 0
+    for t, n in zip(parts, sizes):
+        views.append(d_in[off:off + n].view(t.shape))
+        off += n
+    d_out = torch.empty(LAYERS, B, HQ, D, dtype=torch.bfloat16, device=d_in.device)
+    h_out = torch.empty(d_out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_out.numel() * h_out.element_size()
 
     def step():
         step_prepare(torch, st)
+        d_in.copy_(h_in, non_blocking=True)
         for l in range(LAYERS):
-            st["knew"][l].copy_(hk[l], non_blocking=True)
-            st["vnew"][l].copy_(hv[l], non_blocking=True)
-            st["q"][l].copy_(hq[l], non_blocking=True)
-            layer_step(st, l)
-            ho[l].copy_(st["out"][l], non_blocking=True)
+            k, v, q = views[3 * l], views[3 * l + 1], views[3 * l + 2]
+            st["layers"][l].append_decode(k, v, st["slot_new"], q, st["bt"], st["ctx"], out=d_out[l],
+                                          workspace=st["ws"], num_splits=SPLITS)
+        h_out.copy_(d_out, non_blocking=True)
 
     for _ in range(2):
         step()

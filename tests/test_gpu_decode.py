@@ -159,6 +159,18 @@ def test_split_count_invariance(cuda, tqlib):
         assert max_rel_err(o, outs[0]) < 2e-5
 
 
+def test_many_splits_use_the_combine_kernel(cuda, tqlib):
+    """More than 128 splits of a unit are merged by the separate combine kernel
+    instead of the decode kernel's own merge: same result as a fused call within the
+    split-invariance bound, and the oracle's within tolerance (one sequence of 3,300
+    tokens, 207 blocks, 200 splits, and a shorter one whose later splits are empty)."""
+    ctx = [3300, 170]
+    out200, ref, _ = run_case(cuda, tqlib, B=2, Hq=8, Hkv=2, ctx=ctx, seed=12, num_splits=200)
+    assert_close(out200, ref, TOL_BF16, ctx)
+    out16, _, _ = run_case(cuda, tqlib, B=2, Hq=8, Hkv=2, ctx=ctx, seed=12, num_splits=16)
+    assert max_rel_err(out200, out16) < 2e-5
+
+
 def test_bad_block_table_entry_is_flagged(cuda, tqlib):
     tq = tqlib
     layer = tq.Layer(4, 1)
