@@ -786,9 +786,10 @@ def run_tq(args):
 
 
 def run_e2e(torch, st, args, stream):
-    """Public API, host buffers: per step one H2D copy of the new K/V tokens and queries
-    of every layer from pinned memory (one staging buffer), append + decode per layer
-    through Layer.append_decode, and one D2H copy of all layers' outputs."""
+    """Public API, host buffers: per step the H2D copy of the new K/V tokens and queries
+    of every layer from one pinned staging buffer, append + decode per layer through
+    Layer.append_decode, and the D2H copy of all layers' outputs; the copies go in
+    chunks of 8 layers on a second stream, each layer waiting only for its own chunk."""
     parts = [t for l in range(LAYERS) for t in (st["knew"][l], st["vnew"][l], st["q"][l])]
     sizes = [t.numel() for t in parts]
     h_in = torch.empty(sum(sizes), dtype=torch.bfloat16).pin_memory()
@@ -805,15 +806,37 @@ def run_e2e(torch, st, args, stream):
     h_out = torch.empty(d_out.shape, dtype=torch.bfloat16).pin_memory()
     h2d = h_in.numel() * h_in.element_size()
     d2h = h_out.numel() * h_out.element_size()
+    # the copies run on a second stream in chunks of `per` layers, ordered by events, so
+    # that they overlap the layers that do not need them
+    per = 8 if LAYERS % 8 == 0 else LAYERS
+    n_chunks = LAYERS // per
+    in_bounds = [0]
+    for c in range(n_chunks):
+        in_bounds.append(in_bounds[-1] + sum(sizes[3 * per * c:3 * per * (c + 1)]))
+    cs = torch.cuda.Stream(device=d_in.device)
+    ev_in = [torch.cuda.Event() for _ in range(n_chunks)]
+    ev_out = [torch.cuda.Event() for _ in range(n_chunks)]
 
     def step():
         step_prepare(torch, st)
-        d_in.copy_(h_in, non_blocking=True)
+        cs.wait_stream(stream)  # the previous step is done with the staging buffers
+        with torch.cuda.stream(cs):
+            for c in range(n_chunks):
+                d_in[in_bounds[c]:in_bounds[c + 1]].copy_(h_in[in_bounds[c]:in_bounds[c + 1]], non_blocking=True)
+                ev_in[c].record(cs)
         for l in range(LAYERS):
+            c = l // per
+            if l % per == 0:
+                stream.wait_event(ev_in[c])
             k, v, q = views[3 * l], views[3 * l + 1], views[3 * l + 2]
             st["layers"][l].append_decode(k, v, st["slot_new"], q, st["bt"], st["ctx"], out=d_out[l],
                                           workspace=st["ws"], num_splits=SPLITS)
-        h_out.copy_(d_out, non_blocking=True)
+            if l % per == per - 1:
+                ev_out[c].record(stream)
+                cs.wait_event(ev_out[c])
+                with torch.cuda.stream(cs):
+                    h_out[c * per:(c + 1) * per].copy_(d_out[c * per:(c + 1) * per], non_blocking=True)
+        stream.wait_stream(cs)  # the step ends with its outputs on the host
 
     for _ in range(2):
         step()
