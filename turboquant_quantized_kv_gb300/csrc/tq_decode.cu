@@ -195,7 +195,7 @@ struct DecodeArgs {
   int q_in_kernel;    // 0: read qrot; 1: rotate q here (Hadamard); 2: scale q here (no rotation)
   float q_scale;      // sm_scale * log2 e
   int pdl;            // host side: launched as a programmatic dependent of the previous kernel
-  int overlap_append;  // 1: the previous kernel is this library's append; wait for it before the first page copy
+  int overlap_append;  // 1: follows this library's append (directly or through the query pass): wait before the first page copy
   int Hq, g, ngroups;
   int splits;  // chunks per unit
   int chunks;  // units * splits
@@ -1424,6 +1424,10 @@ __global__ void __launch_bounds__(kRotWarps * 32) k_rotate_q(const TQ* __restric
       for (int k = 0; k < 4; ++k) uq[row * kD + lane + 32 * k] = z[k];
     }
   }
+  // Launched as a programmatic dependent of the append (tq_append_decode), this pass
+  // touches none of the append's memory but completes only after it, so the decode that
+  // waits for this pass finds the pages written.  (No-op for an ordinary launch.)
+  grid_dep_wait();
 }
 
 // ------------------------------------------------------------- combine
@@ -1584,20 +1588,31 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
     if (rgrid == 0) rgrid = (unsigned)((n_counters + kRotWarps * 32 - 1) / (kRotWarps * 32));
     const bool staged = rot_rows > 0 && (kind_q == ROTQ_DENSE || qjl);
     const size_t smem = staged ? (size_t)kD * kD * sizeof(float) : 0;
+    // after this library's append (tq_append_decode) the pass is its programmatic
+    // dependent: it reads only q and writes only the workspace, so it overlaps the append
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rgrid);
+    cfg.blockDim = dim3(kRotWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = c.after_append ? 1 : 0;
+    const float* S = qjl ? d.qjl_proj : nullptr;
     cudaError_t ea = cudaSuccess;
     if (c.q_dtype == TQ_F32) {
       if (staged) ea = cudaFuncSetAttribute(k_rotate_q<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (ea == cudaSuccess)
-        k_rotate_q<float><<<rgrid, kRotWarps * 32, smem, st>>>(reinterpret_cast<const float*>(c.q), rot_rows, kind_q,
-                                                              d.rotation, qjl ? d.qjl_proj : nullptr, scale, qrot, uq,
-                                                              counters, n_counters);
+        ea = cudaLaunchKernelEx(&cfg, k_rotate_q<float>, reinterpret_cast<const float*>(c.q), rot_rows, kind_q,
+                                (const float*)d.rotation, S, scale, qrot, uq, counters, n_counters);
     } else {
       if (staged)
         ea = cudaFuncSetAttribute(k_rotate_q<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (ea == cudaSuccess)
-        k_rotate_q<__nv_bfloat16><<<rgrid, kRotWarps * 32, smem, st>>>(
-            reinterpret_cast<const __nv_bfloat16*>(c.q), rot_rows, kind_q, d.rotation, qjl ? d.qjl_proj : nullptr,
-            scale, qrot, uq, counters, n_counters);
+        ea = cudaLaunchKernelEx(&cfg, k_rotate_q<__nv_bfloat16>, reinterpret_cast<const __nv_bfloat16*>(c.q),
+                                rot_rows, kind_q, (const float*)d.rotation, S, scale, qrot, uq, counters, n_counters);
     }
     if (ea != cudaSuccess) return ea;
     count_launch();
@@ -1624,7 +1639,9 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   // programmatic dependent of the prep pass, or of the append of tq_append_decode (the
   // prep pass itself is an ordinary launch, so it starts after the append has finished)
   a.pdl = (prep || c.after_append) ? 1 : 0;
-  a.overlap_append = (c.after_append && !prep) ? 1 : 0;
+  // after the append: wait before the first page copy (with a query pass in between, the
+  // pass completes only after the append)
+  a.overlap_append = c.after_append ? 1 : 0;
   a.Hq = c.num_q_heads;
   a.g = c.num_q_heads / d.num_kv_heads;
   a.ngroups = (a.g + (a.g <= 4 ? 3 : 7)) / (a.g <= 4 ? 4 : 8);  // head groups of 4 or 8 per warp
