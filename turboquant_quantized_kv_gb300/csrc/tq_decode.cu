@@ -1204,9 +1204,22 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     if (a.fuse_combine == 3) {
       bool any = false;
       for (int ui = 0; ui < nu; ++ui) any |= last_flag[ui] != 0;
-      if (any) {  // uniform
-        for (int e = threadIdx.x; e < kD * kD / 4; e += NW * 32)
-          reinterpret_cast<float4*>(gen(kLutAddr))[e] = __ldg(reinterpret_cast<const float4*>(a.rot) + e);
+      if (any) {  // uniform; a thread's loads go out four at a time
+        constexpr int kIters = (kD * kD / 4 + NW * 32 - 1) / (NW * 32);
+#pragma unroll
+        for (int i0 = 0; i0 < kIters; i0 += 4) {
+          float4 v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int e = (int)threadIdx.x + (i0 + i) * NW * 32;
+            if (i0 + i < kIters && e < kD * kD / 4) v[i] = __ldg(reinterpret_cast<const float4*>(a.rot) + e);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int e = (int)threadIdx.x + (i0 + i) * NW * 32;
+            if (i0 + i < kIters && e < kD * kD / 4) reinterpret_cast<float4*>(gen(kLutAddr))[e] = v[i];
+          }
+        }
         __syncthreads();
       }
     }
@@ -1347,16 +1360,23 @@ __device__ __forceinline__ void staged_matvec(const float* M, const float (&x4)[
   }
 }
 
+// (a CTA of kRotWarps warps; each thread's loads are all in flight before its stores)
 __device__ __forceinline__ void stage_swizzled(const float* __restrict__ src, float* M) {
-  for (int e = threadIdx.x; e < kD * kD / 4; e += blockDim.x) {  // float4 e of row c = e / 32
+  constexpr int kThreads = kRotWarps * 32, kIters = kD * kD / 4 / kThreads;
+  static_assert(kIters * kThreads == kD * kD / 4, "whole float4 per thread");
+  float4 v[kIters];
+#pragma unroll
+  for (int i = 0; i < kIters; ++i) v[i] = __ldg(reinterpret_cast<const float4*>(src) + threadIdx.x + i * kThreads);
+#pragma unroll
+  for (int i = 0; i < kIters; ++i) {  // float4 e of row c = e / 32
+    const int e = threadIdx.x + i * kThreads;
     const int c = e >> 5, j = 4 * (e & 31);
-    const float4 v = __ldg(reinterpret_cast<const float4*>(src) + e);
     float* row = M + c * kD;
     const int sw = c & 31;
-    row[(j + 0) ^ sw] = v.x;
-    row[(j + 1) ^ sw] = v.y;
-    row[(j + 2) ^ sw] = v.z;
-    row[(j + 3) ^ sw] = v.w;
+    row[(j + 0) ^ sw] = v[i].x;
+    row[(j + 1) ^ sw] = v[i].y;
+    row[(j + 2) ^ sw] = v[i].z;
+    row[(j + 3) ^ sw] = v[i].w;
   }
 }
 

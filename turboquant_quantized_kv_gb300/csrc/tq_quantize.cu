@@ -707,11 +707,24 @@ __global__ void __launch_bounds__(kGWarps * 32, 1) k_quantize_dense_mma(const __
   if (warp == 1) tmem_alloc(tmem_slot, 512);
 
   build_pair_cell_tables<BITS>(a.cb, gen(cell_addr), gen(pair_addr));
-  // Pi -> bf16 parts, element (n = i, k = j) of B = Pi at box j / 64, row i, chunk (j % 64) / 8 ^ (i & 7)
-  for (int c = threadIdx.x; c < kD * kD / 8; c += blockDim.x) {
+  // Pi -> bf16 parts, element (n = i, k = j) of B = Pi at box j / 64, row i, chunk (j % 64) / 8 ^ (i & 7);
+  // each thread's loads in flight together
+  constexpr int kPiIters = (kD * kD / 8 + kGWarps * 32 - 1) / (kGWarps * 32);
+  float4 pl[kPiIters][2];
+#pragma unroll
+  for (int it = 0; it < kPiIters; ++it) {
+    const int c = (int)threadIdx.x + it * kGWarps * 32;
+    if (c < kD * kD / 8) {
+      pl[it][0] = __ldg(reinterpret_cast<const float4*>(a.rot) + 2 * c);
+      pl[it][1] = __ldg(reinterpret_cast<const float4*>(a.rot) + 2 * c + 1);
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < kPiIters; ++it) {
+    const int c = (int)threadIdx.x + it * kGWarps * 32;
+    if (c >= kD * kD / 8) break;
     const int i = c >> 4, kc = c & 15;
-    const float4 p0 = __ldg(reinterpret_cast<const float4*>(a.rot + i * kD + 8 * kc));
-    const float4 p1 = __ldg(reinterpret_cast<const float4*>(a.rot + i * kD + 8 * kc) + 1);
+    const float4 p0 = pl[it][0], p1 = pl[it][1];
     const float v[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
     uint32_t hw[4], lw[4];
 #pragma unroll
