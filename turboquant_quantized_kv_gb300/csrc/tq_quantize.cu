@@ -95,13 +95,47 @@ bool cell_table_ok(const float* boundaries, int nb) {
 }
 
 // dst[r][q][k] = transpose ? src[32q + k][r] : src[r][32q + k]   (src row-major d x d)
+// (a CTA of kThreads threads; each thread's loads go out in batches, in flight together
+// before their stores)
 __device__ void stage_matrix(const float* __restrict__ src, float* dst, bool transpose) {
-  for (int e = threadIdx.x; e < kD * kD; e += blockDim.x) {
-    const int i = e / kD, j = e % kD;  // src[i][j], coalesced read
-    const float v = __ldg(src + e);
-    const int r = transpose ? j : i;
-    const int c = transpose ? i : j;
-    dst[(r * 4 + (c >> 5)) * kPadQ + (c & 31)] = v;
+  if (transpose && (reinterpret_cast<uintptr_t>(src) & 15u) == 0u) {
+    // lane = source row (mod 32), so the transposed stores of a warp hit 32 banks
+    constexpr int kWarps = kThreads / 32, kCols = kD / 4 / kWarps;  // float4 columns per warp
+    static_assert(kCols * kWarps * 4 == kD, "whole float4 columns");
+    const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5;
+#pragma unroll
+    for (int rb = 0; rb < kD / 32; ++rb) {  // source rows 32 rb + lane
+      float4 v[kCols];
+#pragma unroll
+      for (int cb = 0; cb < kCols; ++cb)
+        v[cb] = __ldg(reinterpret_cast<const float4*>(src) + (lane + 32 * rb) * (kD / 4) + wq + kWarps * cb);
+#pragma unroll
+      for (int cb = 0; cb < kCols; ++cb) {  // src[i][4 jq + t] -> dst row r = 4 jq + t, column c = i
+        const int jq = wq + kWarps * cb;
+        float* d0 = dst + (16 * jq + rb) * kPadQ + lane;
+        d0[0] = v[cb].x;
+        d0[4 * kPadQ] = v[cb].y;
+        d0[8 * kPadQ] = v[cb].z;
+        d0[12 * kPadQ] = v[cb].w;
+      }
+    }
+  } else {
+    constexpr int kS = kD * kD / kThreads;  // floats per thread; consecutive threads, consecutive j
+    static_assert(kS % 16 == 0 && kS * kThreads == kD * kD, "whole batches");
+#pragma unroll
+    for (int b0 = 0; b0 < kS; b0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = __ldg(src + threadIdx.x + (b0 + k) * kThreads);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int e = (int)threadIdx.x + (b0 + k) * kThreads;
+        const int i = e / kD, j = e % kD;  // src[i][j]
+        const int r = transpose ? j : i;
+        const int c = transpose ? i : j;
+        dst[(r * 4 + (c >> 5)) * kPadQ + (c & 31)] = v[k];
+      }
+    }
   }
 }
 
