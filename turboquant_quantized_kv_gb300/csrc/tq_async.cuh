@@ -1,7 +1,7 @@
 // Asynchronous shared-memory copies for the libtq kernels (sm_103a): mbarrier
-// wrappers, 1-D bulk copies and 2-D tensor copies (cp.async.bulk[.tensor]),
-// and a bounded mbarrier wait that gives up after about a second instead of
-// spinning forever.
+// wrappers, 2-D tensor copies (cp.async.bulk.tensor), an L2 eviction policy for
+// data read once, the programmatic-dependent-launch wait, and a bounded mbarrier
+// wait that gives up after about a second instead of spinning forever.
 #pragma once
 
 #include <cuda.h>  // CUtensorMap (the type only; no driver calls here)
@@ -25,13 +25,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // L2 policy for data read once per call (the decode's pages): evicted first, so
 // the small data every call re-reads (block tables, context lengths, queries,
 // split partials) stays in L2 while gigabytes of pages stream through it.
@@ -39,22 +32,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
-}
-
-// bulk_copy_g2s with an L2 cache policy.
-__device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                                   uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-          "r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-// Starts bringing [src, src + bytes) into L2 (16-byte aligned, a multiple of 16 bytes);
-// nothing waits for it.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Waits for the grid this one was launched as a programmatic dependent of (no-op
@@ -85,41 +62,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t it = 0; it < (1u << 30); ++it) {
     if (mbar_try(addr, parity)) return true;
     if ((it & 63) == 63 && global_ns() - t0 > 1000000000ull) return false;
-  }
-  return false;
-}
-
-// Non-blocking test of an mbarrier phase (each thread may test its own barrier).
-__device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// try_wait that may suspend the thread for up to `ns` nanoseconds while the phase
-// is incomplete (a suspended warp takes no issue slots).
-__device__ __forceinline__ bool mbar_try_sleep(uint32_t addr, uint32_t parity, uint32_t ns) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(addr), "r"(parity), "r"(ns)
-      : "memory");
-  return done != 0;
-}
-
-// Bounded wait on an mbarrier phase that suspends between tests instead of
-// spinning: gives up after ~1 s (returns false).
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t addr, uint32_t parity) {
-  if (mbar_try_sleep(addr, parity, 20000u)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t it = 0; it < (1u << 30); ++it) {
-    if (mbar_try_sleep(addr, parity, 20000u)) return true;
-    if (global_ns() - t0 > 1000000000ull) return false;
   }
   return false;
 }
