@@ -496,3 +496,35 @@ def test_padded_block_table_splits_the_context(cuda, tqlib):
     cuda.cuda.synchronize()
     assert tq.get_device_status() == 0
     assert np.array_equal(out_p.cpu().numpy(), out_t)
+
+
+def _random_case(i):
+    """Seeded random decode configuration i: batch, KV heads, query heads per KV head
+    (partial groups of 4 and 8 included), key / value bits, QJL keys, rotation kind,
+    ragged contexts (empty ones included), split count, data and query precision."""
+    r = np.random.default_rng(1000 + i)
+    hkv = int(r.choice([1, 2, 4]))
+    g = int(r.choice([1, 2, 3, 4, 5, 8, 12, 16]))
+    B = int(r.integers(1, 4))
+    ctx = [int(c) for c in r.integers(1, 700, size=B)]
+    if B > 1 and r.random() < 0.3:  # an empty sequence beside live ones
+        ctx[int(r.integers(0, B))] = 0
+    qjl = bool(r.random() < 0.25)
+    return dict(B=B, Hq=g * hkv, Hkv=hkv, ctx=ctx, bits_k=int(r.choice([2, 3, 4])), bits_v=int(r.choice([2, 3, 4])),
+                qjl=qjl, rot=1 if r.random() < 0.75 else 2, data=str(r.choice(["gauss", "lognormal", "heavy"])),
+                seed=20 + i, num_splits=int(r.choice([0, 0, 1, int(r.integers(2, 41))])),
+                q_f32=bool(r.random() < 0.3))
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_randomized_decode_configurations(cuda, tqlib, i):
+    """Sixteen seeded random configurations against the oracle's exact attention over
+    the GPU's own cache (bf16 inputs: the 5e-3 tolerance)."""
+    kw = _random_case(i)
+    if kw["rot"] == 2:
+        kw["rot"] = tqlib.TQ_ROT_DENSE
+    else:
+        kw["rot"] = tqlib.TQ_ROT_HADAMARD
+    print(kw)
+    out, ref, _ = run_case(cuda, tqlib, **kw)
+    assert_close(out, ref, TOL_BF16, kw["ctx"])
