@@ -445,3 +445,62 @@ def test_append_layers_equals_per_layer_appends(cuda, tqlib, kind):
     # a shared cache is rejected before anything is launched
     with pytest.raises(tq.TQError):
         tq.append_layers([batched[0], batched[0]], ks[:2], vs[:2], slots_d)
+
+
+def _random_append_case(i):
+    """Seeded random append configuration i: heads, tokens (some past the bulk kernels'
+    24,576-vector threshold), key / value bits, rotation kind, QJL keys, input dtype,
+    skipped slots, data."""
+    r = np.random.default_rng(2000 + i)
+    H = int(r.choice([1, 2, 4, 8]))
+    n = int(r.integers(1, 900)) if r.random() < 0.6 else int(24576 // H + r.integers(1, 400))
+    dense = bool(r.random() < 0.35)
+    return dict(H=H, n=n, bits_k=int(r.choice([2, 3, 4])), bits_v=int(r.choice([2, 3, 4])), dense=dense,
+                qjl=bool(r.random() < 0.2), f32=bool(r.random() < 0.25), skip=int(r.choice([0, 7, 37])),
+                lognormal=bool(r.random() < 0.5), seed=40 + i)
+
+
+@pytest.mark.parametrize("i", range(10))
+def test_randomized_append_configurations(cuda, tqlib, i):
+    """Ten seeded random appends against the oracle's quantizer: codes equal except
+    within 1e-5 of a boundary, gamma within 2e-6 relative, skipped slots untouched."""
+    tq = tqlib
+    c = _random_append_case(i)
+    print(c)
+    H, n = c["H"], c["n"]
+    nb = n // 16 + 3
+    rot = tq.TQ_ROT_DENSE if c["dense"] else tq.TQ_ROT_HADAMARD
+    layer = tq.Layer(nb, H, bits_k=c["bits_k"], bits_v=c["bits_v"], qjl=c["qjl"], rot_kind=rot, seed=c["seed"],
+                     layer=3, qjl_seed=c["seed"] + 1, fill=0x5A)
+    if c["lognormal"]:
+        kb, vb = workloads.lognormal_channel_kv(c["seed"], n, H, D)
+    else:
+        kb, vb = workloads.scaled_gaussian_kv(c["seed"], n, H, D)
+    if c["f32"]:
+        kx, vx = workloads.bf16_to_f32(kb), workloads.bf16_to_f32(vb)
+        kt, vt = cuda.from_numpy(kx).cuda(), cuda.from_numpy(vx).cuda()
+        kx, vx = kx.astype(np.float64), vx.astype(np.float64)
+    else:
+        kt, vt = _bf16_dev(cuda, kb), _bf16_dev(cuda, vb)
+        kx, vx = oq.bf16_bits_to_f64(kb), oq.bf16_bits_to_f64(vb)
+    slots, slots_d = make_slots(cuda, n, nb, c["seed"] + 2, skip_every=c["skip"])
+    layer.append(kt, vt, slots_d)
+    assert tq.get_device_status() == 0
+    pi = (orot.dense_rotation_seeded if c["dense"] else orot.hadamard_rotation_seeded)(c["seed"], 3, D)
+    keep = slots >= 0
+    written = np.zeros(nb * 16, bool)
+    written[slots[keep]] = True
+    for which, x, pool, bits in ((0, kx, layer.k_cache, c["bits_k"]), (1, vx, layer.v_cache, c["bits_v"])):
+        c32, b32 = ocb.codebook_fp32(D, bits)
+        host = pool.cpu().numpy()
+        fields = page_fields(layer, which, host)
+        for h in range(H):
+            idx, gamma, y = oq.quantize(x[keep, h], pi, c32, b32)
+            codes, g_gpu = slot_fields(fields, slots[keep], h)[:2]  # (QJL pages add signs and rho)
+            ok, _ = tie_band_ok(y, codes, idx, b32, 1e-5)
+            assert ok, "code mismatch outside the tie band"
+            same = np.all(codes == idx, axis=-1)
+            assert np.all(np.abs(g_gpu[same] - gamma[same]) <= 2e-6 * np.abs(gamma[same]) + 1e-30)
+        if not (which == 0 and c["qjl"]):
+            rec = opack_record_view(host, nb, H, bits)
+            assert np.all(rec[~written.reshape(nb, 16)] == 0x5A)
