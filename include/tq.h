@@ -290,8 +290,13 @@ size_t tq_workspace_bytes(const tq_cache_desc* desc, int batch, int num_q_heads,
  * multiple of num_kv_heads (any group size: a group above TQ_MAX_GROUP heads
  * is split into warps of 8 heads that each stream the KV head's pages).
  * num_splits: 0 = automatic, else the
- * number of contiguous context ranges each (sequence, KV head) is split into;
- * results agree for every split count up to fp32 rounding. */
+ * number of contiguous ranges each (sequence, KV head) is split into;
+ * results agree for every split count up to fp32 rounding.  The ranges cut the
+ * block-table row (max_blocks_per_seq entries), so a sequence's block ids are
+ * read while its context length is still in flight; a row more than a third
+ * wider than the sequence's context (a table padded to a maximum length) is
+ * cut over the context instead, at the cost of reading the block ids after it.
+ * Either way the output is the same function of the inputs. */
 tq_status tq_decode_attention(const tq_cache_desc* desc, const void* q, int q_dtype, int batch,
                               int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
                               const int32_t* context_lens, float sm_scale, void* out, int out_dtype,
@@ -304,7 +309,10 @@ tq_status tq_decode_attention(const tq_cache_desc* desc, const void* q, int q_dt
  * launched).  The decode kernel is launched as a programmatic dependent of the
  * append: its prologue (context lengths, block ids, query rotation, code
  * tables) runs while the append is still writing, and it waits for the append
- * to finish before it reads any page.  q, block_table and context_lens are
+ * to finish before it reads any page.  For dense-rotation and QJL layers the
+ * query pass (q' = Pi q, S q') is the append's dependent instead and the decode
+ * that pass's; the pass reads only q and writes only the workspace, and it
+ * completes only after the append.  q, block_table and context_lens are
  * therefore read while the append runs; the append never writes them. */
 tq_status tq_append_decode(const tq_cache_desc* desc, const void* k, const void* v, int in_dtype,
                            const int64_t* slot_mapping, int64_t n_tokens, const void* q, int q_dtype, int batch,
