@@ -5,8 +5,8 @@ heads, head_dim 128, 32 layers, context 8192 (+1 token per step), bf16 K/V with
 per-(head, channel) lognormal(0, 1) scales, 4-bit keys and values with fp32
 norms, Hadamard rotation per layer, paged 16-token blocks under a shuffled block
 table.  A step appends one new token per sequence to every layer (quantize-
-append) and runs decode attention over every layer (one tq_append_decode call
-per layer: the decode kernel's prologue overlaps the append).  All inputs are synthetic
+append) and runs decode attention over every layer: one tq_decode_step call per
+layer, whose decode kernel quantizes the new token itself.  All inputs are synthetic
 and already resident in HBM; one step reads ~4.6 GB of packed cache, more
 than L2, so no flush is needed between steps.
 
@@ -576,6 +576,7 @@ def incremental_dequant_baseline(torch, tq, st, dev, peak, reps=20):
                       sl)
     out = torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev)
     ws = torch.zeros(shadow.workspace_bytes(B, HQ, st["mb"]), dtype=torch.uint8, device=dev)
+    last_slots(torch, st)
     q, knew, vnew, slot = st["q"][0], st["knew"][0], st["vnew"][0], st["slot_new"]
     ctx = st["ctx"]
 
@@ -618,15 +619,16 @@ def incremental_dequant_baseline(torch, tq, st, dev, peak, reps=20):
 
 
 def step_prepare(torch, st):
-    """ctx += 1 is done after the step; the new token goes to position ctx."""
-    ctx64 = st["ctx"].to(torch.int64)
-    blk = torch.gather(st["bt"], 1, (ctx64 // BLOCK).unsqueeze(1)).squeeze(1).to(torch.int64)
-    st["slot_new"].copy_(blk * BLOCK + ctx64 % BLOCK)
+    """ctx += 1: the step's new token goes to position ctx (tq_decode_step finds its slot
+    from the block table itself)."""
     st["ctx"].add_(1)
 
 
-def layer_append(st, l):
-    st["layers"][l].append(st["knew"][l], st["vnew"][l], st["slot_new"])
+def last_slots(torch, st):
+    """slot_new = the slots of position ctx - 1 of every sequence (the newest token)."""
+    ctx64 = st["ctx"].to(torch.int64) - 1
+    blk = torch.gather(st["bt"], 1, (ctx64 // BLOCK).unsqueeze(1)).squeeze(1).to(torch.int64)
+    st["slot_new"].copy_(blk * BLOCK + ctx64 % BLOCK)
 
 
 def layer_decode(st, l):
@@ -634,10 +636,9 @@ def layer_decode(st, l):
 
 
 def layer_step(st, l):
-    """Append the new token of every sequence, then decode (tq_append_decode: the decode's
-    prologue overlaps the append)."""
-    st["layers"][l].append_decode(st["knew"][l], st["vnew"][l], st["slot_new"], st["q"][l], st["bt"], st["ctx"],
-                                  out=st["out"][l], workspace=st["ws"], num_splits=SPLITS)
+    """Append the new token of every sequence and decode, in one kernel (tq_decode_step)."""
+    st["layers"][l].decode_step(st["knew"][l], st["vnew"][l], st["q"][l], st["bt"], st["ctx"],
+                                out=st["out"][l], workspace=st["ws"], num_splits=SPLITS)
 
 
 def run_tq(args):
@@ -788,7 +789,7 @@ def run_tq(args):
 def run_e2e(torch, st, args, stream):
     """Public API, host buffers: per step the H2D copy of the new K/V tokens and queries
     of every layer from one pinned staging buffer, append + decode per layer through
-    Layer.append_decode, and the D2H copy of all layers' outputs; the copies go in
+    Layer.decode_step, and the D2H copy of all layers' outputs; the copies go in
     chunks of 8 layers on a second stream, each layer waiting only for its own chunk."""
     parts = [t for l in range(LAYERS) for t in (st["knew"][l], st["vnew"][l], st["q"][l])]
     sizes = [t.numel() for t in parts]
@@ -829,8 +830,8 @@ def run_e2e(torch, st, args, stream):
             if l % per == 0:
                 stream.wait_event(ev_in[c])
             k, v, q = views[3 * l], views[3 * l + 1], views[3 * l + 2]
-            st["layers"][l].append_decode(k, v, st["slot_new"], q, st["bt"], st["ctx"], out=d_out[l],
-                                          workspace=st["ws"], num_splits=SPLITS)
+            st["layers"][l].decode_step(k, v, q, st["bt"], st["ctx"], out=d_out[l], workspace=st["ws"],
+                                        num_splits=SPLITS)
             if l % per == per - 1:
                 ev_out[c].record(stream)
                 cs.wait_event(ev_out[c])

@@ -320,6 +320,27 @@ tq_status tq_append_decode(const tq_cache_desc* desc, const void* k, const void*
                            const int32_t* context_lens, float sm_scale, void* out, int out_dtype, void* workspace,
                            size_t workspace_bytes, int num_splits, void* stream);
 
+/* One decode step of a layer in a single kernel: the new token of every sequence
+ * is quantized by the decode kernel itself and attended to in the same call.
+ * k_new, v_new: device [batch][num_kv_heads][head_dim] (in_dtype TQ_F32 or
+ * TQ_BF16, 16-byte aligned); context_lens[b] already counts the new token, which
+ * is written at position context_lens[b] - 1 of sequence b (slot block_table[b]
+ * [(context_lens[b] - 1) / 16] * 16 + (context_lens[b] - 1) % 16); a sequence
+ * with context_lens[b] == 0 gets no token and a zero output row.  The record is
+ * the same quantization as tq_quantize_append's ("Method"), computed by one warp
+ * per (sequence, KV head) in fp32 with its own order of operations, so a code may
+ * differ from the append kernels' only where y lies within ~1e-6 of a boundary.
+ * The warp that reads the new token's block writes the record to the cache and
+ * into its own shared-memory copy of the block, so no other kernel runs and no
+ * CTA waits for another.  Other arguments, the workspace contract and errors as
+ * for tq_decode_attention.  Packed layers with a Hadamard rotation and without
+ * QJL keys only (TQ_ERR_UNSUPPORTED otherwise); every context length must be >= 1
+ * for a sequence whose token is to be appended. */
+tq_status tq_decode_step(const tq_cache_desc* desc, const void* k_new, const void* v_new, int in_dtype,
+                         const void* q, int q_dtype, int batch, int num_q_heads, const int32_t* block_table,
+                         int max_blocks_per_seq, const int32_t* context_lens, float sm_scale, void* out,
+                         int out_dtype, void* workspace, size_t workspace_bytes, int num_splits, void* stream);
+
 /* Dequantize records ([P2] "Incremental dequantization"): slots: device int64[n];
  * out: device [n][num_kv_heads][head_dim] (out_dtype) with
  * x_hat = gamma Pi^T c[idx] of the K (which = 0) or V (which = 1) pool

@@ -528,3 +528,72 @@ def test_randomized_decode_configurations(cuda, tqlib, i):
     print(kw)
     out, ref, _ = run_case(cuda, tqlib, **kw)
     assert_close(out, ref, TOL_BF16, kw["ctx"])
+
+
+@pytest.mark.parametrize("bk,bv,f32", [(4, 4, False), (3, 4, False), (2, 2, True)])
+def test_decode_step_appends_and_attends(cuda, tqlib, bk, bv, f32):
+    """tq_decode_step (the new token quantized by the decode kernel itself) against an
+    append at the same slots followed by a decode, step after step: the new records
+    follow the oracle's quantizer (codes except within 1e-5 of a boundary, gamma within
+    2e-6), every other byte of the cache is the same, and the output matches the
+    oracle's attention over the resulting cache."""
+    from oracle import codebook as ocb
+    from tests._gpu_util import oracle_pi, page_fields, slot_fields, tie_band_ok
+    tq = tqlib
+    B, Hq, Hkv, T = 4, 16, 4, 320
+    mb = T // 16 + 1
+    bt, nb = workloads.shuffled_block_table(15, B, mb, num_blocks=B * mb + 2)
+    kb, vb = workloads.lognormal_channel_kv(16, B * T, Hkv, D)
+    kb, vb = kb.reshape(B, T, Hkv, D), vb.reshape(B, T, Hkv, D)
+    kw = dict(bits_k=bk, bits_v=bv, seed=5, layer=2)
+    la, lb = tq.Layer(nb, Hkv, **kw), tq.Layer(nb, Hkv, **kw)
+    ctx0 = np.array([200, 7, 0, 33], np.int32)  # sequence 2 starts empty
+    for layer in (la, lb):
+        fill_cache(cuda, layer, kb, vb, bt, ctx0, True)
+    bt_d = cuda.from_numpy(bt).cuda()
+    pi = oracle_pi(la)
+    appended = []  # every slot written so far (its gamma may differ in the last bits between the paths)
+    for step in range(3):
+        pos = ctx0 + step
+        slots = workloads.slot_mapping(bt, pos[:, None])[:, 0].astype(np.int64)
+        appended.extend(int(x) for x in slots)
+        kx, vx = kb[np.arange(B), pos], vb[np.arange(B), pos]  # [B][Hkv][D] bf16 bits
+        if f32:
+            knew = cuda.from_numpy(workloads.bf16_to_f32(kx)).cuda()
+            vnew = cuda.from_numpy(workloads.bf16_to_f32(vx)).cuda()
+        else:
+            knew, vnew = to_dev(cuda, kx, True), to_dev(cuda, vx, True)
+        q = to_dev(cuda, workloads.queries(40 + step, B, Hq, D), True)
+        ctx_d = cuda.from_numpy(pos + 1).cuda()
+        out_a = la.decode_step(knew, vnew, q, bt_d, ctx_d, out_dtype=cuda.float32)
+        lb.append(knew, vnew, cuda.from_numpy(slots).cuda())
+        lb.decode(q, bt_d, ctx_d, out_dtype=cuda.float32)
+        cuda.cuda.synchronize()
+        assert tq.get_device_status() == 0
+        # the new records against the oracle's quantizer, the rest of the cache unchanged
+        for which, x, bits, pa, pb in ((0, kx, bk, la.k_cache, lb.k_cache), (1, vx, bv, la.v_cache, lb.v_cache)):
+            ha, hb = pa.cpu().numpy(), pb.cpu().numpy()
+            c32, b32 = ocb.codebook_fp32(D, bits)
+            fa = page_fields(la, which, ha)
+            for h in range(Hkv):
+                idx, gamma, y = oq.quantize(oq.bf16_bits_to_f64(x[:, h]), pi, c32, b32)
+                codes, g = slot_fields(fa, slots, h)[:2]
+                ok, _ = tie_band_ok(y, codes, idx, b32, 1e-5)
+                assert ok, "code mismatch outside the tie band"
+                same = np.all(codes == idx, axis=-1)
+                assert np.all(np.abs(g[same] - gamma[same]) <= 2e-6 * np.abs(gamma[same]) + 1e-30)
+            pb_bytes = ha.reshape(nb, Hkv, -1).shape[-1]
+            mask = np.ones((nb, Hkv, pb_bytes), bool)
+            from oracle import pack as opack
+            rb = opack.page_bytes(D, bits)
+            assert rb == pb_bytes
+            for s_ in appended:  # the new tokens' records and gammas in every head's page
+                blk, off = s_ // 16, s_ % 16
+                mask[blk, :, off * 16 * bits:(off + 1) * 16 * bits] = False
+                mask[blk, :, 16 * 16 * bits + 4 * off:16 * 16 * bits + 4 * off + 4] = False
+            assert np.array_equal(ha.reshape(nb, Hkv, -1)[mask], hb.reshape(nb, Hkv, -1)[mask])
+        # the output against the oracle's attention over this cache
+        kp, vp = la.k_cache.cpu().numpy(), la.v_cache.cpu().numpy()
+        qx = oq.bf16_bits_to_f64(workloads.queries(40 + step, B, Hq, D))
+        ref = oa.decode_packed(qx, kp, vp, oracle_layer(la), nb, Hkv, bt, pos + 1, 1 / math.sqrt(D))
+        assert_close(out_a.cpu().numpy(), ref, TOL_BF16, pos + 1)

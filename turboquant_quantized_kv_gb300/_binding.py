@@ -77,6 +77,10 @@ _SIGNATURES = {
                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                                         ctypes.c_int, ctypes.c_void_p]),
+    "tq_decode_step": (ctypes.c_int, [_D, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]),
     "tq_dequantize": (ctypes.c_int, [_D, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                      ctypes.c_int, ctypes.c_void_p]),
     "tq_image_bytes": (ctypes.c_size_t, [_D, ctypes.c_int64]),
@@ -320,6 +324,28 @@ class Layer:
                                       _ptr(context_lens, "context_lens"), ctypes.c_float(sm_scale),
                                       _ptr(out, "out"), _dtype_code(out), _ptr(workspace, "workspace"),
                                       workspace.numel(), num_splits, _stream(stream)))
+        return out
+
+    def decode_step(self, k_new, v_new, q, block_table, context_lens, sm_scale=None, out=None, out_dtype=None,
+                    num_splits=0, workspace=None, stream=None):
+        """One decode step in one kernel (tq_decode_step): k_new, v_new [B, H_kv, d] are the new
+        tokens, written at position context_lens[b] - 1 of each sequence (context_lens already
+        counts them), then decode(q, ...).  Returns out."""
+        torch = _torch()
+        bsz, hq, _ = q.shape
+        max_blocks = int(block_table.shape[1])
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.head_dim)
+        if out is None:
+            out = torch.empty(q.shape, dtype=q.dtype if out_dtype is None else out_dtype, device=q.device)
+        if workspace is None:
+            workspace = torch.zeros(self.workspace_bytes(bsz, hq, max_blocks, num_splits), dtype=torch.uint8,
+                                    device=q.device)
+        _check(lib().tq_decode_step(ctypes.byref(self.desc), _ptr(k_new, "k_new"), _ptr(v_new, "v_new"),
+                                    _dtype_code(k_new), _ptr(q, "q"), _dtype_code(q), bsz, hq,
+                                    _ptr(block_table, "block_table"), max_blocks, _ptr(context_lens, "context_lens"),
+                                    ctypes.c_float(sm_scale), _ptr(out, "out"), _dtype_code(out),
+                                    _ptr(workspace, "workspace"), workspace.numel(), num_splits, _stream(stream)))
         return out
 
     def image_bytes(self, n_blocks):

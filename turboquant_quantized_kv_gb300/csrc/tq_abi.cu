@@ -253,6 +253,32 @@ tq_status tq_decode_attention(const tq_cache_desc* desc, const void* q, int q_dt
   return cuda_result(launch_decode(c, reinterpret_cast<cudaStream_t>(stream)), "decode attention");
 }
 
+tq_status tq_decode_step(const tq_cache_desc* desc, const void* k_new, const void* v_new, int in_dtype,
+                         const void* q, int q_dtype, int batch, int num_q_heads, const int32_t* block_table,
+                         int max_blocks_per_seq, const int32_t* context_lens, float sm_scale, void* out,
+                         int out_dtype, void* workspace, size_t workspace_bytes, int num_splits, void* stream) {
+  clear_error();
+  tq_status s = check_desc(desc);
+  if (s != TQ_OK) return s;
+  const tq_layer_format& f = desc->fmt;
+  if (f.kv_format != TQ_KV_PACKED || f.qjl_k || f.rot_kind != TQ_ROT_HADAMARD)
+    return fail(TQ_ERR_UNSUPPORTED, "tq_decode_step: packed layers with a Hadamard rotation and no QJL keys only");
+  if (!valid_dtype(in_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_decode_step: in_dtype %d", in_dtype);
+  if (batch > 0 && (!k_new || !v_new)) return fail(TQ_ERR_INVALID_ARG, "tq_decode_step: null k_new or v_new");
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+    return fail(TQ_ERR_INVALID_ARG, "tq_decode_step: k_new/v_new must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(desc->rotation) & 3)
+    return fail(TQ_ERR_INVALID_ARG, "tq_decode_step: rotation must be 4-byte aligned");
+  DecodeCall c;
+  s = prepare_decode(desc, q, q_dtype, batch, num_q_heads, block_table, max_blocks_per_seq, context_lens, sm_scale,
+                     out, out_dtype, workspace, workspace_bytes, num_splits, "tq_decode_step", &c);
+  if (s != TQ_OK || batch == 0) return s;
+  c.new_k = k_new;
+  c.new_v = v_new;
+  c.new_dtype = in_dtype;
+  return cuda_result(launch_decode(c, reinterpret_cast<cudaStream_t>(stream)), "decode step");
+}
+
 tq_status tq_append_decode(const tq_cache_desc* desc, const void* k, const void* v, int in_dtype,
                            const int64_t* slot_mapping, int64_t n_tokens, const void* q, int q_dtype, int batch,
                            int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,

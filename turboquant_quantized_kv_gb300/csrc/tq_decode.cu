@@ -210,7 +210,68 @@ struct DecodeArgs {
   Codebook cbk, cbv;
   float qjl_coef;  // sqrt(pi/2) / m
   unsigned* status;
+  // tq_decode_step (packed Hadamard layers without QJL): the new token of sequence b,
+  // [B][Hkv][d] each, written by the warp that holds block (ctx_b - 1) / 16 of its unit
+  const void* new_k;
+  const void* new_v;
+  int new_bf16;
+  int norm_raw;  // TQ_NORM_RAW: gamma = n
 };
+
+// One new vector quantized by a whole warp (tq_decode_step): lane l holds x_j for
+// j = 4 l .. 4 l + 3.  y = H D x / (sqrt(d) n) with n = ||x||, code_j = #{k : y_j >=
+// beta_k} (ties go up; y = 0 for the zero vector, so its codes are 2^(b-1) and gamma
+// 0), gamma = n / ||c[code]|| (n with TQ_NORM_RAW).  On return lane w < 4 BITS holds
+// word w of the LSB-first record (code j in bits BITS j .. BITS j + BITS - 1).
+template <int BITS>
+__device__ __forceinline__ void warp_quantize_record(const float (&x)[4], const float4& sg, const Codebook& cb,
+                                                     bool norm_raw, int lane, uint32_t& word, float& gamma) {
+  float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float n = sqrtf(ss);
+  float y[4] = {x[0] * sg.x, x[1] * sg.y, x[2] * sg.z, x[3] * sg.w};
+  {  // bits 0, 1 of the coordinate in the lane, bits 2..6 across lanes
+    const float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
+    y[0] = t0 + t2; y[2] = t0 - t2; y[1] = t1 + t3; y[3] = t1 - t3;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const bool upper = (lane & m) != 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float o = __shfl_xor_sync(0xffffffffu, y[k], m);
+        y[k] = upper ? (o - y[k]) : (y[k] + o);
+      }
+    }
+  }
+  const float inv = n > 0.0f ? 0.08838834764831845f / n : 0.0f;  // 1 / (sqrt(128) n)
+  constexpr int NB = (1 << BITS) - 1;
+  uint32_t f = 0u;
+  float c2 = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float yk = y[k] * inv;
+    uint32_t c = 0u;  // #{t : y >= beta_t} by bisection (the boundaries ascend)
+#pragma unroll
+    for (int step = 1 << (BITS - 1); step > 0; step >>= 1)
+      if (yk >= cb.b[c + step - 1]) c += step;
+    const float ck = cb.c[c];
+    c2 = fmaf(ck, ck, c2);
+    f |= c << (BITS * k);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c2 += __shfl_xor_sync(0xffffffffu, c2, o);
+  gamma = norm_raw ? n : ((n > 0.0f && c2 > 0.0f) ? n / sqrtf(c2) : 0.0f);
+  // the lane's 4 BITS bits sit at bit 4 BITS l of the record: words w0 and maybe w0 + 1
+  const int o = 4 * BITS * lane, w0 = o >> 5, sh = o & 31;
+  const uint32_t lo = f << sh, hi = sh + 4 * BITS > 32 ? f >> (32 - sh) : 0u;
+  word = 0u;
+#pragma unroll
+  for (int w = 0; w < 4 * BITS; ++w) {
+    const uint32_t r = __reduce_or_sync(0xffffffffu, (w == w0 ? lo : 0u) | (w == w0 + 1 ? hi : 0u));
+    if (lane == w) word = r;
+  }
+}
 
 // Lane layout of a warp (g_ = lane / 4, tig = lane % 4) for NT n-tiles of 4 heads.
 //
@@ -772,6 +833,23 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   // ---- prologue: the long-latency loads first (context length, query rows), then
   // the block ids and the first copies, the code tables while those are in flight
   const int ctx_raw = has ? __ldg(a.ctx_lens + b) : 0;
+  // tq_decode_step: the last split's warp usually holds the new token's block, so it
+  // requests the new K and V coordinates and the signs now (used below)
+  uint2 pf_k = make_uint2(0u, 0u), pf_v = make_uint2(0u, 0u);
+  float4 pf_kf = make_float4(0.f, 0.f, 0.f, 0.f), pf_vf = pf_kf, pf_sg = pf_kf;
+  const bool pf = KIND == 0 && !QJL && BK <= 4 && a.new_k != nullptr && has && s == a.splits - 1;
+  if (pf) {
+    const int64_t row = ((int64_t)b * a.Hkv + kvh) * kD + 4 * lane;
+    if (a.new_bf16) {
+      pf_k = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.new_k) + row));
+      pf_v = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.new_v) + row));
+    } else {
+      pf_kf = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.new_k) + row));
+      pf_vf = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.new_v) + row));
+    }
+    pf_sg = make_float4(__ldg(a.rot + 4 * lane), __ldg(a.rot + 4 * lane + 1), __ldg(a.rot + 4 * lane + 2),
+                        __ldg(a.rot + 4 * lane + 3));
+  }
 
   // CTA-shared query rotation (q_in_kernel != 0): the rows of this CTA's units are
   // rotated once, one warp per row, into a scratch area past the rings
@@ -1002,6 +1080,60 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
   uint32_t vm = 0u;  // SB bits per slot: blocks present
   if (a.overlap_append) grid_dep_wait();
   for (int k = 0; k < P; ++k) vm |= copy_stage(k, k) << (SB * k);
+
+  // tq_decode_step: the warp whose chunk holds block (ctx - 1) / 16 quantizes the new K
+  // and V vectors of its (sequence, KV head), writes both records to the cache and,
+  // once that block's copy has landed, into its own stage (below)
+  int fz_stage = -1, fz_e = 0, fz_off = 0;
+  uint32_t fz_wk = 0u, fz_wv = 0u;
+  float fz_gk = 0.0f, fz_gv = 0.0f;
+  if constexpr (KIND == 0 && !QJL && BK <= 4) {
+    if (a.new_k != nullptr && has && ctx > 0) {
+      const int jl = (ctx - 1) / kBlock;
+      if (jl >= j0 && jl < j0 + n_my) {  // warp-uniform
+        const int blk = __ldg(a.block_table + (int64_t)b * a.max_blocks + jl);
+        const int64_t row = ((int64_t)b * a.Hkv + kvh) * kD + 4 * lane;
+        float xk[4], xv[4];
+        float4 sg = pf_sg;
+        if (!pf) {  // (another split holds the block: load now)
+          if (a.new_bf16) {
+            pf_k = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.new_k) + row));
+            pf_v = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.new_v) + row));
+          } else {
+            pf_kf = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.new_k) + row));
+            pf_vf = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.new_v) + row));
+          }
+          sg = make_float4(__ldg(a.rot + 4 * lane), __ldg(a.rot + 4 * lane + 1), __ldg(a.rot + 4 * lane + 2),
+                           __ldg(a.rot + 4 * lane + 3));
+        }
+        if (a.new_bf16) {
+          xk[0] = __uint_as_float(pf_k.x << 16); xk[1] = __uint_as_float(pf_k.x & 0xFFFF0000u);
+          xk[2] = __uint_as_float(pf_k.y << 16); xk[3] = __uint_as_float(pf_k.y & 0xFFFF0000u);
+          xv[0] = __uint_as_float(pf_v.x << 16); xv[1] = __uint_as_float(pf_v.x & 0xFFFF0000u);
+          xv[2] = __uint_as_float(pf_v.y << 16); xv[3] = __uint_as_float(pf_v.y & 0xFFFF0000u);
+        } else {
+          xk[0] = pf_kf.x; xk[1] = pf_kf.y; xk[2] = pf_kf.z; xk[3] = pf_kf.w;
+          xv[0] = pf_vf.x; xv[1] = pf_vf.y; xv[2] = pf_vf.z; xv[3] = pf_vf.w;
+        }
+        warp_quantize_record<BK>(xk, sg, a.cbk, a.norm_raw != 0, lane, fz_wk, fz_gk);
+        warp_quantize_record<BV>(xv, sg, a.cbv, a.norm_raw != 0, lane, fz_wv, fz_gv);
+        fz_off = (ctx - 1) % kBlock;
+        if (blk >= 0 && (int64_t)blk < a.num_blocks) {  // (an id out of range is flagged by the copy)
+          constexpr int RK = 16 * BK, RV = 16 * BV;
+          uint8_t* kp = const_cast<uint8_t*>(a.kpool) + ((int64_t)blk * a.Hkv + kvh) * KPAGE;
+          uint8_t* vp = const_cast<uint8_t*>(a.vpool) + ((int64_t)blk * a.Hkv + kvh) * VPAGE;
+          if (lane < 4 * BK) reinterpret_cast<uint32_t*>(kp + fz_off * RK)[lane] = fz_wk;
+          if (lane < 4 * BV) reinterpret_cast<uint32_t*>(vp + fz_off * RV)[lane] = fz_wv;
+          if (lane == 0) {
+            reinterpret_cast<float*>(kp + 16 * RK)[fz_off] = fz_gk;
+            reinterpret_cast<float*>(vp + 16 * RV)[fz_off] = fz_gv;
+          }
+          fz_stage = (jl - j0) / SB;
+          fz_e = (jl - j0) % SB;
+        }
+      }
+    }
+  }
   if (!q_shared && !a.q_in_kernel) {  // the pages do not depend on the rotation pass; its rows do
     grid_dep_wait();
     load_q_rows(true);
@@ -1069,6 +1201,20 @@ __global__ void __launch_bounds__(NW * 32, 1) k_decode(DecodeArgs a) {
     __syncwarp();   // ... and every lane's
     const uint32_t m = (vm >> (SB * slot)) & ((1u << SB) - 1u);
     const uint8_t* sa = gen(ring + (uint32_t)slot * stage_bytes);
+    if constexpr (KIND == 0 && !QJL && BK <= 4) {
+      if (i == fz_stage && ((m >> fz_e) & 1u)) {  // tq_decode_step: the new token into the landed block
+        constexpr int RK = 16 * BK, RV = 16 * BV;
+        uint8_t* kp = const_cast<uint8_t*>(sa) + fz_e * blk_bytes;
+        uint8_t* vp = kp + KPAGE;
+        if (lane < 4 * BK) reinterpret_cast<uint32_t*>(kp + fz_off * RK)[lane] = fz_wk;
+        if (lane < 4 * BV) reinterpret_cast<uint32_t*>(vp + fz_off * RV)[lane] = fz_wv;
+        if (lane == 0) {
+          reinterpret_cast<float*>(kp + 16 * RK)[fz_off] = fz_gk;
+          reinterpret_cast<float*>(vp + 16 * RV)[fz_off] = fz_gv;
+        }
+        __syncwarp();
+      }
+    }
     if constexpr (KIND == 0) {
       if constexpr (SB == 2) {  // two blocks (32 tokens) per stage: keys of both, one softmax update, values of both
         if (m) {
@@ -1683,6 +1829,10 @@ cudaError_t launch_decode(const DecodeCall& c, cudaStream_t st) {
   a.rot = d.rotation;
   a.out = c.out;
   a.out_bf16 = c.out_dtype == TQ_BF16 ? 1 : 0;
+  a.new_k = c.new_k;
+  a.new_v = c.new_v;
+  a.new_bf16 = c.new_dtype == TQ_BF16 ? 1 : 0;
+  a.norm_raw = d.fmt.norm_mode == TQ_NORM_RAW ? 1 : 0;
   if (bf16) {
     e = run_decode<1, 4, 4, false>(a, st);
   } else {

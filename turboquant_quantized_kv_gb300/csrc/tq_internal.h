@@ -63,6 +63,11 @@ struct DecodeCall {
   int splits;
   unsigned* status;
   bool after_append;  // enqueued right after this library's append on the same stream (tq_append_decode)
+  // tq_decode_step: the new token of sequence b ([batch][H_kv][head_dim], new_dtype)
+  // is written by the decode kernel itself at position context_lens[b] - 1
+  const void* new_k = nullptr;
+  const void* new_v = nullptr;
+  int new_dtype = 0;
 };
 
 // True if the append quantizer's cell table can hold these (ascending) boundaries:
