@@ -158,6 +158,34 @@ def test_append_decode_checks_both_calls_before_launching(tqlib):
     assert tq.launch_count() == launches0
 
 
+def test_decode_step_checks(tqlib):
+    """tq_decode_step takes packed Hadamard layers without QJL keys and checks its new
+    tokens before anything is launched (the decode part as tq_decode_attention)."""
+    tq = tqlib
+    lib = tq.lib()
+    launches0 = tq.launch_count()
+    ws = ctypes.c_void_p(0x40000)
+
+    def call(d, k, v, hq=8, batch=2, in_dtype=None):
+        return lib.tq_decode_step(ctypes.byref(d), k, v, tq.TQ_BF16 if in_dtype is None else in_dtype,
+                                  ctypes.c_void_p(0x1000), tq.TQ_F32, batch, hq, ctypes.c_void_p(8), 4,
+                                  ctypes.c_void_p(8), 0.1, ctypes.c_void_p(0x1000), tq.TQ_F32, ws, 1 << 20, 1, None)
+
+    good = ctypes.c_void_p(0x2000)
+    for kw in (dict(rot_kind=tq.TQ_ROT_DENSE), dict(qjl_k=1, qjl_proj=0x50000), dict(kv_format=tq.TQ_KV_BF16),
+               dict(kv_format=tq.TQ_KV_K8V4, bits_k=8)):
+        assert call(fake_desc(tq, **kw), good, good) == tq.TQ_ERR_UNSUPPORTED, kw
+        assert "tq_decode_step" in tq.last_error()
+    d = fake_desc(tq)
+    assert call(d, None, good) == tq.TQ_ERR_INVALID_ARG  # null k_new
+    assert call(d, good, ctypes.c_void_p(0x2008)) == tq.TQ_ERR_INVALID_ARG  # misaligned v_new
+    assert "aligned" in tq.last_error()
+    assert call(d, good, good, in_dtype=7) == tq.TQ_ERR_INVALID_ARG  # bad dtype
+    assert call(d, good, good, hq=12) == tq.TQ_ERR_INVALID_ARG  # 12 % 8 != 0 (the decode's check)
+    assert call(d, good, good, batch=0) == tq.TQ_OK  # nothing to do
+    assert tq.launch_count() == launches0
+
+
 def test_make_args_rejected(tqlib):
     lib = tqlib.lib()
     c = (ctypes.c_float * 16)()
