@@ -329,7 +329,8 @@ tq_status tq_append_decode(const tq_cache_desc* desc, const void* k, const void*
  * with context_lens[b] == 0 gets no token and a zero output row.  The record is
  * the same quantization as tq_quantize_append's ("Method"), computed by one warp
  * per (sequence, KV head) in fp32 with its own order of operations, so a code may
- * differ from the append kernels' only where y lies within ~1e-6 of a boundary.
+ * differ from the append kernels' only where y lies within the 1e-5 tie band of a
+ * boundary (the same bound the append kernels meet against the exact method).
  * The warp that reads the new token's block writes the record to the cache and
  * into its own shared-memory copy of the block, so no other kernel runs and no
  * CTA waits for another.  Other arguments, the workspace contract and errors as
